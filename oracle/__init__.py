@@ -1,0 +1,16 @@
+"""fp64 CPU oracle for kkt_solve (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s cpu_baseline /
+reference leg may import this package.  The product path (the CUDA library and
+its binding in ``gdn_chunkwise_ut_gb300``) never does, and shares no code with
+it.  Parity is unpinned for nothing here: every function is pinned by the
+``-m "not gpu"`` tests in ``tests/test_oracle_pins.py`` and
+``tests/test_oracle_mutations.py``.
+"""
+from .oracle import (  # noqa: F401
+    build,
+    load,
+    oracle_chunk,
+    oracle_fwd,
+    oracle_threads,
+)

@@ -1,0 +1,242 @@
+/*
+ * kkt_oracle.c -- fp64 CPU oracle for kkt_solve, the chunk-local UT transform
+ * of Gated DeltaNet chunked prefill.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path (the CUDA library
+ * and its Python binding) may include, link, load or call this file.  Only
+ * tests/, __graft_entry__.smoke() and bench.py's cpu_baseline / reference leg
+ * use it.  It shares no code, header, table or helper with the CUDA path.
+ *
+ * What it computes, following "TileLang 实战：单位下三角矩阵求逆" (TileLang in
+ * practice: inverting a unit lower-triangular matrix):
+ *
+ *   For every chunk of C consecutive tokens of one sequence and one head
+ *   (the last chunk of a sequence may be shorter: Lc <= C rows):
+ *
+ *   1. §1 (the coefficient matrix) and §3.2 (beta scales rows, the diagonal
+ *      is set to one):
+ *          A = I + strictLower(diag(beta) K K^T)
+ *      i.e. A[i][i] = 1, A[i][j] = beta_i * <k_i, k_j> for i > j, 0 above.
+ *   2. §2.1 (row-wise forward substitution):
+ *          X[r,:] = e_r^T - sum_{j<r} A[r][j] X[j,:],   T = X = A^{-1}.
+ *      The oracle deliberately does NOT use the blocked recursion of §2.2;
+ *      it is the plain definition of the inverse of a unit lower-triangular
+ *      matrix, solved one row after another.
+ *   3. §1 (the two products the inverse feeds):
+ *          W = T diag(beta) K,    U~ = T diag(beta) V.
+ *
+ *   Output layout (the CUDA library's layout, fixed by its C header):
+ *     T_out[n][h][0..C)  row n holds row (n - chunk start) of its chunk's T,
+ *                        with zeros in columns j >= Lc;
+ *     W_out[n][h][0..dk), U_out[n][h][0..dv)  one row per token.
+ *   n is the flat token index (b*T + t for fixed-length batches, or the
+ *   packed index for variable-length batches described by cu_seqlens).
+ *
+ * All arithmetic is in double precision on the values the caller passes (the
+ * tests pass the bf16-rounded inputs widened to double, and beta's fp32
+ * value widened to double).
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Step 1: A = I + strictLower(diag(beta) K K^T), C x C, row-major.  Rows and
+ * columns >= Lc (padding of a short last chunk) are those of the identity. */
+static void build_coefficients(const double *kc, const double *bc, int Lc, int C,
+                               int dk, double *A)
+{
+    for (int i = 0; i < C; ++i) {
+        for (int j = 0; j < C; ++j) {
+            double a = 0.0;
+            if (i == j) {
+                a = 1.0;
+            } else if (i > j && i < Lc) {
+                double dot = 0.0;
+                for (int d = 0; d < dk; ++d)
+                    dot += kc[(int64_t)i * dk + d] * kc[(int64_t)j * dk + d];
+                a = bc[i] * dot;
+            }
+            A[(int64_t)i * C + j] = a;
+        }
+    }
+}
+
+/* Step 2: X = A^{-1} by forward substitution, one row after another. */
+static void invert_unit_lower(const double *A, int C, double *X)
+{
+    for (int r = 0; r < C; ++r) {
+        double *xr = X + (int64_t)r * C;
+        for (int c = 0; c < C; ++c)
+            xr[c] = (c == r) ? 1.0 : 0.0;
+        for (int j = 0; j < r; ++j) {
+            const double arj = A[(int64_t)r * C + j];
+            const double *xj = X + (int64_t)j * C;
+            for (int c = 0; c < C; ++c)
+                xr[c] -= arj * xj[c];
+        }
+    }
+}
+
+/* Step 3: rows of Y = T diag(beta) M for M = K (width dk) or V (width dv). */
+static void apply_scaled(const double *X, const double *bc, const double *mc,
+                         int Lc, int C, int width, double *out)
+{
+    for (int i = 0; i < Lc; ++i) {
+        for (int e = 0; e < width; ++e) {
+            double s = 0.0;
+            for (int j = 0; j < Lc; ++j)
+                s += X[(int64_t)i * C + j] * bc[j] * mc[(int64_t)j * width + e];
+            out[(int64_t)i * width + e] = s;
+        }
+    }
+}
+
+/*
+ * One chunk, contiguous inputs.
+ *   kc [Lc][dk], vc [Lc][dv], bc [Lc]       (rows of one head)
+ *   T  [Lc][C]  (zeros in columns >= Lc), W [Lc][dk], U [Lc][dv]
+ *   A_out, if not NULL, receives the C x C coefficient matrix.
+ * Returns 0, or -1 on bad sizes / allocation failure.
+ */
+int kkt_oracle_chunk(const double *kc, const double *vc, const double *bc,
+                     int Lc, int C, int dk, int dv,
+                     double *T, double *W, double *U, double *A_out)
+{
+    if (Lc < 1 || Lc > C || C < 1 || dk < 1 || dv < 1)
+        return -1;
+    double *A = (double *)malloc(sizeof(double) * (size_t)C * C);
+    double *X = (double *)malloc(sizeof(double) * (size_t)C * C);
+    double *bz = (double *)calloc((size_t)C, sizeof(double));
+    if (!A || !X || !bz) {
+        free(A); free(X); free(bz);
+        return -1;
+    }
+    memcpy(bz, bc, sizeof(double) * (size_t)Lc);
+    build_coefficients(kc, bz, Lc, C, dk, A);
+    invert_unit_lower(A, C, X);
+    for (int i = 0; i < Lc; ++i)
+        for (int j = 0; j < C; ++j)
+            T[(int64_t)i * C + j] = (j < Lc) ? X[(int64_t)i * C + j] : 0.0;
+    apply_scaled(X, bz, kc, Lc, C, dk, W);
+    apply_scaled(X, bz, vc, Lc, C, dv, U);
+    if (A_out)
+        memcpy(A_out, A, sizeof(double) * (size_t)C * C);
+    free(A); free(X); free(bz);
+    return 0;
+}
+
+/*
+ * Whole tensors.
+ *   k    [N][H][dk], v [N][H][dv], beta [N][H]  (N = B*T fixed-length, or the
+ *        packed token count T when cu_seqlens is given)
+ *   cu_seqlens: NULL for B sequences of T tokens each; otherwise B+1
+ *        nondecreasing offsets with cu_seqlens[0] = 0, cu_seqlens[B] = T.
+ *   T_out [N][H][C], W_out [N][H][dk], U_out [N][H][dv].
+ *   nthreads <= 0 uses the OpenMP default.
+ * Returns 0, -1 on bad arguments, -2 on a malformed cu_seqlens.
+ */
+int kkt_oracle_fwd(const double *k, const double *v, const double *beta,
+                   const int64_t *cu_seqlens, int64_t B, int64_t T, int64_t H,
+                   int64_t dk, int64_t dv, int64_t C,
+                   double *T_out, double *W_out, double *U_out, int nthreads)
+{
+    if (B < 1 || T < 0 || H < 1 || dk < 1 || dv < 1 || C < 1)
+        return -1;
+    if (cu_seqlens) {
+        if (cu_seqlens[0] != 0 || cu_seqlens[B] != T)
+            return -2;
+        for (int64_t s = 0; s < B; ++s)
+            if (cu_seqlens[s + 1] < cu_seqlens[s])
+                return -2;
+    }
+    /* Enumerate chunks: (first token, length). */
+    int64_t nchunks = 0;
+    for (int64_t s = 0; s < B; ++s) {
+        int64_t t0 = cu_seqlens ? cu_seqlens[s] : s * T;
+        int64_t t1 = cu_seqlens ? cu_seqlens[s + 1] : (s + 1) * T;
+        nchunks += (t1 - t0 + C - 1) / C;
+    }
+    int64_t *cstart = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nchunks + 1));
+    int *clen = (int *)malloc(sizeof(int) * (size_t)(nchunks + 1));
+    if (!cstart || !clen) {
+        free(cstart); free(clen);
+        return -1;
+    }
+    int64_t q = 0;
+    for (int64_t s = 0; s < B; ++s) {
+        int64_t t0 = cu_seqlens ? cu_seqlens[s] : s * T;
+        int64_t t1 = cu_seqlens ? cu_seqlens[s + 1] : (s + 1) * T;
+        for (int64_t a = t0; a < t1; a += C) {
+            cstart[q] = a;
+            clen[q] = (int)((t1 - a) < C ? (t1 - a) : C);
+            ++q;
+        }
+    }
+    int status = 0;
+    const int64_t units = nchunks * H;
+#ifdef _OPENMP
+    if (nthreads > 0)
+        omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+#pragma omp parallel
+    {
+        double *kc = (double *)malloc(sizeof(double) * (size_t)(C * dk));
+        double *vc = (double *)malloc(sizeof(double) * (size_t)(C * dv));
+        double *bc = (double *)malloc(sizeof(double) * (size_t)C);
+        double *Tc = (double *)malloc(sizeof(double) * (size_t)(C * C));
+        double *Wc = (double *)malloc(sizeof(double) * (size_t)(C * dk));
+        double *Uc = (double *)malloc(sizeof(double) * (size_t)(C * dv));
+        int ok = kc && vc && bc && Tc && Wc && Uc;
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t u = 0; u < units; ++u) {
+            if (!ok)
+                continue;
+            const int64_t c = u / H, h = u % H;
+            const int64_t n0 = cstart[c];
+            const int Lc = clen[c];
+            for (int i = 0; i < Lc; ++i) {
+                const int64_t n = n0 + i;
+                memcpy(kc + (int64_t)i * dk, k + (n * H + h) * dk, sizeof(double) * (size_t)dk);
+                memcpy(vc + (int64_t)i * dv, v + (n * H + h) * dv, sizeof(double) * (size_t)dv);
+                bc[i] = beta[n * H + h];
+            }
+            if (kkt_oracle_chunk(kc, vc, bc, Lc, (int)C, (int)dk, (int)dv, Tc, Wc, Uc, NULL) != 0) {
+#pragma omp atomic write
+                status = -1;
+                continue;
+            }
+            for (int i = 0; i < Lc; ++i) {
+                const int64_t n = n0 + i;
+                memcpy(T_out + (n * H + h) * C, Tc + (int64_t)i * C, sizeof(double) * (size_t)C);
+                memcpy(W_out + (n * H + h) * dk, Wc + (int64_t)i * dk, sizeof(double) * (size_t)dk);
+                memcpy(U_out + (n * H + h) * dv, Uc + (int64_t)i * dv, sizeof(double) * (size_t)dv);
+            }
+        }
+        if (!ok) {
+#pragma omp atomic write
+            status = -1;
+        }
+        free(kc); free(vc); free(bc); free(Tc); free(Wc); free(Uc);
+    }
+    free(cstart);
+    free(clen);
+    return status;
+}
+
+/* Number of OpenMP threads a parallel region of kkt_oracle_fwd would use. */
+int kkt_oracle_threads(int nthreads)
+{
+#ifdef _OPENMP
+    if (nthreads > 0)
+        return nthreads;
+    return omp_get_max_threads();
+#else
+    (void)nthreads;
+    return 1;
+#endif
+}
