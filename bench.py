@@ -1,0 +1,357 @@
+#!/usr/bin/env python
+"""Benchmark of kkt_solve fwd (chunk-local UT transform), one JSON line on stdout.
+
+Workload (default): B=4 sequences x 8192 tokens = 32768 tokens, H=16 heads,
+dk=dv=128, C=64, bf16 K/V/W/U, fp32 beta/T -- synthetic inputs (seeded; K rows
+L2-normalised N(0,1), V ~ N(0,1), beta = sigmoid(N(0,1))).  A step is one call
+of the whole path (A, T, W, U for every chunk and head).  The inputs (270 MB)
+are larger than the 129 MB L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+For N > 1 launch one rank per GPU with torch.distributed.run; every rank runs
+the same per-GPU workload (weak scaling, no collective on the data path) and
+rank 0 prints the line with the max-over-ranks time.  ``--impl reference``
+times the fp64 CPU oracle on the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from pathlib import Path
+
+import numpy as np
+import torch
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+from gdn_chunkwise_ut_gb300 import costmodel  # noqa: E402
+from gdn_chunkwise_ut_gb300.inputs import workloads  # noqa: E402
+
+METRIC = "tokens/sec and achieved HBM GB/s (% of GB300 peak) for kkt_solve fwd, C=64"
+DEFAULT_WORKLOAD = "c3_b4_t8192_h16"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+KERNEL_SOURCES = {"simt": ["kkt_simt.cu"], "tc": ["kkt_tc.cu"]}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc"])
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# --- distributed plumbing -------------------------------------------------------------------
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_value(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Whole-job throughput: units all ranks processed / the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+# --- clocks ---------------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of this GPU's SM clock and throttle reasons."""
+    FIELDS = ("pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.bus = None
+        try:
+            p = torch.cuda.get_device_properties(device_index)
+            self.bus = f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+        except Exception:
+            pass
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                if self.bus and parts[0].upper().lstrip("0") != self.bus.upper().lstrip("0"):
+                    continue
+                rows.append(parts)
+        os.unlink(self.file.name)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, reasons = [], [], set()
+        for r in rows:
+            try:
+                sm.append(float(r[1])); mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --- peaks and recorded ncu traffic -----------------------------------------------------------
+
+def hbm_peak():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            return float(json.loads(p.read_text())["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, copy burst)"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 measurement)"
+
+
+def kernel_source_hash(kernel: str) -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel] + ["kkt_internal.cuh"]:
+        h.update((ROOT / "gdn_chunkwise_ut_gb300" / "csrc" / name).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current source."""
+    p = ROOT / "profiles" / "traffic.json"
+    if not p.exists():
+        return None
+    try:
+        rec = json.loads(p.read_text()).get(f"{kernel}:{workload}")
+    except Exception:
+        return None
+    if not rec or rec.get("source_hash") != kernel_source_hash(kernel):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# --- our path -----------------------------------------------------------------------------------
+
+def bench_ours(args, rank, world, local):
+    from gdn_chunkwise_ut_gb300 import HostRunner, kkt_solve_fwd, select_kernel
+    w = workloads()[args.workload]
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    kernel = select_kernel(w.dk, w.dv, w.C, w.io, args.kernel)
+    k, v, beta, cu = w.make(seed=rank, device=dev)
+    cu_t = None if cu is None else torch.as_tensor(cu, dtype=torch.int32, device=dev)
+    T_out = torch.empty((k.shape[0], k.shape[1], w.H, w.C), device=dev)
+    W_out = torch.empty_like(k)
+    U_out = torch.empty_like(v)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        kkt_solve_fwd(k, v, beta, w.C, cu_t, T_out=T_out, W_out=W_out, U_out=U_out, kernel=args.kernel)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    # let the sampler see the GPU under load before the timed region
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < 0.3:
+        step()
+        torch.cuda.synchronize()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t_stop.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    total_ms = t_start.elapsed_time(t_stop)
+    launch_ms = statistics.fmean(a.elapsed_time(b) for a, b in ev)
+    max_ms = max_over_ranks(total_ms, world)
+
+    units = w.tokens * w.H
+    io_bytes = 4 if w.io == "f32" else 2
+    alg_bytes = units * costmodel.bytes_per_unit(w.C, w.dk, w.dv, io_bytes)
+    tokens_per_s = aggregate_value(w.tokens * K, world, max_ms / 1e3)
+    peak, peak_src = hbm_peak()
+    achieved = alg_bytes / (launch_ms / 1e3) / 1e9
+    traffic = recorded_traffic(kernel, args.workload)
+
+    # end to end through the public API with host buffers (pinned), copies inside the timed region
+    runner = HostRunner(k.shape[0], k.shape[1], w.H, w.dk, w.dv, w.C, dtype=k.dtype, cu_seqlens=cu,
+                        kernel=args.kernel, device=dev)
+    kh, vh, bh = (x.cpu().pin_memory() for x in (k, v, beta))
+    for _ in range(2):
+        runner(kh, vh, bh)
+    n_e2e = max(3, args.e2e_steps)
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        runner(kh, vh, bh)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    e2e = {"value": aggregate_value(w.tokens * n_e2e, world, e2e_s), "unit": "tokens/s",
+           "h2d_bytes_per_step": runner.h2d_bytes, "d2h_bytes_per_step": runner.d2h_bytes,
+           "steps": n_e2e}
+
+    line = {
+        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": max_ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.io == "bf16" else "f32",
+        "data": "synthetic (seeded K rows L2-normalised N(0,1), V ~ N(0,1), beta = sigmoid(N(0,1)))",
+        "config": {"workload": args.workload, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
+                   "C": w.C, "tokens_per_step": w.tokens, "kernel": kernel,
+                   "l2": f"inputs larger than L2 ({(units * (2 * (w.dk + w.dv) + 4)) / 1e6:.0f} MB > 129 MB), no flush"},
+        "hbm_gbs": achieved, "hbm_frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
+        "chunks_per_s": aggregate_value(units / w.C * K, world, max_ms / 1e3),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
+                     "kernel": f"kkt_{kernel}", "alg_bytes_per_launch": alg_bytes,
+                     "avg_launch_ms": launch_ms},
+        "clocks": clocks, "e2e": e2e, "gpu_launches": K,
+    }
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(k, v, beta, cu, w)
+    return line
+
+
+def cpu_baseline(k, v, beta, cu, w, max_tokens=None):
+    """The oracle, as it stands, on the host cores over a bounded sample of the workload."""
+    import oracle
+    oracle.build()
+    if cu is None:
+        nseq = w.B if max_tokens is None else max(1, min(w.B, max_tokens // w.T))
+        ks, vs, bs = (x[:nseq].cpu().double().numpy() for x in (k, v, beta))
+        sample = f"{nseq} of {w.B} sequences x {w.T} tokens x {w.H} heads (fp64 oracle on bf16-rounded inputs)"
+        tokens, cus = nseq * w.T, None
+    else:
+        ks, vs, bs = (x.cpu().double().numpy() for x in (k, v, beta))
+        tokens, cus, sample = w.tokens, cu, f"all {w.tokens} packed tokens x {w.H} heads"
+    cores = oracle.oracle_threads(0)
+    t0 = time.perf_counter()
+    oracle.oracle_fwd(ks, vs, bs, w.C, cu_seqlens=cus, nthreads=cores)
+    dt = time.perf_counter() - t0
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": sample, "seconds": dt}
+
+
+# --- reference arm: the oracle on the host cores -----------------------------------------------
+
+def bench_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    w = workloads()[args.workload]
+    if w.varlen:
+        raise SystemExit("reference arm covers fixed-length workloads")
+    # each step: one chunk-aligned slice of one sequence, all heads, sized so that
+    # warmup + steps fit in about two minutes of wall time
+    from gdn_chunkwise_ut_gb300.inputs import make_inputs
+    cores = oracle.oracle_threads(0)
+    probe_tokens = w.C * 4
+    k, v, b = make_inputs(1, probe_tokens, w.H, w.dk, w.dv, seed=0)
+    kd, vd, bd = (x.double().numpy() for x in (k, v, b))
+    t0 = time.perf_counter()
+    oracle.oracle_fwd(kd, vd, bd, w.C, nthreads=cores)
+    per_token = (time.perf_counter() - t0) / probe_tokens
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    tokens = int(max(w.C, min(w.T, (budget / per_token) // w.C * w.C)))
+    k, v, b = make_inputs(1, tokens, w.H, w.dk, w.dv, seed=0)
+    kd, vd, bd = (x.double().numpy() for x in (k, v, b))
+    for _ in range(args.warmup):
+        oracle.oracle_fwd(kd, vd, bd, w.C, nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.oracle_fwd(kd, vd, bd, w.C, nthreads=cores)
+    dt = time.perf_counter() - t0
+    val = tokens * args.steps / dt
+    sample = f"{tokens} tokens x {w.H} heads of one {w.T}-token sequence per step (fp64 oracle)"
+    return {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": args.workload, "B": w.B, "T": w.T, "H": w.H,
+                                        "dk": w.dk, "dv": w.dv, "C": w.C, "tokens_per_step": tokens},
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        line = bench_reference(args, rank, world)
+    else:
+        line = bench_ours(args, rank, world, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

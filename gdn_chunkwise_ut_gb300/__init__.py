@@ -1,1 +1,12 @@
-"""kkt_solve for GB300: the chunk-local UT transform of Gated DeltaNet prefill."""
+"""kkt_solve for GB300: the chunk-local UT transform of Gated DeltaNet prefill.
+
+    from gdn_chunkwise_ut_gb300 import kkt_solve_fwd
+    T, W, U = kkt_solve_fwd(k, v, beta, C=64)            # k, v bf16 [B,T,H,128] on cuda
+
+The computation runs in libkkt.so (hand-written CUDA for sm_103a, C ABI in
+include/kkt.h); this package only marshals torch tensors.
+"""
+from .api import HostRunner, device_status, kkt_solve_fwd, select_kernel  # noqa: F401
+from ._lib import KktError  # noqa: F401
+
+__all__ = ["kkt_solve_fwd", "device_status", "select_kernel", "HostRunner", "KktError"]

@@ -1,0 +1,139 @@
+"""Python front end of libkkt: torch tensors in, the C ABI underneath.
+
+``kkt_solve_fwd`` checks shapes and dtypes, allocates outputs with torch when
+none are given, and passes raw device pointers and the current CUDA stream to
+``kkt_solve_fwd_ex`` in libkkt.so.  Every step of the computation runs in the
+library's CUDA kernels.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+
+_IO = {torch.bfloat16: _lib.KKT_IO_BF16, torch.float32: _lib.KKT_IO_F32}
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _check(t: torch.Tensor, name: str, dtype, shape):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def kkt_solve_fwd(k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor, C: int,
+                  cu_seqlens: torch.Tensor | None = None, *, T_out=None, W_out=None, U_out=None,
+                  kernel: str = "auto", stream=None):
+    """UT transform of every chunk: returns (T_out, W, U).
+
+    k [B, T, H, dk] and v [B, T, H, dv] (bf16, or fp32 for the fp32-I/O path),
+    beta [B, T, H] fp32.  With ``cu_seqlens`` (int32 [N+1] on the device) the
+    tensors are [1, T, H, .] and hold N packed sequences.  T_out is fp32
+    [B, T, H, C]; W and U have k's dtype.  ``kernel`` is "auto", "simt" or "tc".
+    """
+    if k.dim() != 4 or v.dim() != 4 or beta.dim() != 3:
+        raise ValueError("expected k [B,T,H,dk], v [B,T,H,dv], beta [B,T,H]")
+    Bt, T, H, dk = k.shape
+    dv = v.shape[-1]
+    io = _IO.get(k.dtype)
+    if io is None:
+        raise ValueError(f"unsupported dtype {k.dtype}")
+    _check(k, "k", k.dtype, (Bt, T, H, dk))
+    _check(v, "v", k.dtype, (Bt, T, H, dv))
+    _check(beta, "beta", torch.float32, (Bt, T, H))
+    if cu_seqlens is not None:
+        if Bt != 1:
+            raise ValueError("with cu_seqlens the batch dimension must be 1")
+        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or cu_seqlens.dim() != 1:
+            raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor")
+        B = cu_seqlens.shape[0] - 1
+        cu_ptr = cu_seqlens.data_ptr()
+    else:
+        B, cu_ptr = Bt, None
+    dev = k.device
+    if T_out is None:
+        T_out = torch.empty((Bt, T, H, C), device=dev, dtype=torch.float32)
+    if W_out is None:
+        W_out = torch.empty((Bt, T, H, dk), device=dev, dtype=k.dtype)
+    if U_out is None:
+        U_out = torch.empty((Bt, T, H, dv), device=dev, dtype=k.dtype)
+    _check(T_out, "T_out", torch.float32, (Bt, T, H, C))
+    _check(W_out, "W_out", k.dtype, (Bt, T, H, dk))
+    _check(U_out, "U_out", k.dtype, (Bt, T, H, dv))
+    kern = _lib.KERNELS.get(kernel)
+    if kern is None:
+        raise ValueError(f"kernel must be one of {sorted(_lib.KERNELS)}")
+    rc = _lib.lib().kkt_solve_fwd_ex(k.data_ptr(), v.data_ptr(), beta.data_ptr(), cu_ptr,
+                                     B, T, H, dk, dv, C, T_out.data_ptr(), W_out.data_ptr(),
+                                     U_out.data_ptr(), io, kern, _stream_handle(stream))
+    if rc != _lib.KKT_OK:
+        raise _lib.KktError(rc, "kkt_solve_fwd")
+    return T_out, W_out, U_out
+
+
+def device_status(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device status word."""
+    return int(_lib.lib().kkt_device_status(_stream_handle(stream)))
+
+
+def select_kernel(dk: int, dv: int, C: int, io: str = "bf16", kernel: str = "auto") -> str:
+    """Which kernel a call would run ("simt" / "tc"); raises KktError if unsupported."""
+    iod = _lib.KKT_IO_F32 if io == "f32" else _lib.KKT_IO_BF16
+    r = _lib.lib().kkt_select_kernel(dk, dv, C, iod, _lib.KERNELS[kernel])
+    if r < 0:
+        raise _lib.KktError(-r, "kkt_select_kernel")
+    return {_lib.KKT_KERNEL_SIMT: "simt", _lib.KKT_KERNEL_TC: "tc"}[r]
+
+
+class HostRunner:
+    """End-to-end calls on host tensors: pinned host -> device -> kkt_solve_fwd -> pinned host.
+
+    Device buffers are allocated once; each call copies the inputs in, runs the
+    library on the current stream and copies T, W and U back, then synchronises.
+    """
+
+    def __init__(self, B, T, H, dk, dv, C, *, dtype=torch.bfloat16, cu_seqlens=None,
+                 kernel="auto", device="cuda"):
+        self.C, self.kernel = C, kernel
+        dev = torch.device(device)
+        self.k = torch.empty((B, T, H, dk), device=dev, dtype=dtype)
+        self.v = torch.empty((B, T, H, dv), device=dev, dtype=dtype)
+        self.beta = torch.empty((B, T, H), device=dev, dtype=torch.float32)
+        self.cu = None if cu_seqlens is None else torch.as_tensor(cu_seqlens, dtype=torch.int32).to(dev)
+        self.T_out = torch.empty((B, T, H, C), device=dev, dtype=torch.float32)
+        self.W = torch.empty((B, T, H, dk), device=dev, dtype=dtype)
+        self.U = torch.empty((B, T, H, dv), device=dev, dtype=dtype)
+        self.T_host = torch.empty(self.T_out.shape, dtype=torch.float32, pin_memory=True)
+        self.W_host = torch.empty(self.W.shape, dtype=dtype, pin_memory=True)
+        self.U_host = torch.empty(self.U.shape, dtype=dtype, pin_memory=True)
+
+    @property
+    def h2d_bytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in (self.k, self.v, self.beta))
+
+    @property
+    def d2h_bytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in (self.T_out, self.W, self.U))
+
+    def __call__(self, k_host, v_host, beta_host, sync: bool = True):
+        self.k.copy_(k_host, non_blocking=True)
+        self.v.copy_(v_host, non_blocking=True)
+        self.beta.copy_(beta_host, non_blocking=True)
+        kkt_solve_fwd(self.k, self.v, self.beta, self.C, self.cu, T_out=self.T_out, W_out=self.W,
+                      U_out=self.U, kernel=self.kernel)
+        self.T_host.copy_(self.T_out, non_blocking=True)
+        self.W_host.copy_(self.W, non_blocking=True)
+        self.U_host.copy_(self.U, non_blocking=True)
+        if sync:
+            torch.cuda.current_stream().synchronize()
+        return self.T_host, self.W_host, self.U_host

@@ -1,0 +1,105 @@
+// kkt_api.cu -- the C entry points of libkkt: argument checks, kernel choice,
+// the per-device status word.  Declared in include/kkt.h.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kkt_internal.cuh"
+
+namespace {
+
+// Per-device status word: first device-side error since the last
+// kkt_device_status() (0 = none).
+__device__ int g_kkt_status = 0;
+
+constexpr int kMaxDevices = 64;
+int *g_status_ptr[kMaxDevices] = {};
+
+int status_ptr(int **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KKT_ERR_NO_DEVICE;
+    if (!g_status_ptr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_kkt_status) != cudaSuccess) return KKT_ERR_CUDA;
+        g_status_ptr[dev] = static_cast<int *>(ptr);
+    }
+    *out = g_status_ptr[dev];
+    return KKT_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool head_dim_ok(int d) { return d == 64 || d == 128; }
+bool chunk_ok(int C) { return C == 32 || C == 64 || C == 128; }
+
+}  // namespace
+
+extern "C" int kkt_select_kernel(int dk, int dv, int C, int io_dtype, int kernel) {
+    if (io_dtype != KKT_IO_BF16 && io_dtype != KKT_IO_F32) return -KKT_ERR_ARG;
+    if (!head_dim_ok(dk) || !head_dim_ok(dv) || !chunk_ok(C)) return -KKT_ERR_UNSUPPORTED;
+    const bool tc = kkt::tc_supports(dk, dv, C, io_dtype);
+    switch (kernel) {
+        case KKT_KERNEL_AUTO: return tc ? KKT_KERNEL_TC : KKT_KERNEL_SIMT;
+        case KKT_KERNEL_SIMT: return KKT_KERNEL_SIMT;
+        case KKT_KERNEL_TC: return tc ? KKT_KERNEL_TC : -KKT_ERR_UNSUPPORTED;
+        default: return -KKT_ERR_ARG;
+    }
+}
+
+extern "C" int kkt_solve_fwd_ex(const void *k, const void *v, const float *beta, const int32_t *cu_seqlens,
+                                int B, int T, int H, int dk, int dv, int C,
+                                float *T_out, void *W_out, void *U_out,
+                                int io_dtype, int kernel, struct CUstream_st *stream) {
+    if (!k || !v || !beta || !T_out || !W_out || !U_out) return KKT_ERR_ARG;
+    if (B < 1 || T < 0 || H < 1 || H > 65535) return KKT_ERR_ARG;
+    const int which = kkt_select_kernel(dk, dv, C, io_dtype, kernel);
+    if (which < 0) return -which;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(beta) || !aligned16(T_out) || !aligned16(W_out) ||
+        !aligned16(U_out) || (cu_seqlens && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)))
+        return KKT_ERR_ALIGN;
+    const int64_t ntok = cu_seqlens ? (int64_t)T : (int64_t)B * T;
+    if (ntok == 0) return KKT_OK;
+    // the work-id space and every flat index must fit comfortably in 63 bits / grid limits
+    if (ntok / C + B > 0x7fffffffLL) return KKT_ERR_ARG;
+
+    kkt::Problem p;
+    p.k = k; p.v = v; p.beta = beta; p.cu_seqlens = cu_seqlens;
+    p.nseq = B; p.T = T; p.ntok = ntok;
+    p.H = H; p.dk = dk; p.dv = dv; p.C = C;
+    p.T_out = T_out; p.W_out = W_out; p.U_out = U_out;
+    p.io = io_dtype;
+    p.stream = reinterpret_cast<cudaStream_t>(stream);
+    const int st = status_ptr(&p.status);
+    if (st != KKT_OK) return st;
+    return which == KKT_KERNEL_TC ? kkt::launch_tc(p) : kkt::launch_simt(p);
+}
+
+extern "C" int kkt_solve_fwd(const void *k, const void *v, const float *beta, const int32_t *cu_seqlens,
+                             int B, int T, int H, int dk, int dv, int C,
+                             float *T_out, void *W_out, void *U_out, struct CUstream_st *stream) {
+    return kkt_solve_fwd_ex(k, v, beta, cu_seqlens, B, T, H, dk, dv, C, T_out, W_out, U_out,
+                            KKT_IO_BF16, KKT_KERNEL_AUTO, stream);
+}
+
+extern "C" int kkt_device_status(struct CUstream_st *stream) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return KKT_ERR_CUDA;
+    int value = 0;
+    if (cudaMemcpyFromSymbol(&value, g_kkt_status, sizeof(int)) != cudaSuccess) return KKT_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_kkt_status, &zero, sizeof(int)) != cudaSuccess) return KKT_ERR_CUDA;
+    return value;
+}
+
+extern "C" const char *kkt_status_string(int status) {
+    switch (status) {
+        case KKT_OK: return "ok";
+        case KKT_ERR_ARG: return "invalid argument";
+        case KKT_ERR_UNSUPPORTED: return "unsupported chunk size, head dimension, dtype or kernel";
+        case KKT_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case KKT_ERR_CUDA: return "CUDA error";
+        case KKT_ERR_SEQLENS: return "malformed cu_seqlens";
+        case KKT_ERR_TIMEOUT: return "device-side wait timed out";
+        case KKT_ERR_NO_DEVICE: return "no usable CUDA device";
+        default: return "unknown status";
+    }
+}
+
+extern "C" int kkt_version(void) { return (0 << 16) | (1 << 8) | 0; }

@@ -1,0 +1,98 @@
+// kkt_internal.cuh -- shared host/device definitions of libkkt (not installed).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kkt.h"
+
+namespace kkt {
+
+// Everything a launcher needs, validated by the C entry points.
+struct Problem {
+    const void *k;
+    const void *v;
+    const float *beta;
+    const int32_t *cu_seqlens;  // nullptr: nseq sequences of T tokens each
+    int nseq;                   // number of sequences (B)
+    int T;                      // tokens per sequence, or the packed total with cu_seqlens
+    int64_t ntok;               // rows of the flat token axis (B*T, or T with cu_seqlens)
+    int H, dk, dv, C;
+    float *T_out;
+    void *W_out;
+    void *U_out;
+    int io;                     // KKT_IO_BF16 / KKT_IO_F32
+    cudaStream_t stream;
+    int *status;                // device status word of the current device
+};
+
+// Device-side error codes (first error wins).
+__device__ __forceinline__ void record_error(int *status, int code) {
+    atomicCAS(status, 0, code);
+}
+
+// Work ids and chunks.  Sequence s owns the ids [Q(s), Q(s+1)) with
+// Q(s) = floor(start(s) / C) + s.  Q is strictly increasing for nondecreasing
+// starts, and a sequence of L tokens starting at a gets
+// floor((a mod C + L) / C) + 1 >= ceil(L / C) ids, so every chunk has an id;
+// the surplus ids (at most one per sequence) are idle.  Total ids:
+// Q(nseq) = floor(ntok / C) + nseq.  No host-side pass over cu_seqlens and no
+// device scratch table are needed.
+struct Chunk {
+    int64_t t0;  // first row in the flat token axis
+    int Lc;      // rows in this chunk, 1..C
+};
+
+__device__ __forceinline__ int64_t seq_start(const int32_t *cu, int s, int T) {
+    return cu ? (int64_t)__ldg(cu + s) : (int64_t)s * T;
+}
+
+__host__ __device__ __forceinline__ int64_t total_work_ids(int64_t ntok, int C, int nseq) {
+    return ntok / C + nseq;
+}
+
+// Maps a work id to its chunk.  Returns false for idle ids and for ids whose
+// sequence bounds are malformed (recorded as KKT_ERR_SEQLENS); never touches
+// memory outside cu_seqlens[0..nseq].
+__device__ __forceinline__ bool map_chunk(int64_t id, const int32_t *cu, int nseq, int T, int64_t ntok,
+                                          int C, int *status, Chunk &out) {
+    int lo = 0, hi = nseq - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        const int64_t q = seq_start(cu, mid, T) / C + mid;
+        if (q <= id) lo = mid; else hi = mid - 1;
+    }
+    const int s = lo;
+    const int64_t a = seq_start(cu, s, T);
+    const int64_t b = seq_start(cu, s + 1, T);
+    if (a < 0 || b < a || b > ntok) {
+        record_error(status, KKT_ERR_SEQLENS);
+        return false;
+    }
+    const int64_t c = id - (a / C + s);
+    if (c < 0) {
+        record_error(status, KKT_ERR_SEQLENS);
+        return false;
+    }
+    const int64_t t0 = a + c * C;
+    if (t0 >= b) return false;
+    out.t0 = t0;
+    out.Lc = (int)((b - t0) < C ? (b - t0) : C);
+    return true;
+}
+
+// Checks the global shape of cu_seqlens for sequence s (called once per s).
+__device__ __forceinline__ void check_sequence(const int32_t *cu, int s, int nseq, int64_t ntok, int *status) {
+    if (!cu) return;
+    const int64_t a = __ldg(cu + s), b = __ldg(cu + s + 1);
+    bool bad = (a < 0) || (b < a) || (b > ntok);
+    if (s == 0 && a != 0) bad = true;
+    if (s == nseq - 1 && b != ntok) bad = true;
+    if (bad) record_error(status, KKT_ERR_SEQLENS);
+}
+
+int launch_simt(const Problem &p);
+int launch_tc(const Problem &p);
+bool tc_supports(int dk, int dv, int C, int io);
+
+}  // namespace kkt

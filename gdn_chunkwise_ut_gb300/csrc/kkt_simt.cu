@@ -1,0 +1,209 @@
+// kkt_simt.cu -- one CTA per (chunk, head), fp32 CUDA-core arithmetic.
+//
+// The straightforward kernel: it serves fp32 I/O, every (C, dk, dv) the
+// library accepts, and is the baseline the tcgen05 kernel is measured
+// against.  It runs the same blocked schedule as the tensor-core kernel
+// ("TileLang 实战：单位下三角矩阵求逆" §2.2): 16 x 16 diagonal blocks inverted
+// by forward substitution (§2.1, one thread per column), then the coupling
+// levels -L11^-1 L10 L00^-1 at s = 16, 32, ..., C/2 as shared-memory GEMMs.
+//
+// Shared memory (fp32): K [C][dk+1], V [C][dv+1], A/T [C][C+1], beta [C],
+// coupling scratch [C/2][C/2+1].  The +1 row padding keeps the column walks of
+// the Gram and epilogue loops on distinct banks.
+#include <cuda_bf16.h>
+
+#include "kkt_internal.cuh"
+
+namespace kkt {
+namespace {
+
+constexpr int kSimtThreads = 256;
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+struct SimtParams {
+    const void *k, *v;
+    const float *beta;
+    const int32_t *cu;
+    int nseq, T;
+    int64_t ntok;
+    int H, dk, dv;
+    float *T_out;
+    void *W_out, *U_out;
+    int *status;
+};
+
+template <typename TIn, int C>
+__global__ void __launch_bounds__(kSimtThreads) kkt_simt_kernel(const SimtParams p) {
+    extern __shared__ float smem[];
+    const int DK = p.dk, DV = p.dv;
+    const int KS = DK + 1, VS = DV + 1;
+    constexpr int TS = C + 1;
+    float *Ks = smem;            // [C][KS]
+    float *Vs = Ks + C * KS;     // [C][VS]
+    float *Ts = Vs + C * VS;     // [C][TS]: A, overwritten in place by T, then by T diag(beta)
+    float *bs = Ts + C * TS;     // [C]
+    float *Ys = bs + C;          // coupling scratch, up to (C/2) x (C/2 + 1)
+
+    const int64_t id = blockIdx.x;
+    const int h = blockIdx.y;
+    const int tid = threadIdx.x;
+    if (h == 0 && id < p.nseq && tid == 0) check_sequence(p.cu, (int)id, p.nseq, p.ntok, p.status);
+    Chunk ch;
+    if (!map_chunk(id, p.cu, p.nseq, p.T, p.ntok, C, p.status, ch)) return;
+    const int Lc = ch.Lc;
+    const int64_t t0 = ch.t0;
+    const int64_t H = p.H;
+
+    const TIn *kg = static_cast<const TIn *>(p.k);
+    const TIn *vg = static_cast<const TIn *>(p.v);
+    TIn *wg = static_cast<TIn *>(p.W_out);
+    TIn *ug = static_cast<TIn *>(p.U_out);
+
+    // 1. stage K, V, beta; rows >= Lc are zero
+    for (int e = tid; e < C * DK; e += kSimtThreads) {
+        const int i = e / DK, d = e - (e / DK) * DK;
+        Ks[i * KS + d] = (i < Lc) ? to_f(kg[((t0 + i) * H + h) * DK + d]) : 0.f;
+    }
+    for (int e = tid; e < C * DV; e += kSimtThreads) {
+        const int i = e / DV, d = e - (e / DV) * DV;
+        Vs[i * VS + d] = (i < Lc) ? to_f(vg[((t0 + i) * H + h) * DV + d]) : 0.f;
+    }
+    for (int i = tid; i < C; i += kSimtThreads) bs[i] = (i < Lc) ? p.beta[(t0 + i) * H + h] : 0.f;
+    __syncthreads();
+
+    // 2. A = I + strictLower(diag(beta) K K^T)   (§1; beta on rows, unit diagonal, §3.2)
+    for (int e = tid; e < C * C; e += kSimtThreads) {
+        const int i = e / C, j = e % C;
+        float a = 0.f;
+        if (i == j) {
+            a = 1.f;
+        } else if (i > j) {
+            float s = 0.f;
+            for (int d = 0; d < DK; ++d) s = fmaf(Ks[i * KS + d], Ks[j * KS + d], s);
+            a = bs[i] * s;
+        }
+        Ts[i * TS + j] = a;
+    }
+    __syncthreads();
+
+    // 3. diagonal 16 x 16 blocks: X = L^-1 column by column (thread = block, column)
+    //    X[r][c] = delta_rc - sum_{m<r} L[r][m] X[m][c]   (§2.1)
+    constexpr int NB = C / 16;
+    const bool sub = tid < NB * 16;
+    const int b = tid >> 4, c = tid & 15;
+    float x[16];
+    if (sub) {
+        const float *L = Ts + (16 * b) * TS + 16 * b;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float s = (r == c) ? 1.f : 0.f;
+#pragma unroll
+            for (int m = 0; m < r; ++m) s = fmaf(-L[r * TS + m], x[m], s);
+            x[r] = s;
+        }
+    }
+    __syncthreads();  // every read of the block's L is done before it is overwritten
+    if (sub) {
+        float *X = Ts + (16 * b) * TS + 16 * b;
+#pragma unroll
+        for (int r = 1; r < 16; ++r)
+            if (r > c) X[r * TS + c] = x[r];
+    }
+    __syncthreads();
+
+    // 4. coupling levels: lower block of each pair = -X11 (L10 X00)   (§2.2)
+    for (int s = 16; s < C; s *= 2) {
+        const int npairs = C / (2 * s);
+        const int YS = s + 1;
+        const int n = npairs * s * s;
+        for (int e = tid; e < n; e += kSimtThreads) {
+            const int pr = e / (s * s), r = (e / s) % s, cc = e % s;
+            const int o = 2 * s * pr;
+            const float *L10 = Ts + (o + s) * TS + o;
+            const float *X00 = Ts + o * TS + o;
+            float acc = 0.f;
+            for (int m = cc; m < s; ++m) acc = fmaf(L10[r * TS + m], X00[m * TS + cc], acc);
+            Ys[pr * s * YS + r * YS + cc] = acc;
+        }
+        __syncthreads();
+        for (int e = tid; e < n; e += kSimtThreads) {
+            const int pr = e / (s * s), r = (e / s) % s, cc = e % s;
+            const int o = 2 * s * pr;
+            const float *X11 = Ts + (o + s) * TS + (o + s);
+            const float *Y = Ys + pr * s * YS;
+            float acc = 0.f;
+            for (int m = 0; m <= r; ++m) acc = fmaf(X11[r * TS + m], Y[m * YS + cc], acc);
+            Ts[(o + s + r) * TS + o + cc] = -acc;
+        }
+        __syncthreads();
+    }
+
+    // 5. T_out rows of the chunk (zeros in columns >= Lc)
+    for (int e = tid; e < Lc * C; e += kSimtThreads) {
+        const int i = e / C, j = e % C;
+        p.T_out[((t0 + i) * H + h) * C + j] = (j < Lc) ? Ts[i * TS + j] : 0.f;
+    }
+    __syncthreads();
+
+    // 6. T~ = T diag(beta), in place
+    for (int e = tid; e < C * C; e += kSimtThreads) {
+        const int i = e / C, j = e % C;
+        Ts[i * TS + j] *= bs[j];
+    }
+    __syncthreads();
+
+    // 7. W = T~ K, U~ = T~ V   (§1); T~ is lower triangular, so j <= i
+    for (int e = tid; e < Lc * DK; e += kSimtThreads) {
+        const int i = e / DK, d = e - (e / DK) * DK;
+        float acc = 0.f;
+        for (int j = 0; j <= i; ++j) acc = fmaf(Ts[i * TS + j], Ks[j * KS + d], acc);
+        wg[((t0 + i) * H + h) * DK + d] = from_f<TIn>(acc);
+    }
+    for (int e = tid; e < Lc * DV; e += kSimtThreads) {
+        const int i = e / DV, d = e - (e / DV) * DV;
+        float acc = 0.f;
+        for (int j = 0; j <= i; ++j) acc = fmaf(Ts[i * TS + j], Vs[j * VS + d], acc);
+        ug[((t0 + i) * H + h) * DV + d] = from_f<TIn>(acc);
+    }
+}
+
+template <typename TIn, int C>
+int launch_simt_t(const Problem &pb) {
+    const size_t smem = sizeof(float) * ((size_t)C * (pb.dk + 1) + (size_t)C * (pb.dv + 1) +
+                                         (size_t)C * (C + 1) + C + (size_t)(C / 2) * (C / 2 + 1));
+    auto kern = kkt_simt_kernel<TIn, C>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return KKT_ERR_CUDA;
+    SimtParams p;
+    p.k = pb.k; p.v = pb.v; p.beta = pb.beta; p.cu = pb.cu_seqlens;
+    p.nseq = pb.nseq; p.T = pb.T; p.ntok = pb.ntok;
+    p.H = pb.H; p.dk = pb.dk; p.dv = pb.dv;
+    p.T_out = pb.T_out; p.W_out = pb.W_out; p.U_out = pb.U_out; p.status = pb.status;
+    const int64_t ids = total_work_ids(pb.ntok, C, pb.nseq);
+    dim3 grid((unsigned)ids, (unsigned)pb.H);
+    kern<<<grid, kSimtThreads, smem, pb.stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? KKT_OK : KKT_ERR_CUDA;
+}
+
+template <typename TIn>
+int dispatch_c(const Problem &p) {
+    switch (p.C) {
+        case 32: return launch_simt_t<TIn, 32>(p);
+        case 64: return launch_simt_t<TIn, 64>(p);
+        case 128: return launch_simt_t<TIn, 128>(p);
+        default: return KKT_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace
+
+int launch_simt(const Problem &p) {
+    return p.io == KKT_IO_F32 ? dispatch_c<float>(p) : dispatch_c<__nv_bfloat16>(p);
+}
+
+}  // namespace kkt

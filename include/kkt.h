@@ -1,0 +1,125 @@
+/*
+ * kkt.h -- C ABI of the GB300 (sm_103a) kkt_solve library, libkkt.so.
+ *
+ * kkt_solve is the chunk-local UT transform of Gated DeltaNet chunked
+ * prefill, as described on the page "TileLang 实战：单位下三角矩阵求逆"
+ * (TileLang in practice: inverting a unit lower-triangular matrix):
+ *
+ *   For every chunk of C consecutive tokens of one sequence and one head
+ *   (section 1, the coefficient matrix; section 3.2, beta scales rows and the
+ *   diagonal is one):
+ *       A  = I + strictLower(diag(beta) K K^T)          (C x C)
+ *       T  = A^-1                                        (section 2.2 blocked recursion)
+ *       W  = T diag(beta) K,   U~ = T diag(beta) V       (section 1)
+ *   Chunks restart at every sequence start; the last chunk of a sequence may
+ *   be shorter than C (Lc rows), and is the leading Lc x Lc block of the
+ *   general case (A is lower triangular, so padding never reaches it).
+ *
+ * Tensor layouts follow the [B, T, H, d] convention of the FlashQLA API
+ * (FlashQLA announcement, section "使用方式" / usage): row-major, contiguous,
+ * one K per value head (H_k = H_v = H).
+ *
+ *   k     [B, T, H, dk]   input  (bf16, or fp32 with KKT_IO_F32)
+ *   v     [B, T, H, dv]   input  (same dtype as k)
+ *   beta  [B, T, H]       input  fp32, expected in (0, 1)
+ *   T_out [B, T, H, C]    output fp32; row (b, t, h) holds row (t - chunk start)
+ *                         of its chunk's T, zeros in columns >= Lc
+ *   W_out [B, T, H, dk]   output (dtype of k)
+ *   U_out [B, T, H, dv]   output (dtype of k)
+ *
+ * Variable-length batches: pass cu_seqlens = int32[B + 1] offsets into a
+ * packed token axis (cu_seqlens[0] = 0, nondecreasing, cu_seqlens[B] = T);
+ * the tensors are then [1, T, H, .] with T the total token count and B the
+ * number of sequences.  With cu_seqlens == NULL the batch is B sequences of
+ * T tokens each.
+ *
+ * Ownership and execution: every pointer is a device pointer owned by the
+ * caller (cu_seqlens included).  The library allocates no memory.  Calls are
+ * asynchronous on `stream` (NULL = the legacy default stream) and never
+ * synchronise the host.  Pointers must be 16-byte aligned.  Outputs must not
+ * alias inputs.
+ *
+ * Errors: invalid arguments return a nonzero kkt_status WITHOUT launching.
+ * Problems only the device can see (a malformed cu_seqlens, a bounded wait
+ * that expired) are recorded in a per-device status word, read and cleared by
+ * kkt_device_status(); the kernels skip the affected chunks and never fault
+ * or trap on them.
+ */
+#ifndef KKT_H_
+#define KKT_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t is `struct CUstream_st *` */
+
+typedef enum kkt_status {
+    KKT_OK = 0,
+    KKT_ERR_ARG = 1,         /* null pointer, nonpositive size, inconsistent shapes */
+    KKT_ERR_UNSUPPORTED = 2, /* (C, dk, dv, io dtype, kernel) combination not built */
+    KKT_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
+    KKT_ERR_CUDA = 4,        /* a CUDA runtime / driver call failed */
+    KKT_ERR_SEQLENS = 5,     /* device saw a malformed cu_seqlens (kkt_device_status) */
+    KKT_ERR_TIMEOUT = 6,     /* a device-side bounded wait expired (kkt_device_status) */
+    KKT_ERR_NO_DEVICE = 7    /* no usable CUDA device / not an sm_103 device */
+} kkt_status;
+
+/* I/O dtype of k, v, W_out, U_out (beta and T_out are always fp32). */
+enum { KKT_IO_BF16 = 0, KKT_IO_F32 = 1 };
+
+/* Kernel selection for kkt_solve_fwd_ex. */
+enum {
+    KKT_KERNEL_AUTO = 0, /* tcgen05/TMA kernel when it supports the shape, else the SIMT kernel */
+    KKT_KERNEL_SIMT = 1, /* one CTA per (chunk, head), fp32 CUDA-core arithmetic throughout */
+    KKT_KERNEL_TC = 2    /* persistent tcgen05 + TMA kernel (bf16 I/O only) */
+};
+
+/*
+ * kkt_solve_fwd -- bf16 k, v, W_out, U_out; fp32 beta, T_out.
+ *   B, T, H   batch, tokens per sequence (total tokens with cu_seqlens), heads (>= 1; T >= 0)
+ *   dk, dv    64 or 128
+ *   C         chunk size: 32, 64 or 128 (recursion depth 1, 2, 3 to a 16 x 16 base,
+ *             "TileLang 实战：单位下三角矩阵求逆" section 2.3, second table)
+ * Returns KKT_OK or a kkt_status.  T == 0 is valid and launches nothing.
+ */
+int kkt_solve_fwd(const void *k, const void *v, const float *beta, const int32_t *cu_seqlens,
+                  int B, int T, int H, int dk, int dv, int C,
+                  float *T_out, void *W_out, void *U_out, struct CUstream_st *stream);
+
+/*
+ * kkt_solve_fwd_ex -- as kkt_solve_fwd, with the I/O dtype (KKT_IO_BF16 or
+ * KKT_IO_F32) and the kernel (KKT_KERNEL_*) chosen explicitly.  fp32 I/O runs
+ * the SIMT kernel only; asking for KKT_KERNEL_TC with it, or with a shape the
+ * tcgen05 kernel does not cover, returns KKT_ERR_UNSUPPORTED.
+ */
+int kkt_solve_fwd_ex(const void *k, const void *v, const float *beta, const int32_t *cu_seqlens,
+                     int B, int T, int H, int dk, int dv, int C,
+                     float *T_out, void *W_out, void *U_out,
+                     int io_dtype, int kernel, struct CUstream_st *stream);
+
+/*
+ * kkt_device_status -- synchronises `stream`, then returns and clears the
+ * status word of the current device: KKT_OK, or the first device-side error
+ * (KKT_ERR_SEQLENS, KKT_ERR_TIMEOUT) recorded since the last call; KKT_ERR_CUDA
+ * if the synchronisation itself failed.
+ */
+int kkt_device_status(struct CUstream_st *stream);
+
+/* Which kernel kkt_solve_fwd_ex would run (KKT_KERNEL_SIMT / _TC), or a
+ * negated kkt_status if the arguments are unsupported.  Host-only, no CUDA call. */
+int kkt_select_kernel(int dk, int dv, int C, int io_dtype, int kernel);
+
+/* Static string for a kkt_status value. */
+const char *kkt_status_string(int status);
+
+/* Library version, (major << 16) | (minor << 8) | patch. */
+int kkt_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KKT_H_ */

@@ -1,0 +1,214 @@
+"""CUDA path against the fp64 oracle, element by element (GPU).
+
+Every call goes through the C ABI (libkkt.so via the ctypes binding).  Small
+cases are compared in full; the full-size workloads are compared on sampled
+(chunk, head) units that the oracle computes one by one, plus properties that
+hold at any size (no NaN, unit diagonal, zero upper triangle, zero padding).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gdn_chunkwise_ut_gb300 import _lib, device_status, kkt_solve_fwd, select_kernel
+from gdn_chunkwise_ut_gb300.inputs import make_inputs, workloads
+from tests.compare import check_T, check_WU, chunks, to64
+from tests.pins import subdiagonal_only_case
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def kernels_for(dk, dv, C, io="bf16"):
+    out = []
+    for kern in ("simt", "tc"):
+        try:
+            select_kernel(dk, dv, C, io, kern)
+            out.append(kern)
+        except _lib.KktError:
+            pass
+    return out
+
+
+ALL_KERNELS = ["simt", "tc"]
+
+
+def _skip_unless(kernel, dk, dv, C, io="bf16"):
+    if kernel not in kernels_for(dk, dv, C, io):
+        pytest.skip(f"{kernel} kernel does not cover dk={dk} dv={dv} C={C} io={io}")
+
+
+def run(k, v, beta, C, cu=None, kernel="auto", poison=True):
+    """Calls the library with NaN-poisoned outputs; returns (T, W, U) on the device."""
+    Bt, T, H, dk = k.shape
+    dv = v.shape[-1]
+    T_out = torch.full((Bt, T, H, C), float("nan"), device=DEV)
+    W = torch.full((Bt, T, H, dk), float("nan"), device=DEV, dtype=k.dtype)
+    U = torch.full((Bt, T, H, dv), float("nan"), device=DEV, dtype=k.dtype)
+    cu_t = None if cu is None else torch.as_tensor(np.asarray(cu), dtype=torch.int32, device=DEV)
+    kkt_solve_fwd(k, v, beta, C, cu_t, T_out=T_out, W_out=W, U_out=U, kernel=kernel)
+    torch.cuda.synchronize()
+    assert device_status() == 0
+    return T_out, W, U
+
+
+def full_compare(k, v, beta, C, cu, outs, io="bf16"):
+    T_ref, W_ref, U_ref = oracle.oracle_fwd(to64(k), to64(v), to64(beta), C, cu_seqlens=cu)
+    T_g, W_g, U_g = (to64(x) for x in outs)
+    check_T(T_g, T_ref)
+    check_WU(W_g, W_ref, io, "W")
+    check_WU(U_g, U_ref, io, "U")
+    return T_g, T_ref
+
+
+# --- small cases, compared in full --------------------------------------------------------
+
+@pytest.mark.parametrize("kernel", ALL_KERNELS)
+@pytest.mark.parametrize("C", [32, 64, 128])
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 128), (128, 64), (64, 64)])
+def test_small_fixed_length(kernel, C, dk, dv):
+    """Two sequences of 200 tokens (several chunks and a ragged tail), three heads."""
+    _skip_unless(kernel, dk, dv, C)
+    k, v, beta = make_inputs(2, 200, 3, dk, dv, seed=C + dk + 2 * dv, device=DEV)
+    outs = run(k, v, beta, C, kernel=kernel)
+    T_g, _ = full_compare(k, v, beta, C, None, outs)
+    # structure: zero padding beyond the short last chunk, exact unit diagonal
+    for t0, Lc in chunks(C, 2, 200):
+        blk = T_g.reshape(400, 3, C)[t0:t0 + Lc]
+        assert np.all(blk[:, :, Lc:] == 0.0)
+        for i in range(Lc):
+            assert np.all(blk[i, :, i] == 1.0) and np.all(blk[i, :, i + 1:] == 0.0)
+
+
+def test_config1_fp32_io():
+    """Single head, 128 tokens, C=32, dk=dv=64, fp32 in and out (SIMT kernel)."""
+    w = workloads()["c1_small_f32"]
+    k, v, beta, _ = w.make(seed=0, device=DEV)
+    outs = run(k, v, beta, w.C)
+    full_compare(k, v, beta, w.C, None, outs, io="f32")
+    T = outs[0].reshape(4, 32, 32)  # the four chunks' T matrices
+    assert torch.all(torch.diagonal(T, dim1=1, dim2=2) == 1.0)
+
+
+@pytest.mark.parametrize("kernel", ALL_KERNELS)
+@pytest.mark.parametrize("C", [32, 64, 128])
+def test_small_varlen(kernel, C):
+    """Packed sequences with empty, single-token, chunk-aligned and ragged lengths."""
+    _skip_unless(kernel, 128, 128, C)
+    lengths = [1, 63, 64, 65, 0, 130, 7, 200]
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    k, v, beta = make_inputs(1, int(cu[-1]), 2, 128, 128, seed=5, device=DEV)
+    outs = run(k, v, beta, C, cu, kernel=kernel)
+    full_compare(k, v, beta, C, cu, outs)
+    # equal to each sequence run on its own
+    for s in range(len(lengths)):
+        a, b = int(cu[s]), int(cu[s + 1])
+        if a == b:
+            continue
+        alone = run(k[:, a:b].contiguous(), v[:, a:b].contiguous(), beta[:, a:b].contiguous(), C,
+                    kernel=kernel)
+        for x, y in zip(outs, alone):
+            assert torch.equal(x[:, a:b], y)
+
+
+# --- degenerate cases and traps -----------------------------------------------------------
+
+@pytest.mark.parametrize("kernel", ALL_KERNELS)
+def test_beta_zero_gives_identity(kernel):
+    """beta = 0: T = I exactly, W = U = 0 (degenerate test 1 of the page's section 4)."""
+    _skip_unless(kernel, 128, 128, 64)
+    k, v, beta = make_inputs(1, 256, 2, 128, 128, seed=3, device=DEV)
+    T, W, U = run(k, v, torch.zeros_like(beta), 64, kernel=kernel)
+    eye = torch.eye(64, device=DEV).repeat(4, 1).reshape(256, 1, 64).expand(256, 2, 64)
+    assert torch.equal(T[0], eye)
+    assert torch.all(W == 0) and torch.all(U == 0)
+
+
+@pytest.mark.parametrize("kernel", ALL_KERNELS)
+def test_subdiagonal_block_sign(kernel):
+    """Only L10 nonzero (L00 = L11 = I): T's lower-left block is -L10 (degenerate test 2)."""
+    _skip_unless(kernel, 128, 128, 32)
+    rng = np.random.default_rng(4)
+    beta = rng.integers(1, 64, 32) / 64.0
+    kk, L10 = subdiagonal_only_case(beta)
+    k = torch.zeros((1, 32, 1, 128), dtype=torch.bfloat16)
+    k[0, :, 0, :32] = torch.from_numpy(kk).to(torch.bfloat16)
+    v = torch.from_numpy(rng.standard_normal((1, 32, 1, 128))).to(torch.bfloat16)
+    b = torch.from_numpy(beta).float().reshape(1, 32, 1)
+    T, W, U = run(k.to(DEV), v.to(DEV), b.to(DEV), 32, kernel=kernel)
+    Tn = to64(T)[0, :, 0, :]
+    np.testing.assert_allclose(Tn[16:, :16], -L10, atol=1e-6, rtol=0)
+    np.testing.assert_array_equal(Tn[:16, :16], np.eye(16))
+    np.testing.assert_array_equal(Tn[16:, 16:], np.eye(16))
+
+
+@pytest.mark.parametrize("kernel", ALL_KERNELS)
+def test_no_state_carried_between_chunks(kernel):
+    """Chunks with beta = 0 between ordinary ones stay exactly the identity, so no buffer
+    reused across chunks leaks the previous chunk's values (section 3.6 trap)."""
+    _skip_unless(kernel, 128, 128, 64)
+    k, v, beta = make_inputs(2, 64 * 40, 4, 128, 128, seed=9, device=DEV)
+    mask = torch.zeros(2, 40, 1, 4, device=DEV)
+    mask[:, 1::3] = 1.0
+    beta0 = (beta.reshape(2, 40, 64, 4) * (1 - mask)).reshape_as(beta).contiguous()
+    T, W, U = run(k, v, beta0, 64, kernel=kernel)
+    Tz = T.reshape(2, 40, 64, 4, 64)[:, 1::3]
+    eye = torch.eye(64, device=DEV).reshape(1, 1, 64, 1, 64)
+    assert torch.equal(Tz, eye.expand_as(Tz))
+    assert torch.all(W.reshape(2, 40, 64, 4, 128)[:, 1::3] == 0)
+    full_compare(k, v, beta0, 64, None, (T, W, U))
+
+
+def test_malformed_cu_seqlens_is_reported_not_faulted():
+    """A decreasing cu_seqlens is skipped by the kernel and reported by the status word."""
+    k, v, beta = make_inputs(1, 300, 2, 128, 128, seed=6, device=DEV)
+    cu = torch.tensor([0, 200, 100, 300], dtype=torch.int32, device=DEV)
+    T_out = torch.zeros((1, 300, 2, 64), device=DEV)
+    W = torch.zeros((1, 300, 2, 128), device=DEV, dtype=torch.bfloat16)
+    U = torch.zeros_like(W)
+    kkt_solve_fwd(k, v, beta, 64, cu, T_out=T_out, W_out=W, U_out=U)
+    assert device_status() == _lib.KKT_ERR_SEQLENS
+    assert device_status() == 0
+    cu_ok = np.array([0, 100, 300])
+    outs = run(k, v, beta, 64, cu_ok)
+    full_compare(k, v, beta, 64, cu_ok, outs)
+
+
+# --- full-size workloads, sampled -----------------------------------------------------------
+
+FULL = ["c2_t8192_h16", "c3_b4_t8192_h16", "c3_b4_t8192_h64", "c4_varlen32_h32",
+        "c5_b2_t16384_h24_c32", "c5_b2_t16384_h24_c64", "c5_b2_t16384_h24_c128"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(name):
+    """Full-size workload in the bench's launch configuration (kernel "auto"); 40 sampled
+    (chunk, head) units against the oracle; whole-tensor structural properties."""
+    w = workloads()[name]
+    k, v, beta, cu = w.make(seed=0, device=DEV)
+    T_out, W, U = run(k, v, beta, w.C, cu)
+    H, C = w.H, w.C
+    flat = lambda x: x.reshape(w.tokens, H, -1)
+    kf, vf, bf = flat(k), flat(v), beta.reshape(w.tokens, H)
+    Tf, Wf, Uf = flat(T_out), flat(W), flat(U)
+    assert not torch.isnan(Tf).any() and not torch.isnan(Wf.float()).any() and not torch.isnan(Uf.float()).any()
+    ch = chunks(C, w.B, w.T, cu)
+    rng = np.random.default_rng(1)
+    picks = [ch[0], ch[-1]] + [ch[i] for i in rng.integers(0, len(ch), 38)]
+    heads = [0, H - 1] + list(rng.integers(0, H, 38))
+    for (t0, Lc), h in zip(picks, heads):
+        h = int(h)
+        Tr, Wr, Ur, _ = oracle.oracle_chunk(to64(kf[t0:t0 + Lc, h]), to64(vf[t0:t0 + Lc, h]),
+                                            to64(bf[t0:t0 + Lc, h]), C)
+        check_T(to64(Tf[t0:t0 + Lc, h]), Tr)
+        check_WU(to64(Wf[t0:t0 + Lc, h]), Wr, "bf16", "W")
+        check_WU(to64(Uf[t0:t0 + Lc, h]), Ur, "bf16", "U")
+    # unit diagonal and zero upper triangle of every chunk, at full size
+    idx = torch.arange(w.tokens, device=DEV)
+    starts = torch.zeros(w.tokens, dtype=torch.long, device=DEV)
+    for t0, Lc in ch:
+        starts[t0:t0 + Lc] = t0
+    row = (idx - starts).reshape(-1, 1, 1)
+    col = torch.arange(C, device=DEV).reshape(1, 1, C)
+    assert torch.all(Tf[(col == row).expand_as(Tf)] == 1.0)
+    assert torch.all(Tf[(col > row).expand_as(Tf)] == 0.0)
