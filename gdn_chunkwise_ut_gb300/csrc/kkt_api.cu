@@ -27,6 +27,7 @@ int status_ptr(int **out) {
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 bool head_dim_ok(int d) { return d == 64 || d == 128; }
 bool chunk_ok(int C) { return C == 32 || C == 64 || C == 128; }
 
@@ -52,8 +53,8 @@ extern "C" int kkt_solve_fwd_ex(const void *k, const void *v, const float *beta,
     if (B < 1 || T < 0 || H < 1 || H > 65535) return KKT_ERR_ARG;
     const int which = kkt_select_kernel(dk, dv, C, io_dtype, kernel);
     if (which < 0) return -which;
-    if (!aligned16(k) || !aligned16(v) || !aligned16(beta) || !aligned16(T_out) || !aligned16(W_out) ||
-        !aligned16(U_out) || (cu_seqlens && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)))
+    if (!aligned16(k) || !aligned16(v) || !aligned16(T_out) || !aligned16(W_out) || !aligned16(U_out) ||
+        !aligned4(beta) || (cu_seqlens && !aligned4(cu_seqlens)))
         return KKT_ERR_ALIGN;
     const int64_t ntok = cu_seqlens ? (int64_t)T : (int64_t)B * T;
     if (ntok == 0) return KKT_OK;
@@ -93,7 +94,7 @@ extern "C" const char *kkt_status_string(int status) {
         case KKT_OK: return "ok";
         case KKT_ERR_ARG: return "invalid argument";
         case KKT_ERR_UNSUPPORTED: return "unsupported chunk size, head dimension, dtype or kernel";
-        case KKT_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case KKT_ERR_ALIGN: return "pointer misaligned (16 B for k, v, T_out, W_out, U_out; 4 B for beta, cu_seqlens)";
         case KKT_ERR_CUDA: return "CUDA error";
         case KKT_ERR_SEQLENS: return "malformed cu_seqlens";
         case KKT_ERR_TIMEOUT: return "device-side wait timed out";

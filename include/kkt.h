@@ -36,8 +36,9 @@
  * Ownership and execution: every pointer is a device pointer owned by the
  * caller (cu_seqlens included).  The library allocates no memory.  Calls are
  * asynchronous on `stream` (NULL = the legacy default stream) and never
- * synchronise the host.  Pointers must be 16-byte aligned.  Outputs must not
- * alias inputs.
+ * synchronise the host.  k, v, T_out, W_out and U_out must be 16-byte aligned
+ * (they are moved by TMA), beta and cu_seqlens 4-byte aligned.  Outputs must
+ * not alias inputs.
  *
  * Errors: invalid arguments return a nonzero kkt_status WITHOUT launching.
  * Problems only the device can see (a malformed cu_seqlens, a bounded wait
@@ -60,7 +61,7 @@ typedef enum kkt_status {
     KKT_OK = 0,
     KKT_ERR_ARG = 1,         /* null pointer, nonpositive size, inconsistent shapes */
     KKT_ERR_UNSUPPORTED = 2, /* (C, dk, dv, io dtype, kernel) combination not built */
-    KKT_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
+    KKT_ERR_ALIGN = 3,       /* a pointer is misaligned (16 B for tensors moved by TMA, 4 B for beta) */
     KKT_ERR_CUDA = 4,        /* a CUDA runtime / driver call failed */
     KKT_ERR_SEQLENS = 5,     /* device saw a malformed cu_seqlens (kkt_device_status) */
     KKT_ERR_TIMEOUT = 6,     /* a device-side bounded wait expired (kkt_device_status) */

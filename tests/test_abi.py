@@ -89,6 +89,7 @@ def test_argument_errors_return_before_launch(lib):
     assert _call(lib, k=0x1008) == _lib.KKT_ERR_ALIGN
     assert _call(lib, W_out=0x5004) == _lib.KKT_ERR_ALIGN
     assert _call(lib, cu=0x7002) == _lib.KKT_ERR_ALIGN
+    assert _call(lib, beta=0x3002) == _lib.KKT_ERR_ALIGN
     assert _call(lib, T=0) == _lib.KKT_OK               # empty batch: nothing to launch
     assert _call(lib, cu=0x7000, B=3, T=0) == _lib.KKT_OK
     assert lib.kkt_solve_fwd(None, 0x2000, 0x3000, None, 1, 64, 1, 128, 128, 64,
