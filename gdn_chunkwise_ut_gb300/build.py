@@ -40,17 +40,25 @@ def _stale(out: Path, deps) -> bool:
     return any(Path(d).stat().st_mtime > t for d in deps)
 
 
-def build(verbose: bool = False, force: bool = False, extra_flags=()) -> Path:
-    """Compile every csrc/*.cu and link libkkt.so; returns the library path."""
-    BUILD.mkdir(parents=True, exist_ok=True)
+def build(verbose: bool = False, force: bool = False, extra_flags=(), trace: bool = False) -> Path:
+    """Compile every csrc/*.cu and link libkkt.so; returns the library path.
+
+    ``trace=True`` builds a separate libkkt_trace.so (in _build/trace) with the
+    pipeline time stamps of the tensor-core kernel compiled in (see trace.py).
+    """
+    out_dir = BUILD / "trace" if trace else BUILD
+    lib_path = out_dir / ("libkkt_trace.so" if trace else "libkkt.so")
+    if trace:
+        extra_flags = (*extra_flags, "-DKKT_TRACE")
+    out_dir.mkdir(parents=True, exist_ok=True)
     headers = list(CSRC.glob("*.cuh")) + list(INCLUDE.glob("*.h"))
     nvcc = _nvcc()
     procs, objs = [], []
     for src in sources():
-        obj = BUILD / (src.stem + ".o")
+        obj = out_dir / (src.stem + ".o")
         objs.append(obj)
         if force or _stale(obj, [src, *headers]):
-            log = BUILD / (src.stem + ".log")
+            log = out_dir / (src.stem + ".log")
             cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", str(src), "-o", str(obj)]
             procs.append((src, log, subprocess.Popen(cmd, stdout=open(log, "w"), stderr=subprocess.STDOUT)))
     failed = []
@@ -62,12 +70,12 @@ def build(verbose: bool = False, force: bool = False, extra_flags=()) -> Path:
     if failed:
         msg = "\n".join(f"--- {s.name} ---\n{l.read_text()}" for s, l in failed)
         raise RuntimeError(f"nvcc failed:\n{msg}")
-    if force or _stale(LIB, objs):
-        tmp = BUILD / f"libkkt.{os.getpid()}.tmp.so"
+    if force or _stale(lib_path, objs):
+        tmp = out_dir / f"libkkt.{os.getpid()}.tmp.so"
         cmd = [nvcc, *ARCH, "-shared", "-o", str(tmp), *map(str, objs)]
         subprocess.run(cmd, check=True)
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":  # pragma: no cover

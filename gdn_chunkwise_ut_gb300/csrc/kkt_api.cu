@@ -26,6 +26,10 @@ int status_ptr(int **out) {
     return KKT_OK;
 }
 
+#ifdef KKT_TRACE
+void *g_trace = nullptr;
+#endif
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 bool head_dim_ok(int d) { return d == 64 || d == 128; }
@@ -68,6 +72,11 @@ extern "C" int kkt_solve_fwd_ex(const void *k, const void *v, const float *beta,
     p.T_out = T_out; p.W_out = W_out; p.U_out = U_out;
     p.io = io_dtype;
     p.stream = reinterpret_cast<cudaStream_t>(stream);
+#ifdef KKT_TRACE
+    p.trace = g_trace;
+#else
+    p.trace = nullptr;
+#endif
     const int st = status_ptr(&p.status);
     if (st != KKT_OK) return st;
     return which == KKT_KERNEL_TC ? kkt::launch_tc(p) : kkt::launch_simt(p);
@@ -104,3 +113,9 @@ extern "C" const char *kkt_status_string(int status) {
 }
 
 extern "C" int kkt_version(void) { return (0 << 16) | (1 << 8) | 0; }
+
+#ifdef KKT_TRACE
+// Trace builds only: device buffer of kTraceCtas x kTraceTiles x 16 uint64 time stamps
+// (see trace.py), or NULL to stop tracing.
+extern "C" void kkt_set_trace_buffer(void *buf) { g_trace = buf; }
+#endif

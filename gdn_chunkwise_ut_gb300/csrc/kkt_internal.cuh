@@ -24,6 +24,7 @@ struct Problem {
     int io;                     // KKT_IO_BF16 / KKT_IO_F32
     cudaStream_t stream;
     int *status;                // device status word of the current device
+    void *trace;                // pipeline trace buffer (KKT_TRACE builds only), else nullptr
 };
 
 // Device-side error codes (first error wins).

@@ -5,30 +5,41 @@
 // ("TileLang 实战：单位下三角矩阵求逆" §1, §2.2, §3):
 //
 //   producer warp   TMA: K and V boxes {64 cols, 1 head, C rows} (128-byte
-//                   swizzle) into a stage of the shared-memory ring; beta with
-//                   plain loads.
-//   MMA warp        tcgen05.mma S = K K^T  (M = N = 128, K = 128, bf16 -> fp32
-//                   in tensor memory); later D = T~ [K | V] with T~ = T diag(beta)
-//                   taken from tensor memory as a bf16 hi + lo pair (two
-//                   accumulating passes, M = 128, N = 256, K = 128; T~ is block
-//                   diagonal over the G heads).
-//   inverse warps   one thread per row: tcgen05.ld of its Gram row, beta row
-//                   scale, strict-lower mask and unit diagonal (§3.2); 16 x 16
-//                   diagonal blocks by forward substitution with warp shuffles
-//                   (§2.1, §3.4; the original row lives in registers, so the
-//                   in-place update needs no backup copy); coupling
-//                   -L11^-1 L10 L00^-1 at s = 16 (shuffles) and s = 32 (shared
-//                   memory between the two warps of a head) (§2.2, §3.5);
-//                   T rows to a swizzled staging buffer + TMA store; T~ hi / lo
-//                   to tensor memory with tcgen05.st.
-//   epilogue warps  tcgen05.ld of D, bf16 conversion, swizzled staging in the
-//                   stage's K/V buffers (free once the MMA has read them), TMA
-//                   stores of W and U~; then the stage goes back to the producer.
+//                   swizzle) into a stage of a two-deep shared-memory ring;
+//                   beta with plain loads.
+//   MMA warp        an event loop, one elected lane issuing tcgen05.mma:
+//                   S = K K^T (M = N = 128, K = 128, bf16 -> fp32 in tensor
+//                   memory), and D = T~ [K | V] with T~ = T diag(beta) read from
+//                   tensor memory as a bf16 hi + lo pair (two accumulating
+//                   passes, M = 128, N = 256, K = 128; T~ is block diagonal over
+//                   the G heads).  The commit after D frees the stage.
+//   inverse warps   a thread per row loads its Gram row (tcgen05.ld), applies
+//                   the beta row scale, strict-lower mask and unit diagonal
+//                   (§3.2) and writes the row of A into the tile's fp32 T
+//                   buffer in shared memory (128-byte swizzle, TMA layout),
+//                   which is then turned into T = A^-1 in place:
+//                   16 x 16 diagonal blocks by right-looking forward
+//                   substitution, one column per lane, so the dependency chain
+//                   is 15 FMAs (§2.1; in-place, with the L values read before
+//                   any column is written back, §3.4); coupling
+//                   -L11^-1 L10 L00^-1 at s = 16 (inside a warp) and s = 32
+//                   (the two warps of a head) as register-tiled shared-memory
+//                   GEMMs with L10 consumed before it is overwritten (§2.2,
+//                   §3.5).  Each warp TMA-stores its 32 rows of T from that
+//                   buffer, and writes its rows of T~ = T diag(beta) as a bf16
+//                   hi / lo pair into tensor memory (tcgen05.st).
+//   epilogue warps  per warp: tcgen05.ld of its 32 rows of D, bf16 conversion,
+//                   a double-buffered swizzled staging and TMA stores of W, U~.
 //
-// Short last chunks (Lc < C) are zero-padded in shared memory before the Gram
-// MMA and written back with plain stores of the Lc valid rows.  Every wait is
-// bounded: on expiry the kernel records KKT_ERR_TIMEOUT, stops all roles,
-// drains its own copies and MMAs, frees tensor memory and returns.
+// Rows of a short last chunk (Lc < C) past Lc are zeroed in shared memory
+// before the Gram MMA; warps whose 32 rows are not all valid write their valid
+// rows with plain stores.  Every wait is bounded: on expiry the kernel records
+// KKT_ERR_TIMEOUT, stops all roles, drains its own copies and MMAs, frees
+// tensor memory and returns.
+//
+// Building with -DKKT_TRACE adds time stamps of the pipeline events of the
+// first CTAs to a caller-provided buffer (see trace.py); the default build has
+// none of it.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -46,12 +57,12 @@ constexpr int kWarpProducer = 0;
 constexpr int kWarpMma = 1;
 constexpr int kWarpInv0 = 4;             // warps 4..7
 constexpr int kWarpEpi0 = 8;             // warps 8..11
+constexpr int kNS = 2;                   // stages
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColGram = 0;         // 128 fp32 columns
 constexpr uint32_t kColD = 128;          // 256 fp32 columns: W | U~
 constexpr uint32_t kColTT = 384;         // 64 packed bf16x2 hi + 64 lo
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
-
 
 struct TileInfo {
     int64_t t0;
@@ -63,33 +74,31 @@ struct TileInfo {
 
 template <int C>
 struct Cfg {
-    static constexpr int G = 128 / C;             // heads per tile
-    static constexpr int NS = 2;                  // stages
-    static constexpr int KV_BYTES = 65536;        // K 32 KB + V 32 KB, [colhalf][row][128 B]
-    static constexpr int STAGE_BYTES = KV_BYTES + 1024;  // + beta[128] + info, 1 KB aligned
-    static constexpr int OFF_BETA = KV_BYTES;
-    static constexpr int OFF_INFO = KV_BYTES + 512;
-    static constexpr int T_HALVES = C / 32;       // 128-byte column blocks of a T row
-    static constexpr int T_STAGE_BYTES = T_HALVES * 16384;
-    static constexpr int XCH_BYTES = (C >= 64) ? G * (2 * 4096 + 4096) : 0;  // level-32 exchange
-    static constexpr int OFF_T = NS * STAGE_BYTES;
-    static constexpr int OFF_XCH = OFF_T + T_STAGE_BYTES;
+    static constexpr int G = 128 / C;                         // heads per tile
+    static constexpr int KV_BYTES = 65536;                    // K 32 KB + V 32 KB, [box][row][128 B]
+    static constexpr int OFF_META = kNS * KV_BYTES;           // per stage: beta[128] + TileInfo
+    static constexpr int META_BYTES = 1024;
+    static constexpr int T_HALVES = C / 32;                   // 128-byte column blocks of a T row
+    static constexpr int OFF_T = OFF_META + kNS * META_BYTES; // T of the tile: [half][128 rows][128 B]
+    static constexpr int OFF_WU = OFF_T + T_HALVES * 16384;   // 2 x 4 KB per epilogue warp
+    static constexpr int OFF_XCH = OFF_WU + 4 * 8192;         // coupling products: 4 x [16][16] fp32,
+    static constexpr int XCH_BYTES = 4096 + ((C >= 64) ? G * 4096 : 0);  // + G x [32][32] fp32
     static constexpr int OFF_BAR = OFF_XCH + XCH_BYTES;
-    static constexpr int BAR_BYTES = 256;
+    static constexpr int BAR_BYTES = 512;
     static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
     static constexpr uint32_t TX_BYTES = G * 4 * C * 128;           // K + V boxes of one stage
 };
 
 struct Barriers {
-    uint64_t full[2];
-    uint64_t empty[2];
+    uint64_t full[kNS];
+    uint64_t empty[kNS];
     uint64_t gram_full, gram_empty;
     uint64_t tt_full, tt_empty;
     uint64_t d_full, d_empty;
+    uint64_t einfo_full[2];
     uint64_t mma_final;
-    uint64_t inv_sync;       // 128 inverse threads
-    uint64_t epi_sync;       // 128 epilogue threads
     uint64_t pair_sync[2];   // the two warps of one head (C = 64)
+    TileInfo einfo[2];       // tile info for the epilogue warps, written by the MMA warp
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -105,10 +114,35 @@ struct TcParams {
     float *T_out;
     __nv_bfloat16 *W_out, *U_out;
     int *status;
+    unsigned long long *trace;
 };
 
+// ---- optional pipeline trace ------------------------------------------------------------------
+enum TraceEvent {
+    EV_P_EMPTY = 0, EV_P_ISSUE, EV_M_FULL, EV_M_GRAM, EV_M_EPI, EV_I_GRAM, EV_I_INV, EV_I_TSTORE,
+    EV_I_TT, EV_E_DFULL, EV_E_DEMPTY, EV_E_DONE, EV_I_LD, EV_I_DIAG, EV_I_C16, EV_I_PAIR, EV_COUNT
+};
+constexpr int kTraceCtas = 8;
+constexpr int kTraceTiles = 64;
+constexpr int kTraceSlots = 16;
+#ifdef KKT_TRACE
+#define KKT_TRACE_EVENT(ev, tile)                                                                        \
+    do {                                                                                               \
+        if (p.trace && blockIdx.x < kTraceCtas && (tile) < kTraceTiles)                                \
+            p.trace[((size_t)blockIdx.x * kTraceTiles + (tile)) * kTraceSlots + (ev)] = globaltimer_ns(); \
+    } while (0)
+#else
+#define KKT_TRACE_EVENT(ev, tile) \
+    do {                          \
+    } while (0)
+#endif
+
+// First 1024-byte-aligned byte of the dynamic shared memory.  The offset is
+// computed in the shared window and added to the shared pointer itself, so the
+// compiler keeps the shared address space (LDS/STS rather than generic loads).
 __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
-    return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+    const uint32_t a = smem_u32(p);
+    return p + (((a + 1023u) & ~1023u) - a);
 }
 
 __device__ __forceinline__ void fail(Barriers *bars, int *status) {
@@ -130,66 +164,35 @@ __device__ __forceinline__ bool group_sync(uint64_t *bar, uint32_t &uses, Barrie
     return ok;
 }
 
+// Element (row m, column j) of a fp32 matrix stored as 32-column halves of 128-byte rows,
+// [half][128 rows][128 B], with the 128-byte swizzle that TMA uses (16-byte chunk index XOR
+// row mod 8): rows are conflict-free for a thread per row, and a row is a TMA box row.
+__device__ __forceinline__ float *tm_elem(uint8_t *tm, int m, int j) {
+    return reinterpret_cast<float *>(tm + (j >> 5) * 16384 + m * 128 + ((((j & 31) >> 2) ^ (m & 7)) << 4) +
+                                     (j & 3) * 4);
+}
+__device__ __forceinline__ float4 *tm_vec(uint8_t *tm, int m, int j) {  // j a multiple of 4
+    return reinterpret_cast<float4 *>(tm + (j >> 5) * 16384 + m * 128 + ((((j & 31) >> 2) ^ (m & 7)) << 4));
+}
+
+// Two bf16 (round to nearest even) in one register: lo in bits 0..15, hi in 16..31.
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
-           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-// ---------------------------------------------------------------------------------------------
-// Inverse of one 16 x 16 unit lower-triangular block, one row per lane of a half warp:
-// lb[c] = L[k][c] (zero for c >= k), x[c] <- (L^-1)[k][c].  Right-looking substitution:
-// once row m is final, every later row subtracts L[k][m] * row m (§2.1).
-__device__ __forceinline__ void diag16(const float (&lb)[16], float (&x)[16], int lane) {
-    const int k = lane & 15;
-    const int base = lane & 16;
-#pragma unroll
-    for (int c = 0; c < 16; ++c) x[c] = (c == k) ? 1.f : 0.f;
-#pragma unroll
-    for (int m = 0; m < 15; ++m) {
-        const float lm = lb[m];
-        x[m] -= lm;
-#pragma unroll
-        for (int c = 0; c < m; ++c) {
-            const float xm = __shfl_sync(0xffffffffu, x[c], base + m);
-            x[c] = fmaf(-lm, xm, x[c]);
-        }
-    }
-}
-
-// Level-16 coupling inside one warp: lanes 16..31 (block 1) get
-// T10[k][:] = -X11[k][:] (L10 X00), with X00 rows on lanes 0..15.
-// l10[j] = L[row][first column of block 0 + j].  Returns m32: the lane's row of the
-// warp's 32 x 32 inverse (columns of block 0 then block 1).
-__device__ __forceinline__ void couple16(const float (&l10)[16], const float (&x)[16], int lane,
-                                         float (&m32)[32]) {
-    float y[16];
-#pragma unroll
-    for (int c = 0; c < 16; ++c) y[c] = 0.f;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-#pragma unroll
-        for (int c = 0; c <= j; ++c) {
-            const float xjc = __shfl_sync(0xffffffffu, x[c], j);
-            y[c] = fmaf(l10[j], xjc, y[c]);
-        }
-    }
-    float z[16];
-#pragma unroll
-    for (int c = 0; c < 16; ++c) z[c] = 0.f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            const float yic = __shfl_sync(0xffffffffu, y[c], 16 + i);
-            z[c] = fmaf(x[i], yic, z[c]);
-        }
-    }
-    const bool upper = lane >= 16;
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-        m32[c] = upper ? -z[c] : x[c];
-        m32[16 + c] = upper ? x[c] : 0.f;
-    }
+// Packed fp32 FMA on a pair (one f32x2 instruction): a * b + c, elementwise.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -200,17 +203,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap map_t, const TcParams p) {
     using CF = Cfg<C>;
     constexpr int G = CF::G;
-    constexpr int NS = CF::NS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     Barriers *bars = reinterpret_cast<Barriers *>(smem + CF::OFF_BAR);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    auto stage_ptr = [&](int s) { return smem + s * CF::STAGE_BYTES; };
+    auto stage_kv = [&](int s) { return smem + s * CF::KV_BYTES; };
+    auto stage_beta = [&](int s) { return reinterpret_cast<float *>(smem + CF::OFF_META + s * CF::META_BYTES); };
+    auto stage_info = [&](int s) {
+        return reinterpret_cast<TileInfo *>(smem + CF::OFF_META + s * CF::META_BYTES + 512);
+    };
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) {
+        for (int s = 0; s < kNS; ++s) {
             mbar_init(&bars->full[s], 1);
             mbar_init(&bars->empty[s], 1);
         }
@@ -220,9 +226,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->tt_empty, 1);
         mbar_init(&bars->d_full, 1);
         mbar_init(&bars->d_empty, 4);
+        mbar_init(&bars->einfo_full[0], 1);
+        mbar_init(&bars->einfo_full[1], 1);
         mbar_init(&bars->mma_final, 1);
-        mbar_init(&bars->inv_sync, 128);
-        mbar_init(&bars->epi_sync, 128);
         mbar_init(&bars->pair_sync[0], 64);
         mbar_init(&bars->pair_sync[1], 64);
         bars->abort_flag = 0;
@@ -245,25 +251,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         int i = 0;
         bool ok = true;
-        for (int64_t t = blockIdx.x; t < p.tiles && ok; t += gridDim.x) {
+        for (int64_t t = blockIdx.x; t < p.tiles; t += gridDim.x) {
             const int64_t id = t / p.HG;
             const int h0 = (int)(t % p.HG) * G;
             if (h0 == 0 && id < p.nseq && lane == 0) check_sequence(p.cu, (int)id, p.nseq, p.ntok, p.status);
             Chunk ch;
             if (!map_chunk(id, p.cu, p.nseq, p.T, p.ntok, C, p.status, ch)) continue;
-            const int s = i % NS;
-            const uint32_t u = (uint32_t)(i / NS);
-            if (!wait_bar(&bars->empty[s], (u & 1u) ^ 1u, bars, p.status)) { ok = false; break; }
-            uint8_t *st = stage_ptr(s);
-            float *sb = reinterpret_cast<float *>(st + CF::OFF_BETA);
-            for (int idx = lane; idx < G * C; idx += 32) {
+            // beta of the tile (G x C values, 4 per lane), loaded before waiting for the stage
+            float bv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int idx = lane + 32 * e;
                 const int g = idx / C, r = idx % C;
-                float b = 0.f;
-                if (r < ch.Lc && h0 + g < p.H) b = __ldg(p.beta + (ch.t0 + r) * p.H + h0 + g);
-                sb[idx] = b;
+                bv[e] = (r < ch.Lc && h0 + g < p.H) ? __ldg(p.beta + (ch.t0 + r) * p.H + h0 + g) : 0.f;
             }
+            const int s = i % kNS;
+            const uint32_t u = (uint32_t)(i / kNS);
+            if (!wait_bar(&bars->empty[s], (u & 1u) ^ 1u, bars, p.status)) { ok = false; break; }
+            if (lane == 0) KKT_TRACE_EVENT(EV_P_EMPTY, i);
+            float *sb = stage_beta(s);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sb[lane + 32 * e] = bv[e];
             if (lane == 0) {
-                TileInfo *info = reinterpret_cast<TileInfo *>(st + CF::OFF_INFO);
+                TileInfo *info = stage_info(s);
                 info->t0 = ch.t0;
                 info->Lc = ch.Lc;
                 info->h0 = h0;
@@ -271,6 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             if (lane == 0) {
+                uint8_t *st = stage_kv(s);
                 mbar_arrive_expect_tx(&bars->full[s], CF::TX_BYTES);
                 for (int g = 0; g < G; ++g)
                     for (int c2 = 0; c2 < 2; ++c2) {
@@ -279,16 +290,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_3d(st + 32768 + c2 * 16384 + g * C * 128, &map_v, &bars->full[s], c2 * 64,
                                     h0 + g, (int)ch.t0);
                     }
+                KKT_TRACE_EVENT(EV_P_ISSUE, i);
             }
             __syncwarp();
             ++i;
         }
         if (ok) {
-            const int s = i % NS;
-            const uint32_t u = (uint32_t)(i / NS);
+            const int s = i % kNS;
+            const uint32_t u = (uint32_t)(i / kNS);
             if (wait_bar(&bars->empty[s], (u & 1u) ^ 1u, bars, p.status)) {
                 if (lane == 0) {
-                    reinterpret_cast<TileInfo *>(stage_ptr(s) + CF::OFF_INFO)->done = 1;
+                    stage_info(s)->done = 1;
                     mbar_arrive(&bars->full[s]);
                 }
             } else {
@@ -298,88 +310,120 @@ __global__ void __launch_bounds__(kThreads, 1)
         // after a timeout: our last TMA loads must land before shared memory is released
         // (on the normal path every load was consumed through its full barrier)
         if (!ok && lane == 0) {
-            for (int back = 1; back <= NS && back <= i; ++back) {
+            for (int back = 1; back <= kNS && back <= i; ++back) {
                 const int j = i - back;
                 volatile int never = 0;
-                mbar_wait(&bars->full[j % NS], (uint32_t)(j / NS) & 1u, &never, kWaitLimitNs);
+                mbar_wait(&bars->full[j % kNS], (uint32_t)(j / kNS) & 1u, &never, kWaitLimitNs);
             }
         }
         __syncwarp();
     } else if (warp == kWarpMma) {
-        // ------------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------------ MMA issuer (event loop)
         const uint32_t idesc_gram = idesc_bf16_f32(128, 128, 0, 0);
         const uint32_t idesc_epi = idesc_bf16_f32(128, 256, 0, 1);
-        auto zero_tail = [&](uint8_t *st, int Lc) {
-            // rows Lc..C-1 of every head's K and V boxes
-            const int rows = C - Lc;
-            const int per_box = rows * 8;  // 16-byte chunks
-            for (int e = lane; e < G * 4 * per_box; e += 32) {
-                const int box = e / per_box, w = e % per_box;
-                const int g = box % G, kvh = box / G;  // kvh: 0,1 = K halves, 2,3 = V halves
-                uint8_t *b = st + kvh * 16384 + g * C * 128;
-                *reinterpret_cast<uint4 *>(b + (Lc + w / 8) * 128 + (w % 8) * 16) = make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-        };
-        auto issue_gram = [&](uint8_t *st) {
-            if (lane == 0) {
-                tc_fence_after();
-                const uint32_t a0 = smem_u32(st);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t d = sw128_desc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-                    mma_ss(tmem + kColGram, d, d, idesc_gram, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(&bars->gram_full);
-            }
-            __syncwarp();
-        };
-        auto issue_epi = [&](uint8_t *st) {
-            if (lane == 0) {
-                tc_fence_after();
-                const uint32_t b0 = smem_u32(st);
-#pragma unroll
-                for (int pass = 0; pass < 2; ++pass)
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t d = sw128_desc(b0 + kk * 2048, 16384, 1024);
-                        mma_ts(tmem + kColD, tmem + kColTT + pass * 64 + kk * 8, d, idesc_epi,
-                               (pass | kk) ? 1u : 0u);
+        int g_next = 0;        // next tile whose Gram MMA is due
+        int e_next = 0;        // next tile whose W|U MMA is due
+        int done_at = -1;      // tile index of the end-of-work marker
+        bool g_ready = false;  // stage of g_next has landed (and is zero-padded)
+        uint64_t t_idle = globaltimer_ns();
+        while (true) {
+            bool progress = false;
+            if (done_at < 0 && !g_ready && g_next - e_next < kNS) {
+                const int s = g_next % kNS;
+                const bool landed = __shfl_sync(0xffffffffu, mbar_test(&bars->full[s], (uint32_t)(g_next / kNS) & 1u), 0);
+                if (landed) {
+                    const TileInfo info = *stage_info(s);
+                    if (lane == 0) KKT_TRACE_EVENT(EV_M_FULL, g_next);
+                    if (info.done) {
+                        done_at = g_next;
+                    } else {
+                        if (info.Lc < C) {
+                            // zero rows Lc..C-1 of every head's K and V boxes
+                            uint8_t *st = stage_kv(s);
+                            const int per_box = (C - info.Lc) * 8;  // 16-byte chunks
+                            for (int e = lane; e < G * 4 * per_box; e += 32) {
+                                const int box = e / per_box, w = e % per_box;
+                                const int g = box % G, kvh = box / G;  // kvh: K half 0, 1, V half 0, 1
+                                *reinterpret_cast<uint4 *>(st + kvh * 16384 + g * C * 128 + (info.Lc + w / 8) * 128 +
+                                                           (w % 8) * 16) = make_uint4(0, 0, 0, 0);
+                            }
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                        }
+                        g_ready = true;
                     }
-                mma_commit(&bars->tt_empty);
-                mma_commit(&bars->d_full);
+                    progress = true;
+                }
             }
-            __syncwarp();
-        };
-        int i = 0;
-        bool ok = wait_bar(&bars->full[0], 0u, bars, p.status);
-        const TileInfo *info0 = reinterpret_cast<const TileInfo *>(stage_ptr(0) + CF::OFF_INFO);
-        bool have = ok && !info0->done;
-        if (have) {
-            if (info0->Lc < C) zero_tail(stage_ptr(0), info0->Lc);
-            ok = wait_bar(&bars->gram_empty, 1u, bars, p.status);
-            if (ok) issue_gram(stage_ptr(0));
-        }
-        while (ok && have) {
-            const int n = i + 1;
-            const int sn = n % NS;
-            ok = wait_bar(&bars->full[sn], (uint32_t)(n / NS) & 1u, bars, p.status);
-            if (!ok) break;
-            const TileInfo *infn = reinterpret_cast<const TileInfo *>(stage_ptr(sn) + CF::OFF_INFO);
-            const bool has_next = !infn->done;
-            if (has_next) {
-                if (infn->Lc < C) zero_tail(stage_ptr(sn), infn->Lc);
-                ok = wait_bar(&bars->gram_empty, ((uint32_t)n & 1u) ^ 1u, bars, p.status);
-                if (!ok) break;
-                issue_gram(stage_ptr(sn));
+            if (g_ready) {
+                const bool free = __shfl_sync(0xffffffffu, mbar_test(&bars->gram_empty, ((uint32_t)g_next & 1u) ^ 1u), 0);
+                if (free) {
+                    if (lane == 0) {
+                        tc_fence_after();
+                        const uint32_t a0 = smem_u32(stage_kv(g_next % kNS));
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t d = sw128_desc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                            mma_ss(tmem + kColGram, d, d, idesc_gram, kk > 0 ? 1u : 0u);
+                        }
+                        mma_commit(&bars->gram_full);
+                        KKT_TRACE_EVENT(EV_M_GRAM, g_next);
+                    }
+                    __syncwarp();
+                    ++g_next;
+                    g_ready = false;
+                    progress = true;
+                }
             }
-            ok = wait_bar(&bars->tt_full, (uint32_t)i & 1u, bars, p.status) &&
-                 wait_bar(&bars->d_empty, ((uint32_t)i & 1u) ^ 1u, bars, p.status);
-            if (!ok) break;
-            issue_epi(stage_ptr(i % NS));
-            i = n;
-            have = has_next;
+            if (e_next < g_next) {
+                const bool ready = __shfl_sync(0xffffffffu,
+                                               mbar_test(&bars->tt_full, (uint32_t)e_next & 1u) &&
+                                                   mbar_test(&bars->d_empty, ((uint32_t)e_next & 1u) ^ 1u),
+                                               0);
+                if (ready) {
+                    const int s = e_next % kNS;
+                    if (lane == 0) {
+                        bars->einfo[e_next & 1] = *stage_info(s);
+                        mbar_arrive(&bars->einfo_full[e_next & 1]);
+                        tc_fence_after();
+                        const uint32_t b0 = smem_u32(stage_kv(s));
+#pragma unroll
+                        for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint64_t d = sw128_desc(b0 + kk * 2048, 16384, 1024);
+                                mma_ts(tmem + kColD, tmem + kColTT + pass * 64 + kk * 8, d, idesc_epi,
+                                       (pass | kk) ? 1u : 0u);
+                            }
+                        mma_commit(&bars->tt_empty);
+                        mma_commit(&bars->d_full);
+                        mma_commit(&bars->empty[s]);
+                        KKT_TRACE_EVENT(EV_M_EPI, e_next);
+                    }
+                    __syncwarp();
+                    ++e_next;
+                    progress = true;
+                }
+            }
+            if (done_at >= 0 && e_next == done_at) {
+                if (lane == 0) {
+                    bars->einfo[e_next & 1].done = 1;
+                    mbar_arrive(&bars->einfo_full[e_next & 1]);
+                }
+                __syncwarp();
+                break;
+            }
+            if (progress) {
+                t_idle = globaltimer_ns();
+            } else {
+                __nanosleep(64);  // leave issue slots to the inverse warp on this sub-partition
+                const bool stop = __shfl_sync(0xffffffffu, bars->abort_flag != 0 ||
+                                                               globaltimer_ns() - t_idle > kWaitLimitNs, 0);
+                if (stop) {
+                    if (lane == 0) fail(bars, p.status);
+                    break;
+                }
+            }
         }
         // every MMA issued by this thread has completed before tensor memory is freed
         if (lane == 0) {
@@ -396,8 +440,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = m % C;                // row within the chunk
         const int wp = r / 32;              // warp position within the head (0 for C = 32)
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        uint8_t *tstage = smem + CF::OFF_T;
+        uint8_t *tm = smem + CF::OFF_T;     // the tile's T, [half][128 rows][128 B], 128-byte swizzle
+        float *ybuf16 = reinterpret_cast<float *>(smem + CF::OFF_XCH) + q * 256;           // [16][16]
+        uint8_t *ybuf32 = smem + CF::OFF_XCH + 4096 + g * 4096;   // [32][32] fp32, 128-byte rows, swizzled
         // zero this lane's T~ columns (other heads' blocks and the upper triangle stay zero)
+        // and its row of T (the upper triangle stays zero there too)
         {
             uint32_t zz[16];
 #pragma unroll
@@ -405,180 +452,239 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int c = 0; c < 128; c += 16) tmem_st16(tmem + lane_base + kColTT + c, zz);
             tmem_wait_st();
-            for (int h = 0; h < CF::T_HALVES; ++h)
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<uint4 *>(tstage + h * 16384 + m * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+            for (int j = 0; j < C; j += 4) *tm_vec(tm, m, j) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         int i = 0;
-        uint32_t inv_uses = 0, pair_uses = 0;
+        uint32_t pair_uses = 0;
         while (true) {
-            const int s = i % NS;
-            if (!wait_bar(&bars->full[s], (uint32_t)(i / NS) & 1u, bars, p.status)) break;
-            const uint8_t *st = stage_ptr(s);
-            const TileInfo info = *reinterpret_cast<const TileInfo *>(st + CF::OFF_INFO);
+            const int s = i % kNS;
+            if (!wait_bar(&bars->full[s], (uint32_t)(i / kNS) & 1u, bars, p.status)) break;
+            const TileInfo info = *stage_info(s);
             if (info.done) break;
-            const float *sb = reinterpret_cast<const float *>(st + CF::OFF_BETA) + g * C;
+            const float *sb = stage_beta(s) + g * C;
             const float beta_r = sb[r];
 
             if (!wait_bar(&bars->gram_full, (uint32_t)i & 1u, bars, p.status)) break;
             tc_fence_after();
-            // Gram row -> strictly-lower L row (beta on rows, §3.2); only columns < 32 (wp + 1) matter
-            float l[C >= 64 ? 64 : 32];
+            if (q == 0 && lane == 0) KKT_TRACE_EVENT(EV_I_GRAM, i);
+            // this warp's previous T store has read its rows of the T buffer
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
+            // Gram row -> row of A = I + strictLower(diag(beta) S) (beta on rows, unit diagonal,
+            // §3.2) into the T buffer; columns above 32 (wp + 1) stay zero
             {
                 uint32_t v[32];
-                tmem_ld32(tmem + lane_base + kColGram + g * C, v);
-                tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) l[j] = (j < r) ? beta_r * __uint_as_float(v[j]) : 0.f;
-                if constexpr (C >= 64) {
-                    tmem_ld32(tmem + lane_base + kColGram + g * C + 32, v);
-                    tmem_wait_ld();
+                for (int h = 0; h < CF::T_HALVES; ++h) {
+                    if (h <= wp) {
+                        tmem_ld32(tmem + lane_base + kColGram + g * C + 32 * h, v);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) l[32 + j] = (32 + j < r) ? beta_r * __uint_as_float(v[j]) : 0.f;
+                        for (int c = 0; c < 32; c += 4) {
+                            float e[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int j = 32 * h + c + u;
+                                e[u] = (j < r) ? beta_r * __uint_as_float(v[c + u]) : (j == r ? 1.f : 0.f);
+                            }
+                            *tm_vec(tm, m, 32 * h + c) = make_float4(e[0], e[1], e[2], e[3]);
+                        }
+                    }
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->gram_empty);
+            if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_LD, i);
 
-            // this warp's 32-column slab of L: columns 32 wp .. 32 wp + 31
-            float slab[32];
+            // diagonal 16 x 16 blocks (§2.1), one column per lane: right-looking substitution,
+            // s[k] <- s[k] - L[k][m] x_m once x_m = s[m] is final; L is read as broadcasts
+            {
+                const int c = lane & 15;
+                const int rb = 32 * wp + 16 * (lane >> 4);  // first row / column of the block in the head
+                const int mb = g * C + rb;                  // its tile row
+                float sc[16];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                if constexpr (C >= 64) slab[j] = wp ? l[32 + j] : l[j];
-                else slab[j] = l[j];
-            }
-            // diagonal 16 x 16 block of this half warp
-            const bool upper = lane >= 16;
-            float lb[16], x[16];
+                for (int k = 0; k < 16; ++k) sc[k] = (k == c) ? 1.f : 0.f;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) lb[c] = upper ? slab[16 + c] : slab[c];
-            diag16(lb, x, lane);
-            // level 16: couple the warp's two diagonal blocks
-            float l10[16];
+                for (int ms = 0; ms < 15; ++ms) {
+                    const float xm = sc[ms];
 #pragma unroll
-            for (int c = 0; c < 16; ++c) l10[c] = slab[c];
-            float m32[32];
-            couple16(l10, x, lane, m32);
-
-            // the lane's row of T over columns 0 .. C-1 (zero above the diagonal)
-            float trow[C >= 64 ? 64 : 32];
-            if constexpr (C >= 64) {
-                // level 32: rows 32..63 of the head get -M11^-1 M10 M00^-1, with M00^-1 rows
-                // shared by the lower warp through shared memory
-                float *xbuf = reinterpret_cast<float *>(smem + CF::OFF_XCH) + g * 3072 + (i & 1) * 1024;
-                float *ybuf = reinterpret_cast<float *>(smem + CF::OFF_XCH) + g * 3072 + 2048;
-                if (wp == 0) {
-#pragma unroll
-                    for (int c = 0; c < 32; c += 4)
-                        *reinterpret_cast<float4 *>(xbuf + lane * 32 + c) =
-                            make_float4(m32[c], m32[c + 1], m32[c + 2], m32[c + 3]);
+                    for (int k = ms + 1; k < 16; ++k) sc[k] = fmaf(-*tm_elem(tm, mb + k, rb + ms), xm, sc[k]);
                 }
-                if (!group_sync(&bars->pair_sync[g], pair_uses, bars, p.status)) break;
-                if (wp == 1) {
-                    float y[32];
+                __syncwarp();
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) y[c] = 0.f;
+                for (int k = 1; k < 16; ++k) *tm_elem(tm, mb + k, rb + c) = sc[k];
+                __syncwarp();
+            }
+            if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_DIAG, i);
+
+            // level 16 (§2.2): the warp's two diagonal blocks, T10 = -X11 (L10 X00); lane -> row
+            // i of the 16 x 16 result, columns jb .. jb + 7
+            {
+                const int ii = lane >> 1;
+                const int jb = (lane & 1) * 8;
+                const int m0 = g * C + 32 * wp;
+                const int c0 = 32 * wp;
+                float a[16];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float lj = l[j];
+                for (int k = 0; k < 16; k += 4) {
+                    const float4 t4 = *tm_vec(tm, m0 + 16 + ii, c0 + k);
+                    a[k] = t4.x; a[k + 1] = t4.y; a[k + 2] = t4.z; a[k + 3] = t4.w;
+                }
+                float2 y[4];
 #pragma unroll
-                        for (int c = 0; c <= (j | 3); c += 4) {
-                            const float4 xv = *reinterpret_cast<const float4 *>(xbuf + j * 32 + c);
-                            y[c] = fmaf(lj, xv.x, y[c]);
-                            y[c + 1] = fmaf(lj, xv.y, y[c + 1]);
-                            y[c + 2] = fmaf(lj, xv.z, y[c + 2]);
-                            y[c + 3] = fmaf(lj, xv.w, y[c + 3]);
+                for (int e = 0; e < 4; ++e) y[e] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const float4 b0 = *tm_vec(tm, m0 + k, c0 + jb);
+                    const float4 b1 = *tm_vec(tm, m0 + k, c0 + jb + 4);
+                    const float2 ak = make_float2(a[k], a[k]);
+                    y[0] = ffma2(ak, make_float2(b0.x, b0.y), y[0]);
+                    y[1] = ffma2(ak, make_float2(b0.z, b0.w), y[1]);
+                    y[2] = ffma2(ak, make_float2(b1.x, b1.y), y[2]);
+                    y[3] = ffma2(ak, make_float2(b1.z, b1.w), y[3]);
+                }
+                *reinterpret_cast<float4 *>(ybuf16 + ii * 16 + jb) = make_float4(y[0].x, y[0].y, y[1].x, y[1].y);
+                *reinterpret_cast<float4 *>(ybuf16 + ii * 16 + jb + 4) = make_float4(y[2].x, y[2].y, y[3].x, y[3].y);
+#pragma unroll
+                for (int k = 0; k < 16; k += 4) {
+                    const float4 t4 = *tm_vec(tm, m0 + 16 + ii, c0 + 16 + k);
+                    a[k] = t4.x; a[k + 1] = t4.y; a[k + 2] = t4.z; a[k + 3] = t4.w;
+                }
+                __syncwarp();
+#pragma unroll
+                for (int e = 0; e < 4; ++e) y[e] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const float4 b0 = *reinterpret_cast<const float4 *>(ybuf16 + k * 16 + jb);
+                    const float4 b1 = *reinterpret_cast<const float4 *>(ybuf16 + k * 16 + jb + 4);
+                    const float2 ak = make_float2(a[k], a[k]);
+                    y[0] = ffma2(ak, make_float2(b0.x, b0.y), y[0]);
+                    y[1] = ffma2(ak, make_float2(b0.z, b0.w), y[1]);
+                    y[2] = ffma2(ak, make_float2(b1.x, b1.y), y[2]);
+                    y[3] = ffma2(ak, make_float2(b1.z, b1.w), y[3]);
+                }
+                *tm_vec(tm, m0 + 16 + ii, c0 + jb) = make_float4(-y[0].x, -y[0].y, -y[1].x, -y[1].y);
+                *tm_vec(tm, m0 + 16 + ii, c0 + jb + 4) = make_float4(-y[2].x, -y[2].y, -y[3].x, -y[3].y);
+                __syncwarp();
+            }
+            if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_C16, i);
+
+            bool ok = true;
+            if constexpr (C >= 64) {
+                // level 32: rows 32..63 of the head get -M11^-1 M10 M00^-1.  The head's two warps
+                // split the 32 x 32 result by columns (warp wp: columns 16 wp .. 16 wp + 15, a
+                // uniform block, so every B address is a base plus a constant); lane -> row.
+                ok = group_sync(&bars->pair_sync[g], pair_uses, bars, p.status);
+                if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_PAIR, i);
+                const int ii = lane;
+                const int m0 = g * C;
+                // B bases: chunk (4 wp + e) of row k lands at chunk (4 wp + e) ^ (k & 7); with
+                // k & 4 folded into the base, the rest is a compile-time offset
+                const uint32_t cw0 = (uint32_t)(4 * wp) << 4, cw1 = (uint32_t)((4 * wp) ^ 4) << 4;
+                float2 y[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) y[e] = make_float2(0.f, 0.f);
+                if (ok) {
+                    // Y[ii][16 wp ..] = M10[ii][:] M00^-1[:][16 wp ..]; M00^-1[k][j] = 0 for k < j
+#pragma unroll 1
+                    for (int kb = 16 * wp; kb < 32; kb += 8) {
+                        const float4 a0 = *tm_vec(tm, m0 + 32 + ii, kb);
+                        const float4 a1 = *tm_vec(tm, m0 + 32 + ii, kb + 4);
+                        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                        const uint8_t *rb = tm + (m0 + kb) * 128;
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint8_t *row = rb + kk * 128 + ((kk & 4) ? cw1 : cw0);
+                            const float2 ak = make_float2(av[kk], av[kk]);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float4 b = *reinterpret_cast<const float4 *>(row + ((e ^ (kk & 3)) << 4));
+                                y[2 * e] = ffma2(ak, make_float2(b.x, b.y), y[2 * e]);
+                                y[2 * e + 1] = ffma2(ak, make_float2(b.z, b.w), y[2 * e + 1]);
+                            }
+                        }
+                    }
+                    // Y into the head's [32][32] scratch, same swizzle as T
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        *tm_vec(ybuf32, ii, 16 * wp + 4 * e) =
+                            make_float4(y[2 * e].x, y[2 * e].y, y[2 * e + 1].x, y[2 * e + 1].y);
+                    ok = group_sync(&bars->pair_sync[g], pair_uses, bars, p.status);
+                }
+                if (ok) {
+                    // Z[ii][16 wp ..] = M11^-1[ii][:] Y[:][16 wp ..]
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) y[e] = make_float2(0.f, 0.f);
+#pragma unroll 1
+                    for (int kb = 0; kb < 32; kb += 8) {
+                        const float4 a0 = *tm_vec(tm, m0 + 32 + ii, 32 + kb);
+                        const float4 a1 = *tm_vec(tm, m0 + 32 + ii, 32 + kb + 4);
+                        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                        const uint8_t *rb = ybuf32 + kb * 128;
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint8_t *row = rb + kk * 128 + ((kk & 4) ? cw1 : cw0);
+                            const float2 ak = make_float2(av[kk], av[kk]);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float4 b = *reinterpret_cast<const float4 *>(row + ((e ^ (kk & 3)) << 4));
+                                y[2 * e] = ffma2(ak, make_float2(b.x, b.y), y[2 * e]);
+                                y[2 * e + 1] = ffma2(ak, make_float2(b.z, b.w), y[2 * e + 1]);
+                            }
                         }
                     }
 #pragma unroll
-                    for (int c = 0; c < 32; c += 4)
-                        *reinterpret_cast<float4 *>(ybuf + lane * 32 + c) = make_float4(y[c], y[c + 1], y[c + 2], y[c + 3]);
-                    __syncwarp();
-                    float z[32];
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) z[c] = 0.f;
-#pragma unroll
-                    for (int k2 = 0; k2 < 32; ++k2) {
-                        const float mk = m32[k2];
-#pragma unroll
-                        for (int c = 0; c < 32; c += 4) {
-                            const float4 yv = *reinterpret_cast<const float4 *>(ybuf + k2 * 32 + c);
-                            z[c] = fmaf(mk, yv.x, z[c]);
-                            z[c + 1] = fmaf(mk, yv.y, z[c + 1]);
-                            z[c + 2] = fmaf(mk, yv.z, z[c + 2]);
-                            z[c + 3] = fmaf(mk, yv.w, z[c + 3]);
-                        }
-                    }
-                    __syncwarp();
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        trow[c] = -z[c];
-                        trow[32 + c] = m32[c];
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        trow[c] = m32[c];
-                        trow[32 + c] = 0.f;
-                    }
+                    for (int e = 0; e < 4; ++e)
+                        *tm_vec(tm, m0 + 32 + ii, 16 * wp + 4 * e) =
+                            make_float4(-y[2 * e].x, -y[2 * e].y, -y[2 * e + 1].x, -y[2 * e + 1].y);
+                    fence_proxy_async_smem();
+                    ok = group_sync(&bars->pair_sync[g], pair_uses, bars, p.status);
                 }
             } else {
-#pragma unroll
-                for (int c = 0; c < 32; ++c) trow[c] = m32[c];
-            }
-
-            // T rows: staging + TMA store for a full chunk, plain stores for a short one
-            const bool full_chunk = info.Lc == C;
-            if (full_chunk) {
-                if (threadIdx.x == kWarpInv0 * 32) bulk_wait_read<0>();
-                if (!group_sync(&bars->inv_sync, inv_uses, bars, p.status)) break;
-#pragma unroll
-                for (int h = 0; h < CF::T_HALVES; ++h) {
-                    if (h <= wp) {
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const uint32_t off = sw128((uint32_t)(m * 128 + c * 16));
-                            *reinterpret_cast<float4 *>(tstage + h * 16384 + off) =
-                                make_float4(trow[32 * h + 4 * c], trow[32 * h + 4 * c + 1], trow[32 * h + 4 * c + 2],
-                                            trow[32 * h + 4 * c + 3]);
-                        }
-                    }
-                }
                 fence_proxy_async_smem();
-                if (!group_sync(&bars->inv_sync, inv_uses, bars, p.status)) break;
-                if (threadIdx.x == kWarpInv0 * 32) {
-                    for (int gg = 0; gg < G; ++gg)
-                        for (int h = 0; h < CF::T_HALVES; ++h)
-                            tma_store_3d(&map_t, tstage + h * 16384 + gg * C * 128, 32 * h, info.h0 + gg,
-                                         (int)info.t0);
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_INV, i);
+
+            // T rows: TMA store of the warp's 32 rows when all are valid, else plain stores
+            if (32 * wp + 32 <= info.Lc) {
+                if (lane == 0) {
+                    for (int h = 0; h < CF::T_HALVES; ++h)
+                        tma_store_3d(&map_t, tm + h * 16384 + 32 * q * 128, 32 * h, info.h0 + g,
+                                     (int)(info.t0 + 32 * wp));
                     bulk_commit();
                 }
             } else if (r < info.Lc && info.h0 + g < p.H) {
                 float4 *dst = reinterpret_cast<float4 *>(p.T_out + ((info.t0 + r) * p.H + info.h0 + g) * C);
 #pragma unroll
-                for (int c = 0; c < C / 4; ++c)
-                    dst[c] = make_float4(trow[4 * c], trow[4 * c + 1], trow[4 * c + 2], trow[4 * c + 3]);
+                for (int j = 0; j < C; j += 4) dst[j / 4] = *tm_vec(tm, m, j);
             }
+            if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_TSTORE, i);
 
             // T~ = T diag(beta), split into bf16 hi + lo, into tensor memory (A operand)
             if (!wait_bar(&bars->tt_empty, ((uint32_t)i & 1u) ^ 1u, bars, p.status)) break;
             tc_fence_after();
             {
-                constexpr int NJ = C >= 64 ? 64 : 32;
                 uint32_t hi[16], lo[16];
 #pragma unroll
-                for (int blk = 0; blk < NJ / 32; ++blk) {
+                for (int blk = 0; blk < CF::T_HALVES; ++blk) {
                     if (blk <= wp) {
 #pragma unroll
-                        for (int c = 0; c < 16; ++c) {
-                            const int j = 32 * blk + 2 * c;
-                            const float a = trow[j] * sb[j];
-                            const float b = trow[j + 1] * sb[j + 1];
-                            const __nv_bfloat16 ah = __float2bfloat16_rn(a), bh = __float2bfloat16_rn(b);
-                            hi[c] = (uint32_t)__bfloat16_as_ushort(ah) | ((uint32_t)__bfloat16_as_ushort(bh) << 16);
-                            lo[c] = pack_bf16(a - __bfloat162float(ah), b - __bfloat162float(bh));
+                        for (int c = 0; c < 32; c += 4) {
+                            const float4 t4 = *tm_vec(tm, m, 32 * blk + c);
+                            const float4 b4 = *reinterpret_cast<const float4 *>(sb + 32 * blk + c);
+                            const float v4[4] = {t4.x * b4.x, t4.y * b4.y, t4.z * b4.z, t4.w * b4.w};
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const float a = v4[2 * u], b = v4[2 * u + 1];
+                                const uint32_t h = pack_bf16(a, b);
+                                hi[c / 2 + u] = h;
+                                lo[c / 2 + u] = pack_bf16(a - __uint_as_float(h << 16), b - __uint_as_float(h & 0xffff0000u));
+                            }
                         }
                         const uint32_t col = (uint32_t)(g * C + 32 * blk) / 2;
                         tmem_st16(tmem + lane_base + kColTT + col, hi);
@@ -589,10 +695,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->tt_full);
+            if (lane == 0) {
+                mbar_arrive(&bars->tt_full);
+                if (q == 1) KKT_TRACE_EVENT(EV_I_TT, i);
+            }
             ++i;
         }
-        if (threadIdx.x == kWarpInv0 * 32) bulk_wait<0>();
+        if (lane == 0) bulk_wait<0>();
         __syncwarp();
     } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
         // ------------------------------------------------------------------ epilogue warps
@@ -600,66 +709,68 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int m = 32 * q + lane;
         const int g = m / C;
         const int r = m % C;
+        const int wp = r / 32;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        uint8_t *wstage = smem + CF::OFF_WU + q * 8192;   // 2 buffers x [32 rows][128 B]
         int i = 0;
-        uint32_t epi_uses = 0;
+        uint32_t nstore = 0;  // TMA store groups issued by this warp
         while (true) {
-            const int s = i % NS;
-            if (!wait_bar(&bars->full[s], (uint32_t)(i / NS) & 1u, bars, p.status)) break;
-            uint8_t *st = stage_ptr(s);
-            const TileInfo info = *reinterpret_cast<const TileInfo *>(st + CF::OFF_INFO);
+            if (!wait_bar(&bars->einfo_full[i & 1], (uint32_t)(i >> 1) & 1u, bars, p.status)) break;
+            const TileInfo info = bars->einfo[i & 1];
             if (info.done) break;
             if (!wait_bar(&bars->d_full, (uint32_t)i & 1u, bars, p.status)) break;
             tc_fence_after();
-            const bool full_chunk = info.Lc == C;
+            if (q == 0 && lane == 0) KKT_TRACE_EVENT(EV_E_DFULL, i);
+            const bool warp_full = 32 * wp + 32 <= info.Lc;
             const bool row_ok = r < info.Lc && info.h0 + g < p.H;
             const int64_t grow = (info.t0 + r) * p.H + info.h0 + g;
 #pragma unroll 1
-            for (int c = 0; c < 8; ++c) {  // 32 fp32 columns of D at a time: W cols 0..127, U~ 128..255
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_base + kColD + 32 * c, v);
+            for (int cc = 0; cc < 4; ++cc) {  // 64 columns of D at a time: W 0..63, W 64..127, U~ 0..63, U~ 64..127
+                uint32_t v0[32], v1[32];
+                tmem_ld32(tmem + lane_base + kColD + 64 * cc, v0);
+                tmem_ld32(tmem + lane_base + kColD + 64 * cc + 32, v1);
                 tmem_wait_ld();
-                uint32_t pk[16];
+                if (cc == 3) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&bars->d_empty);
+                        if (q == 0) KKT_TRACE_EVENT(EV_E_DEMPTY, i);
+                    }
+                }
+                uint32_t pk[32];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) pk[e] = pack_bf16(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
-                const int n0 = 32 * c;              // first column in [W | U~]
-                const int kv = n0 / 128;            // 0: W, 1: U~
-                const int half = (n0 % 128) / 64;   // 64-column box
-                const int cb = (n0 % 64) * 2;       // byte offset inside the 128-byte row
-                if (full_chunk) {
-                    uint8_t *dst = st + kv * 32768 + half * 16384;
+                for (int e = 0; e < 16; ++e) {
+                    pk[e] = pack_bf16(__uint_as_float(v0[2 * e]), __uint_as_float(v0[2 * e + 1]));
+                    pk[16 + e] = pack_bf16(__uint_as_float(v1[2 * e]), __uint_as_float(v1[2 * e + 1]));
+                }
+                if (warp_full) {
+                    uint8_t *buf = wstage + (nstore & 1u) * 4096;
+                    if (lane == 0) bulk_wait_read<1>();
+                    __syncwarp();
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        *reinterpret_cast<uint4 *>(dst + sw128((uint32_t)(m * 128 + cb + 16 * e))) =
+                    for (int e = 0; e < 8; ++e)
+                        *reinterpret_cast<uint4 *>(buf + sw128((uint32_t)(lane * 128 + 16 * e))) =
                             make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(cc < 2 ? &map_w : &map_u, buf, 64 * (cc & 1), info.h0 + g,
+                                     (int)(info.t0 + 32 * wp));
+                        bulk_commit();
+                    }
+                    ++nstore;
                 } else if (row_ok) {
-                    __nv_bfloat16 *base = (kv == 0 ? p.W_out : p.U_out) + grow * 128 + (n0 % 128);
+                    __nv_bfloat16 *base = (cc < 2 ? p.W_out : p.U_out) + grow * 128 + 64 * (cc & 1);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
+                    for (int e = 0; e < 8; ++e)
                         reinterpret_cast<uint4 *>(base)[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->d_empty);
-            if (full_chunk) fence_proxy_async_smem();
-            if (!group_sync(&bars->epi_sync, epi_uses, bars, p.status)) break;
-            if (threadIdx.x == kWarpEpi0 * 32) {
-                if (full_chunk) {
-                    for (int gg = 0; gg < G; ++gg)
-                        for (int h = 0; h < 2; ++h) {
-                            tma_store_3d(&map_w, st + h * 16384 + gg * C * 128, 64 * h, info.h0 + gg, (int)info.t0);
-                            tma_store_3d(&map_u, st + 32768 + h * 16384 + gg * C * 128, 64 * h, info.h0 + gg,
-                                         (int)info.t0);
-                        }
-                    bulk_commit();
-                    bulk_wait_read<0>();
-                }
-                mbar_arrive(&bars->empty[s]);
-            }
+            if (q == 0 && lane == 0) KKT_TRACE_EVENT(EV_E_DONE, i);
             ++i;
         }
-        if (threadIdx.x == kWarpEpi0 * 32) bulk_wait<0>();
+        if (lane == 0) bulk_wait<0>();
         __syncwarp();
     }
 
@@ -716,9 +827,9 @@ int launch_tc_t(const Problem &pb) {
     CUtensorMap mk, mv, mw, mu, mt;
     if (!make_map(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.k, pb.ntok, pb.H, pb.dk, 64, C) ||
         !make_map(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.v, pb.ntok, pb.H, pb.dv, 64, C) ||
-        !make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.W_out, pb.ntok, pb.H, pb.dk, 64, C) ||
-        !make_map(&mu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.U_out, pb.ntok, pb.H, pb.dv, 64, C) ||
-        !make_map(&mt, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pb.T_out, pb.ntok, pb.H, C, 32, C))
+        !make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.W_out, pb.ntok, pb.H, pb.dk, 64, 32) ||
+        !make_map(&mu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.U_out, pb.ntok, pb.H, pb.dv, 64, 32) ||
+        !make_map(&mt, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pb.T_out, pb.ntok, pb.H, C, 32, 32))
         return KKT_ERR_CUDA;
     TcParams p;
     p.beta = pb.beta;
@@ -733,6 +844,7 @@ int launch_tc_t(const Problem &pb) {
     p.W_out = static_cast<__nv_bfloat16 *>(pb.W_out);
     p.U_out = static_cast<__nv_bfloat16 *>(pb.U_out);
     p.status = pb.status;
+    p.trace = static_cast<unsigned long long *>(pb.trace);
     auto kern = kkt_tc_kernel<C>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_BYTES) != cudaSuccess)
         return KKT_ERR_CUDA;
