@@ -122,7 +122,7 @@ enum TraceEvent {
     EV_P_EMPTY = 0, EV_P_ISSUE, EV_M_FULL, EV_M_GRAM, EV_M_EPI, EV_I_GRAM, EV_I_INV, EV_I_TSTORE,
     EV_I_TT, EV_E_DFULL, EV_E_DEMPTY, EV_E_DONE, EV_I_LD, EV_I_DIAG, EV_I_C16, EV_I_PAIR, EV_COUNT
 };
-constexpr int kTraceCtas = 8;
+constexpr int kTraceCtas = 160;
 constexpr int kTraceTiles = 64;
 constexpr int kTraceSlots = 16;
 #ifdef KKT_TRACE
@@ -474,19 +474,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Gram row -> row of A = I + strictLower(diag(beta) S) (beta on rows, unit diagonal,
             // §3.2) into the T buffer; columns above 32 (wp + 1) stay zero
             {
-                uint32_t v[32];
+                uint32_t v[CF::T_HALVES][32];
+#pragma unroll
+                for (int h = 0; h < CF::T_HALVES; ++h)
+                    if (h <= wp) tmem_ld32(tmem + lane_base + kColGram + g * C + 32 * h, v[h]);
+                tmem_wait_ld();
 #pragma unroll
                 for (int h = 0; h < CF::T_HALVES; ++h) {
                     if (h <= wp) {
-                        tmem_ld32(tmem + lane_base + kColGram + g * C + 32 * h, v);
-                        tmem_wait_ld();
 #pragma unroll
                         for (int c = 0; c < 32; c += 4) {
                             float e[4];
 #pragma unroll
                             for (int u = 0; u < 4; ++u) {
                                 const int j = 32 * h + c + u;
-                                e[u] = (j < r) ? beta_r * __uint_as_float(v[c + u]) : (j == r ? 1.f : 0.f);
+                                e[u] = (j < r) ? beta_r * __uint_as_float(v[h][c + u]) : (j == r ? 1.f : 0.f);
                             }
                             *tm_vec(tm, m, 32 * h + c) = make_float4(e[0], e[1], e[2], e[3]);
                         }
@@ -574,72 +576,94 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             bool ok = true;
             if constexpr (C >= 64) {
-                // level 32: rows 32..63 of the head get -M11^-1 M10 M00^-1.  The head's two warps
-                // split the 32 x 32 result by columns (warp wp: columns 16 wp .. 16 wp + 15, a
-                // uniform block, so every B address is a base plus a constant); lane -> row.
+                // level 32: rows 32..63 of the head get -M11^-1 M10 M00^-1.  With 16 x 16 blocks
+                // M00^-1 = [[A, 0], [Cb, D]], M10 = [P, Q], M11^-1 = [[A', 0], [Cb', D']]:
+                //   Y = M10 M00^-1 = [P A + Q Cb, Q D],  Z = M11^-1 Y = [A' Y_top ; Cb' Y_top + D' Y_bot].
+                // Warp 0 takes Y_left (K = 32) and Z_top (K = 16), warp 1 Y_right (K = 16) and Z_bot
+                // (K = 32): the zero blocks are skipped and both warps do 384 packed FMAs per lane.
                 ok = group_sync(&bars->pair_sync[g], pair_uses, bars, p.status);
                 if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_PAIR, i);
-                const int ii = lane;
                 const int m0 = g * C;
-                // B bases: chunk (4 wp + e) of row k lands at chunk (4 wp + e) ^ (k & 7); with
-                // k & 4 folded into the base, the rest is a compile-time offset
-                const uint32_t cw0 = (uint32_t)(4 * wp) << 4, cw1 = (uint32_t)((4 * wp) ^ 4) << 4;
-                float2 y[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) y[e] = make_float2(0.f, 0.f);
                 if (ok) {
-                    // Y[ii][16 wp ..] = M10[ii][:] M00^-1[:][16 wp ..]; M00^-1[k][j] = 0 for k < j
+                    // Y part: rows yr + 8 rr (rr = 0..3) of all 32, columns 16 wp + 4 yc .. + 3
+                    const int yr = lane >> 2, yc = lane & 3;
+                    const int ycol = 16 * wp + 4 * yc;
+                    const int k0 = 16 * wp;        // rows of M00^-1 below the zero block of the column half
+                    float2 y[4][2];
+#pragma unroll
+                    for (int rr = 0; rr < 4; ++rr) y[rr][0] = y[rr][1] = make_float2(0.f, 0.f);
+                    uint32_t swz[8];
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) swz[kk] = (uint32_t)((ycol >> 2) ^ kk) << 4;
 #pragma unroll 1
-                    for (int kb = 16 * wp; kb < 32; kb += 8) {
-                        const float4 a0 = *tm_vec(tm, m0 + 32 + ii, kb);
-                        const float4 a1 = *tm_vec(tm, m0 + 32 + ii, kb + 4);
-                        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                        const uint8_t *rb = tm + (m0 + kb) * 128;
+                    for (int kb = k0; kb < 32; kb += 8) {
+                        float av[4][8];
+#pragma unroll
+                        for (int rr = 0; rr < 4; ++rr) {
+                            const float4 a0 = *tm_vec(tm, m0 + 32 + yr + 8 * rr, kb);
+                            const float4 a1 = *tm_vec(tm, m0 + 32 + yr + 8 * rr, kb + 4);
+                            av[rr][0] = a0.x; av[rr][1] = a0.y; av[rr][2] = a0.z; av[rr][3] = a0.w;
+                            av[rr][4] = a1.x; av[rr][5] = a1.y; av[rr][6] = a1.z; av[rr][7] = a1.w;
+                        }
+                        const uint8_t *rowb = tm + (m0 + kb) * 128;
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {
-                            const uint8_t *row = rb + kk * 128 + ((kk & 4) ? cw1 : cw0);
-                            const float2 ak = make_float2(av[kk], av[kk]);
+                            const float4 bq = *reinterpret_cast<const float4 *>(rowb + kk * 128 + swz[kk]);
+                            const float2 b01 = make_float2(bq.x, bq.y), b23 = make_float2(bq.z, bq.w);
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float4 b = *reinterpret_cast<const float4 *>(row + ((e ^ (kk & 3)) << 4));
-                                y[2 * e] = ffma2(ak, make_float2(b.x, b.y), y[2 * e]);
-                                y[2 * e + 1] = ffma2(ak, make_float2(b.z, b.w), y[2 * e + 1]);
+                            for (int rr = 0; rr < 4; ++rr) {
+                                const float2 ak = make_float2(av[rr][kk], av[rr][kk]);
+                                y[rr][0] = ffma2(ak, b01, y[rr][0]);
+                                y[rr][1] = ffma2(ak, b23, y[rr][1]);
                             }
                         }
                     }
-                    // Y into the head's [32][32] scratch, same swizzle as T
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        *tm_vec(ybuf32, ii, 16 * wp + 4 * e) =
-                            make_float4(y[2 * e].x, y[2 * e].y, y[2 * e + 1].x, y[2 * e + 1].y);
+                    for (int rr = 0; rr < 4; ++rr)
+                        *tm_vec(ybuf32, yr + 8 * rr, ycol) = make_float4(y[rr][0].x, y[rr][0].y, y[rr][1].x, y[rr][1].y);
                     ok = group_sync(&bars->pair_sync[g], pair_uses, bars, p.status);
                 }
                 if (ok) {
-                    // Z[ii][16 wp ..] = M11^-1[ii][:] Y[:][16 wp ..]
+                    // Z part: rows 16 wp + zr + 8 rr (rr = 0, 1), columns 8 zc .. 8 zc + 7; K runs over
+                    // the nonzero columns of those M11^-1 rows: 0..15 (wp 0) or 0..31 (wp 1)
+                    const int zr = lane >> 2, zc = lane & 3;
+                    const int kend = 16 + 16 * wp;
+                    float2 z[2][4];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) y[e] = make_float2(0.f, 0.f);
+                    for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) z[rr][e] = make_float2(0.f, 0.f);
 #pragma unroll 1
-                    for (int kb = 0; kb < 32; kb += 8) {
-                        const float4 a0 = *tm_vec(tm, m0 + 32 + ii, 32 + kb);
-                        const float4 a1 = *tm_vec(tm, m0 + 32 + ii, 32 + kb + 4);
-                        const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                        const uint8_t *rb = ybuf32 + kb * 128;
+                    for (int kb = 0; kb < kend; kb += 8) {
+                        float av[2][8];
+#pragma unroll
+                        for (int rr = 0; rr < 2; ++rr) {
+                            const int row = m0 + 32 + 16 * wp + zr + 8 * rr;
+                            const float4 a0 = *tm_vec(tm, row, 32 + kb);
+                            const float4 a1 = *tm_vec(tm, row, 32 + kb + 4);
+                            av[rr][0] = a0.x; av[rr][1] = a0.y; av[rr][2] = a0.z; av[rr][3] = a0.w;
+                            av[rr][4] = a1.x; av[rr][5] = a1.y; av[rr][6] = a1.z; av[rr][7] = a1.w;
+                        }
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {
-                            const uint8_t *row = rb + kk * 128 + ((kk & 4) ? cw1 : cw0);
-                            const float2 ak = make_float2(av[kk], av[kk]);
+                            const float4 b0 = *tm_vec(ybuf32, kb + kk, 8 * zc);
+                            const float4 b1 = *tm_vec(ybuf32, kb + kk, 8 * zc + 4);
+                            const float2 bb[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
+                                                  make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float4 b = *reinterpret_cast<const float4 *>(row + ((e ^ (kk & 3)) << 4));
-                                y[2 * e] = ffma2(ak, make_float2(b.x, b.y), y[2 * e]);
-                                y[2 * e + 1] = ffma2(ak, make_float2(b.z, b.w), y[2 * e + 1]);
+                            for (int rr = 0; rr < 2; ++rr) {
+                                const float2 ak = make_float2(av[rr][kk], av[rr][kk]);
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) z[rr][e] = ffma2(ak, bb[e], z[rr][e]);
                             }
                         }
                     }
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        *tm_vec(tm, m0 + 32 + ii, 16 * wp + 4 * e) =
-                            make_float4(-y[2 * e].x, -y[2 * e].y, -y[2 * e + 1].x, -y[2 * e + 1].y);
+                    for (int rr = 0; rr < 2; ++rr) {
+                        const int row = m0 + 32 + 16 * wp + zr + 8 * rr;
+                        *tm_vec(tm, row, 8 * zc) = make_float4(-z[rr][0].x, -z[rr][0].y, -z[rr][1].x, -z[rr][1].y);
+                        *tm_vec(tm, row, 8 * zc + 4) = make_float4(-z[rr][2].x, -z[rr][2].y, -z[rr][3].x, -z[rr][3].y);
+                    }
                     fence_proxy_async_smem();
                     ok = group_sync(&bars->pair_sync[g], pair_uses, bars, p.status);
                 }

@@ -19,7 +19,7 @@ from .inputs import workloads
 
 EVENTS = ["P_EMPTY", "P_ISSUE", "M_FULL", "M_GRAM", "M_EPI", "I_GRAM", "I_INV", "I_TSTORE", "I_TT",
           "E_DFULL", "E_DEMPTY", "E_DONE", "I_LD", "I_DIAG", "I_C16", "I_PAIR"]
-TRACE_CTAS, TRACE_TILES, TRACE_SLOTS = 8, 64, 16
+TRACE_CTAS, TRACE_TILES, TRACE_SLOTS = 160, 64, 16
 
 
 def run(workload: str, warmup: int = 3):
@@ -83,6 +83,28 @@ def report(tr: np.ndarray, ctas: int, tiles: int) -> str:
         ok = (t[:, 1:, ev[e]] > 0) & (t[:, :-1, ev[e]] > 0)
         return float(np.mean(x[:, 1:][ok[:, 1:]])) / 1e3 if ok[:, 1:].any() else float("nan")
 
+    # whole grid: first event and last epilogue completion per CTA
+    starts, ends, ntiles = [], [], []
+    for b in range(t.shape[0]):
+        tb = t[b]
+        if not (tb > 0).any():
+            continue
+        starts.append(tb[tb > 0].min())
+        done = tb[:, ev["E_DONE"]]
+        ends.append(done[done > 0].max() if (done > 0).any() else np.nan)
+        ntiles.append(int((done > 0).sum()))
+    if starts:
+        g0 = min(starts)
+        st = (np.array(starts) - g0) / 1e3
+        en = (np.array(ends) - g0) / 1e3
+        nt = np.array(ntiles)
+        lines.append("")
+        lines.append(f"grid: {len(st)} CTAs traced; start spread {st.min():.2f}..{st.max():.2f} us; "
+                     f"end {np.nanmin(en):.2f}..{np.nanmax(en):.2f} us (median {np.nanmedian(en):.2f}); "
+                     f"tiles per CTA {nt.min()}..{nt.max()}")
+        for k_ in sorted(set(nt.tolist())):
+            sel = nt == k_
+            lines.append(f"  CTAs with {k_} tiles: {sel.sum()}, end {np.nanmin(en[sel]):.2f}..{np.nanmax(en[sel]):.2f} us")
     lines.append("")
     lines.append(f"period per tile (M_EPI to M_EPI)         {period('M_EPI'):7.2f} us")
     lines.append(f"load: issue -> landed (P_ISSUE->M_FULL)  {span('P_ISSUE', 'M_FULL'):7.2f} us")
