@@ -195,6 +195,98 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
     return d;
 }
 
+// D (4 x 4 tile, as 4 rows x 2 packed pairs) += A B over NKB blocks of 8 k.  A rows: byte pointers to
+// the start of the rows' 128-byte lines in the k range's half, with their swizzle phases as XOR
+// masks; acol0 is the first k column (a multiple of 8) inside that half.  B rows: base pointer of
+// row 0 of the k range (its row index a multiple of 8), bsw[kk] the byte offset of this lane's
+// 16-byte column chunk in a row with phase kk.
+// A loop over 8-k blocks rather than an unrolled sequence: the kernel is sensitive to its
+// instruction-cache footprint, so the code size of this inner product is kept small.
+__device__ __forceinline__ void tile4x4_fma(float2 (&y)[4][2], const uint8_t *const (&arow)[4],
+                                         const uint32_t (&axor)[4], int acol0, const uint8_t *brow0,
+                                         const uint32_t (&bsw)[8], int nkb) {
+#pragma unroll 1
+    for (int kb = 0; kb < nkb; ++kb) {
+        float av[4][8];
+        const uint32_t ca = (uint32_t)((acol0 >> 2) + 2 * kb) << 4;
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(arow[rr] + (ca ^ axor[rr]));
+            const float4 a1 = *reinterpret_cast<const float4 *>(arow[rr] + ((ca + 16u) ^ axor[rr]));
+            av[rr][0] = a0.x; av[rr][1] = a0.y; av[rr][2] = a0.z; av[rr][3] = a0.w;
+            av[rr][4] = a1.x; av[rr][5] = a1.y; av[rr][6] = a1.z; av[rr][7] = a1.w;
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const float4 b = *reinterpret_cast<const float4 *>(brow0 + (8 * kb + kk) * 128 + bsw[kk]);
+            const float2 b01 = make_float2(b.x, b.y), b23 = make_float2(b.z, b.w);
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+                const float2 ak = make_float2(av[rr][kk], av[rr][kk]);
+                y[rr][0] = ffma2(ak, b01, y[rr][0]);
+                y[rr][1] = ffma2(ak, b23, y[rr][1]);
+            }
+        }
+    }
+}
+
+// Level-32 coupling of one head (rows m0 .. m0 + 63 of the tile's T buffer) for warp WP (0 or 1)
+// of its two warps.  With 16 x 16 blocks M00^-1 = [[A, 0], [Cb, D]], M10 = [P, Q],
+// M11^-1 = [[A', 0], [Cb', D']]:  Y = M10 M00^-1 = [P A + Q Cb, Q D] and
+// Z = M11^-1 Y = [A' Y_top ; Cb' Y_top + D' Y_bot].  Warp 0 computes Y_left (K = 32) and Z_top
+// (K = 16), warp 1 Y_right (K = 16) and Z_bot (K = 32): the zero blocks are skipped and both
+// warps do 384 packed FMAs per lane.  Rows 32..63, columns 0..31 of the head receive -Z.
+__device__ __forceinline__ bool level32(const int WP, uint8_t *tm, uint8_t *ybuf32, int m0, int lane,
+                                        uint64_t *pair_bar, uint32_t &pair_uses, Barriers *bars, int *status) {
+    {
+        // Y part: rows yr + 8 rr of 32, columns 16 WP + 4 yc .. + 3; k in [16 WP, 32)
+        const int yr = lane >> 2, yc = lane & 3;
+        const uint8_t *arow[4];
+        uint32_t axor[4];
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+            arow[rr] = tm + (m0 + 32 + yr + 8 * rr) * 128;
+            axor[rr] = (uint32_t)(yr & 7) << 4;
+        }
+        uint32_t bsw[8];
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) bsw[kk] = (uint32_t)((4 * WP + yc) ^ kk) << 4;
+        float2 y[4][2];
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) y[rr][0] = y[rr][1] = make_float2(0.f, 0.f);
+        tile4x4_fma(y, arow, axor, 16 * WP, tm + (m0 + 16 * WP) * 128, bsw, 4 - 2 * WP);
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr)
+            *tm_vec(ybuf32, yr + 8 * rr, 16 * WP + 4 * yc) = make_float4(y[rr][0].x, y[rr][0].y, y[rr][1].x, y[rr][1].y);
+    }
+    if (!group_sync(pair_bar, pair_uses, bars, status)) return false;
+    {
+        // Z part: rows 16 WP + zr + 4 rr (zr = 0..3), columns 4 zc .. + 3 (zc = 0..7); k in [0, 16 + 16 WP)
+        const int zr = lane >> 3, zc = lane & 7;
+        const uint8_t *arow[4];
+        uint32_t axor[4];
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+            const int row = m0 + 32 + 16 * WP + zr + 4 * rr;
+            arow[rr] = tm + 16384 + row * 128;  // columns 32..63 of the head: the second half
+            axor[rr] = (uint32_t)(row & 7) << 4;
+        }
+        uint32_t bsw[8];
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) bsw[kk] = (uint32_t)(zc ^ kk) << 4;
+        float2 z[4][2];
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) z[rr][0] = z[rr][1] = make_float2(0.f, 0.f);
+        tile4x4_fma(z, arow, axor, 0, ybuf32, bsw, 2 + 2 * WP);
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr)
+            *tm_vec(tm, m0 + 32 + 16 * WP + zr + 4 * rr, 4 * zc) =
+                make_float4(-z[rr][0].x, -z[rr][0].y, -z[rr][1].x, -z[rr][1].y);
+    }
+    fence_proxy_async_smem();
+    return group_sync(pair_bar, pair_uses, bars, status);
+}
+
 // ---------------------------------------------------------------------------------------------
 template <int C>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -576,96 +668,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             bool ok = true;
             if constexpr (C >= 64) {
-                // level 32: rows 32..63 of the head get -M11^-1 M10 M00^-1.  With 16 x 16 blocks
-                // M00^-1 = [[A, 0], [Cb, D]], M10 = [P, Q], M11^-1 = [[A', 0], [Cb', D']]:
-                //   Y = M10 M00^-1 = [P A + Q Cb, Q D],  Z = M11^-1 Y = [A' Y_top ; Cb' Y_top + D' Y_bot].
-                // Warp 0 takes Y_left (K = 32) and Z_top (K = 16), warp 1 Y_right (K = 16) and Z_bot
-                // (K = 32): the zero blocks are skipped and both warps do 384 packed FMAs per lane.
+                // level 32: rows 32..63 of the head get -M11^-1 M10 M00^-1 (see level32)
                 ok = group_sync(&bars->pair_sync[g], pair_uses, bars, p.status);
                 if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_PAIR, i);
-                const int m0 = g * C;
                 if (ok) {
-                    // Y part: rows yr + 8 rr (rr = 0..3) of all 32, columns 16 wp + 4 yc .. + 3
-                    const int yr = lane >> 2, yc = lane & 3;
-                    const int ycol = 16 * wp + 4 * yc;
-                    const int k0 = 16 * wp;        // rows of M00^-1 below the zero block of the column half
-                    float2 y[4][2];
-#pragma unroll
-                    for (int rr = 0; rr < 4; ++rr) y[rr][0] = y[rr][1] = make_float2(0.f, 0.f);
-                    uint32_t swz[8];
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) swz[kk] = (uint32_t)((ycol >> 2) ^ kk) << 4;
-#pragma unroll 1
-                    for (int kb = k0; kb < 32; kb += 8) {
-                        float av[4][8];
-#pragma unroll
-                        for (int rr = 0; rr < 4; ++rr) {
-                            const float4 a0 = *tm_vec(tm, m0 + 32 + yr + 8 * rr, kb);
-                            const float4 a1 = *tm_vec(tm, m0 + 32 + yr + 8 * rr, kb + 4);
-                            av[rr][0] = a0.x; av[rr][1] = a0.y; av[rr][2] = a0.z; av[rr][3] = a0.w;
-                            av[rr][4] = a1.x; av[rr][5] = a1.y; av[rr][6] = a1.z; av[rr][7] = a1.w;
-                        }
-                        const uint8_t *rowb = tm + (m0 + kb) * 128;
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const float4 bq = *reinterpret_cast<const float4 *>(rowb + kk * 128 + swz[kk]);
-                            const float2 b01 = make_float2(bq.x, bq.y), b23 = make_float2(bq.z, bq.w);
-#pragma unroll
-                            for (int rr = 0; rr < 4; ++rr) {
-                                const float2 ak = make_float2(av[rr][kk], av[rr][kk]);
-                                y[rr][0] = ffma2(ak, b01, y[rr][0]);
-                                y[rr][1] = ffma2(ak, b23, y[rr][1]);
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int rr = 0; rr < 4; ++rr)
-                        *tm_vec(ybuf32, yr + 8 * rr, ycol) = make_float4(y[rr][0].x, y[rr][0].y, y[rr][1].x, y[rr][1].y);
-                    ok = group_sync(&bars->pair_sync[g], pair_uses, bars, p.status);
-                }
-                if (ok) {
-                    // Z part: rows 16 wp + zr + 8 rr (rr = 0, 1), columns 8 zc .. 8 zc + 7; K runs over
-                    // the nonzero columns of those M11^-1 rows: 0..15 (wp 0) or 0..31 (wp 1)
-                    const int zr = lane >> 2, zc = lane & 3;
-                    const int kend = 16 + 16 * wp;
-                    float2 z[2][4];
-#pragma unroll
-                    for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) z[rr][e] = make_float2(0.f, 0.f);
-#pragma unroll 1
-                    for (int kb = 0; kb < kend; kb += 8) {
-                        float av[2][8];
-#pragma unroll
-                        for (int rr = 0; rr < 2; ++rr) {
-                            const int row = m0 + 32 + 16 * wp + zr + 8 * rr;
-                            const float4 a0 = *tm_vec(tm, row, 32 + kb);
-                            const float4 a1 = *tm_vec(tm, row, 32 + kb + 4);
-                            av[rr][0] = a0.x; av[rr][1] = a0.y; av[rr][2] = a0.z; av[rr][3] = a0.w;
-                            av[rr][4] = a1.x; av[rr][5] = a1.y; av[rr][6] = a1.z; av[rr][7] = a1.w;
-                        }
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const float4 b0 = *tm_vec(ybuf32, kb + kk, 8 * zc);
-                            const float4 b1 = *tm_vec(ybuf32, kb + kk, 8 * zc + 4);
-                            const float2 bb[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
-                                                  make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
-#pragma unroll
-                            for (int rr = 0; rr < 2; ++rr) {
-                                const float2 ak = make_float2(av[rr][kk], av[rr][kk]);
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) z[rr][e] = ffma2(ak, bb[e], z[rr][e]);
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int rr = 0; rr < 2; ++rr) {
-                        const int row = m0 + 32 + 16 * wp + zr + 8 * rr;
-                        *tm_vec(tm, row, 8 * zc) = make_float4(-z[rr][0].x, -z[rr][0].y, -z[rr][1].x, -z[rr][1].y);
-                        *tm_vec(tm, row, 8 * zc + 4) = make_float4(-z[rr][2].x, -z[rr][2].y, -z[rr][3].x, -z[rr][3].y);
-                    }
-                    fence_proxy_async_smem();
-                    ok = group_sync(&bars->pair_sync[g], pair_uses, bars, p.status);
+                    ok = level32(wp, tm, ybuf32, g * C, lane, &bars->pair_sync[g], pair_uses, bars, p.status);
                 }
             } else {
                 fence_proxy_async_smem();
