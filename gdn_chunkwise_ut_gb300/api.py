@@ -31,15 +31,31 @@ def _check(t: torch.Tensor, name: str, dtype, shape):
         raise ValueError(f"{name} must be contiguous")
 
 
+_WORKSPACES = {}
+
+
+def _workspace(device: torch.device) -> torch.Tensor:
+    """The per-device scratch buffer the default calls share (stream-ordered use)."""
+    key = (device.type, device.index)
+    ws = _WORKSPACES.get(key)
+    if ws is None:
+        ws = torch.zeros(_lib.KKT_WORKSPACE_BYTES // 4, dtype=torch.int32, device=device)
+        _WORKSPACES[key] = ws
+    return ws
+
+
 def kkt_solve_fwd(k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor, C: int,
                   cu_seqlens: torch.Tensor | None = None, *, T_out=None, W_out=None, U_out=None,
-                  kernel: str = "auto", stream=None):
+                  kernel: str = "auto", workspace="auto", stream=None):
     """UT transform of every chunk: returns (T_out, W, U).
 
     k [B, T, H, dk] and v [B, T, H, dv] (bf16, or fp32 for the fp32-I/O path),
     beta [B, T, H] fp32.  With ``cu_seqlens`` (int32 [N+1] on the device) the
     tensors are [1, T, H, .] and hold N packed sequences.  T_out is fp32
     [B, T, H, C]; W and U have k's dtype.  ``kernel`` is "auto", "simt" or "tc".
+    ``workspace``: "auto" uses a cached per-device scratch buffer (dynamic tile
+    scheduling; calls on concurrent streams should pass their own), a CUDA tensor
+    of at least KKT_WORKSPACE_BYTES, or None for the fixed round-robin schedule.
     """
     if k.dim() != 4 or v.dim() != 4 or beta.dim() != 3:
         raise ValueError("expected k [B,T,H,dk], v [B,T,H,dv], beta [B,T,H]")
@@ -73,9 +89,17 @@ def kkt_solve_fwd(k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor, C: int,
     kern = _lib.KERNELS.get(kernel)
     if kern is None:
         raise ValueError(f"kernel must be one of {sorted(_lib.KERNELS)}")
+    if isinstance(workspace, str) and workspace == "auto":
+        workspace = _workspace(dev)
+    if workspace is None:
+        ws_ptr, ws_bytes = None, 0
+    else:
+        if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda:
+            raise ValueError("workspace must be a CUDA tensor, 'auto' or None")
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     rc = _lib.lib().kkt_solve_fwd_ex(k.data_ptr(), v.data_ptr(), beta.data_ptr(), cu_ptr,
                                      B, T, H, dk, dv, C, T_out.data_ptr(), W_out.data_ptr(),
-                                     U_out.data_ptr(), io, kern, _stream_handle(stream))
+                                     U_out.data_ptr(), io, kern, ws_ptr, ws_bytes, _stream_handle(stream))
     if rc != _lib.KKT_OK:
         raise _lib.KktError(rc, "kkt_solve_fwd")
     return T_out, W_out, U_out

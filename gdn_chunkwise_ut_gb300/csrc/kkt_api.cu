@@ -52,8 +52,11 @@ extern "C" int kkt_select_kernel(int dk, int dv, int C, int io_dtype, int kernel
 extern "C" int kkt_solve_fwd_ex(const void *k, const void *v, const float *beta, const int32_t *cu_seqlens,
                                 int B, int T, int H, int dk, int dv, int C,
                                 float *T_out, void *W_out, void *U_out,
-                                int io_dtype, int kernel, struct CUstream_st *stream) {
+                                int io_dtype, int kernel, void *workspace, size_t workspace_bytes,
+                                struct CUstream_st *stream) {
     if (!k || !v || !beta || !T_out || !W_out || !U_out) return KKT_ERR_ARG;
+    if (workspace && workspace_bytes < KKT_WORKSPACE_BYTES) return KKT_ERR_ARG;
+    if (workspace && !aligned16(workspace)) return KKT_ERR_ALIGN;
     if (B < 1 || T < 0 || H < 1 || H > 65535) return KKT_ERR_ARG;
     const int which = kkt_select_kernel(dk, dv, C, io_dtype, kernel);
     if (which < 0) return -which;
@@ -77,8 +80,13 @@ extern "C" int kkt_solve_fwd_ex(const void *k, const void *v, const float *beta,
 #else
     p.trace = nullptr;
 #endif
+    p.tile_counter = nullptr;
     const int st = status_ptr(&p.status);
     if (st != KKT_OK) return st;
+    if (which == KKT_KERNEL_TC && workspace) {
+        if (cudaMemsetAsync(workspace, 0, sizeof(unsigned long long), p.stream) != cudaSuccess) return KKT_ERR_CUDA;
+        p.tile_counter = static_cast<unsigned long long *>(workspace);
+    }
     return which == KKT_KERNEL_TC ? kkt::launch_tc(p) : kkt::launch_simt(p);
 }
 
@@ -86,7 +94,7 @@ extern "C" int kkt_solve_fwd(const void *k, const void *v, const float *beta, co
                              int B, int T, int H, int dk, int dv, int C,
                              float *T_out, void *W_out, void *U_out, struct CUstream_st *stream) {
     return kkt_solve_fwd_ex(k, v, beta, cu_seqlens, B, T, H, dk, dv, C, T_out, W_out, U_out,
-                            KKT_IO_BF16, KKT_KERNEL_AUTO, stream);
+                            KKT_IO_BF16, KKT_KERNEL_AUTO, nullptr, 0, stream);
 }
 
 extern "C" int kkt_device_status(struct CUstream_st *stream) {

@@ -25,6 +25,7 @@ struct Problem {
     cudaStream_t stream;
     int *status;                // device status word of the current device
     void *trace;                // pipeline trace buffer (KKT_TRACE builds only), else nullptr
+    unsigned long long *tile_counter;  // zeroed work counter for dynamic scheduling, or nullptr
 };
 
 // Device-side error codes (first error wins).

@@ -115,6 +115,7 @@ struct TcParams {
     __nv_bfloat16 *W_out, *U_out;
     int *status;
     unsigned long long *trace;
+    unsigned long long *tile_counter;  // dynamic scheduling when not null (zeroed before the launch)
 };
 
 // ---- optional pipeline trace ------------------------------------------------------------------
@@ -343,9 +344,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         int i = 0;
         bool ok = true;
-        for (int64_t t = blockIdx.x; t < p.tiles; t += gridDim.x) {
-            const int64_t id = t / p.HG;
-            const int h0 = (int)(t % p.HG) * G;
+        // next tile: a fixed round robin, or claimed from the shared counter one tile ahead so
+        // that the atomic's round trip overlaps the current tile
+        auto claim = [&]() -> int64_t {
+            unsigned long long v = 0;
+            if (lane == 0) v = atomicAdd(p.tile_counter, 1ull);
+            return (int64_t)__shfl_sync(0xffffffffu, v, 0);
+        };
+        const bool dyn = p.tile_counter != nullptr;
+        int64_t t = dyn ? claim() : (int64_t)blockIdx.x;
+        for (; t < p.tiles;) {
+            const int64_t t_now = t;
+            t = dyn ? claim() : t + gridDim.x;
+            const int64_t id = t_now / p.HG;
+            const int h0 = (int)(t_now % p.HG) * G;
             if (h0 == 0 && id < p.nseq && lane == 0) check_sequence(p.cu, (int)id, p.nseq, p.ntok, p.status);
             Chunk ch;
             if (!map_chunk(id, p.cu, p.nseq, p.T, p.ntok, C, p.status, ch)) continue;
@@ -876,6 +888,7 @@ int launch_tc_t(const Problem &pb) {
     p.U_out = static_cast<__nv_bfloat16 *>(pb.U_out);
     p.status = pb.status;
     p.trace = static_cast<unsigned long long *>(pb.trace);
+    p.tile_counter = pb.tile_counter;
     auto kern = kkt_tc_kernel<C>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_BYTES) != cudaSuccess)
         return KKT_ERR_CUDA;

@@ -22,7 +22,7 @@ EVENTS = ["P_EMPTY", "P_ISSUE", "M_FULL", "M_GRAM", "M_EPI", "I_GRAM", "I_INV", 
 TRACE_CTAS, TRACE_TILES, TRACE_SLOTS = 160, 64, 16
 
 
-def run(workload: str, warmup: int = 3):
+def run(workload: str, warmup: int = 3, dynamic: bool = True):
     path = build.build(trace=True)
     lib = _lib.lib(path)
     lib.kkt_set_trace_buffer.argtypes = [ctypes.c_void_p]
@@ -35,13 +35,15 @@ def run(workload: str, warmup: int = 3):
     W = torch.empty_like(k)
     U = torch.empty_like(v)
     buf = torch.zeros(TRACE_CTAS * TRACE_TILES * TRACE_SLOTS, dtype=torch.int64, device="cuda")
+    ws = torch.zeros(_lib.KKT_WORKSPACE_BYTES // 4, dtype=torch.int32, device="cuda") if dynamic else None
     stream = torch.cuda.current_stream().cuda_stream
 
     def call():
         rc = lib.kkt_solve_fwd_ex(k.data_ptr(), v.data_ptr(), beta.data_ptr(),
                                   None if cu_t is None else cu_t.data_ptr(), B, k.shape[1], w.H, w.dk, w.dv,
                                   w.C, T_out.data_ptr(), W.data_ptr(), U.data_ptr(), _lib.KKT_IO_BF16,
-                                  _lib.KKT_KERNEL_TC, stream)
+                                  _lib.KKT_KERNEL_TC, None if ws is None else ws.data_ptr(),
+                                  0 if ws is None else ws.numel() * 4, stream)
         if rc != 0:
             raise _lib.KktError(rc, "kkt_solve_fwd_ex")
 
@@ -130,8 +132,9 @@ def main():
     ap.add_argument("--workload", default="c3_b4_t8192_h16")
     ap.add_argument("--ctas", type=int, default=2)
     ap.add_argument("--tiles", type=int, default=12)
+    ap.add_argument("--static", action="store_true", help="fixed round-robin schedule (no workspace)")
     a = ap.parse_args()
-    print(report(run(a.workload), a.ctas, a.tiles))
+    print(report(run(a.workload, dynamic=not a.static), a.ctas, a.tiles))
 
 
 if __name__ == "__main__":

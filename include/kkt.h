@@ -49,6 +49,7 @@
 #ifndef KKT_H_
 #define KKT_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -70,6 +71,9 @@ typedef enum kkt_status {
 
 /* I/O dtype of k, v, W_out, U_out (beta and T_out are always fp32). */
 enum { KKT_IO_BF16 = 0, KKT_IO_F32 = 1 };
+
+/* Minimum size of the optional workspace of kkt_solve_fwd_ex, in bytes. */
+#define KKT_WORKSPACE_BYTES 256
 
 /* Kernel selection for kkt_solve_fwd_ex. */
 enum {
@@ -95,11 +99,20 @@ int kkt_solve_fwd(const void *k, const void *v, const float *beta, const int32_t
  * KKT_IO_F32) and the kernel (KKT_KERNEL_*) chosen explicitly.  fp32 I/O runs
  * the SIMT kernel only; asking for KKT_KERNEL_TC with it, or with a shape the
  * tcgen05 kernel does not cover, returns KKT_ERR_UNSUPPORTED.
+ *
+ * workspace: NULL, or caller-owned device memory of at least
+ * KKT_WORKSPACE_BYTES (workspace_bytes), 16-byte aligned.  With it the
+ * tensor-core kernel hands out work dynamically (an atomic tile counter) instead
+ * of in a fixed round robin, which evens out SMs that run at different speeds.
+ * The call resets the counter on `stream` before its launch (a memset, no
+ * allocation); calls that may run at the same time need distinct workspaces.
+ * The contents are scratch and may be left in any state.
  */
 int kkt_solve_fwd_ex(const void *k, const void *v, const float *beta, const int32_t *cu_seqlens,
                      int B, int T, int H, int dk, int dv, int C,
                      float *T_out, void *W_out, void *U_out,
-                     int io_dtype, int kernel, struct CUstream_st *stream);
+                     int io_dtype, int kernel, void *workspace, size_t workspace_bytes,
+                     struct CUstream_st *stream);
 
 /*
  * kkt_device_status -- synchronises `stream`, then returns and clears the

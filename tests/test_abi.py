@@ -27,6 +27,12 @@ def declared_functions():
     return sorted(names)
 
 
+def test_workspace_size_constant_matches_header():
+    text = open(os.path.join(ROOT, "include", "kkt.h")).read()
+    m = re.search(r"#define\s+KKT_WORKSPACE_BYTES\s+(\d+)", text)
+    assert m and int(m.group(1)) == _lib.KKT_WORKSPACE_BYTES
+
+
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
     assert "kkt_solve_fwd" in names and "kkt_solve_fwd_ex" in names
@@ -67,11 +73,11 @@ def test_select_kernel(lib):
 
 def _call(lib, **kw):
     a = dict(k=0x1000, v=0x2000, beta=0x3000, cu=None, B=1, T=64, H=1, dk=128, dv=128, C=64,
-             T_out=0x4000, W_out=0x5000, U_out=0x6000, io=0, kernel=0, stream=None)
+             T_out=0x4000, W_out=0x5000, U_out=0x6000, io=0, kernel=0, ws=None, ws_bytes=0, stream=None)
     a.update(kw)
     return lib.kkt_solve_fwd_ex(a["k"], a["v"], a["beta"], a["cu"], a["B"], a["T"], a["H"], a["dk"],
                                 a["dv"], a["C"], a["T_out"], a["W_out"], a["U_out"], a["io"],
-                                a["kernel"], a["stream"])
+                                a["kernel"], a["ws"], a["ws_bytes"], a["stream"])
 
 
 def test_argument_errors_return_before_launch(lib):
@@ -90,6 +96,8 @@ def test_argument_errors_return_before_launch(lib):
     assert _call(lib, W_out=0x5004) == _lib.KKT_ERR_ALIGN
     assert _call(lib, cu=0x7002) == _lib.KKT_ERR_ALIGN
     assert _call(lib, beta=0x3002) == _lib.KKT_ERR_ALIGN
+    assert _call(lib, ws=0x8000, ws_bytes=_lib.KKT_WORKSPACE_BYTES - 1) == _lib.KKT_ERR_ARG
+    assert _call(lib, ws=0x8004, ws_bytes=_lib.KKT_WORKSPACE_BYTES) == _lib.KKT_ERR_ALIGN
     assert _call(lib, T=0) == _lib.KKT_OK               # empty batch: nothing to launch
     assert _call(lib, cu=0x7000, B=3, T=0) == _lib.KKT_OK
     assert lib.kkt_solve_fwd(None, 0x2000, 0x3000, None, 1, 64, 1, 128, 128, 64,
@@ -106,4 +114,4 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
 
 def test_ctypes_signature_arity():
     for name, (_, args) in _lib.SIGNATURES.items():
-        assert all(a in (ctypes.c_void_p, ctypes.c_int) for a in args), name
+        assert all(a in (ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t) for a in args), name

@@ -38,7 +38,7 @@ def _skip_unless(kernel, dk, dv, C, io="bf16"):
         pytest.skip(f"{kernel} kernel does not cover dk={dk} dv={dv} C={C} io={io}")
 
 
-def run(k, v, beta, C, cu=None, kernel="auto", poison=True):
+def run(k, v, beta, C, cu=None, kernel="auto", poison=True, workspace="auto"):
     """Calls the library with NaN-poisoned outputs; returns (T, W, U) on the device."""
     Bt, T, H, dk = k.shape
     dv = v.shape[-1]
@@ -46,7 +46,7 @@ def run(k, v, beta, C, cu=None, kernel="auto", poison=True):
     W = torch.full((Bt, T, H, dk), float("nan"), device=DEV, dtype=k.dtype)
     U = torch.full((Bt, T, H, dv), float("nan"), device=DEV, dtype=k.dtype)
     cu_t = None if cu is None else torch.as_tensor(np.asarray(cu), dtype=torch.int32, device=DEV)
-    kkt_solve_fwd(k, v, beta, C, cu_t, T_out=T_out, W_out=W, U_out=U, kernel=kernel)
+    kkt_solve_fwd(k, v, beta, C, cu_t, T_out=T_out, W_out=W, U_out=U, kernel=kernel, workspace=workspace)
     torch.cuda.synchronize()
     assert device_status() == 0
     return T_out, W, U
@@ -109,6 +109,20 @@ def test_small_varlen(kernel, C):
                     kernel=kernel)
         for x, y in zip(outs, alone):
             assert torch.equal(x[:, a:b], y)
+
+
+@pytest.mark.parametrize("C", [32, 64])
+def test_dynamic_and_static_schedules_agree(C):
+    """Tiles claimed from the workspace counter or dealt round robin: identical bits, and the
+    oracle agrees (odd head count: the last head group runs past H)."""
+    _skip_unless("tc", 128, 128, C)
+    k, v, beta = make_inputs(3, 1000, 5, 128, 128, seed=11, device=DEV)
+    dyn = run(k, v, beta, C, kernel="tc", workspace="auto")
+    sta = run(k, v, beta, C, kernel="tc", workspace=None)
+    own = run(k, v, beta, C, kernel="tc", workspace=torch.zeros(64, dtype=torch.int32, device=DEV))
+    for a, b, c in zip(dyn, sta, own):
+        assert torch.equal(a, b) and torch.equal(a, c)
+    full_compare(k, v, beta, C, None, dyn)
 
 
 # --- degenerate cases and traps -----------------------------------------------------------
