@@ -29,6 +29,7 @@ KKT_KERNEL_TC = 2
 KERNELS = {"auto": KKT_KERNEL_AUTO, "simt": KKT_KERNEL_SIMT, "tc": KKT_KERNEL_TC}
 
 KKT_WORKSPACE_BYTES = 256
+KKT_NOALLOC_SCRATCH_BYTES = 256
 
 _vp = ctypes.c_void_p
 _i = ctypes.c_int
@@ -37,6 +38,7 @@ _sz = ctypes.c_size_t
 SIGNATURES = {
     "kkt_solve_fwd": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
     "kkt_solve_fwd_ex": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _i, _i, _vp, _sz, _vp]),
+    "kkt_solve_fwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
     "kkt_device_status": (_i, [_vp]),
     "kkt_select_kernel": (_i, [_i, _i, _i, _i, _i]),
     "kkt_status_string": (ctypes.c_char_p, [_i]),

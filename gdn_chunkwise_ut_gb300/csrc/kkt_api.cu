@@ -14,6 +14,10 @@ __device__ int g_kkt_status = 0;
 constexpr int kMaxDevices = 64;
 int *g_status_ptr[kMaxDevices] = {};
 
+}  // namespace
+
+namespace kkt {
+
 int status_ptr(int **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KKT_ERR_NO_DEVICE;
@@ -25,6 +29,10 @@ int status_ptr(int **out) {
     *out = g_status_ptr[dev];
     return KKT_OK;
 }
+
+}  // namespace kkt
+
+namespace {
 
 #ifdef KKT_TRACE
 void *g_trace = nullptr;
@@ -81,7 +89,7 @@ extern "C" int kkt_solve_fwd_ex(const void *k, const void *v, const float *beta,
     p.trace = nullptr;
 #endif
     p.tile_counter = nullptr;
-    const int st = status_ptr(&p.status);
+    const int st = kkt::status_ptr(&p.status);
     if (st != KKT_OK) return st;
     if (which == KKT_KERNEL_TC && workspace) {
         if (cudaMemsetAsync(workspace, 0, sizeof(unsigned long long), p.stream) != cudaSuccess) return KKT_ERR_CUDA;

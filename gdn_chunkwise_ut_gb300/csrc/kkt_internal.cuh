@@ -93,6 +93,9 @@ __device__ __forceinline__ void check_sequence(const int32_t *cu, int s, int nse
     if (bad) record_error(status, KKT_ERR_SEQLENS);
 }
 
+// Address of the current device's status word (looked up once per device).
+int status_ptr(int **out);
+
 int launch_simt(const Problem &p);
 int launch_tc(const Problem &p);
 bool tc_supports(int dk, int dv, int C, int io);

@@ -114,6 +114,38 @@ int kkt_solve_fwd_ex(const void *k, const void *v, const float *beta, const int3
                      int io_dtype, int kernel, void *workspace, size_t workspace_bytes,
                      struct CUstream_st *stream);
 
+/* Size of the scratch array compiled into the library for kkt_solve_fwd_noalloc. */
+#define KKT_NOALLOC_SCRATCH_BYTES 256
+
+/*
+ * kkt_solve_fwd_noalloc -- kkt_solve_fwd for callers that cannot allocate.
+ * The pages have no counterpart to this entry point; it is a deployment aid.
+ *
+ * Some callers may not allocate device memory at all: code that runs under a
+ * framework which has already handed every byte of the GPU to its own caching
+ * allocator, plug-ins and custom operators that receive only their inputs and
+ * outputs, and serving loops where a cudaMalloc would synchronise the device and
+ * stall other work.  kkt_solve_fwd_ex needs a caller-provided workspace for the
+ * tensor-core kernel's work counter; this entry point uses instead a
+ * KKT_NOALLOC_SCRATCH_BYTES array compiled into the library (one per device,
+ * kept by every GPU that loads the library until the process exits), so it
+ * allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *
+ *   Arguments, layouts, ownership and errors: as kkt_solve_fwd (bf16 I/O), run
+ *   on the tensor-core kernel only.  Shapes that kernel does not cover
+ *   (d_k, d_v != 128, C = 128) return KKT_ERR_UNSUPPORTED; a problem that would
+ *   need more scratch than the array holds returns KKT_ERR_ARG (a call needs
+ *   8 bytes, one 64-bit counter, whatever the problem size).
+ *   The first call on a device looks up the array's device address (with that
+ *   device current); make that first call before any stream capture.
+ *   Every call shares the array and resets the counter on `stream` before its
+ *   launch; calls whose work overlaps on the GPU (other streams, other host
+ *   threads) race on it and must be serialised by the caller.
+ */
+int kkt_solve_fwd_noalloc(const void *k, const void *v, const float *beta, const int32_t *cu_seqlens,
+                          int B, int T, int H, int dk, int dv, int C,
+                          float *T_out, void *W_out, void *U_out, struct CUstream_st *stream);
+
 /*
  * kkt_device_status -- synchronises `stream`, then returns and clears the
  * status word of the current device: KKT_OK, or the first device-side error
