@@ -41,7 +41,8 @@ DEFAULT_WORKLOAD = "c3_b4_t8192_h16"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
-KERNEL_SOURCES = {"simt": ["kkt_simt.cu"], "tc": ["kkt_tc.cu"]}
+KERNEL_SOURCES = {"simt": ["kkt_simt.cu", "kkt_internal.cuh"],
+                  "tc": ["kkt_tc.cu", "sm100_ptx.cuh", "kkt_internal.cuh"]}
 
 
 def parse_args():
@@ -165,7 +166,7 @@ def hbm_peak():
 
 def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES[kernel] + ["kkt_internal.cuh"]:
+    for name in KERNEL_SOURCES[kernel]:
         h.update((ROOT / "gdn_chunkwise_ut_gb300" / "csrc" / name).read_bytes())
     return h.hexdigest()[:16]
 
