@@ -605,19 +605,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_LD, i);
 
             // diagonal 16 x 16 blocks (§2.1), one column per lane: right-looking substitution,
-            // s[k] <- s[k] - L[k][m] x_m once x_m = s[m] is final; L is read as broadcasts
+            // s[k] <- s[k] - L[k][m] x_m once x_m = s[m] is final.  L is read four columns at a
+            // time (one 16-byte chunk per row) before the four steps that use them.
+
             {
                 const int c = lane & 15;
-                const int rb = 32 * wp + 16 * (lane >> 4);  // first row / column of the block in the head
-                const int mb = g * C + rb;                  // its tile row
+                const int rb = 32 * wp + 16 * (lane >> 4);
+                const int mb = g * C + rb;
                 float sc[16];
 #pragma unroll
                 for (int k = 0; k < 16; ++k) sc[k] = (k == c) ? 1.f : 0.f;
 #pragma unroll
-                for (int ms = 0; ms < 15; ++ms) {
-                    const float xm = sc[ms];
+                for (int m0s = 0; m0s < 16; m0s += 4) {
+                    float4 lk[16];
 #pragma unroll
-                    for (int k = ms + 1; k < 16; ++k) sc[k] = fmaf(-*tm_elem(tm, mb + k, rb + ms), xm, sc[k]);
+                    for (int k = m0s + 1; k < 16; ++k) lk[k] = *tm_vec(tm, mb + k, rb + m0s);
+#pragma unroll
+                    for (int d = 0; d < 4; ++d) {
+                        const int ms = m0s + d;
+                        if (ms < 15) {
+                            const float xm = sc[ms];
+#pragma unroll
+                            for (int k = ms + 1; k < 16; ++k) {
+                                const float l = d == 0 ? lk[k].x : d == 1 ? lk[k].y : d == 2 ? lk[k].z : lk[k].w;
+                                sc[k] = fmaf(-l, xm, sc[k]);
+                            }
+                        }
+                    }
                 }
                 __syncwarp();
 #pragma unroll
