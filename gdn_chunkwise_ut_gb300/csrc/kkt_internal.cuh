@@ -28,9 +28,9 @@ struct Problem {
     unsigned long long *tile_counter;  // zeroed work counter for dynamic scheduling, or nullptr
 };
 
-// Device-side error codes (first error wins).
+// Device-side error codes (first error wins); a null status records nothing.
 __device__ __forceinline__ void record_error(int *status, int code) {
-    atomicCAS(status, 0, code);
+    if (status) atomicCAS(status, 0, code);
 }
 
 // Work ids and chunks.  Sequence s owns the ids [Q(s), Q(s+1)) with

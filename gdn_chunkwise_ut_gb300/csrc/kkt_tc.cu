@@ -121,20 +121,35 @@ struct TcParams {
 // ---- optional pipeline trace ------------------------------------------------------------------
 enum TraceEvent {
     EV_P_EMPTY = 0, EV_P_ISSUE, EV_M_FULL, EV_M_GRAM, EV_M_EPI, EV_I_GRAM, EV_I_INV, EV_I_TSTORE,
-    EV_I_TT, EV_E_DFULL, EV_E_DEMPTY, EV_E_DONE, EV_I_LD, EV_I_DIAG, EV_I_C16, EV_I_PAIR, EV_COUNT
+    EV_I_TT, EV_E_DFULL, EV_E_DEMPTY, EV_E_DONE, EV_I_LD, EV_I_DIAG, EV_I_C16, EV_I_PAIR, EV_M_LATE,
+    EV_M_READY, EV_I_BW, EV_I_TTW, EV_COUNT
 };
 constexpr int kTraceCtas = 160;
-constexpr int kTraceTiles = 64;
-constexpr int kTraceSlots = 16;
+constexpr int kTraceTiles = 64;  // the last tile row holds the CTA's clock calibration
+constexpr int kTraceSlots = 24;
+static_assert(EV_COUNT <= kTraceSlots, "trace slots");
 #ifdef KKT_TRACE
+// SM cycle counter at each event; trace.py maps it to ns with the (globaltimer, clock) pairs that
+// thread 0 records at the start and end of the CTA
 #define KKT_TRACE_EVENT(ev, tile)                                                                        \
     do {                                                                                               \
-        if (p.trace && blockIdx.x < kTraceCtas && (tile) < kTraceTiles)                                \
-            p.trace[((size_t)blockIdx.x * kTraceTiles + (tile)) * kTraceSlots + (ev)] = globaltimer_ns(); \
+        if (p.trace && blockIdx.x < kTraceCtas && (tile) < kTraceTiles - 1)                            \
+            p.trace[((size_t)blockIdx.x * kTraceTiles + (tile)) * kTraceSlots + (ev)] = clock64();      \
+    } while (0)
+#define KKT_TRACE_CALIB(slot)                                                                            \
+    do {                                                                                               \
+        if (p.trace && blockIdx.x < kTraceCtas && threadIdx.x == 0) {                                  \
+            unsigned long long *c = p.trace + ((size_t)blockIdx.x * kTraceTiles + kTraceTiles - 1) * kTraceSlots; \
+            c[2 * (slot)] = globaltimer_ns();                                                          \
+            c[2 * (slot) + 1] = clock64();                                                             \
+        }                                                                                              \
     } while (0)
 #else
 #define KKT_TRACE_EVENT(ev, tile) \
     do {                          \
+    } while (0)
+#define KKT_TRACE_CALIB(slot) \
+    do {                      \
     } while (0)
 #endif
 
@@ -335,6 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+    KKT_TRACE_CALIB(0);
 
     if (warp == kWarpProducer) {
         // ------------------------------------------------------------------ producer
@@ -487,6 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ready) {
                     const int s = e_next % kNS;
                     if (lane == 0) {
+                        KKT_TRACE_EVENT(EV_M_READY, e_next);
                         bars->einfo[e_next & 1] = *stage_info(s);
                         mbar_arrive(&bars->einfo_full[e_next & 1]);
                         tc_fence_after();
@@ -575,6 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // this warp's previous T store has read its rows of the T buffer
             if (lane == 0) bulk_wait_read<0>();
             __syncwarp();
+            if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_BW, i);
             // Gram row -> row of A = I + strictLower(diag(beta) S) (beta on rows, unit diagonal,
             // §3.2) into the T buffer; columns above 32 (wp + 1) stay zero
             {
@@ -725,6 +743,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // T~ = T diag(beta), split into bf16 hi + lo, into tensor memory (A operand)
             if (!wait_bar(&bars->tt_empty, ((uint32_t)i & 1u) ^ 1u, bars, p.status)) break;
             tc_fence_after();
+            if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_TTW, i);
             {
                 uint32_t hi[16], lo[16];
 #pragma unroll
@@ -834,6 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    KKT_TRACE_CALIB(1);
     if (warp == kWarpMma) tmem_dealloc(tmem, kTmemCols);
 }
 

@@ -2,7 +2,9 @@
 
 Builds libkkt_trace.so (the same sources compiled with -DKKT_TRACE), runs one
 workload and prints, for the first CTAs, when each role reached each event of
-every tile (microseconds from the CTA's first event), plus per-role averages:
+every tile (microseconds from the CTA's first event), plus per-role averages.
+Events are SM cycle counts, mapped to the global timer with the pairs of
+(global timer, cycle count) that each CTA records at its start and end.
 
     python -m gdn_chunkwise_ut_gb300.trace [--workload c3_b4_t8192_h16] [--ctas 2] [--tiles 12]
 """
@@ -18,8 +20,8 @@ from . import _lib, build
 from .inputs import workloads
 
 EVENTS = ["P_EMPTY", "P_ISSUE", "M_FULL", "M_GRAM", "M_EPI", "I_GRAM", "I_INV", "I_TSTORE", "I_TT",
-          "E_DFULL", "E_DEMPTY", "E_DONE", "I_LD", "I_DIAG", "I_C16", "I_PAIR"]
-TRACE_CTAS, TRACE_TILES, TRACE_SLOTS = 160, 64, 16
+          "E_DFULL", "E_DEMPTY", "E_DONE", "I_LD", "I_DIAG", "I_C16", "I_PAIR", "M_LATE", "M_READY", "I_BW", "I_TTW"]
+TRACE_CTAS, TRACE_TILES, TRACE_SLOTS = 160, 64, 24
 
 
 def run(workload: str, warmup: int = 3, dynamic: bool = True):
@@ -49,52 +51,80 @@ def run(workload: str, warmup: int = 3, dynamic: bool = True):
 
     for _ in range(warmup):
         call()
+    # untraced launches of the trace build, timed with CUDA events on the launching stream
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 20
+    torch.cuda.synchronize()
+    ev0.record()
+    for _ in range(reps):
+        call()
+    ev1.record()
+    torch.cuda.synchronize()
+    run.last_ms = ev0.elapsed_time(ev1) / reps
     lib.kkt_set_trace_buffer(buf.data_ptr())
     call()
     torch.cuda.synchronize()
     lib.kkt_set_trace_buffer(None)
-    return buf.cpu().numpy().reshape(TRACE_CTAS, TRACE_TILES, TRACE_SLOTS)[:, :, :len(EVENTS)]
+    raw = buf.cpu().numpy().reshape(TRACE_CTAS, TRACE_TILES, TRACE_SLOTS)
+    run.last_raw = raw
+    return to_ns(raw)
+
+
+def to_ns(raw: np.ndarray) -> np.ndarray:
+    """Cycle counts -> global-timer ns per CTA (NaN where an event was not recorded)."""
+    cal = raw[:, -1, :4].astype(np.float64)  # g0, c0, g1, c1
+    ev = raw[:, :-1, :len(EVENTS)].astype(np.float64)
+    out = np.full(ev.shape, np.nan)
+    for b in range(raw.shape[0]):
+        g0, c0, g1, c1 = cal[b]
+        if c1 <= c0 or g1 <= g0:
+            continue
+        ns_per_clk = (g1 - g0) / (c1 - c0)
+        ok = ev[b] > 0
+        out[b][ok] = g0 + (ev[b][ok] - c0) * ns_per_clk
+    return out
 
 
 def report(tr: np.ndarray, ctas: int, tiles: int) -> str:
     lines = []
+    shown = EVENTS[:12] + ["M_LATE", "M_READY"]
+    idx = [EVENTS.index(e) for e in shown]
     for b in range(ctas):
-        t = tr[b].astype(np.float64)
-        valid = t > 0
-        if not valid.any():
+        t = tr[b]
+        if not np.isfinite(t).any():
             continue
-        t0 = t[valid].min()
-        us = np.where(valid, (t - t0) / 1e3, np.nan)
+        us = (t - np.nanmin(t)) / 1e3
         lines.append(f"CTA {b} (us from its first event)")
-        lines.append("tile " + " ".join(f"{e:>9s}" for e in EVENTS[:12]))
+        lines.append("tile " + " ".join(f"{e:>9s}" for e in shown))
         for i in range(min(tiles, us.shape[0])):
             if not np.isfinite(us[i]).any():
                 break
-            lines.append(f"{i:4d} " + " ".join(f"{x:9.2f}" if np.isfinite(x) else f"{'':9s}" for x in us[i][:12]))
+            lines.append(f"{i:4d} " + " ".join(f"{us[i][k]:9.2f}" if np.isfinite(us[i][k]) else f"{'':9s}" for k in idx))
     # averages over all traced CTAs and tiles (steady state: skip the first two tiles)
-    t = tr.astype(np.float64)
+    t = tr
     ev = {e: i for i, e in enumerate(EVENTS)}
 
-    def span(a, b_):
-        x = t[:, 2:, ev[b_]] - t[:, 2:, ev[a]]
-        ok = (t[:, 2:, ev[a]] > 0) & (t[:, 2:, ev[b_]] > 0)
-        return float(np.mean(x[ok])) / 1e3 if ok.any() else float("nan")
+    def span(a, b_, shift=0):
+        """mean of event b_ of tile i + shift minus event a of tile i"""
+        x = t[:, 2:t.shape[1] - shift, ev[b_]] if shift == 0 else t[:, 2 + shift:, ev[b_]]
+        y = t[:, 2:t.shape[1] - shift, ev[a]]
+        d = x - y
+        return float(np.nanmean(d)) / 1e3 if np.isfinite(d).any() else float("nan")
 
     def period(e):
-        x = np.diff(t[:, :, ev[e]], axis=1)
-        ok = (t[:, 1:, ev[e]] > 0) & (t[:, :-1, ev[e]] > 0)
-        return float(np.mean(x[:, 1:][ok[:, 1:]])) / 1e3 if ok[:, 1:].any() else float("nan")
+        x = np.diff(t[:, 2:, ev[e]], axis=1)
+        return float(np.nanmean(x)) / 1e3 if np.isfinite(x).any() else float("nan")
 
     # whole grid: first event and last epilogue completion per CTA
     starts, ends, ntiles = [], [], []
     for b in range(t.shape[0]):
         tb = t[b]
-        if not (tb > 0).any():
+        if not np.isfinite(tb).any():
             continue
-        starts.append(tb[tb > 0].min())
+        starts.append(np.nanmin(tb))
         done = tb[:, ev["E_DONE"]]
-        ends.append(done[done > 0].max() if (done > 0).any() else np.nan)
-        ntiles.append(int((done > 0).sum()))
+        ends.append(np.nanmax(done) if np.isfinite(done).any() else np.nan)
+        ntiles.append(int(np.isfinite(done).sum()))
     if starts:
         g0 = min(starts)
         st = (np.array(starts) - g0) / 1e3
@@ -107,23 +137,32 @@ def report(tr: np.ndarray, ctas: int, tiles: int) -> str:
         for k_ in sorted(set(nt.tolist())):
             sel = nt == k_
             lines.append(f"  CTAs with {k_} tiles: {sel.sum()}, end {np.nanmin(en[sel]):.2f}..{np.nanmax(en[sel]):.2f} us")
+    rows = [
+        ("period per tile (M_EPI to M_EPI)", period("M_EPI")),
+        ("K load: issue -> landed", span("P_ISSUE", "M_FULL")),
+        ("stage empty wait -> loads issued", span("P_EMPTY", "P_ISSUE")),
+        ("landed -> Gram issued", span("M_FULL", "M_GRAM")),
+        ("Gram issued -> inverse starts", span("M_GRAM", "I_GRAM")),
+        ("inverse: Gram ready -> T~ written", span("I_GRAM", "I_TT")),
+        ("  wait for the previous T store to read", span("I_GRAM", "I_BW")),
+        ("  Gram row load + L row", span("I_BW", "I_LD")),
+        ("  16x16 diagonal substitution", span("I_LD", "I_DIAG")),
+        ("  level-16 coupling", span("I_DIAG", "I_C16")),
+        ("  pair sync", span("I_C16", "I_PAIR")),
+        ("  level-32 coupling", span("I_PAIR", "I_INV")),
+        ("  T store", span("I_INV", "I_TSTORE")),
+        ("  wait T~ free", span("I_TSTORE", "I_TTW")),
+        ("  write T~", span("I_TTW", "I_TT")),
+        ("T~ written -> W|U MMA ready", span("I_TT", "M_READY")),
+        ("W|U MMA ready -> issued", span("M_READY", "M_EPI")),
+        ("W|U MMA issued -> epilogue starts", span("M_EPI", "E_DFULL")),
+        ("epilogue: D loads", span("E_DFULL", "E_DEMPTY")),
+        ("epilogue: total", span("E_DFULL", "E_DONE")),
+        ("D drained -> next W|U MMA ready", span("E_DEMPTY", "M_READY", shift=1)),
+    ]
     lines.append("")
-    lines.append(f"period per tile (M_EPI to M_EPI)         {period('M_EPI'):7.2f} us")
-    lines.append(f"load: issue -> landed (P_ISSUE->M_FULL)  {span('P_ISSUE', 'M_FULL'):7.2f} us")
-    lines.append(f"inverse: Gram ready -> T~ written        {span('I_GRAM', 'I_TT'):7.2f} us")
-    lines.append(f"  Gram row load + L row                  {span('I_GRAM', 'I_LD'):7.2f} us")
-    lines.append(f"  16x16 diagonal substitution            {span('I_LD', 'I_DIAG'):7.2f} us")
-    lines.append(f"  level-16 coupling                      {span('I_DIAG', 'I_C16'):7.2f} us")
-    lines.append(f"  pair sync                              {span('I_C16', 'I_PAIR'):7.2f} us")
-    lines.append(f"  level-32 coupling                      {span('I_PAIR', 'I_INV'):7.2f} us")
-    lines.append(f"  T store                                {span('I_INV', 'I_TSTORE'):7.2f} us")
-    lines.append(f"  wait T~ free + write T~                {span('I_TSTORE', 'I_TT'):7.2f} us")
-    lines.append(f"Gram issued -> inverse starts            {span('M_GRAM', 'I_GRAM'):7.2f} us")
-    lines.append(f"T~ written -> W|U MMA issued             {span('I_TT', 'M_EPI'):7.2f} us")
-    lines.append(f"W|U MMA issued -> epilogue starts        {span('M_EPI', 'E_DFULL'):7.2f} us")
-    lines.append(f"epilogue: D loads                        {span('E_DFULL', 'E_DEMPTY'):7.2f} us")
-    lines.append(f"epilogue: total                          {span('E_DFULL', 'E_DONE'):7.2f} us")
-    lines.append(f"stage empty wait -> issue                {span('P_EMPTY', 'P_ISSUE'):7.2f} us")
+    for name, val in rows:
+        lines.append(f"{name:42s} {val:7.2f} us")
     return "\n".join(lines)
 
 
@@ -133,8 +172,13 @@ def main():
     ap.add_argument("--ctas", type=int, default=2)
     ap.add_argument("--tiles", type=int, default=12)
     ap.add_argument("--static", action="store_true", help="fixed round-robin schedule (no workspace)")
+    ap.add_argument("--save", default=None, help="also save the raw cycle counts (.npy)")
     a = ap.parse_args()
-    print(report(run(a.workload, dynamic=not a.static), a.ctas, a.tiles))
+    tr = run(a.workload, dynamic=not a.static)
+    print(f"untraced launch of the trace build: {run.last_ms * 1e3:.1f} us")
+    print(report(tr, a.ctas, a.tiles))
+    if a.save:
+        np.save(a.save, run.last_raw)
 
 
 if __name__ == "__main__":
