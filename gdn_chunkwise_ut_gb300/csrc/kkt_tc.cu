@@ -80,13 +80,16 @@ struct Cfg {
     static constexpr int META_BYTES = 1024;
     static constexpr int T_HALVES = C / 32;                   // 128-byte column blocks of a T row
     static constexpr int OFF_T = OFF_META + kNS * META_BYTES; // T of the tile: [half][128 rows][128 B]
-    static constexpr int OFF_WU = OFF_T + T_HALVES * 16384;   // 2 x 4 KB per epilogue warp
-    static constexpr int OFF_XCH = OFF_WU + 4 * 8192;         // coupling products: 4 x [16][16] fp32,
-    static constexpr int XCH_BYTES = 4096 + ((C >= 64) ? G * 4096 : 0);  // + G x [32][32] fp32
+    // W / U~ staging per epilogue warp: two 4 KB buffers, one at C = 128 (whose T takes 64 KB)
+    static constexpr int WU_BUFS = C == 128 ? 1 : 2;
+    static constexpr int OFF_WU = OFF_T + T_HALVES * 16384;
+    static constexpr int OFF_XCH = OFF_WU + 4 * WU_BUFS * 4096;  // coupling products: 4 x [16][16] fp32,
+    static constexpr int XCH_BYTES = 4096 + ((C >= 64) ? 2 * 4096 : 0);  // + 2 x [32][32] fp32
     static constexpr int OFF_BAR = OFF_XCH + XCH_BYTES;
     static constexpr int BAR_BYTES = 512;
     static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
     static constexpr uint32_t TX_BYTES = G * 4 * C * 128;           // K + V boxes of one stage
+    static_assert(SMEM_BYTES <= 232448, "shared memory over the per-block limit");
 };
 
 struct Barriers {
@@ -97,7 +100,8 @@ struct Barriers {
     uint64_t d_full, d_empty;
     uint64_t einfo_full[2];
     uint64_t mma_final;
-    uint64_t pair_sync[2];   // the two warps of one head (C = 64)
+    uint64_t pair_sync[2];   // warps 2p and 2p + 1: one 64-row block (C = 64, 128)
+    uint64_t quad_sync;      // all four inverse warps (C = 128)
     TileInfo einfo[2];       // tile info for the epilogue warps, written by the MMA warp
     uint32_t tmem_base;
     int abort_flag;
@@ -246,14 +250,16 @@ __device__ __forceinline__ void tile4x4_fma(float2 (&y)[4][2], const uint8_t *co
     }
 }
 
-// Level-32 coupling of one head (rows m0 .. m0 + 63 of the tile's T buffer) for warp WP (0 or 1)
-// of its two warps.  With 16 x 16 blocks M00^-1 = [[A, 0], [Cb, D]], M10 = [P, Q],
-// M11^-1 = [[A', 0], [Cb', D']]:  Y = M10 M00^-1 = [P A + Q Cb, Q D] and
-// Z = M11^-1 Y = [A' Y_top ; Cb' Y_top + D' Y_bot].  Warp 0 computes Y_left (K = 32) and Z_top
-// (K = 16), warp 1 Y_right (K = 16) and Z_bot (K = 32): the zero blocks are skipped and both
-// warps do 384 packed FMAs per lane.  Rows 32..63, columns 0..31 of the head receive -Z.
-__device__ __forceinline__ bool level32(const int WP, uint8_t *tm, uint8_t *ybuf32, int m0, int lane,
+// Level-32 coupling of one 64 x 64 diagonal block (rows m0 .. m0 + 63, columns c0 .. c0 + 63 of
+// the chunk, in the tile's T buffer) for warp WP (0 or 1) of its two warps.  With 16 x 16 blocks
+// M00^-1 = [[A, 0], [Cb, D]], M10 = [P, Q], M11^-1 = [[A', 0], [Cb', D']]:
+// Y = M10 M00^-1 = [P A + Q Cb, Q D] and Z = M11^-1 Y = [A' Y_top ; Cb' Y_top + D' Y_bot].
+// Warp 0 computes Y_left (K = 32) and Z_top (K = 16), warp 1 Y_right (K = 16) and Z_bot (K = 32):
+// the zero blocks are skipped and both warps do 384 packed FMAs per lane.  Rows 32..63, columns
+// 0..31 of the block receive -Z.
+__device__ __forceinline__ bool level32(const int WP, uint8_t *tm, uint8_t *ybuf32, int m0, int c0, int lane,
                                         uint64_t *pair_bar, uint32_t &pair_uses, Barriers *bars, int *status) {
+    uint8_t *th = tm + (c0 >> 5) * 16384;  // the 32-column half holding the block's first columns
     {
         // Y part: rows yr + 8 rr of 32, columns 16 WP + 4 yc .. + 3; k in [16 WP, 32)
         const int yr = lane >> 2, yc = lane & 3;
@@ -261,7 +267,7 @@ __device__ __forceinline__ bool level32(const int WP, uint8_t *tm, uint8_t *ybuf
         uint32_t axor[4];
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr) {
-            arow[rr] = tm + (m0 + 32 + yr + 8 * rr) * 128;
+            arow[rr] = th + (m0 + 32 + yr + 8 * rr) * 128;
             axor[rr] = (uint32_t)(yr & 7) << 4;
         }
         uint32_t bsw[8];
@@ -270,7 +276,7 @@ __device__ __forceinline__ bool level32(const int WP, uint8_t *tm, uint8_t *ybuf
         float2 y[4][2];
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr) y[rr][0] = y[rr][1] = make_float2(0.f, 0.f);
-        tile4x4_fma(y, arow, axor, 16 * WP, tm + (m0 + 16 * WP) * 128, bsw, 4 - 2 * WP);
+        tile4x4_fma(y, arow, axor, 16 * WP, th + (m0 + 16 * WP) * 128, bsw, 4 - 2 * WP);
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr)
             *tm_vec(ybuf32, yr + 8 * rr, 16 * WP + 4 * yc) = make_float4(y[rr][0].x, y[rr][0].y, y[rr][1].x, y[rr][1].y);
@@ -284,7 +290,7 @@ __device__ __forceinline__ bool level32(const int WP, uint8_t *tm, uint8_t *ybuf
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr) {
             const int row = m0 + 32 + 16 * WP + zr + 4 * rr;
-            arow[rr] = tm + 16384 + row * 128;  // columns 32..63 of the head: the second half
+            arow[rr] = th + 16384 + row * 128;  // columns 32..63 of the block: the next half
             axor[rr] = (uint32_t)(row & 7) << 4;
         }
         uint32_t bsw[8];
@@ -296,11 +302,82 @@ __device__ __forceinline__ bool level32(const int WP, uint8_t *tm, uint8_t *ybuf
         tile4x4_fma(z, arow, axor, 0, ybuf32, bsw, 2 + 2 * WP);
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr)
-            *tm_vec(tm, m0 + 32 + 16 * WP + zr + 4 * rr, 4 * zc) =
+            *tm_vec(tm, m0 + 32 + 16 * WP + zr + 4 * rr, c0 + 4 * zc) =
                 make_float4(-z[rr][0].x, -z[rr][0].y, -z[rr][1].x, -z[rr][1].y);
     }
     fence_proxy_async_smem();
     return group_sync(pair_bar, pair_uses, bars, status);
+}
+
+// Level-64 coupling of a 128-token chunk (C = 128; the tile's rows are the chunk's rows), split
+// over the four inverse warps by columns (§2.2): rows 64..127, columns 0..63 receive
+// -Z = -M11^-1 M10 M00^-1 with 64 x 64 blocks M00^-1 = T[0..63][0..63], M11^-1 = T[64..][64..],
+// M10 = L[64..][0..63].  Warp w computes columns 16w .. 16w + 15 of Y = M10 M00^-1 and of
+// Z = M11^-1 Y; a column of Z needs only the same column of Y, so Y is produced and consumed by
+// one warp.  Zero blocks are skipped: columns >= 32 of M00^-1 vanish above row 32, and rows < 32 of
+// M11^-1 vanish beyond column 32.  Y is kept in rows 0..63, columns 64..127 (zero in T) and
+// cleared again by the warp that wrote it.  Lane: rows yr + 8 rr (+ 32 for the lower row group),
+// columns 16w + 4 yc .. + 3.
+__device__ __forceinline__ bool level64(const int w, uint8_t *tm, int lane, uint64_t *quad_bar, uint32_t &uses,
+                                        Barriers *bars, int *status) {
+    const int yr = lane >> 2, yc = lane & 3;
+    const int cj = 16 * w + 4 * yc;                              // this lane's first column (0..63)
+    const uint32_t axor = (uint32_t)(yr & 7) << 4;               // swizzle phase of every A row used
+    uint32_t bsw[8];
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) bsw[kk] = (uint32_t)(((cj & 31) >> 2) ^ kk) << 4;
+    const uint32_t axr[4] = {axor, axor, axor, axor};
+    // Y = M10 M00^-1, rows 32 rg .. 32 rg + 31 of Y (chunk rows 64 + 32 rg + ...)
+#pragma unroll 1
+    for (int rg = 0; rg < 2; ++rg) {
+        float2 y[4][2];
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) y[rr][0] = y[rr][1] = make_float2(0.f, 0.f);
+        const uint8_t *brow = tm + (cj >> 5) * 16384;  // M00^-1, the half of columns cj
+#pragma unroll 1
+        for (int kh = (w < 2 ? 0 : 1); kh < 2; ++kh) {  // k in [32 kh, 32 kh + 32)
+            const uint8_t *arow[4];
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) arow[rr] = tm + kh * 16384 + (64 + 32 * rg + yr + 8 * rr) * 128;
+            tile4x4_fma(y, arow, axr, 0, brow + 32 * kh * 128, bsw, 4);
+        }
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr)
+            *tm_vec(tm, 32 * rg + yr + 8 * rr, 64 + cj) = make_float4(y[rr][0].x, y[rr][0].y, y[rr][1].x, y[rr][1].y);
+    }
+    __syncwarp();
+    // Z = M11^-1 Y, both row groups kept in registers until every warp has read M10
+    float2 z[2][4][2];
+#pragma unroll
+    for (int rg = 0; rg < 2; ++rg)
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) z[rg][rr][0] = z[rg][rr][1] = make_float2(0.f, 0.f);
+    const uint8_t *ybrow = tm + (2 + (cj >> 5)) * 16384;  // Y, the half of columns 64 + cj
+#pragma unroll
+    for (int rg = 0; rg < 2; ++rg) {
+#pragma unroll 1
+        for (int kh = 0; kh <= rg; ++kh) {  // rows < 32 of M11^-1: k < 32 only
+            const uint8_t *arow[4];
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) arow[rr] = tm + (2 + kh) * 16384 + (64 + 32 * rg + yr + 8 * rr) * 128;
+            tile4x4_fma(z[rg], arow, axr, 0, ybrow + 32 * kh * 128, bsw, 4);
+        }
+    }
+    // every warp has read M10: overwrite it with -Z, and clear this warp's Y columns
+    if (!group_sync(quad_bar, uses, bars, status)) return false;
+#pragma unroll
+    for (int rg = 0; rg < 2; ++rg)
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr)
+            *tm_vec(tm, 64 + 32 * rg + yr + 8 * rr, cj) =
+                make_float4(-z[rg][rr][0].x, -z[rg][rr][0].y, -z[rg][rr][1].x, -z[rg][rr][1].y);
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int c4 = 0; c4 < 16; c4 += 4)
+            *tm_vec(tm, lane + 32 * h, 64 + 16 * w + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
+    fence_proxy_async_smem();
+    return group_sync(quad_bar, uses, bars, status);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -339,6 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->mma_final, 1);
         mbar_init(&bars->pair_sync[0], 64);
         mbar_init(&bars->pair_sync[1], 64);
+        mbar_init(&bars->quad_sync, 128);
         bars->abort_flag = 0;
         fence_mbar_init();
     }
@@ -563,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         uint8_t *tm = smem + CF::OFF_T;     // the tile's T, [half][128 rows][128 B], 128-byte swizzle
         float *ybuf16 = reinterpret_cast<float *>(smem + CF::OFF_XCH) + q * 256;           // [16][16]
-        uint8_t *ybuf32 = smem + CF::OFF_XCH + 4096 + g * 4096;   // [32][32] fp32, 128-byte rows, swizzled
+        uint8_t *ybuf32 = smem + CF::OFF_XCH + 4096 + (q >> 1) * 4096;  // [32][32] fp32, 128-byte rows, swizzled
         // zero this lane's T~ columns (other heads' blocks and the upper triangle stay zero)
         // and its row of T (the upper triangle stays zero there too)
         {
@@ -577,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < C; j += 4) *tm_vec(tm, m, j) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         int i = 0;
-        uint32_t pair_uses = 0;
+        uint32_t pair_uses = 0, quad_uses = 0;
         while (true) {
             const int s = i % kNS;
             if (!wait_bar(&bars->full[s], (uint32_t)(i / kNS) & 1u, bars, p.status)) break;
@@ -595,7 +673,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_BW, i);
             // Gram row -> row of A = I + strictLower(diag(beta) S) (beta on rows, unit diagonal,
             // §3.2) into the T buffer; columns above 32 (wp + 1) stay zero
-            {
+            if constexpr (C == 128) {
+                // up to four 32-column blocks: one tensor-memory load at a time
+#pragma unroll 1
+                for (int h = 0; h <= wp; ++h) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_base + kColGram + 32 * h, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4) {
+                        float e[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int j = 32 * h + c + u;
+                            e[u] = (j < r) ? beta_r * __uint_as_float(v[c + u]) : (j == r ? 1.f : 0.f);
+                        }
+                        *tm_vec(tm, m, 32 * h + c) = make_float4(e[0], e[1], e[2], e[3]);
+                    }
+                }
+            } else {
                 uint32_t v[CF::T_HALVES][32];
 #pragma unroll
                 for (int h = 0; h < CF::T_HALVES; ++h)
@@ -712,11 +808,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             bool ok = true;
             if constexpr (C >= 64) {
-                // level 32: rows 32..63 of the head get -M11^-1 M10 M00^-1 (see level32)
-                ok = group_sync(&bars->pair_sync[g], pair_uses, bars, p.status);
+                // level 32 in each 64-row block (a head at C = 64, half the chunk at C = 128): its
+                // rows 32..63 get -M11^-1 M10 M00^-1 (see level32)
+                const int pr = q >> 1;
+                ok = group_sync(&bars->pair_sync[pr], pair_uses, bars, p.status);
                 if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_PAIR, i);
                 if (ok) {
-                    ok = level32(wp, tm, ybuf32, g * C, lane, &bars->pair_sync[g], pair_uses, bars, p.status);
+                    ok = level32(wp & 1, tm, ybuf32, 64 * pr, C == 128 ? 64 * pr : 0, lane, &bars->pair_sync[pr],
+                                 pair_uses, bars, p.status);
+                }
+                if constexpr (C == 128) {
+                    // level 64: rows 64..127 of the chunk (see level64)
+                    if (ok) ok = group_sync(&bars->quad_sync, quad_uses, bars, p.status);
+                    if (ok) ok = level64(q, tm, lane, &bars->quad_sync, quad_uses, bars, p.status);
                 }
             } else {
                 fence_proxy_async_smem();
@@ -746,7 +850,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_TTW, i);
             {
                 uint32_t hi[16], lo[16];
-#pragma unroll
+#pragma unroll(C == 128 ? 1 : CF::T_HALVES)
                 for (int blk = 0; blk < CF::T_HALVES; ++blk) {
                     if (blk <= wp) {
 #pragma unroll
@@ -787,7 +891,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = m % C;
         const int wp = r / 32;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        uint8_t *wstage = smem + CF::OFF_WU + q * 8192;   // 2 buffers x [32 rows][128 B]
+        uint8_t *wstage = smem + CF::OFF_WU + q * CF::WU_BUFS * 4096;  // WU_BUFS x [32 rows][128 B]
         int i = 0;
         uint32_t nstore = 0;  // TMA store groups issued by this warp
         while (true) {
@@ -821,8 +925,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pk[16 + e] = pack_bf16(__uint_as_float(v1[2 * e]), __uint_as_float(v1[2 * e + 1]));
                 }
                 if (warp_full) {
-                    uint8_t *buf = wstage + (nstore & 1u) * 4096;
-                    if (lane == 0) bulk_wait_read<1>();
+                    uint8_t *buf = wstage + (nstore % CF::WU_BUFS) * 4096;
+                    if (lane == 0) bulk_wait_read<CF::WU_BUFS - 1>();
                     __syncwarp();
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
@@ -936,13 +1040,14 @@ int launch_tc_t(const Problem &pb) {
 }  // namespace
 
 bool tc_supports(int dk, int dv, int C, int io) {
-    return io == KKT_IO_BF16 && dk == 128 && dv == 128 && (C == 32 || C == 64);
+    return io == KKT_IO_BF16 && dk == 128 && dv == 128 && (C == 32 || C == 64 || C == 128);
 }
 
 int launch_tc(const Problem &p) {
     switch (p.C) {
         case 32: return launch_tc_t<32>(p);
         case 64: return launch_tc_t<64>(p);
+        case 128: return launch_tc_t<128>(p);
         default: return KKT_ERR_UNSUPPORTED;
     }
 }

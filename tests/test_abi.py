@@ -66,6 +66,8 @@ def test_select_kernel(lib):
     assert sel(128, 128, 64, 7, 0) == -_lib.KKT_ERR_ARG
     assert sel(128, 128, 64, _lib.KKT_IO_BF16, 9) == -_lib.KKT_ERR_ARG
     for C in (32, 64, 128):
+        # the tensor-core kernel covers bf16 with dk = dv = 128 at every chunk size
+        assert sel(128, 128, C, _lib.KKT_IO_BF16, _lib.KKT_KERNEL_AUTO) == _lib.KKT_KERNEL_TC
         for dk in (64, 128):
             for dv in (64, 128):
                 assert sel(dk, dv, C, _lib.KKT_IO_BF16, 0) in (_lib.KKT_KERNEL_SIMT, _lib.KKT_KERNEL_TC)

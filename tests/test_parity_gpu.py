@@ -111,7 +111,7 @@ def test_small_varlen(kernel, C):
             assert torch.equal(x[:, a:b], y)
 
 
-@pytest.mark.parametrize("C", [32, 64])
+@pytest.mark.parametrize("C", [32, 64, 128])
 def test_dynamic_and_static_schedules_agree(C):
     """Tiles claimed from the workspace counter or dealt round robin: identical bits, and the
     oracle agrees (odd head count: the last head group runs past H)."""
