@@ -221,11 +221,13 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
 // row 0 of the k range (its row index a multiple of 8), bsw[kk] the byte offset of this lane's
 // 16-byte column chunk in a row with phase kk.
 // A loop over 8-k blocks rather than an unrolled sequence: the kernel is sensitive to its
-// instruction-cache footprint, so the code size of this inner product is kept small.
+// instruction-cache footprint, so the code size of this inner product is kept small (UNROLL
+// blocks per iteration: 1 at C <= 64, 2 at C = 128, where the longer level-64 products gain).
+template <int UNROLL>
 __device__ __forceinline__ void tile4x4_fma(float2 (&y)[4][2], const uint8_t *const (&arow)[4],
                                          const uint32_t (&axor)[4], int acol0, const uint8_t *brow0,
                                          const uint32_t (&bsw)[8], int nkb) {
-#pragma unroll 1
+#pragma unroll UNROLL
     for (int kb = 0; kb < nkb; ++kb) {
         float av[4][8];
         const uint32_t ca = (uint32_t)((acol0 >> 2) + 2 * kb) << 4;
@@ -257,6 +259,7 @@ __device__ __forceinline__ void tile4x4_fma(float2 (&y)[4][2], const uint8_t *co
 // Warp 0 computes Y_left (K = 32) and Z_top (K = 16), warp 1 Y_right (K = 16) and Z_bot (K = 32):
 // the zero blocks are skipped and both warps do 384 packed FMAs per lane.  Rows 32..63, columns
 // 0..31 of the block receive -Z.
+template <int UNROLL>
 __device__ __forceinline__ bool level32(const int WP, uint8_t *tm, uint8_t *ybuf32, int m0, int c0, int lane,
                                         uint64_t *pair_bar, uint32_t &pair_uses, Barriers *bars, int *status) {
     uint8_t *th = tm + (c0 >> 5) * 16384;  // the 32-column half holding the block's first columns
@@ -276,7 +279,7 @@ __device__ __forceinline__ bool level32(const int WP, uint8_t *tm, uint8_t *ybuf
         float2 y[4][2];
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr) y[rr][0] = y[rr][1] = make_float2(0.f, 0.f);
-        tile4x4_fma(y, arow, axor, 16 * WP, th + (m0 + 16 * WP) * 128, bsw, 4 - 2 * WP);
+        tile4x4_fma<UNROLL>(y, arow, axor, 16 * WP, th + (m0 + 16 * WP) * 128, bsw, 4 - 2 * WP);
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr)
             *tm_vec(ybuf32, yr + 8 * rr, 16 * WP + 4 * yc) = make_float4(y[rr][0].x, y[rr][0].y, y[rr][1].x, y[rr][1].y);
@@ -299,7 +302,7 @@ __device__ __forceinline__ bool level32(const int WP, uint8_t *tm, uint8_t *ybuf
         float2 z[4][2];
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr) z[rr][0] = z[rr][1] = make_float2(0.f, 0.f);
-        tile4x4_fma(z, arow, axor, 0, ybuf32, bsw, 2 + 2 * WP);
+        tile4x4_fma<UNROLL>(z, arow, axor, 0, ybuf32, bsw, 2 + 2 * WP);
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr)
             *tm_vec(tm, m0 + 32 + 16 * WP + zr + 4 * rr, c0 + 4 * zc) =
@@ -339,7 +342,7 @@ __device__ __forceinline__ bool level64(const int w, uint8_t *tm, int lane, uint
             const uint8_t *arow[4];
 #pragma unroll
             for (int rr = 0; rr < 4; ++rr) arow[rr] = tm + kh * 16384 + (64 + 32 * rg + yr + 8 * rr) * 128;
-            tile4x4_fma(y, arow, axr, 0, brow + 32 * kh * 128, bsw, 4);
+            tile4x4_fma<2>(y, arow, axr, 0, brow + 32 * kh * 128, bsw, 4);
         }
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr)
@@ -360,7 +363,7 @@ __device__ __forceinline__ bool level64(const int w, uint8_t *tm, int lane, uint
             const uint8_t *arow[4];
 #pragma unroll
             for (int rr = 0; rr < 4; ++rr) arow[rr] = tm + (2 + kh) * 16384 + (64 + 32 * rg + yr + 8 * rr) * 128;
-            tile4x4_fma(z[rg], arow, axr, 0, ybrow + 32 * kh * 128, bsw, 4);
+            tile4x4_fma<2>(z[rg], arow, axr, 0, ybrow + 32 * kh * 128, bsw, 4);
         }
     }
     // every warp has read M10: overwrite it with -Z, and clear this warp's Y columns
@@ -814,8 +817,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = group_sync(&bars->pair_sync[pr], pair_uses, bars, p.status);
                 if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_PAIR, i);
                 if (ok) {
-                    ok = level32(wp & 1, tm, ybuf32, 64 * pr, C == 128 ? 64 * pr : 0, lane, &bars->pair_sync[pr],
-                                 pair_uses, bars, p.status);
+                    ok = level32<C == 128 ? 2 : 1>(wp & 1, tm, ybuf32, 64 * pr, C == 128 ? 64 * pr : 0, lane,
+                                                   &bars->pair_sync[pr], pair_uses, bars, p.status);
                 }
                 if constexpr (C == 128) {
                     // level 64: rows 64..127 of the chunk (see level64)
