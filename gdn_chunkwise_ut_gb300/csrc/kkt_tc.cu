@@ -22,10 +22,11 @@
 //                   substitution, one column per lane, so the dependency chain
 //                   is 15 FMAs (§2.1; in-place, with the L values read before
 //                   any column is written back, §3.4); coupling
-//                   -L11^-1 L10 L00^-1 at s = 16 (inside a warp) and s = 32
-//                   (the two warps of a head) as register-tiled shared-memory
-//                   GEMMs with L10 consumed before it is overwritten (§2.2,
-//                   §3.5).  Each warp TMA-stores its 32 rows of T from that
+//                   -L11^-1 L10 L00^-1 at s = 16 (inside a warp), s = 32 (the
+//                   two warps of a 64-row block) and, at C = 128, s = 64 (all
+//                   four warps, split by columns) as register-tiled shared-
+//                   memory GEMMs with L10 consumed before it is overwritten
+//                   (§2.2, §3.5).  Each warp TMA-stores its 32 rows of T from that
 //                   buffer, and writes its rows of T~ = T diag(beta) as a bf16
 //                   hi / lo pair into tensor memory (tcgen05.st).
 //   epilogue warps  per warp: tcgen05.ld of its 32 rows of D, bf16 conversion,

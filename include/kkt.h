@@ -133,7 +133,7 @@ int kkt_solve_fwd_ex(const void *k, const void *v, const float *beta, const int3
  *
  *   Arguments, layouts, ownership and errors: as kkt_solve_fwd (bf16 I/O), run
  *   on the tensor-core kernel only.  Shapes that kernel does not cover
- *   (d_k, d_v != 128, C = 128) return KKT_ERR_UNSUPPORTED; a problem that would
+ *   (d_k or d_v other than 128) return KKT_ERR_UNSUPPORTED; a problem that would
  *   need more scratch than the array holds returns KKT_ERR_ARG (a call needs
  *   8 bytes, one 64-bit counter, whatever the problem size).
  *   The first call on a device looks up the array's device address (with that
