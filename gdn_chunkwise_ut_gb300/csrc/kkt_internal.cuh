@@ -26,6 +26,7 @@ struct Problem {
     int *status;                // device status word of the current device
     void *trace;                // pipeline trace buffer (KKT_TRACE builds only), else nullptr
     unsigned long long *tile_counter;  // zeroed work counter for dynamic scheduling, or nullptr
+    int stall_first_tile = 0;   // test hook: the tensor-core kernel never fills its first stage
 };
 
 // Device-side error codes (first error wins); a null status records nothing.

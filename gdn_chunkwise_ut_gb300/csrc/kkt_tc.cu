@@ -121,6 +121,7 @@ struct TcParams {
     int *status;
     unsigned long long *trace;
     unsigned long long *tile_counter;  // dynamic scheduling when not null (zeroed before the launch)
+    int stall_first_tile;              // test hook: every CTA skips the loads of its first tile
 };
 
 // ---- optional pipeline trace ------------------------------------------------------------------
@@ -459,6 +460,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (h0 == 0 && id < p.nseq && lane == 0) check_sequence(p.cu, (int)id, p.nseq, p.ntok, p.status);
             Chunk ch;
             if (!map_chunk(id, p.cu, p.nseq, p.T, p.ntok, C, p.status, ch)) continue;
+            if (p.stall_first_tile && i == 0) {
+                // test hook: stage 0 is never filled, so every wait on it runs out (failure detection)
+                ++i;
+                continue;
+            }
             // beta of the tile (G x C values, 4 per lane), loaded before waiting for the stage
             float bv[4];
 #pragma unroll
@@ -1031,6 +1037,7 @@ int launch_tc_t(const Problem &pb) {
     p.status = pb.status;
     p.trace = static_cast<unsigned long long *>(pb.trace);
     p.tile_counter = pb.tile_counter;
+    p.stall_first_tile = pb.stall_first_tile;
     auto kern = kkt_tc_kernel<C>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_BYTES) != cudaSuccess)
         return KKT_ERR_CUDA;

@@ -1,0 +1,41 @@
+/*
+ * kkt_test.h -- test hooks of libkkt.  Not part of the solve API: these entry points
+ * exist so that tests can drive code paths that correct inputs never reach.
+ */
+#ifndef KKT_TEST_H
+#define KKT_TEST_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "kkt.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * kkt_test_stalled_solve -- failure detection of the tensor-core kernel.
+ *
+ * Arguments, layouts, ownership and validation: as kkt_solve_fwd (bf16 I/O, shapes the
+ * tensor-core kernel covers; others return KKT_ERR_UNSUPPORTED).  The kernel is launched
+ * with the fixed round-robin schedule and with one deliberate omission: no CTA loads the
+ * shared-memory stage of its first tile, so the barrier that stage would complete never
+ * completes.  Every wait in the kernel is bounded (2 s), so the roles waiting on it give up,
+ * record KKT_ERR_TIMEOUT in the device status word, stop the other roles of their CTA, wait
+ * for their own copies and tensor-core work in flight, free tensor memory and return.  No
+ * fault, trap or unbounded wait is involved and the context stays usable.
+ *
+ * Returns KKT_OK when the launch was made (the timeout is reported by kkt_device_status
+ * after the kernel ends, about two seconds later).  The contents of T_out, W_out and U_out
+ * are unspecified afterwards.
+ */
+int kkt_test_stalled_solve(const void *k, const void *v, const float *beta, const int32_t *cu_seqlens,
+                           int B, int T, int H, int dk, int dv, int C,
+                           float *T_out, void *W_out, void *U_out, struct CUstream_st *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KKT_TEST_H */
