@@ -77,16 +77,14 @@ template <int C>
 struct Cfg {
     static constexpr int G = 128 / C;                         // heads per tile
     static constexpr int KV_BYTES = 65536;                    // K 32 KB + V 32 KB, [box][row][128 B]
-    static constexpr int OFF_META = kNS * KV_BYTES;           // per stage: beta[128] + TileInfo
-    static constexpr int META_BYTES = 1024;
+    static constexpr int META_BYTES = 544;                    // beta[128] + TileInfo (at byte 512)
     static constexpr int T_HALVES = C / 32;                   // 128-byte column blocks of a T row
-    static constexpr int OFF_T = OFF_META + kNS * META_BYTES; // T of the tile: [half][128 rows][128 B]
+    static constexpr int OFF_T = kNS * KV_BYTES;              // T of the tile: [half][128 rows][128 B]
     // W / U~ staging per epilogue warp: two 4 KB buffers, one at C = 128 (whose T takes 64 KB)
     static constexpr int WU_BUFS = C == 128 ? 1 : 2;
     static constexpr int OFF_WU = OFF_T + T_HALVES * 16384;
-    static constexpr int OFF_XCH = OFF_WU + 4 * WU_BUFS * 4096;  // coupling products: 4 x [16][16] fp32,
-    static constexpr int XCH_BYTES = 4096 + ((C >= 64) ? 2 * 4096 : 0);  // + 2 x [32][32] fp32
-    static constexpr int OFF_BAR = OFF_XCH + XCH_BYTES;
+    static constexpr int OFF_META = OFF_WU + 4 * WU_BUFS * 4096;  // per stage: beta[128] + TileInfo
+    static constexpr int OFF_BAR = OFF_META + kNS * META_BYTES;
     static constexpr int BAR_BYTES = 512;
     static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
     static constexpr uint32_t TX_BYTES = G * 4 * C * 128;           // K + V boxes of one stage
@@ -260,7 +258,8 @@ __device__ __forceinline__ void tile4x4_fma(float2 (&y)[4][2], const uint8_t *co
 // Y = M10 M00^-1 = [P A + Q Cb, Q D] and Z = M11^-1 Y = [A' Y_top ; Cb' Y_top + D' Y_bot].
 // Warp 0 computes Y_left (K = 32) and Z_top (K = 16), warp 1 Y_right (K = 16) and Z_bot (K = 32):
 // the zero blocks are skipped and both warps do 384 packed FMAs per lane.  Rows 32..63, columns
-// 0..31 of the block receive -Z.
+// 0..31 of the block receive -Z.  ybuf32 points at row 0 of the block's upper-right 32 x 32 (rows
+// 0..31, columns 32..63 of the block, zero in T), which holds Y and is cleared again at the end.
 template <int UNROLL>
 __device__ __forceinline__ bool level32(const int WP, uint8_t *tm, uint8_t *ybuf32, int m0, int c0, int lane,
                                         uint64_t *pair_bar, uint32_t &pair_uses, Barriers *bars, int *status) {
@@ -310,8 +309,15 @@ __device__ __forceinline__ bool level32(const int WP, uint8_t *tm, uint8_t *ybuf
             *tm_vec(tm, m0 + 32 + 16 * WP + zr + 4 * rr, c0 + 4 * zc) =
                 make_float4(-z[rr][0].x, -z[rr][0].y, -z[rr][1].x, -z[rr][1].y);
     }
+    if (!group_sync(pair_bar, pair_uses, bars, status)) return false;
+    if (WP == 0) {
+        // ybuf32 is the block's upper-right 32 x 32, zero in T: clear it again
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) *tm_vec(ybuf32, lane, j) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     fence_proxy_async_smem();
-    return group_sync(pair_bar, pair_uses, bars, status);
+    __syncwarp();
+    return true;
 }
 
 // Level-64 coupling of a 128-token chunk (C = 128; the tile's rows are the chunk's rows), split
@@ -650,8 +656,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int wp = r / 32;              // warp position within the head (0 for C = 32)
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         uint8_t *tm = smem + CF::OFF_T;     // the tile's T, [half][128 rows][128 B], 128-byte swizzle
-        float *ybuf16 = reinterpret_cast<float *>(smem + CF::OFF_XCH) + q * 256;           // [16][16]
-        uint8_t *ybuf32 = smem + CF::OFF_XCH + 4096 + (q >> 1) * 4096;  // [32][32] fp32, 128-byte rows, swizzled
+        // level-32 product Y: the upper-right 32 x 32 of this warp's 64-row block (zero in T)
+        uint8_t *ybuf32 = tm + (((C == 128 ? 64 * (q >> 1) : 0) + 32) >> 5) * 16384 + 64 * (q >> 1) * 128;
         // zero this lane's T~ columns (other heads' blocks and the upper triangle stay zero)
         // and its row of T (the upper triangle stays zero there too)
         {
@@ -765,7 +771,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_DIAG, i);
 
             // level 16 (§2.2): the warp's two diagonal blocks, T10 = -X11 (L10 X00); lane -> row
-            // i of the 16 x 16 result, columns jb .. jb + 7
+            // i of the 16 x 16 result, columns jb .. jb + 7.  Y = L10 X00 is kept in the block's
+            // upper-right 16 x 16 (rows m0 .. m0 + 15, columns c0 + 16 .. c0 + 31), zero in T and
+            // cleared again once read.
             {
                 const int ii = lane >> 1;
                 const int jb = (lane & 1) * 8;
@@ -790,8 +798,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     y[2] = ffma2(ak, make_float2(b1.x, b1.y), y[2]);
                     y[3] = ffma2(ak, make_float2(b1.z, b1.w), y[3]);
                 }
-                *reinterpret_cast<float4 *>(ybuf16 + ii * 16 + jb) = make_float4(y[0].x, y[0].y, y[1].x, y[1].y);
-                *reinterpret_cast<float4 *>(ybuf16 + ii * 16 + jb + 4) = make_float4(y[2].x, y[2].y, y[3].x, y[3].y);
+                *tm_vec(tm, m0 + ii, c0 + 16 + jb) = make_float4(y[0].x, y[0].y, y[1].x, y[1].y);
+                *tm_vec(tm, m0 + ii, c0 + 16 + jb + 4) = make_float4(y[2].x, y[2].y, y[3].x, y[3].y);
 #pragma unroll
                 for (int k = 0; k < 16; k += 4) {
                     const float4 t4 = *tm_vec(tm, m0 + 16 + ii, c0 + 16 + k);
@@ -802,8 +810,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < 4; ++e) y[e] = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
-                    const float4 b0 = *reinterpret_cast<const float4 *>(ybuf16 + k * 16 + jb);
-                    const float4 b1 = *reinterpret_cast<const float4 *>(ybuf16 + k * 16 + jb + 4);
+                    const float4 b0 = *tm_vec(tm, m0 + k, c0 + 16 + jb);
+                    const float4 b1 = *tm_vec(tm, m0 + k, c0 + 16 + jb + 4);
                     const float2 ak = make_float2(a[k], a[k]);
                     y[0] = ffma2(ak, make_float2(b0.x, b0.y), y[0]);
                     y[1] = ffma2(ak, make_float2(b0.z, b0.w), y[1]);
@@ -813,6 +821,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *tm_vec(tm, m0 + 16 + ii, c0 + jb) = make_float4(-y[0].x, -y[0].y, -y[1].x, -y[1].y);
                 *tm_vec(tm, m0 + 16 + ii, c0 + jb + 4) = make_float4(-y[2].x, -y[2].y, -y[3].x, -y[3].y);
                 __syncwarp();
+                *tm_vec(tm, m0 + ii, c0 + 16 + jb) = make_float4(0.f, 0.f, 0.f, 0.f);
+                *tm_vec(tm, m0 + ii, c0 + 16 + jb + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
             }
             if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_C16, i);
 
