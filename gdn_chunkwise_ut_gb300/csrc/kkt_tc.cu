@@ -201,6 +201,19 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
+// Packed fp32 product of a pair (one f32x2 instruction): a * b, elementwise.
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
 // Packed fp32 FMA on a pair (one f32x2 instruction): a * b + c, elementwise.
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
     float2 d;
@@ -213,6 +226,16 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
         : "=f"(d.x), "=f"(d.y)
         : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
     return d;
+}
+
+// bf16 hi + lo split of a pair, packed as two bf16x2 words: hi = bf16(x), lo = bf16(x - hi)
+// (the difference is exact in fp32).
+__device__ __forceinline__ void split_bf16(float2 x, uint32_t &hi, uint32_t &lo) {
+    const uint32_t h = pack_bf16(x.x, x.y);
+    const float2 hf = make_float2(__uint_as_float(h << 16), __uint_as_float(h & 0xffff0000u));
+    hi = h;
+    const float2 r = ffma2(hf, make_float2(-1.f, -1.f), x);
+    lo = pack_bf16(r.x, r.y);
 }
 
 // D (4 x 4 tile, as 4 rows x 2 packed pairs) += A B over NKB blocks of 8 k.  A rows: byte pointers to
@@ -715,15 +738,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_ld();
 #pragma unroll
                 for (int h = 0; h < CF::T_HALVES; ++h) {
-                    if (h <= wp) {
+                    if (h < wp) {
+                        // the whole block lies below the diagonal (columns < 32 wp <= r): beta scale only
+                        const float2 bb = make_float2(beta_r, beta_r);
+#pragma unroll
+                        for (int c = 0; c < 32; c += 4) {
+                            const float2 e0 = fmul2(make_float2(__uint_as_float(v[h][c]), __uint_as_float(v[h][c + 1])), bb);
+                            const float2 e1 = fmul2(make_float2(__uint_as_float(v[h][c + 2]), __uint_as_float(v[h][c + 3])), bb);
+                            *tm_vec(tm, m, 32 * h + c) = make_float4(e0.x, e0.y, e1.x, e1.y);
+                        }
+                    } else if (h == wp) {
+                        // the diagonal block: column 32 h + cc is below the diagonal when cc < lane
 #pragma unroll
                         for (int c = 0; c < 32; c += 4) {
                             float e[4];
 #pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                const int j = 32 * h + c + u;
-                                e[u] = (j < r) ? beta_r * __uint_as_float(v[h][c + u]) : (j == r ? 1.f : 0.f);
-                            }
+                            for (int u = 0; u < 4; ++u)
+                                e[u] = (c + u < lane) ? beta_r * __uint_as_float(v[h][c + u]) : (c + u == lane ? 1.f : 0.f);
                             *tm_vec(tm, m, 32 * h + c) = make_float4(e[0], e[1], e[2], e[3]);
                         }
                     }
@@ -877,14 +908,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int c = 0; c < 32; c += 4) {
                             const float4 t4 = *tm_vec(tm, m, 32 * blk + c);
                             const float4 b4 = *reinterpret_cast<const float4 *>(sb + 32 * blk + c);
-                            const float v4[4] = {t4.x * b4.x, t4.y * b4.y, t4.z * b4.z, t4.w * b4.w};
-#pragma unroll
-                            for (int u = 0; u < 2; ++u) {
-                                const float a = v4[2 * u], b = v4[2 * u + 1];
-                                const uint32_t h = pack_bf16(a, b);
-                                hi[c / 2 + u] = h;
-                                lo[c / 2 + u] = pack_bf16(a - __uint_as_float(h << 16), b - __uint_as_float(h & 0xffff0000u));
-                            }
+                            split_bf16(fmul2(make_float2(t4.x, t4.y), make_float2(b4.x, b4.y)), hi[c / 2], lo[c / 2]);
+                            split_bf16(fmul2(make_float2(t4.z, t4.w), make_float2(b4.z, b4.w)), hi[c / 2 + 1], lo[c / 2 + 1]);
                         }
                         const uint32_t col = (uint32_t)(g * C + 32 * blk) / 2;
                         tmem_st16(tmem + lane_base + kColTT + col, hi);
