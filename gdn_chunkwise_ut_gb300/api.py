@@ -55,7 +55,8 @@ def kkt_solve_fwd(k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor, C: int,
     [B, T, H, C]; W and U have k's dtype.  ``kernel`` is "auto", "simt" or "tc".
     ``workspace``: "auto" uses a cached per-device scratch buffer (dynamic tile
     scheduling; calls on concurrent streams should pass their own), a CUDA tensor
-    of at least KKT_WORKSPACE_BYTES, or None for the fixed round-robin schedule.
+    of at least KKT_WORKSPACE_BYTES, zero-filled before its first use (every call
+    leaves it zero), or None for the fixed round-robin schedule.
     """
     if k.dim() != 4 or v.dim() != 4 or beta.dim() != 3:
         raise ValueError("expected k [B,T,H,dk], v [B,T,H,dv], beta [B,T,H]")

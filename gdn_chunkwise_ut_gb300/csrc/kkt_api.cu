@@ -91,10 +91,8 @@ extern "C" int kkt_solve_fwd_ex(const void *k, const void *v, const float *beta,
     p.tile_counter = nullptr;
     const int st = kkt::status_ptr(&p.status);
     if (st != KKT_OK) return st;
-    if (which == KKT_KERNEL_TC && workspace) {
-        if (cudaMemsetAsync(workspace, 0, sizeof(unsigned long long), p.stream) != cudaSuccess) return KKT_ERR_CUDA;
-        p.tile_counter = static_cast<unsigned long long *>(workspace);
-    }
+    // the workspace is zero on entry (zero-filled before first use, and left zero by every call)
+    if (which == KKT_KERNEL_TC && workspace) p.tile_counter = static_cast<unsigned long long *>(workspace);
     return which == KKT_KERNEL_TC ? kkt::launch_tc(p) : kkt::launch_simt(p);
 }
 

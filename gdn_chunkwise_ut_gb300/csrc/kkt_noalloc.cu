@@ -12,13 +12,13 @@
 namespace {
 
 // The scratch of kkt_solve_fwd_noalloc: one array per device, held by every GPU
-// that loads the library until the process exits.  The call uses its first
-// 8 bytes (the tile counter) and clears them before each launch.
+// that loads the library until the process exits.  A call uses its first 16
+// bytes (the tile counter and the count of CTAs done claiming): zero when the
+// module loads, and left zero by every call's kernel.
 __device__ __align__(256) unsigned char g_noalloc_scratch[KKT_NOALLOC_SCRATCH_BYTES];
 
-// Bytes of scratch one call needs: a single 64-bit tile counter, whatever the
-// problem size.
-constexpr size_t kNoallocNeed = sizeof(unsigned long long);
+// Bytes of scratch one call needs: two 64-bit counters, whatever the problem size.
+constexpr size_t kNoallocNeed = 2 * sizeof(unsigned long long);
 static_assert(kNoallocNeed <= KKT_NOALLOC_SCRATCH_BYTES, "scratch array too small");
 
 constexpr int kMaxDevices = 64;
@@ -71,7 +71,7 @@ extern "C" int kkt_solve_fwd_noalloc(const void *k, const void *v, const float *
     if (st != KKT_OK) return st;
     st = noalloc_scratch(&p.tile_counter);
     if (st != KKT_OK) return st;
-    // the counter must start at zero; the array keeps whatever the last call left
-    if (cudaMemsetAsync(p.tile_counter, 0, kNoallocNeed, p.stream) != cudaSuccess) return KKT_ERR_CUDA;
+    // the counters start at zero: zero-initialised with the module, and cleared by the last CTA of
+    // every earlier call
     return kkt::launch_tc(p);
 }

@@ -118,7 +118,8 @@ struct TcParams {
     __nv_bfloat16 *W_out, *U_out;
     int *status;
     unsigned long long *trace;
-    unsigned long long *tile_counter;  // dynamic scheduling when not null (zeroed before the launch)
+    unsigned long long *tile_counter;  // dynamic scheduling when not null: [0] tiles claimed, [1] CTAs done
+                                       // claiming; zero at launch, left zero by the last CTA
     int stall_first_tile;              // test hook: every CTA skips the loads of its first tile
 };
 
@@ -462,6 +463,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+    // The next call on the stream may be scheduled now: its CTAs take SMs as this grid's CTAs leave
+    // them and run their set-up meanwhile.  This grid's own global-memory work (tile claims, loads
+    // of k / v / beta, stores of T / W / U) waits for the previous grid on the stream to complete.
+    griddep_launch_dependents();
+    griddep_wait();
     KKT_TRACE_CALIB(0);
 
     if (warp == kWarpProducer) {
@@ -542,6 +548,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             } else {
                 ok = false;
+            }
+        }
+        // This CTA claims no more tiles.  The workspace holds the tile counter and a count of CTAs
+        // done claiming; the last CTA to finish claiming zeroes both, so the next call on the same
+        // workspace starts from zero without a clear of its own (the fence orders this CTA's
+        // claims before its count; every other CTA has counted itself, so none claims again).
+        if (dyn && lane == 0) {
+            __threadfence();
+            if (atomicAdd(p.tile_counter + 1, 1ull) == gridDim.x - 1ull) {
+                atomicExch(p.tile_counter, 0ull);
+                atomicExch(p.tile_counter + 1, 0ull);
             }
         }
         // after a timeout: our last TMA loads must land before shared memory is released
@@ -1079,7 +1096,19 @@ int launch_tc_t(const Problem &pb) {
     const int sms = sm_count();
     if (sms <= 0) return KKT_ERR_CUDA;
     const int64_t grid = p.tiles < sms ? p.tiles : sms;
-    kern<<<(unsigned)grid, kThreads, CF::SMEM_BYTES, pb.stream>>>(mk, mv, mw, mu, mt, p);
+    // programmatic stream serialisation: this launch may start while the previous kernel on the
+    // stream finishes (the kernel waits for it before touching global memory)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = CF::SMEM_BYTES;
+    cfg.stream = pb.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, mk, mv, mw, mu, mt, p) != cudaSuccess) return KKT_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? KKT_OK : KKT_ERR_CUDA;
 }
 

@@ -81,6 +81,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
     return false;
 }
 
+// ---- programmatic dependent launch --------------------------------------------------------------
+
+// Lets the next grid on the stream (launched with programmatic stream serialisation) be scheduled:
+// its CTAs take SMs as this grid's CTAs leave them.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Waits until the previous grid on the stream has completed and its memory operations are visible
+// (returns at once when the launch had no programmatic dependency).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- async proxy fences and TMA ----------------------------------------------------------------
 
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -101,12 +101,18 @@ int kkt_solve_fwd(const void *k, const void *v, const float *beta, const int32_t
  * tcgen05 kernel does not cover, returns KKT_ERR_UNSUPPORTED.
  *
  * workspace: NULL, or caller-owned device memory of at least
- * KKT_WORKSPACE_BYTES (workspace_bytes), 16-byte aligned.  With it the
- * tensor-core kernel hands out work dynamically (an atomic tile counter) instead
- * of in a fixed round robin, which evens out SMs that run at different speeds.
- * The call resets the counter on `stream` before its launch (a memset, no
- * allocation); calls that may run at the same time need distinct workspaces.
- * The contents are scratch and may be left in any state.
+ * KKT_WORKSPACE_BYTES (workspace_bytes), 16-byte aligned, zero-filled before its
+ * first use.  With it the tensor-core kernel hands out work dynamically (an
+ * atomic tile counter) instead of in a fixed round robin, which evens out SMs
+ * that run at different speeds.  Every call leaves the workspace zero-filled
+ * again when its kernel ends (the kernel's last CTA clears it), so consecutive
+ * calls on one stream share it with no clear in between, and back-to-back calls
+ * are plain kernel launches; calls that may run at the same time need distinct
+ * workspaces.
+ *
+ * The tensor-core kernel is launched with programmatic stream serialisation: its
+ * CTAs may be scheduled while the previous kernel on the stream finishes, and
+ * they wait for that kernel to complete before touching global memory.
  */
 int kkt_solve_fwd_ex(const void *k, const void *v, const float *beta, const int32_t *cu_seqlens,
                      int B, int T, int H, int dk, int dv, int C,
@@ -135,7 +141,8 @@ int kkt_solve_fwd_ex(const void *k, const void *v, const float *beta, const int3
  *   on the tensor-core kernel only.  Shapes that kernel does not cover
  *   (d_k or d_v other than 128) return KKT_ERR_UNSUPPORTED; a problem that would
  *   need more scratch than the array holds returns KKT_ERR_ARG (a call needs
- *   8 bytes, one 64-bit counter, whatever the problem size).
+ *   16 bytes, two 64-bit counters, whatever the problem size; the array is zero
+ *   when the library loads and every call leaves it zero).
  *   The first call on a device looks up the array's device address (with that
  *   device current); make that first call before any stream capture.
  *   Every call shares the array and resets the counter on `stream` before its

@@ -114,14 +114,19 @@ def test_small_varlen(kernel, C):
 @pytest.mark.parametrize("C", [32, 64, 128])
 def test_dynamic_and_static_schedules_agree(C):
     """Tiles claimed from the workspace counter or dealt round robin: identical bits, and the
-    oracle agrees (odd head count: the last head group runs past H)."""
+    oracle agrees (odd head count: the last head group runs past H).  A caller's workspace is
+    left zero-filled by every call, so it serves the next call as it is."""
     _skip_unless("tc", 128, 128, C)
     k, v, beta = make_inputs(3, 1000, 5, 128, 128, seed=11, device=DEV)
     dyn = run(k, v, beta, C, kernel="tc", workspace="auto")
     sta = run(k, v, beta, C, kernel="tc", workspace=None)
-    own = run(k, v, beta, C, kernel="tc", workspace=torch.zeros(64, dtype=torch.int32, device=DEV))
-    for a, b, c in zip(dyn, sta, own):
-        assert torch.equal(a, b) and torch.equal(a, c)
+    ws = torch.zeros(64, dtype=torch.int32, device=DEV)
+    own = run(k, v, beta, C, kernel="tc", workspace=ws)
+    assert torch.count_nonzero(ws).item() == 0
+    again = run(k, v, beta, C, kernel="tc", workspace=ws)
+    assert torch.count_nonzero(ws).item() == 0
+    for a, b, c, d in zip(dyn, sta, own, again):
+        assert torch.equal(a, b) and torch.equal(a, c) and torch.equal(a, d)
     full_compare(k, v, beta, C, None, dyn)
 
 
