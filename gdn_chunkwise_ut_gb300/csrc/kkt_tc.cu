@@ -818,59 +818,68 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_DIAG, i);
 
-            // level 16 (§2.2): the warp's two diagonal blocks, T10 = -X11 (L10 X00); lane -> row
-            // i of the 16 x 16 result, columns jb .. jb + 7.  Y = L10 X00 is kept in the block's
-            // upper-right 16 x 16 (rows m0 .. m0 + 15, columns c0 + 16 .. c0 + 31), zero in T and
-            // cleared again once read.
+            // level 16 (§2.2): the warp's two diagonal blocks, T10 = -X11 (L10 X00).  Y = L10 X00 is
+            // kept in the block's upper-right 16 x 16 (rows m0 .. m0 + 15, columns c0 + 16 .. c0 + 31),
+            // zero in T and cleared again once read.
             {
-                const int ii = lane >> 1;
-                const int jb = (lane & 1) * 8;
+                // lane -> rows ii and ii + 8 of the 16 x 16 result, columns jb .. jb + 3
+                const int ii = lane >> 2;
+                const int jb = (lane & 3) * 4;
                 const int m0 = g * C + 32 * wp;
                 const int c0 = 32 * wp;
-                float a[16];
+                float a[2][16];
 #pragma unroll
-                for (int k = 0; k < 16; k += 4) {
-                    const float4 t4 = *tm_vec(tm, m0 + 16 + ii, c0 + k);
-                    a[k] = t4.x; a[k + 1] = t4.y; a[k + 2] = t4.z; a[k + 3] = t4.w;
-                }
-                float2 y[4];
+                for (int h = 0; h < 2; ++h)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) y[e] = make_float2(0.f, 0.f);
+                    for (int k = 0; k < 16; k += 4) {
+                        const float4 t4 = *tm_vec(tm, m0 + 16 + ii + 8 * h, c0 + k);
+                        a[h][k] = t4.x; a[h][k + 1] = t4.y; a[h][k + 2] = t4.z; a[h][k + 3] = t4.w;
+                    }
+                float2 y[2][2];
 #pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float4 b0 = *tm_vec(tm, m0 + k, c0 + jb);
-                    const float4 b1 = *tm_vec(tm, m0 + k, c0 + jb + 4);
-                    const float2 ak = make_float2(a[k], a[k]);
-                    y[0] = ffma2(ak, make_float2(b0.x, b0.y), y[0]);
-                    y[1] = ffma2(ak, make_float2(b0.z, b0.w), y[1]);
-                    y[2] = ffma2(ak, make_float2(b1.x, b1.y), y[2]);
-                    y[3] = ffma2(ak, make_float2(b1.z, b1.w), y[3]);
-                }
-                *tm_vec(tm, m0 + ii, c0 + 16 + jb) = make_float4(y[0].x, y[0].y, y[1].x, y[1].y);
-                *tm_vec(tm, m0 + ii, c0 + 16 + jb + 4) = make_float4(y[2].x, y[2].y, y[3].x, y[3].y);
-#pragma unroll
-                for (int k = 0; k < 16; k += 4) {
-                    const float4 t4 = *tm_vec(tm, m0 + 16 + ii, c0 + 16 + k);
-                    a[k] = t4.x; a[k + 1] = t4.y; a[k + 2] = t4.z; a[k + 3] = t4.w;
-                }
-                __syncwarp();
-#pragma unroll
-                for (int e = 0; e < 4; ++e) y[e] = make_float2(0.f, 0.f);
+                for (int h = 0; h < 2; ++h) y[h][0] = y[h][1] = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
-                    const float4 b0 = *tm_vec(tm, m0 + k, c0 + 16 + jb);
-                    const float4 b1 = *tm_vec(tm, m0 + k, c0 + 16 + jb + 4);
-                    const float2 ak = make_float2(a[k], a[k]);
-                    y[0] = ffma2(ak, make_float2(b0.x, b0.y), y[0]);
-                    y[1] = ffma2(ak, make_float2(b0.z, b0.w), y[1]);
-                    y[2] = ffma2(ak, make_float2(b1.x, b1.y), y[2]);
-                    y[3] = ffma2(ak, make_float2(b1.z, b1.w), y[3]);
+                    const float4 b = *tm_vec(tm, m0 + k, c0 + jb);
+                    const float2 b01 = make_float2(b.x, b.y), b23 = make_float2(b.z, b.w);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const float2 ak = make_float2(a[h][k], a[h][k]);
+                        y[h][0] = ffma2(ak, b01, y[h][0]);
+                        y[h][1] = ffma2(ak, b23, y[h][1]);
+                    }
                 }
-                *tm_vec(tm, m0 + 16 + ii, c0 + jb) = make_float4(-y[0].x, -y[0].y, -y[1].x, -y[1].y);
-                *tm_vec(tm, m0 + 16 + ii, c0 + jb + 4) = make_float4(-y[2].x, -y[2].y, -y[3].x, -y[3].y);
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    *tm_vec(tm, m0 + ii + 8 * h, c0 + 16 + jb) = make_float4(y[h][0].x, y[h][0].y, y[h][1].x, y[h][1].y);
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int k = 0; k < 16; k += 4) {
+                        const float4 t4 = *tm_vec(tm, m0 + 16 + ii + 8 * h, c0 + 16 + k);
+                        a[h][k] = t4.x; a[h][k + 1] = t4.y; a[h][k + 2] = t4.z; a[h][k + 3] = t4.w;
+                    }
                 __syncwarp();
-                *tm_vec(tm, m0 + ii, c0 + 16 + jb) = make_float4(0.f, 0.f, 0.f, 0.f);
-                *tm_vec(tm, m0 + ii, c0 + 16 + jb + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) y[h][0] = y[h][1] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const float4 b = *tm_vec(tm, m0 + k, c0 + 16 + jb);
+                    const float2 b01 = make_float2(b.x, b.y), b23 = make_float2(b.z, b.w);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const float2 ak = make_float2(a[h][k], a[h][k]);
+                        y[h][0] = ffma2(ak, b01, y[h][0]);
+                        y[h][1] = ffma2(ak, b23, y[h][1]);
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    *tm_vec(tm, m0 + 16 + ii + 8 * h, c0 + jb) = make_float4(-y[h][0].x, -y[h][0].y, -y[h][1].x, -y[h][1].y);
+                __syncwarp();
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    *tm_vec(tm, m0 + ii + 8 * h, c0 + 16 + jb) = make_float4(0.f, 0.f, 0.f, 0.f);
             }
             if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_C16, i);
 
