@@ -55,6 +55,7 @@ def parse_args():
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc"])
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-t-out", action="store_true", help="W and U~ only: T computed, not written")
     return ap.parse_args()
 
 
@@ -201,7 +202,8 @@ def bench_ours(args, rank, world, local):
     stream = torch.cuda.current_stream()
 
     def step():
-        kkt_solve_fwd(k, v, beta, w.C, cu_t, T_out=T_out, W_out=W_out, U_out=U_out, kernel=args.kernel)
+        kkt_solve_fwd(k, v, beta, w.C, cu_t, T_out=None if args.no_t_out else T_out, W_out=W_out, U_out=U_out,
+                      kernel=args.kernel, materialize_T=not args.no_t_out)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -248,15 +250,15 @@ def bench_ours(args, rank, world, local):
 
     units = w.tokens * w.H
     io_bytes = 4 if w.io == "f32" else 2
-    alg_bytes = units * costmodel.bytes_per_unit(w.C, w.dk, w.dv, io_bytes)
+    alg_bytes = units * costmodel.bytes_per_unit(w.C, w.dk, w.dv, io_bytes, t_out=not args.no_t_out)
     tokens_per_s = aggregate_value(w.tokens * K, world, max_ms / 1e3)
     peak, peak_src = hbm_peak()
     achieved = alg_bytes / (launch_ms / 1e3) / 1e9
-    traffic = recorded_traffic(kernel, args.workload)
+    traffic = None if args.no_t_out else recorded_traffic(kernel, args.workload)
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     runner = HostRunner(k.shape[0], k.shape[1], w.H, w.dk, w.dv, w.C, dtype=k.dtype, cu_seqlens=cu,
-                        kernel=args.kernel, device=dev)
+                        kernel=args.kernel, device=dev, materialize_T=not args.no_t_out)
     kh, vh, bh = (x.cpu().pin_memory() for x in (k, v, beta))
     for _ in range(2):
         runner(kh, vh, bh)
@@ -276,7 +278,7 @@ def bench_ours(args, rank, world, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.io == "bf16" else "f32",
         "data": "synthetic (seeded K rows L2-normalised N(0,1), V ~ N(0,1), beta = sigmoid(N(0,1)))",
         "config": {"workload": args.workload, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
-                   "C": w.C, "tokens_per_step": w.tokens, "kernel": kernel,
+                   "C": w.C, "tokens_per_step": w.tokens, "kernel": kernel, "T_out": not args.no_t_out,
                    "l2": (f"inputs ({in_bytes / 1e6:.0f} MB) fit in the 129 MB L2: flushed before every step"
                           if flush else f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB > 129 MB), no flush")},
         "hbm_gbs": achieved, "hbm_frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,

@@ -46,8 +46,11 @@ def _workspace(device: torch.device) -> torch.Tensor:
 
 def kkt_solve_fwd(k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor, C: int,
                   cu_seqlens: torch.Tensor | None = None, *, T_out=None, W_out=None, U_out=None,
-                  kernel: str = "auto", workspace="auto", stream=None):
+                  kernel: str = "auto", workspace="auto", stream=None, materialize_T: bool = True):
     """UT transform of every chunk: returns (T_out, W, U).
+
+    ``materialize_T=False`` computes T but does not write it: the call returns (None, W, U) and
+    moves 4C bytes less per token and head.
 
     k [B, T, H, dk] and v [B, T, H, dv] (bf16, or fp32 for the fp32-I/O path),
     beta [B, T, H] fp32.  With ``cu_seqlens`` (int32 [N+1] on the device) the
@@ -78,13 +81,17 @@ def kkt_solve_fwd(k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor, C: int,
     else:
         B, cu_ptr = Bt, None
     dev = k.device
-    if T_out is None:
+    if not materialize_T:
+        if T_out is not None:
+            raise ValueError("T_out given with materialize_T=False")
+    elif T_out is None:
         T_out = torch.empty((Bt, T, H, C), device=dev, dtype=torch.float32)
     if W_out is None:
         W_out = torch.empty((Bt, T, H, dk), device=dev, dtype=k.dtype)
     if U_out is None:
         U_out = torch.empty((Bt, T, H, dv), device=dev, dtype=k.dtype)
-    _check(T_out, "T_out", torch.float32, (Bt, T, H, C))
+    if materialize_T:
+        _check(T_out, "T_out", torch.float32, (Bt, T, H, C))
     _check(W_out, "W_out", k.dtype, (Bt, T, H, dk))
     _check(U_out, "U_out", k.dtype, (Bt, T, H, dv))
     kern = _lib.KERNELS.get(kernel)
@@ -99,7 +106,8 @@ def kkt_solve_fwd(k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor, C: int,
             raise ValueError("workspace must be a CUDA tensor, 'auto' or None")
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     rc = _lib.lib().kkt_solve_fwd_ex(k.data_ptr(), v.data_ptr(), beta.data_ptr(), cu_ptr,
-                                     B, T, H, dk, dv, C, T_out.data_ptr(), W_out.data_ptr(),
+                                     B, T, H, dk, dv, C, T_out.data_ptr() if materialize_T else None,
+                                     W_out.data_ptr(),
                                      U_out.data_ptr(), io, kern, ws_ptr, ws_bytes, _stream_handle(stream))
     if rc != _lib.KKT_OK:
         raise _lib.KktError(rc, "kkt_solve_fwd")
@@ -128,17 +136,18 @@ class HostRunner:
     """
 
     def __init__(self, B, T, H, dk, dv, C, *, dtype=torch.bfloat16, cu_seqlens=None,
-                 kernel="auto", device="cuda"):
-        self.C, self.kernel = C, kernel
+                 kernel="auto", device="cuda", materialize_T: bool = True):
+        self.C, self.kernel, self.materialize_T = C, kernel, materialize_T
         dev = torch.device(device)
         self.k = torch.empty((B, T, H, dk), device=dev, dtype=dtype)
         self.v = torch.empty((B, T, H, dv), device=dev, dtype=dtype)
         self.beta = torch.empty((B, T, H), device=dev, dtype=torch.float32)
         self.cu = None if cu_seqlens is None else torch.as_tensor(cu_seqlens, dtype=torch.int32).to(dev)
-        self.T_out = torch.empty((B, T, H, C), device=dev, dtype=torch.float32)
+        self.T_out = torch.empty((B, T, H, C), device=dev, dtype=torch.float32) if materialize_T else None
         self.W = torch.empty((B, T, H, dk), device=dev, dtype=dtype)
         self.U = torch.empty((B, T, H, dv), device=dev, dtype=dtype)
-        self.T_host = torch.empty(self.T_out.shape, dtype=torch.float32, pin_memory=True)
+        self.T_host = (torch.empty(self.T_out.shape, dtype=torch.float32, pin_memory=True)
+                       if materialize_T else None)
         self.W_host = torch.empty(self.W.shape, dtype=dtype, pin_memory=True)
         self.U_host = torch.empty(self.U.shape, dtype=dtype, pin_memory=True)
 
@@ -148,15 +157,16 @@ class HostRunner:
 
     @property
     def d2h_bytes(self) -> int:
-        return sum(t.numel() * t.element_size() for t in (self.T_out, self.W, self.U))
+        return sum(t.numel() * t.element_size() for t in (self.T_out, self.W, self.U) if t is not None)
 
     def __call__(self, k_host, v_host, beta_host, sync: bool = True):
         self.k.copy_(k_host, non_blocking=True)
         self.v.copy_(v_host, non_blocking=True)
         self.beta.copy_(beta_host, non_blocking=True)
         kkt_solve_fwd(self.k, self.v, self.beta, self.C, self.cu, T_out=self.T_out, W_out=self.W,
-                      U_out=self.U, kernel=self.kernel)
-        self.T_host.copy_(self.T_out, non_blocking=True)
+                      U_out=self.U, kernel=self.kernel, materialize_T=self.materialize_T)
+        if self.T_out is not None:
+            self.T_host.copy_(self.T_out, non_blocking=True)
         self.W_host.copy_(self.W, non_blocking=True)
         self.U_host.copy_(self.U, non_blocking=True)
         if sync:

@@ -62,7 +62,7 @@ extern "C" int kkt_solve_fwd_ex(const void *k, const void *v, const float *beta,
                                 float *T_out, void *W_out, void *U_out,
                                 int io_dtype, int kernel, void *workspace, size_t workspace_bytes,
                                 struct CUstream_st *stream) {
-    if (!k || !v || !beta || !T_out || !W_out || !U_out) return KKT_ERR_ARG;
+    if (!k || !v || !beta || !W_out || !U_out) return KKT_ERR_ARG;  // T_out may be NULL
     if (workspace && workspace_bytes < KKT_WORKSPACE_BYTES) return KKT_ERR_ARG;
     if (workspace && !aligned16(workspace)) return KKT_ERR_ALIGN;
     if (B < 1 || T < 0 || H < 1 || H > 65535) return KKT_ERR_ARG;

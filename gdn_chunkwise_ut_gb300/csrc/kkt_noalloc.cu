@@ -46,7 +46,7 @@ bool aligned_to(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t
 extern "C" int kkt_solve_fwd_noalloc(const void *k, const void *v, const float *beta, const int32_t *cu_seqlens,
                                      int B, int T, int H, int dk, int dv, int C,
                                      float *T_out, void *W_out, void *U_out, struct CUstream_st *stream) {
-    if (!k || !v || !beta || !T_out || !W_out || !U_out) return KKT_ERR_ARG;
+    if (!k || !v || !beta || !W_out || !U_out) return KKT_ERR_ARG;  // T_out may be NULL
     if (B < 1 || T < 0 || H < 1 || H > 65535) return KKT_ERR_ARG;
     // only the tensor-core kernel uses scratch; shapes it does not cover are rejected
     const int which = kkt_select_kernel(dk, dv, C, KKT_IO_BF16, KKT_KERNEL_TC);

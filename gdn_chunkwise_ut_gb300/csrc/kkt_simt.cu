@@ -143,8 +143,8 @@ __global__ void __launch_bounds__(kSimtThreads) kkt_simt_kernel(const SimtParams
         __syncthreads();
     }
 
-    // 5. T_out rows of the chunk (zeros in columns >= Lc)
-    for (int e = tid; e < Lc * C; e += kSimtThreads) {
+    // 5. T_out rows of the chunk (zeros in columns >= Lc); none without T_out (W and U~ only)
+    for (int e = tid; p.T_out && e < Lc * C; e += kSimtThreads) {
         const int i = e / C, j = e % C;
         p.T_out[((t0 + i) * H + h) * C + j] = (j < Lc) ? Ts[i * TS + j] : 0.f;
     }

@@ -906,8 +906,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_INV, i);
 
-            // T rows: TMA store of the warp's 32 rows when all are valid, else plain stores
-            if (32 * wp + 32 <= info.Lc) {
+            // T rows: TMA store of the warp's 32 rows when all are valid, else plain stores (none
+            // without T_out: W and U~ only)
+            if (p.T_out == nullptr) {
+            } else if (32 * wp + 32 <= info.Lc) {
                 if (lane == 0) {
                     for (int h = 0; h < CF::T_HALVES; ++h)
                         tma_store_3d(&map_t, tm + h * 16384 + 32 * q * 128, 32 * h, info.h0 + g,
@@ -1081,8 +1083,9 @@ int launch_tc_t(const Problem &pb) {
         !make_map(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.v, pb.ntok, pb.H, pb.dv, 64, C) ||
         !make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.W_out, pb.ntok, pb.H, pb.dk, 64, 32) ||
         !make_map(&mu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.U_out, pb.ntok, pb.H, pb.dv, 64, 32) ||
-        !make_map(&mt, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pb.T_out, pb.ntok, pb.H, C, 32, 32))
+        (pb.T_out && !make_map(&mt, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pb.T_out, pb.ntok, pb.H, C, 32, 32)))
         return KKT_ERR_CUDA;
+    if (!pb.T_out) mt = CUtensorMap{};  // never used: the kernel stores no T
     TcParams p;
     p.beta = pb.beta;
     p.cu = pb.cu_seqlens;

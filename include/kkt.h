@@ -23,7 +23,12 @@
  *   v     [B, T, H, dv]   input  (same dtype as k)
  *   beta  [B, T, H]       input  fp32, expected in (0, 1)
  *   T_out [B, T, H, C]    output fp32; row (b, t, h) holds row (t - chunk start)
- *                         of its chunk's T, zeros in columns >= Lc
+ *                         of its chunk's T, zeros in columns >= Lc.  May be NULL:
+ *                         T is then computed but not written, and the call
+ *                         produces W and U~ only (the page materialises T
+ *                         because W and U~ both use it, section 5 item 10; a
+ *                         caller that needs only W and U~ saves the 4C bytes
+ *                         per token and head of the T write)
  *   W_out [B, T, H, dk]   output (dtype of k)
  *   U_out [B, T, H, dv]   output (dtype of k)
  *

@@ -101,6 +101,8 @@ def test_argument_errors_return_before_launch(lib):
     assert _call(lib, ws=0x8000, ws_bytes=_lib.KKT_WORKSPACE_BYTES - 1) == _lib.KKT_ERR_ARG
     assert _call(lib, ws=0x8004, ws_bytes=_lib.KKT_WORKSPACE_BYTES) == _lib.KKT_ERR_ALIGN
     assert _call(lib, T=0) == _lib.KKT_OK               # empty batch: nothing to launch
+    assert _call(lib, T_out=None, T=0) == _lib.KKT_OK   # T_out may be NULL (W and U~ only)
+    assert _call(lib, T_out=0x4004) == _lib.KKT_ERR_ALIGN
     assert _call(lib, cu=0x7000, B=3, T=0) == _lib.KKT_OK
     assert lib.kkt_solve_fwd(None, 0x2000, 0x3000, None, 1, 64, 1, 128, 128, 64,
                              0x4000, 0x5000, 0x6000, None) == _lib.KKT_ERR_ARG

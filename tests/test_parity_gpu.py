@@ -130,6 +130,26 @@ def test_dynamic_and_static_schedules_agree(C):
     full_compare(k, v, beta, C, None, dyn)
 
 
+@pytest.mark.parametrize("kernel", ALL_KERNELS)
+@pytest.mark.parametrize("C", [32, 64, 128])
+def test_w_and_u_only_without_t(kernel, C):
+    """T_out = NULL: T is computed but not written, and W, U~ are bit-identical to those of the
+    materialising call (which the other tests compare with the oracle); varlen with a ragged tail."""
+    _skip_unless(kernel, 128, 128, C)
+    lengths = [1, 63, 64, 65, 0, 130, 7, 200]
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    k, v, beta = make_inputs(1, int(cu[-1]), 3, 128, 128, seed=21, device=DEV)
+    cu_t = torch.as_tensor(cu, dtype=torch.int32, device=DEV)
+    T_full, W_full, U_full = run(k, v, beta, C, cu, kernel=kernel)
+    W = torch.full_like(W_full, float("nan"))
+    U = torch.full_like(U_full, float("nan"))
+    T_none, W, U = kkt_solve_fwd(k, v, beta, C, cu_t, W_out=W, U_out=U, kernel=kernel, materialize_T=False)
+    torch.cuda.synchronize()
+    assert device_status() == 0
+    assert T_none is None
+    assert torch.equal(W, W_full) and torch.equal(U, U_full)
+
+
 # --- degenerate cases and traps -----------------------------------------------------------
 
 @pytest.mark.parametrize("kernel", ALL_KERNELS)
