@@ -56,7 +56,11 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-t-out", action="store_true", help="W and U~ only: T computed, not written")
-    return ap.parse_args()
+    ap.add_argument("--t-f16", action="store_true", help="T written in fp16 instead of fp32")
+    args = ap.parse_args()
+    if args.no_t_out and args.t_f16:
+        ap.error("--no-t-out and --t-f16 exclude each other")
+    return args
 
 
 # --- distributed plumbing -------------------------------------------------------------------
@@ -196,14 +200,15 @@ def bench_ours(args, rank, world, local):
     kernel = select_kernel(w.dk, w.dv, w.C, w.io, args.kernel)
     k, v, beta, cu = w.make(seed=rank, device=dev)
     cu_t = None if cu is None else torch.as_tensor(cu, dtype=torch.int32, device=dev)
-    T_out = torch.empty((k.shape[0], k.shape[1], w.H, w.C), device=dev)
+    T_dtype = torch.float16 if args.t_f16 else torch.float32
+    T_out = torch.empty((k.shape[0], k.shape[1], w.H, w.C), device=dev, dtype=T_dtype)
     W_out = torch.empty_like(k)
     U_out = torch.empty_like(v)
     stream = torch.cuda.current_stream()
 
     def step():
         kkt_solve_fwd(k, v, beta, w.C, cu_t, T_out=None if args.no_t_out else T_out, W_out=W_out, U_out=U_out,
-                      kernel=args.kernel, materialize_T=not args.no_t_out)
+                      kernel=args.kernel, materialize_T=not args.no_t_out, T_dtype=T_dtype)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -250,15 +255,17 @@ def bench_ours(args, rank, world, local):
 
     units = w.tokens * w.H
     io_bytes = 4 if w.io == "f32" else 2
-    alg_bytes = units * costmodel.bytes_per_unit(w.C, w.dk, w.dv, io_bytes, t_out=not args.no_t_out)
+    alg_bytes = units * costmodel.bytes_per_unit(w.C, w.dk, w.dv, io_bytes, t_out=not args.no_t_out,
+                                                  t_bytes=2 if args.t_f16 else 4)
     tokens_per_s = aggregate_value(w.tokens * K, world, max_ms / 1e3)
     peak, peak_src = hbm_peak()
     achieved = alg_bytes / (launch_ms / 1e3) / 1e9
-    traffic = None if args.no_t_out else recorded_traffic(kernel, args.workload)
+    # the recorded counters are those of the default call (fp32 T)
+    traffic = None if (args.no_t_out or args.t_f16) else recorded_traffic(kernel, args.workload)
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     runner = HostRunner(k.shape[0], k.shape[1], w.H, w.dk, w.dv, w.C, dtype=k.dtype, cu_seqlens=cu,
-                        kernel=args.kernel, device=dev, materialize_T=not args.no_t_out)
+                        kernel=args.kernel, device=dev, materialize_T=not args.no_t_out, T_dtype=T_dtype)
     kh, vh, bh = (x.cpu().pin_memory() for x in (k, v, beta))
     for _ in range(2):
         runner(kh, vh, bh)
@@ -278,7 +285,8 @@ def bench_ours(args, rank, world, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.io == "bf16" else "f32",
         "data": "synthetic (seeded K rows L2-normalised N(0,1), V ~ N(0,1), beta = sigmoid(N(0,1)))",
         "config": {"workload": args.workload, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
-                   "C": w.C, "tokens_per_step": w.tokens, "kernel": kernel, "T_out": not args.no_t_out,
+                   "C": w.C, "tokens_per_step": w.tokens, "kernel": kernel,
+                   "T_out": False if args.no_t_out else "fp16" if args.t_f16 else "fp32",
                    "l2": (f"inputs ({in_bytes / 1e6:.0f} MB) fit in the 129 MB L2: flushed before every step"
                           if flush else f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB > 129 MB), no flush")},
         "hbm_gbs": achieved, "hbm_frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,

@@ -21,6 +21,7 @@ KKT_ERR_NO_DEVICE = 7
 
 KKT_IO_BF16 = 0
 KKT_IO_F32 = 1
+KKT_T_OUT_F16 = 0x100  # ORed into the io dtype: T_out in fp16
 
 KKT_KERNEL_AUTO = 0
 KKT_KERNEL_SIMT = 1

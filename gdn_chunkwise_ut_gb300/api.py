@@ -12,6 +12,7 @@ import torch
 from . import _lib
 
 _IO = {torch.bfloat16: _lib.KKT_IO_BF16, torch.float32: _lib.KKT_IO_F32}
+_T_FLAG = {torch.float32: 0, torch.float16: _lib.KKT_T_OUT_F16}
 
 
 def _stream_handle(stream) -> int:
@@ -46,16 +47,18 @@ def _workspace(device: torch.device) -> torch.Tensor:
 
 def kkt_solve_fwd(k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor, C: int,
                   cu_seqlens: torch.Tensor | None = None, *, T_out=None, W_out=None, U_out=None,
-                  kernel: str = "auto", workspace="auto", stream=None, materialize_T: bool = True):
+                  kernel: str = "auto", workspace="auto", stream=None, materialize_T: bool = True,
+                  T_dtype=torch.float32):
     """UT transform of every chunk: returns (T_out, W, U).
 
     ``materialize_T=False`` computes T but does not write it: the call returns (None, W, U) and
-    moves 4C bytes less per token and head.
+    moves 4C bytes less per token and head.  ``T_dtype=torch.float16`` writes T rounded to fp16
+    (2C bytes per token and head); W and U are the same as with fp32 T.
 
     k [B, T, H, dk] and v [B, T, H, dv] (bf16, or fp32 for the fp32-I/O path),
     beta [B, T, H] fp32.  With ``cu_seqlens`` (int32 [N+1] on the device) the
-    tensors are [1, T, H, .] and hold N packed sequences.  T_out is fp32
-    [B, T, H, C]; W and U have k's dtype.  ``kernel`` is "auto", "simt" or "tc".
+    tensors are [1, T, H, .] and hold N packed sequences.  T_out is [B, T, H, C]
+    of ``T_dtype``; W and U have k's dtype.  ``kernel`` is "auto", "simt" or "tc".
     ``workspace``: "auto" uses a cached per-device scratch buffer (dynamic tile
     scheduling; calls on concurrent streams should pass their own), a CUDA tensor
     of at least KKT_WORKSPACE_BYTES, zero-filled before its first use (every call
@@ -68,6 +71,9 @@ def kkt_solve_fwd(k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor, C: int,
     io = _IO.get(k.dtype)
     if io is None:
         raise ValueError(f"unsupported dtype {k.dtype}")
+    t_flag = _T_FLAG.get(T_dtype)
+    if t_flag is None:
+        raise ValueError(f"T_dtype must be torch.float32 or torch.float16, got {T_dtype}")
     _check(k, "k", k.dtype, (Bt, T, H, dk))
     _check(v, "v", k.dtype, (Bt, T, H, dv))
     _check(beta, "beta", torch.float32, (Bt, T, H))
@@ -85,13 +91,13 @@ def kkt_solve_fwd(k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor, C: int,
         if T_out is not None:
             raise ValueError("T_out given with materialize_T=False")
     elif T_out is None:
-        T_out = torch.empty((Bt, T, H, C), device=dev, dtype=torch.float32)
+        T_out = torch.empty((Bt, T, H, C), device=dev, dtype=T_dtype)
     if W_out is None:
         W_out = torch.empty((Bt, T, H, dk), device=dev, dtype=k.dtype)
     if U_out is None:
         U_out = torch.empty((Bt, T, H, dv), device=dev, dtype=k.dtype)
     if materialize_T:
-        _check(T_out, "T_out", torch.float32, (Bt, T, H, C))
+        _check(T_out, "T_out", T_dtype, (Bt, T, H, C))
     _check(W_out, "W_out", k.dtype, (Bt, T, H, dk))
     _check(U_out, "U_out", k.dtype, (Bt, T, H, dv))
     kern = _lib.KERNELS.get(kernel)
@@ -108,7 +114,7 @@ def kkt_solve_fwd(k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor, C: int,
     rc = _lib.lib().kkt_solve_fwd_ex(k.data_ptr(), v.data_ptr(), beta.data_ptr(), cu_ptr,
                                      B, T, H, dk, dv, C, T_out.data_ptr() if materialize_T else None,
                                      W_out.data_ptr(),
-                                     U_out.data_ptr(), io, kern, ws_ptr, ws_bytes, _stream_handle(stream))
+                                     U_out.data_ptr(), io | t_flag, kern, ws_ptr, ws_bytes, _stream_handle(stream))
     if rc != _lib.KKT_OK:
         raise _lib.KktError(rc, "kkt_solve_fwd")
     return T_out, W_out, U_out
@@ -136,17 +142,17 @@ class HostRunner:
     """
 
     def __init__(self, B, T, H, dk, dv, C, *, dtype=torch.bfloat16, cu_seqlens=None,
-                 kernel="auto", device="cuda", materialize_T: bool = True):
-        self.C, self.kernel, self.materialize_T = C, kernel, materialize_T
+                 kernel="auto", device="cuda", materialize_T: bool = True, T_dtype=torch.float32):
+        self.C, self.kernel, self.materialize_T, self.T_dtype = C, kernel, materialize_T, T_dtype
         dev = torch.device(device)
         self.k = torch.empty((B, T, H, dk), device=dev, dtype=dtype)
         self.v = torch.empty((B, T, H, dv), device=dev, dtype=dtype)
         self.beta = torch.empty((B, T, H), device=dev, dtype=torch.float32)
         self.cu = None if cu_seqlens is None else torch.as_tensor(cu_seqlens, dtype=torch.int32).to(dev)
-        self.T_out = torch.empty((B, T, H, C), device=dev, dtype=torch.float32) if materialize_T else None
+        self.T_out = torch.empty((B, T, H, C), device=dev, dtype=T_dtype) if materialize_T else None
         self.W = torch.empty((B, T, H, dk), device=dev, dtype=dtype)
         self.U = torch.empty((B, T, H, dv), device=dev, dtype=dtype)
-        self.T_host = (torch.empty(self.T_out.shape, dtype=torch.float32, pin_memory=True)
+        self.T_host = (torch.empty(self.T_out.shape, dtype=T_dtype, pin_memory=True)
                        if materialize_T else None)
         self.W_host = torch.empty(self.W.shape, dtype=dtype, pin_memory=True)
         self.U_host = torch.empty(self.U.shape, dtype=dtype, pin_memory=True)
@@ -164,7 +170,8 @@ class HostRunner:
         self.v.copy_(v_host, non_blocking=True)
         self.beta.copy_(beta_host, non_blocking=True)
         kkt_solve_fwd(self.k, self.v, self.beta, self.C, self.cu, T_out=self.T_out, W_out=self.W,
-                      U_out=self.U, kernel=self.kernel, materialize_T=self.materialize_T)
+                      U_out=self.U, kernel=self.kernel, materialize_T=self.materialize_T,
+                      T_dtype=self.T_dtype)
         if self.T_out is not None:
             self.T_host.copy_(self.T_out, non_blocking=True)
         self.W_host.copy_(self.W, non_blocking=True)

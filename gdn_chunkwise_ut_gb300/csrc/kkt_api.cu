@@ -46,6 +46,7 @@ bool chunk_ok(int C) { return C == 32 || C == 64 || C == 128; }
 }  // namespace
 
 extern "C" int kkt_select_kernel(int dk, int dv, int C, int io_dtype, int kernel) {
+    io_dtype &= ~KKT_T_OUT_F16;  // the T_out precision does not affect the choice
     if (io_dtype != KKT_IO_BF16 && io_dtype != KKT_IO_F32) return -KKT_ERR_ARG;
     if (!head_dim_ok(dk) || !head_dim_ok(dv) || !chunk_ok(C)) return -KKT_ERR_UNSUPPORTED;
     const bool tc = kkt::tc_supports(dk, dv, C, io_dtype);
@@ -59,7 +60,7 @@ extern "C" int kkt_select_kernel(int dk, int dv, int C, int io_dtype, int kernel
 
 extern "C" int kkt_solve_fwd_ex(const void *k, const void *v, const float *beta, const int32_t *cu_seqlens,
                                 int B, int T, int H, int dk, int dv, int C,
-                                float *T_out, void *W_out, void *U_out,
+                                void *T_out, void *W_out, void *U_out,
                                 int io_dtype, int kernel, void *workspace, size_t workspace_bytes,
                                 struct CUstream_st *stream) {
     if (!k || !v || !beta || !W_out || !U_out) return KKT_ERR_ARG;  // T_out may be NULL
@@ -81,7 +82,8 @@ extern "C" int kkt_solve_fwd_ex(const void *k, const void *v, const float *beta,
     p.nseq = B; p.T = T; p.ntok = ntok;
     p.H = H; p.dk = dk; p.dv = dv; p.C = C;
     p.T_out = T_out; p.W_out = W_out; p.U_out = U_out;
-    p.io = io_dtype;
+    p.io = io_dtype & ~KKT_T_OUT_F16;
+    p.t_f16 = (io_dtype & KKT_T_OUT_F16) != 0;
     p.stream = reinterpret_cast<cudaStream_t>(stream);
 #ifdef KKT_TRACE
     p.trace = g_trace;

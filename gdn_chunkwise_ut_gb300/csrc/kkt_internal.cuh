@@ -18,10 +18,11 @@ struct Problem {
     int T;                      // tokens per sequence, or the packed total with cu_seqlens
     int64_t ntok;               // rows of the flat token axis (B*T, or T with cu_seqlens)
     int H, dk, dv, C;
-    float *T_out;
+    void *T_out;                // fp32, or fp16 with t_f16; nullptr: T is not written
     void *W_out;
     void *U_out;
     int io;                     // KKT_IO_BF16 / KKT_IO_F32
+    int t_f16 = 0;              // T_out holds fp16
     cudaStream_t stream;
     int *status;                // device status word of the current device
     void *trace;                // pipeline trace buffer (KKT_TRACE builds only), else nullptr

@@ -11,6 +11,7 @@
 // coupling scratch [C/2][C/2+1].  The +1 row padding keeps the column walks of
 // the Gram and epilogue loops on distinct banks.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "kkt_internal.cuh"
 
@@ -32,7 +33,8 @@ struct SimtParams {
     int nseq, T;
     int64_t ntok;
     int H, dk, dv;
-    float *T_out;
+    void *T_out;  // fp32, or fp16 with t_f16; nullptr: T is not written
+    int t_f16;
     void *W_out, *U_out;
     int *status;
 };
@@ -146,7 +148,12 @@ __global__ void __launch_bounds__(kSimtThreads) kkt_simt_kernel(const SimtParams
     // 5. T_out rows of the chunk (zeros in columns >= Lc); none without T_out (W and U~ only)
     for (int e = tid; p.T_out && e < Lc * C; e += kSimtThreads) {
         const int i = e / C, j = e % C;
-        p.T_out[((t0 + i) * H + h) * C + j] = (j < Lc) ? Ts[i * TS + j] : 0.f;
+        const float x = (j < Lc) ? Ts[i * TS + j] : 0.f;
+        const int64_t at = ((t0 + i) * H + h) * C + j;
+        if (p.t_f16)
+            static_cast<__half *>(p.T_out)[at] = __float2half_rn(x);
+        else
+            static_cast<float *>(p.T_out)[at] = x;
     }
     __syncthreads();
 
@@ -183,7 +190,7 @@ int launch_simt_t(const Problem &pb) {
     p.k = pb.k; p.v = pb.v; p.beta = pb.beta; p.cu = pb.cu_seqlens;
     p.nseq = pb.nseq; p.T = pb.T; p.ntok = pb.ntok;
     p.H = pb.H; p.dk = pb.dk; p.dv = pb.dv;
-    p.T_out = pb.T_out; p.W_out = pb.W_out; p.U_out = pb.U_out; p.status = pb.status;
+    p.T_out = pb.T_out; p.t_f16 = pb.t_f16; p.W_out = pb.W_out; p.U_out = pb.U_out; p.status = pb.status;
     const int64_t ids = total_work_ids(pb.ntok, C, pb.nseq);
     dim3 grid((unsigned)ids, (unsigned)pb.H);
     kern<<<grid, kSimtThreads, smem, pb.stream>>>(p);

@@ -43,6 +43,7 @@
 // none of it.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "kkt_internal.cuh"
@@ -114,7 +115,7 @@ struct TcParams {
     int H;
     int64_t tiles;   // work ids x head groups
     int HG;          // head groups
-    float *T_out;
+    void *T_out;     // fp32, or fp16 in the TF16 kernels; nullptr: T is not written
     __nv_bfloat16 *W_out, *U_out;
     int *status;
     unsigned long long *trace;
@@ -194,6 +195,12 @@ __device__ __forceinline__ float *tm_elem(uint8_t *tm, int m, int j) {
 }
 __device__ __forceinline__ float4 *tm_vec(uint8_t *tm, int m, int j) {  // j a multiple of 4
     return reinterpret_cast<float4 *>(tm + (j >> 5) * 16384 + m * 128 + ((((j & 31) >> 2) ^ (m & 7)) << 4));
+}
+
+// Two fp16 (round to nearest even) in the bits of one float: lo in bits 0..15, hi in 16..31.
+__device__ __forceinline__ float pack_f16(float lo, float hi) {
+    const __half2 v = __floats2half2_rn(lo, hi);
+    return __uint_as_float(*reinterpret_cast<const uint32_t *>(&v));
 }
 
 // Two bf16 (round to nearest even) in one register: lo in bits 0..15, hi in 16..31.
@@ -416,7 +423,7 @@ __device__ __forceinline__ bool level64(const int w, uint8_t *tm, int lane, uint
 }
 
 // ---------------------------------------------------------------------------------------------
-template <int C>
+template <int C, bool TF16>
 __global__ void __launch_bounds__(kThreads, 1)
     kkt_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                   const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_u,
@@ -906,9 +913,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_INV, i);
 
-            // T rows: TMA store of the warp's 32 rows when all are valid, else plain stores (none
-            // without T_out: W and U~ only)
-            if (p.T_out == nullptr) {
+            // T rows in fp32: TMA store of the warp's 32 rows when all are valid, else plain stores
+            // (none without T_out: W and U~ only; fp16 T is written after T~, below)
+            if (p.T_out == nullptr || TF16) {
             } else if (32 * wp + 32 <= info.Lc) {
                 if (lane == 0) {
                     for (int h = 0; h < CF::T_HALVES; ++h)
@@ -917,7 +924,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bulk_commit();
                 }
             } else if (r < info.Lc && info.h0 + g < p.H) {
-                float4 *dst = reinterpret_cast<float4 *>(p.T_out + ((info.t0 + r) * p.H + info.h0 + g) * C);
+                float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.T_out) +
+                                                         ((info.t0 + r) * p.H + info.h0 + g) * C);
 #pragma unroll
                 for (int j = 0; j < C; j += 4) dst[j / 4] = *tm_vec(tm, m, j);
             }
@@ -927,21 +935,54 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!wait_bar(&bars->tt_empty, ((uint32_t)i & 1u) ^ 1u, bars, p.status)) break;
             tc_fence_after();
             if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_TTW, i);
+            // fp16 T (TF16): each row rounded to fp16 as T~ reads it.  The warp's 32 rows go out by
+            // one TMA store per 64 columns when all are valid: columns 64 h .. 64 h + 63 of a row are
+            // packed into the first 128 bytes of its block h (the 128-byte-swizzled layout of a TMA box
+            // of 64 fp16), which hold fp32 values T~ has already read.  Other rows (and C = 32) are
+            // written by plain stores.
+            const bool t16_tma = TF16 && C >= 64 && p.T_out != nullptr && 32 * wp + 32 <= info.Lc;
+            const bool t16_row = TF16 && !t16_tma && p.T_out != nullptr && r < info.Lc && info.h0 + g < p.H;
             {
                 uint32_t hi[16], lo[16];
 #pragma unroll(C == 128 ? 1 : CF::T_HALVES)
                 for (int blk = 0; blk < CF::T_HALVES; ++blk) {
+                    float4 *t16s = tm_vec(tm, m, 0);  // row m of block blk / 2, chunk base below
+                    if constexpr (TF16) t16s = reinterpret_cast<float4 *>(tm + (blk >> 1) * 16384 + m * 128);
                     if (blk <= wp) {
 #pragma unroll
-                        for (int c = 0; c < 32; c += 4) {
-                            const float4 t4 = *tm_vec(tm, m, 32 * blk + c);
-                            const float4 b4 = *reinterpret_cast<const float4 *>(sb + 32 * blk + c);
-                            split_bf16(fmul2(make_float2(t4.x, t4.y), make_float2(b4.x, b4.y)), hi[c / 2], lo[c / 2]);
-                            split_bf16(fmul2(make_float2(t4.z, t4.w), make_float2(b4.z, b4.w)), hi[c / 2 + 1], lo[c / 2 + 1]);
+                        for (int c = 0; c < 32; c += 8) {
+                            const float4 ta = *tm_vec(tm, m, 32 * blk + c);
+                            const float4 tb = *tm_vec(tm, m, 32 * blk + c + 4);
+                            const float4 ba = *reinterpret_cast<const float4 *>(sb + 32 * blk + c);
+                            const float4 bb = *reinterpret_cast<const float4 *>(sb + 32 * blk + c + 4);
+                            split_bf16(fmul2(make_float2(ta.x, ta.y), make_float2(ba.x, ba.y)), hi[c / 2], lo[c / 2]);
+                            split_bf16(fmul2(make_float2(ta.z, ta.w), make_float2(ba.z, ba.w)), hi[c / 2 + 1], lo[c / 2 + 1]);
+                            split_bf16(fmul2(make_float2(tb.x, tb.y), make_float2(bb.x, bb.y)), hi[c / 2 + 2], lo[c / 2 + 2]);
+                            split_bf16(fmul2(make_float2(tb.z, tb.w), make_float2(bb.z, bb.w)), hi[c / 2 + 3], lo[c / 2 + 3]);
+                            if constexpr (TF16) {
+                                const float4 h8 = make_float4(pack_f16(ta.x, ta.y), pack_f16(ta.z, ta.w),
+                                                              pack_f16(tb.x, tb.y), pack_f16(tb.z, tb.w));
+                                if (t16_tma)
+                                    t16s[(4 * (blk & 1) + c / 8) ^ (m & 7)] = h8;
+                                else if (t16_row)
+                                    *reinterpret_cast<float4 *>(static_cast<__half *>(p.T_out) +
+                                                                ((info.t0 + r) * p.H + info.h0 + g) * C + 32 * blk + c) = h8;
+                            }
                         }
                         const uint32_t col = (uint32_t)(g * C + 32 * blk) / 2;
                         tmem_st16(tmem + lane_base + kColTT + col, hi);
                         tmem_st16(tmem + lane_base + kColTT + 64 + col, lo);
+                    } else if constexpr (TF16) {
+                        // columns above the diagonal block: zeros
+                        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            if (t16_tma)
+                                t16s[(4 * (blk & 1) + e) ^ (m & 7)] = z;
+                            else if (t16_row)
+                                *reinterpret_cast<float4 *>(static_cast<__half *>(p.T_out) +
+                                                            ((info.t0 + r) * p.H + info.h0 + g) * C + 32 * blk + 8 * e) = z;
+                        }
                     }
                 }
                 tmem_wait_st();
@@ -951,6 +992,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 mbar_arrive(&bars->tt_full);
                 if (q == 1) KKT_TRACE_EVENT(EV_I_TT, i);
+            }
+            if (t16_tma) {
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    for (int h = 0; h < C / 64; ++h)
+                        tma_store_3d(&map_t, tm + h * 16384 + 32 * q * 128, 64 * h, info.h0 + g,
+                                     (int)(info.t0 + 32 * wp));
+                    bulk_commit();
+                }
             }
             ++i;
         }
@@ -1083,9 +1134,10 @@ int launch_tc_t(const Problem &pb) {
         !make_map(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.v, pb.ntok, pb.H, pb.dv, 64, C) ||
         !make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.W_out, pb.ntok, pb.H, pb.dk, 64, 32) ||
         !make_map(&mu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.U_out, pb.ntok, pb.H, pb.dv, 64, 32) ||
-        (pb.T_out && !make_map(&mt, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pb.T_out, pb.ntok, pb.H, C, 32, 32)))
+        (pb.T_out && !pb.t_f16 && !make_map(&mt, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pb.T_out, pb.ntok, pb.H, C, 32, 32)) ||
+        (pb.T_out && pb.t_f16 && C >= 64 && !make_map(&mt, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, pb.T_out, pb.ntok, pb.H, C, 64, 32)))
         return KKT_ERR_CUDA;
-    if (!pb.T_out) mt = CUtensorMap{};  // never used: the kernel stores no T
+    if (!pb.T_out || (pb.t_f16 && C < 64)) mt = CUtensorMap{};  // never used: no T, or fp16 T by plain stores
     TcParams p;
     p.beta = pb.beta;
     p.cu = pb.cu_seqlens;
@@ -1102,7 +1154,7 @@ int launch_tc_t(const Problem &pb) {
     p.trace = static_cast<unsigned long long *>(pb.trace);
     p.tile_counter = pb.tile_counter;
     p.stall_first_tile = pb.stall_first_tile;
-    auto kern = kkt_tc_kernel<C>;
+    auto kern = pb.t_f16 ? kkt_tc_kernel<C, true> : kkt_tc_kernel<C, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_BYTES) != cudaSuccess)
         return KKT_ERR_CUDA;
     const int sms = sm_count();

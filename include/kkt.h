@@ -22,7 +22,8 @@
  *   k     [B, T, H, dk]   input  (bf16, or fp32 with KKT_IO_F32)
  *   v     [B, T, H, dv]   input  (same dtype as k)
  *   beta  [B, T, H]       input  fp32, expected in (0, 1)
- *   T_out [B, T, H, C]    output fp32; row (b, t, h) holds row (t - chunk start)
+ *   T_out [B, T, H, C]    output fp32 (fp16 with KKT_T_OUT_F16, kkt_solve_fwd_ex
+ *                         only); row (b, t, h) holds row (t - chunk start)
  *                         of its chunk's T, zeros in columns >= Lc.  May be NULL:
  *                         T is then computed but not written, and the call
  *                         produces W and U~ only (the page materialises T
@@ -74,8 +75,14 @@ typedef enum kkt_status {
     KKT_ERR_NO_DEVICE = 7    /* no usable CUDA device / not an sm_103 device */
 } kkt_status;
 
-/* I/O dtype of k, v, W_out, U_out (beta and T_out are always fp32). */
+/* I/O dtype of k, v, W_out, U_out (beta is always fp32; T_out is fp32 unless KKT_T_OUT_F16). */
 enum { KKT_IO_BF16 = 0, KKT_IO_F32 = 1 };
+
+/* Flag for the io_dtype of kkt_solve_fwd_ex: T_out holds fp16 (2C bytes per row, round to
+ * nearest) instead of fp32.  The page's own kernel stores T in the input's half precision
+ * ("TileLang 实战：单位下三角矩阵求逆" section 3.1); W and U~ are unchanged (they are formed from
+ * T before it is rounded). */
+#define KKT_T_OUT_F16 0x100
 
 /* Minimum size of the optional workspace of kkt_solve_fwd_ex, in bytes. */
 #define KKT_WORKSPACE_BYTES 256
@@ -101,7 +108,8 @@ int kkt_solve_fwd(const void *k, const void *v, const float *beta, const int32_t
 
 /*
  * kkt_solve_fwd_ex -- as kkt_solve_fwd, with the I/O dtype (KKT_IO_BF16 or
- * KKT_IO_F32) and the kernel (KKT_KERNEL_*) chosen explicitly.  fp32 I/O runs
+ * KKT_IO_F32, optionally ORed with KKT_T_OUT_F16) and the kernel (KKT_KERNEL_*)
+ * chosen explicitly.  fp32 I/O runs
  * the SIMT kernel only; asking for KKT_KERNEL_TC with it, or with a shape the
  * tcgen05 kernel does not cover, returns KKT_ERR_UNSUPPORTED.
  *
@@ -121,7 +129,7 @@ int kkt_solve_fwd(const void *k, const void *v, const float *beta, const int32_t
  */
 int kkt_solve_fwd_ex(const void *k, const void *v, const float *beta, const int32_t *cu_seqlens,
                      int B, int T, int H, int dk, int dv, int C,
-                     float *T_out, void *W_out, void *U_out,
+                     void *T_out, void *W_out, void *U_out,
                      int io_dtype, int kernel, void *workspace, size_t workspace_bytes,
                      struct CUstream_st *stream);
 

@@ -31,6 +31,8 @@ def test_workspace_size_constant_matches_header():
     text = open(os.path.join(ROOT, "include", "kkt.h")).read()
     m = re.search(r"#define\s+KKT_WORKSPACE_BYTES\s+(\d+)", text)
     assert m and int(m.group(1)) == _lib.KKT_WORKSPACE_BYTES
+    m = re.search(r"#define\s+KKT_T_OUT_F16\s+(0x[0-9a-fA-F]+)", text)
+    assert m and int(m.group(1), 16) == _lib.KKT_T_OUT_F16
 
 
 def test_exports_every_declared_symbol(lib):
@@ -65,6 +67,10 @@ def test_select_kernel(lib):
     assert sel(128, 128, 256, _lib.KKT_IO_BF16, 0) == -_lib.KKT_ERR_UNSUPPORTED
     assert sel(128, 128, 64, 7, 0) == -_lib.KKT_ERR_ARG
     assert sel(128, 128, 64, _lib.KKT_IO_BF16, 9) == -_lib.KKT_ERR_ARG
+    # the precision of T_out does not change the kernel chosen
+    assert sel(128, 128, 64, _lib.KKT_IO_BF16 | _lib.KKT_T_OUT_F16, 0) == _lib.KKT_KERNEL_TC
+    assert sel(128, 128, 64, _lib.KKT_IO_F32 | _lib.KKT_T_OUT_F16, 0) == _lib.KKT_KERNEL_SIMT
+    assert sel(128, 128, 64, 0x200, 0) == -_lib.KKT_ERR_ARG
     for C in (32, 64, 128):
         # the tensor-core kernel covers bf16 with dk = dv = 128 at every chunk size
         assert sel(128, 128, C, _lib.KKT_IO_BF16, _lib.KKT_KERNEL_AUTO) == _lib.KKT_KERNEL_TC
@@ -103,6 +109,9 @@ def test_argument_errors_return_before_launch(lib):
     assert _call(lib, T=0) == _lib.KKT_OK               # empty batch: nothing to launch
     assert _call(lib, T_out=None, T=0) == _lib.KKT_OK   # T_out may be NULL (W and U~ only)
     assert _call(lib, T_out=0x4004) == _lib.KKT_ERR_ALIGN
+    assert _call(lib, T_out=0x4004, io=_lib.KKT_T_OUT_F16) == _lib.KKT_ERR_ALIGN
+    assert _call(lib, io=0x200) == _lib.KKT_ERR_ARG
+    assert _call(lib, T=0, io=_lib.KKT_T_OUT_F16) == _lib.KKT_OK
     assert _call(lib, cu=0x7000, B=3, T=0) == _lib.KKT_OK
     assert lib.kkt_solve_fwd(None, 0x2000, 0x3000, None, 1, 64, 1, 128, 128, 64,
                              0x4000, 0x5000, 0x6000, None) == _lib.KKT_ERR_ARG

@@ -150,6 +150,36 @@ def test_w_and_u_only_without_t(kernel, C):
     assert torch.equal(W, W_full) and torch.equal(U, U_full)
 
 
+@pytest.mark.parametrize("kernel", ALL_KERNELS)
+@pytest.mark.parametrize("C", [32, 64, 128])
+@pytest.mark.parametrize("varlen", [False, True])
+def test_t_out_fp16(kernel, C, varlen):
+    """T_dtype = fp16: T rounded to nearest from the fp32 T, so equal to the fp32 call's T cast to
+    fp16, and within 1e-4 + 2^-11 |T_ref| of the oracle (a half ulp of fp16 on top of the fp32
+    bound); W, U~ bit-identical to the fp32 call's.  Fixed length with a ragged tail, or varlen."""
+    _skip_unless(kernel, 128, 128, C)
+    if varlen:
+        lengths = [1, 63, 64, 65, 0, 130, 7, 200, 128]
+        cu = np.concatenate([[0], np.cumsum(lengths)])
+        k, v, beta = make_inputs(1, int(cu[-1]), 3, 128, 128, seed=23, device=DEV)
+        cu_t = torch.as_tensor(cu, dtype=torch.int32, device=DEV)
+    else:
+        cu, cu_t = None, None
+        k, v, beta = make_inputs(2, 3 * C + 17, 5, 128, 128, seed=24, device=DEV)
+    T32, W32, U32 = run(k, v, beta, C, cu, kernel=kernel)
+    T16 = torch.full(T32.shape, float("nan"), device=DEV, dtype=torch.float16)
+    W = torch.full_like(W32, float("nan"))
+    U = torch.full_like(U32, float("nan"))
+    kkt_solve_fwd(k, v, beta, C, cu_t, T_out=T16, W_out=W, U_out=U, kernel=kernel, T_dtype=torch.float16)
+    torch.cuda.synchronize()
+    assert device_status() == 0
+    assert torch.equal(T16, T32.to(torch.float16))
+    assert torch.equal(W, W32) and torch.equal(U, U32)
+    T_ref, _, _ = oracle.oracle_fwd(to64(k), to64(v), to64(beta), C, cu_seqlens=cu)
+    err = np.abs(to64(T16) - T_ref)
+    assert (err <= 1e-4 + 2.0 ** -11 * np.abs(T_ref)).all(), float(err.max())
+
+
 # --- degenerate cases and traps -----------------------------------------------------------
 
 @pytest.mark.parametrize("kernel", ALL_KERNELS)
