@@ -56,7 +56,8 @@ using namespace ptx;
 
 constexpr int kThreads = 384;            // 12 warps
 constexpr int kWarpProducer = 0;
-constexpr int kWarpMma = 1;
+constexpr int kWarpMma = 1;              // W|U MMAs
+constexpr int kWarpGram = 2;             // Gram MMAs
 constexpr int kWarpInv0 = 4;             // warps 4..7
 constexpr int kWarpEpi0 = 8;             // warps 8..11
 constexpr int kNS = 2;                   // stages
@@ -99,10 +100,10 @@ struct Barriers {
     uint64_t tt_full, tt_empty;
     uint64_t d_full, d_empty;
     uint64_t einfo_full[2];
-    uint64_t mma_final;
+    uint64_t mma_final, gram_final;
     uint64_t pair_sync[2];   // warps 2p and 2p + 1: one 64-row block (C = 64, 128)
     uint64_t quad_sync;      // all four inverse warps (C = 128)
-    TileInfo einfo[2];       // tile info for the epilogue warps, written by the MMA warp
+    TileInfo einfo[2];       // tile info for the epilogue warps, written by the W|U warp
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -456,6 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->einfo_full[0], 1);
         mbar_init(&bars->einfo_full[1], 1);
         mbar_init(&bars->mma_final, 1);
+        mbar_init(&bars->gram_final, 1);
         mbar_init(&bars->pair_sync[0], 64);
         mbar_init(&bars->pair_sync[1], 64);
         mbar_init(&bars->quad_sync, 128);
@@ -578,114 +580,92 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
-    } else if (warp == kWarpMma) {
-        // ------------------------------------------------------------------ MMA issuer (event loop)
+    } else if (warp == kWarpGram) {
+        // ------------------------------------------------------------------ Gram issuer
+        // Tile by tile: wait for the stage, zero the rows of a short chunk, wait for the Gram
+        // columns of tensor memory, issue S = K K^T.  A thread of its own, so that a Gram is never
+        // held up behind the issue of a W|U MMA (whose instructions wait for the tensor pipe).
         const uint32_t idesc_gram = idesc_bf16_f32(128, 128, 0, 0);
+        for (int i = 0;; ++i) {
+            const int s = i % kNS;
+            if (!wait_bar(&bars->full[s], (uint32_t)(i / kNS) & 1u, bars, p.status)) break;
+            const TileInfo info = *stage_info(s);
+            if (info.done) break;
+            if (lane == 0) KKT_TRACE_EVENT(EV_M_FULL, i);
+            if (info.Lc < C) {
+                // zero rows Lc..C-1 of every head's K and V boxes
+                uint8_t *st = stage_kv(s);
+                const int per_box = (C - info.Lc) * 8;  // 16-byte chunks
+                for (int e = lane; e < G * 4 * per_box; e += 32) {
+                    const int box = e / per_box, w = e % per_box;
+                    const int g = box % G, kvh = box / G;  // kvh: K half 0, 1, V half 0, 1
+                    *reinterpret_cast<uint4 *>(st + kvh * 16384 + g * C * 128 + (info.Lc + w / 8) * 128 +
+                                               (w % 8) * 16) = make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            if (!wait_bar(&bars->gram_empty, ((uint32_t)i & 1u) ^ 1u, bars, p.status)) break;
+            if (lane == 0) {
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(stage_kv(s));
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t d = sw128_desc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                    mma_ss(tmem + kColGram, d, d, idesc_gram, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&bars->gram_full);
+                KKT_TRACE_EVENT(EV_M_GRAM, i);
+            }
+            __syncwarp();
+        }
+        // every MMA issued by this thread has completed before tensor memory is freed
+        if (lane == 0) {
+            mma_commit(&bars->gram_final);
+            volatile int never = 0;
+            mbar_wait(&bars->gram_final, 0u, &never, kWaitLimitNs);
+        }
+        __syncwarp();
+    } else if (warp == kWarpMma) {
+        // ------------------------------------------------------------------ W|U issuer
+        // Tile by tile: once T~ is in tensor memory and the epilogue has drained D, hand the tile
+        // info to the epilogue and issue D = T~ [K|V] (hi and lo passes); the commit frees T~, the
+        // stage, and tells the epilogue that D is ready.  The stage's info marks the end of work.
         const uint32_t idesc_epi = idesc_bf16_f32(128, 256, 0, 1);
-        int g_next = 0;        // next tile whose Gram MMA is due
-        int e_next = 0;        // next tile whose W|U MMA is due
-        int done_at = -1;      // tile index of the end-of-work marker
-        bool g_ready = false;  // stage of g_next has landed (and is zero-padded)
-        uint64_t t_idle = globaltimer_ns();
-        while (true) {
-            bool progress = false;
-            if (done_at < 0 && !g_ready && g_next - e_next < kNS) {
-                const int s = g_next % kNS;
-                const bool landed = __shfl_sync(0xffffffffu, mbar_test(&bars->full[s], (uint32_t)(g_next / kNS) & 1u), 0);
-                if (landed) {
-                    const TileInfo info = *stage_info(s);
-                    if (lane == 0) KKT_TRACE_EVENT(EV_M_FULL, g_next);
-                    if (info.done) {
-                        done_at = g_next;
-                    } else {
-                        if (info.Lc < C) {
-                            // zero rows Lc..C-1 of every head's K and V boxes
-                            uint8_t *st = stage_kv(s);
-                            const int per_box = (C - info.Lc) * 8;  // 16-byte chunks
-                            for (int e = lane; e < G * 4 * per_box; e += 32) {
-                                const int box = e / per_box, w = e % per_box;
-                                const int g = box % G, kvh = box / G;  // kvh: K half 0, 1, V half 0, 1
-                                *reinterpret_cast<uint4 *>(st + kvh * 16384 + g * C * 128 + (info.Lc + w / 8) * 128 +
-                                                           (w % 8) * 16) = make_uint4(0, 0, 0, 0);
-                            }
-                            fence_proxy_async_smem();
-                            __syncwarp();
-                        }
-                        g_ready = true;
-                    }
-                    progress = true;
-                }
-            }
-            if (g_ready) {
-                const bool free = __shfl_sync(0xffffffffu, mbar_test(&bars->gram_empty, ((uint32_t)g_next & 1u) ^ 1u), 0);
-                if (free) {
-                    if (lane == 0) {
-                        tc_fence_after();
-                        const uint32_t a0 = smem_u32(stage_kv(g_next % kNS));
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint64_t d = sw128_desc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-                            mma_ss(tmem + kColGram, d, d, idesc_gram, kk > 0 ? 1u : 0u);
-                        }
-                        mma_commit(&bars->gram_full);
-                        KKT_TRACE_EVENT(EV_M_GRAM, g_next);
-                    }
-                    __syncwarp();
-                    ++g_next;
-                    g_ready = false;
-                    progress = true;
-                }
-            }
-            if (e_next < g_next) {
-                const bool ready = __shfl_sync(0xffffffffu,
-                                               mbar_test(&bars->tt_full, (uint32_t)e_next & 1u) &&
-                                                   mbar_test(&bars->d_empty, ((uint32_t)e_next & 1u) ^ 1u),
-                                               0);
-                if (ready) {
-                    const int s = e_next % kNS;
-                    if (lane == 0) {
-                        KKT_TRACE_EVENT(EV_M_READY, e_next);
-                        bars->einfo[e_next & 1] = *stage_info(s);
-                        mbar_arrive(&bars->einfo_full[e_next & 1]);
-                        tc_fence_after();
-                        const uint32_t b0 = smem_u32(stage_kv(s));
-#pragma unroll
-                        for (int pass = 0; pass < 2; ++pass)
-#pragma unroll
-                            for (int kk = 0; kk < 8; ++kk) {
-                                const uint64_t d = sw128_desc(b0 + kk * 2048, 16384, 1024);
-                                mma_ts(tmem + kColD, tmem + kColTT + pass * 64 + kk * 8, d, idesc_epi,
-                                       (pass | kk) ? 1u : 0u);
-                            }
-                        mma_commit(&bars->tt_empty);
-                        mma_commit(&bars->d_full);
-                        mma_commit(&bars->empty[s]);
-                        KKT_TRACE_EVENT(EV_M_EPI, e_next);
-                    }
-                    __syncwarp();
-                    ++e_next;
-                    progress = true;
-                }
-            }
-            if (done_at >= 0 && e_next == done_at) {
+        for (int i = 0;; ++i) {
+            const int s = i % kNS;
+            if (!wait_bar(&bars->full[s], (uint32_t)(i / kNS) & 1u, bars, p.status)) break;
+            const TileInfo info = *stage_info(s);
+            if (info.done) {
                 if (lane == 0) {
-                    bars->einfo[e_next & 1].done = 1;
-                    mbar_arrive(&bars->einfo_full[e_next & 1]);
+                    bars->einfo[i & 1] = info;
+                    mbar_arrive(&bars->einfo_full[i & 1]);
                 }
                 __syncwarp();
                 break;
             }
-            if (progress) {
-                t_idle = globaltimer_ns();
-            } else {
-                __nanosleep(64);  // leave issue slots to the inverse warp on this sub-partition
-                const bool stop = __shfl_sync(0xffffffffu, bars->abort_flag != 0 ||
-                                                               globaltimer_ns() - t_idle > kWaitLimitNs, 0);
-                if (stop) {
-                    if (lane == 0) fail(bars, p.status);
-                    break;
-                }
+            if (!wait_bar(&bars->tt_full, (uint32_t)i & 1u, bars, p.status)) break;
+            if (!wait_bar(&bars->d_empty, ((uint32_t)i & 1u) ^ 1u, bars, p.status)) break;
+            if (lane == 0) {
+                KKT_TRACE_EVENT(EV_M_READY, i);
+                bars->einfo[i & 1] = info;
+                mbar_arrive(&bars->einfo_full[i & 1]);
+                tc_fence_after();
+                const uint32_t b0 = smem_u32(stage_kv(s));
+#pragma unroll
+                for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t d = sw128_desc(b0 + kk * 2048, 16384, 1024);
+                        mma_ts(tmem + kColD, tmem + kColTT + pass * 64 + kk * 8, d, idesc_epi,
+                               (pass | kk) ? 1u : 0u);
+                    }
+                mma_commit(&bars->tt_empty);
+                mma_commit(&bars->d_full);
+                mma_commit(&bars->empty[s]);
+                KKT_TRACE_EVENT(EV_M_EPI, i);
             }
+            __syncwarp();
         }
         // every MMA issued by this thread has completed before tensor memory is freed
         if (lane == 0) {
