@@ -25,6 +25,17 @@
  *   3. §1 (the two products the inverse feeds):
  *          W = T diag(beta) K,    U~ = T diag(beta) V.
  *
+ *   Gated variant ("TileLang 实战：单位下三角矩阵求逆" §5 item 12: with a gate
+ *   the coefficient becomes diag(beta)(Gamma o K K^T)).  The gate input is a
+ *   per-token log decay g_t (the FlashQLA page's `g`, "FlashQLA" usage
+ *   section; its decay alpha_t = exp(g_t) lies in (0, 1), "Gate 衰减性质"
+ *   section).  Gamma[i][j] is the decay from token j to token i of the same
+ *   chunk, the product of alpha_t over j < t <= i, computed as
+ *   exp(sum_{t=j+1..i} g_t).  Only the coefficient changes: step 1 becomes
+ *          A = I + strictLower(diag(beta)(Gamma o K K^T)),
+ *   steps 2 and 3 are as above (the page states no other change).  The gate
+ *   restarts at every chunk: Gamma involves only tokens of the chunk.
+ *
  *   Output layout (the CUDA library's layout, fixed by its C header):
  *     T_out[n][h][0..C)  row n holds row (n - chunk start) of its chunk's T,
  *                        with zeros in columns j >= Lc;
@@ -36,6 +47,7 @@
  * tests pass the bf16-rounded inputs widened to double, and beta's fp32
  * value widened to double).
  */
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -43,10 +55,22 @@
 #include <omp.h>
 #endif
 
-/* Step 1: A = I + strictLower(diag(beta) K K^T), C x C, row-major.  Rows and
- * columns >= Lc (padding of a short last chunk) are those of the identity. */
-static void build_coefficients(const double *kc, const double *bc, int Lc, int C,
-                               int dk, double *A)
+/* Gamma[i][j] for j < i: the gate's decay from token j to token i of the
+ * chunk, exp of the sum of the log decays of tokens j+1 .. i. */
+static double gate_decay(const double *gc, int j, int i)
+{
+    double s = 0.0;
+    for (int t = j + 1; t <= i; ++t)
+        s += gc[t];
+    return exp(s);
+}
+
+/* Step 1: A = I + strictLower(diag(beta) K K^T), C x C, row-major, times
+ * Gamma elementwise when the chunk has a gate (gc: its log decays, or NULL).
+ * Rows and columns >= Lc (padding of a short last chunk) are those of the
+ * identity. */
+static void build_coefficients(const double *kc, const double *bc, const double *gc,
+                               int Lc, int C, int dk, double *A)
 {
     for (int i = 0; i < C; ++i) {
         for (int j = 0; j < C; ++j) {
@@ -58,6 +82,8 @@ static void build_coefficients(const double *kc, const double *bc, int Lc, int C
                 for (int d = 0; d < dk; ++d)
                     dot += kc[(int64_t)i * dk + d] * kc[(int64_t)j * dk + d];
                 a = bc[i] * dot;
+                if (gc)
+                    a *= gate_decay(gc, j, i);
             }
             A[(int64_t)i * C + j] = a;
         }
@@ -97,12 +123,13 @@ static void apply_scaled(const double *X, const double *bc, const double *mc,
 /*
  * One chunk, contiguous inputs.
  *   kc [Lc][dk], vc [Lc][dv], bc [Lc]       (rows of one head)
+ *   gc [Lc] log decays of the gated variant, or NULL
  *   T  [Lc][C]  (zeros in columns >= Lc), W [Lc][dk], U [Lc][dv]
  *   A_out, if not NULL, receives the C x C coefficient matrix.
  * Returns 0, or -1 on bad sizes / allocation failure.
  */
 int kkt_oracle_chunk(const double *kc, const double *vc, const double *bc,
-                     int Lc, int C, int dk, int dv,
+                     const double *gc, int Lc, int C, int dk, int dv,
                      double *T, double *W, double *U, double *A_out)
 {
     if (Lc < 1 || Lc > C || C < 1 || dk < 1 || dv < 1)
@@ -115,7 +142,7 @@ int kkt_oracle_chunk(const double *kc, const double *vc, const double *bc,
         return -1;
     }
     memcpy(bz, bc, sizeof(double) * (size_t)Lc);
-    build_coefficients(kc, bz, Lc, C, dk, A);
+    build_coefficients(kc, bz, gc, Lc, C, dk, A);
     invert_unit_lower(A, C, X);
     for (int i = 0; i < Lc; ++i)
         for (int j = 0; j < C; ++j)
@@ -132,6 +159,7 @@ int kkt_oracle_chunk(const double *kc, const double *vc, const double *bc,
  * Whole tensors.
  *   k    [N][H][dk], v [N][H][dv], beta [N][H]  (N = B*T fixed-length, or the
  *        packed token count T when cu_seqlens is given)
+ *   g    [N][H] log decays of the gated variant, or NULL
  *   cu_seqlens: NULL for B sequences of T tokens each; otherwise B+1
  *        nondecreasing offsets with cu_seqlens[0] = 0, cu_seqlens[B] = T.
  *   T_out [N][H][C], W_out [N][H][dk], U_out [N][H][dv].
@@ -139,7 +167,7 @@ int kkt_oracle_chunk(const double *kc, const double *vc, const double *bc,
  * Returns 0, -1 on bad arguments, -2 on a malformed cu_seqlens.
  */
 int kkt_oracle_fwd(const double *k, const double *v, const double *beta,
-                   const int64_t *cu_seqlens, int64_t B, int64_t T, int64_t H,
+                   const double *g, const int64_t *cu_seqlens, int64_t B, int64_t T, int64_t H,
                    int64_t dk, int64_t dv, int64_t C,
                    double *T_out, double *W_out, double *U_out, int nthreads)
 {
@@ -188,10 +216,11 @@ int kkt_oracle_fwd(const double *k, const double *v, const double *beta,
         double *kc = (double *)malloc(sizeof(double) * (size_t)(C * dk));
         double *vc = (double *)malloc(sizeof(double) * (size_t)(C * dv));
         double *bc = (double *)malloc(sizeof(double) * (size_t)C);
+        double *gc = (double *)malloc(sizeof(double) * (size_t)C);
         double *Tc = (double *)malloc(sizeof(double) * (size_t)(C * C));
         double *Wc = (double *)malloc(sizeof(double) * (size_t)(C * dk));
         double *Uc = (double *)malloc(sizeof(double) * (size_t)(C * dv));
-        int ok = kc && vc && bc && Tc && Wc && Uc;
+        int ok = kc && vc && bc && gc && Tc && Wc && Uc;
 #pragma omp for schedule(dynamic, 4)
         for (int64_t u = 0; u < units; ++u) {
             if (!ok)
@@ -204,8 +233,11 @@ int kkt_oracle_fwd(const double *k, const double *v, const double *beta,
                 memcpy(kc + (int64_t)i * dk, k + (n * H + h) * dk, sizeof(double) * (size_t)dk);
                 memcpy(vc + (int64_t)i * dv, v + (n * H + h) * dv, sizeof(double) * (size_t)dv);
                 bc[i] = beta[n * H + h];
+                if (g)
+                    gc[i] = g[n * H + h];
             }
-            if (kkt_oracle_chunk(kc, vc, bc, Lc, (int)C, (int)dk, (int)dv, Tc, Wc, Uc, NULL) != 0) {
+            if (kkt_oracle_chunk(kc, vc, bc, g ? gc : NULL, Lc, (int)C, (int)dk, (int)dv, Tc, Wc, Uc,
+                                 NULL) != 0) {
 #pragma omp atomic write
                 status = -1;
                 continue;
@@ -221,7 +253,7 @@ int kkt_oracle_fwd(const double *k, const double *v, const double *beta,
 #pragma omp atomic write
             status = -1;
         }
-        free(kc); free(vc); free(bc); free(Tc); free(Wc); free(Uc);
+        free(kc); free(vc); free(bc); free(gc); free(Tc); free(Wc); free(Uc);
     }
     free(cstart);
     free(clen);

@@ -11,8 +11,12 @@ and raises AssertionError when the oracle disagrees with:
     block nonzero) and orthogonal keys,
   * causality of the chunk (a short last chunk equals the top-left block of a
     full one), the varlen/fixed-length equivalence and the tensor layout,
-  * the page's measured cond(A) bounds.
-Sources: "TileLang 实战：单位下三角矩阵求逆" §1, §2.1, §2.2, §2.4, §3.2, §4.
+  * the page's measured cond(A) bounds,
+  * the gated coefficient diag(beta)(Gamma o K K^T) (§5 item 12): no decay is the
+    ungated oracle; the page's two differently scaled copies of K; a constant gate
+    is a diagonal similarity of the ungated matrix; a token with zero decay cuts the
+    chunk into independent blocks; the tensor layout of the gate.
+Sources: "TileLang 实战：单位下三角矩阵求逆" §1, §2.1, §2.2, §2.4, §3.2, §4, §5.
 """
 from __future__ import annotations
 
@@ -280,6 +284,100 @@ def pin_cond_bounds(lib):
         assert worst <= bounds[str(C)], (C, worst)
 
 
+# --- the gated coefficient ------------------------------------------------------------------
+
+def pin_gate_zero_is_ungated(lib):
+    """g = 0 (decay alpha = 1 everywhere): the gated oracle is the ungated one, bit for bit."""
+    rng = np.random.default_rng(30)
+    k, v, beta = _rand_chunk(rng, 50, 32, 16)
+    ref = oracle.oracle_chunk(k, v, beta, 64, lib=lib)
+    got = oracle.oracle_chunk(k, v, beta, 64, lib=lib, g=np.zeros(50))
+    for a, b in zip(ref, got):
+        np.testing.assert_array_equal(a, b)
+
+
+def pin_gate_two_scaled_keys(lib):
+    """The gated A is I + strictLower((diag(beta e^G) K)(diag(e^-G) K)^T), G the prefix sums of
+    the chunk's log decays: the two differently scaled copies of K of §5 item 12."""
+    rng = np.random.default_rng(31)
+    for Lc, C in ((64, 64), (40, 64), (128, 128), (9, 32)):
+        k, v, beta = _rand_chunk(rng, Lc, 32, 8)
+        g = rng.uniform(-0.2, 0.0, Lc)
+        G = np.cumsum(g)
+        left = (beta * np.exp(G))[:, None] * k
+        right = np.exp(-G)[:, None] * k
+        _, _, _, A = oracle.oracle_chunk(k, v, beta, C, lib=lib, g=g)
+        expect = np.eye(C)
+        expect[:Lc, :Lc] += np.tril(left @ right.T, -1)
+        np.testing.assert_allclose(A, expect, atol=1e-13, rtol=0)
+
+
+def pin_gate_constant_similarity(lib):
+    """A constant gate g_t = c gives Gamma[i][j] = e^{c (i - j)}: A = D A0 D^-1 with D = diag(e^{c i})
+    and A0 the ungated matrix, so T = D T0 D^-1 with T0 the ungated inverse."""
+    rng = np.random.default_rng(32)
+    Lc, C, c = 48, 64, -0.15
+    k, v, beta = _rand_chunk(rng, Lc, 32, 16)
+    T0, _, _, _ = oracle.oracle_chunk(k, v, beta, C, lib=lib)
+    T, W, U, _ = oracle.oracle_chunk(k, v, beta, C, lib=lib, g=np.full(Lc, c))
+    idx = np.arange(Lc)
+    expect = T0[:, :Lc] * np.exp(c * (idx[:, None] - idx[None, :]))
+    np.testing.assert_allclose(T[:, :Lc], expect, atol=1e-13, rtol=0)
+    assert np.all(T[:, Lc:] == 0.0)
+    np.testing.assert_allclose(W, expect @ (beta[:, None] * k), atol=1e-12, rtol=0)
+    np.testing.assert_allclose(U, expect @ (beta[:, None] * v), atol=1e-12, rtol=0)
+
+
+def pin_gate_cut_decouples(lib):
+    """A token whose decay is zero (g_c = -1000: exp underflows to 0) cuts the chunk: Gamma[i][j] = 0
+    for j < c <= i, so T is block diagonal; the leading block is the chunk of tokens 0..c-1 alone and
+    the trailing block the chunk of tokens c.. alone (g_c itself enters no product there)."""
+    rng = np.random.default_rng(33)
+    Lc, C, cut = 60, 64, 23
+    k, v, beta = _rand_chunk(rng, Lc, 32, 16)
+    g = rng.uniform(-0.3, 0.0, Lc)
+    g[cut] = -1000.0
+    T, W, U, _ = oracle.oracle_chunk(k, v, beta, C, lib=lib, g=g)
+    T1, W1, U1, _ = oracle.oracle_chunk(k[:cut], v[:cut], beta[:cut], C, lib=lib, g=g[:cut])
+    T2, W2, U2, _ = oracle.oracle_chunk(k[cut:], v[cut:], beta[cut:], C, lib=lib, g=g[cut:])
+    assert np.all(T[cut:, :cut] == 0.0) and np.all(T[:cut, cut:] == 0.0)
+    np.testing.assert_allclose(T[:cut, :cut], T1[:, :cut], atol=1e-14, rtol=0)
+    np.testing.assert_allclose(T[cut:, cut:Lc], T2[:, :Lc - cut], atol=1e-14, rtol=0)
+    for X, X1, X2 in ((W, W1, W2), (U, U1, U2)):
+        np.testing.assert_allclose(X[:cut], X1, atol=1e-14, rtol=0)
+        np.testing.assert_allclose(X[cut:], X2, atol=1e-14, rtol=0)
+
+
+def pin_gate_tensor_layout(lib):
+    """Whole-tensor driver with a gate: token n, head h of chunk c equals the chunk computed alone
+    with that chunk's own gates (the gate restarts at every chunk), fixed length and varlen."""
+    rng = np.random.default_rng(34)
+    B, T, H, dk, dv, C = 2, 70, 3, 16, 8, 32
+    k = rng.standard_normal((B, T, H, dk)); k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((B, T, H, dv))
+    beta = rng.uniform(0.05, 0.95, (B, T, H))
+    g = rng.uniform(-0.5, 0.0, (B, T, H))
+    To, Wo, Uo = oracle.oracle_fwd(k, v, beta, C, lib=lib, g=g)
+    for b in range(B):
+        for h in range(H):
+            for t0 in range(0, T, C):
+                t1 = min(T, t0 + C)
+                Tc, Wc, Uc, _ = oracle.oracle_chunk(k[b, t0:t1, h], v[b, t0:t1, h], beta[b, t0:t1, h], C,
+                                                    lib=lib, g=g[b, t0:t1, h])
+                np.testing.assert_array_equal(To[b, t0:t1, h], Tc)
+                np.testing.assert_array_equal(Wo[b, t0:t1, h], Wc)
+                np.testing.assert_array_equal(Uo[b, t0:t1, h], Uc)
+    cu = [0, 20, 20, 101, 140]
+    kf, vf, bf, gf = (x.reshape((1, B * T) + x.shape[2:]) for x in (k, v, beta, g))
+    To, Wo, Uo = oracle.oracle_fwd(kf, vf, bf, C, cu_seqlens=cu, lib=lib, g=gf)
+    for s in range(len(cu) - 1):
+        a, e = cu[s], cu[s + 1]
+        Ts, Ws, Us = oracle.oracle_fwd(kf[:, a:e], vf[:, a:e], bf[:, a:e], C, lib=lib, g=gf[:, a:e])
+        np.testing.assert_array_equal(To[:, a:e], Ts)
+        np.testing.assert_array_equal(Wo[:, a:e], Ws)
+        np.testing.assert_array_equal(Uo[:, a:e], Us)
+
+
 PINS = [
     pin_closed_form_c3,
     pin_exact_rational_bruteforce,
@@ -293,4 +391,9 @@ PINS = [
     pin_tensor_layout,
     pin_varlen_equals_fixed,
     pin_cond_bounds,
+    pin_gate_zero_is_ungated,
+    pin_gate_two_scaled_keys,
+    pin_gate_constant_similarity,
+    pin_gate_cut_decouples,
+    pin_gate_tensor_layout,
 ]

@@ -27,6 +27,12 @@ MUTATIONS = {
     "beta_wrong_head": ("bc[i] = beta[n * H + h];", "bc[i] = beta[n * H + (H - 1 - h)];"),
     "short_chunk_length": ("clen[q] = (int)((t1 - a) < C ? (t1 - a) : C);",
                            "clen[q] = (int)((t1 - a) < C ? (t1 - a) : C - 1);"),
+    # the gated coefficient
+    "gate_includes_first_token": ("for (int t = j + 1; t <= i; ++t)", "for (int t = j; t <= i; ++t)"),
+    "gate_drops_last_token": ("for (int t = j + 1; t <= i; ++t)", "for (int t = j + 1; t < i; ++t)"),
+    "gate_sign": ("return exp(s);", "return exp(-s);"),
+    "gate_wrong_head": ("gc[i] = g[n * H + h];", "gc[i] = g[n * H + (H - 1 - h)];"),
+    "gate_ignored": ("a *= gate_decay(gc, j, i);", "a *= 1.0;"),
 }
 
 
