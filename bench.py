@@ -34,7 +34,7 @@ ROOT = Path(__file__).resolve().parent
 sys.path.insert(0, str(ROOT))
 
 from gdn_chunkwise_ut_gb300 import costmodel  # noqa: E402
-from gdn_chunkwise_ut_gb300.inputs import workloads  # noqa: E402
+from gdn_chunkwise_ut_gb300.inputs import make_gate, workloads  # noqa: E402
 
 METRIC = "tokens/sec and achieved HBM GB/s (% of GB300 peak) for kkt_solve fwd, C=64"
 DEFAULT_WORKLOAD = "c3_b4_t8192_h16"
@@ -57,6 +57,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-t-out", action="store_true", help="W and U~ only: T computed, not written")
     ap.add_argument("--t-f16", action="store_true", help="T written in fp16 instead of fp32")
+    ap.add_argument("--gated", action="store_true",
+                    help="gated variant: coefficient diag(beta)(Gamma o K K^T) from per-token log decays g")
     args = ap.parse_args()
     if args.no_t_out and args.t_f16:
         ap.error("--no-t-out and --t-f16 exclude each other")
@@ -199,6 +201,7 @@ def bench_ours(args, rank, world, local):
     torch.cuda.set_device(dev)
     kernel = select_kernel(w.dk, w.dv, w.C, w.io, args.kernel)
     k, v, beta, cu = w.make(seed=rank, device=dev)
+    g = make_gate(k.shape[0], k.shape[1], w.H, seed=rank, device=dev) if args.gated else None
     cu_t = None if cu is None else torch.as_tensor(cu, dtype=torch.int32, device=dev)
     T_dtype = torch.float16 if args.t_f16 else torch.float32
     T_out = torch.empty((k.shape[0], k.shape[1], w.H, w.C), device=dev, dtype=T_dtype)
@@ -208,7 +211,7 @@ def bench_ours(args, rank, world, local):
 
     def step():
         kkt_solve_fwd(k, v, beta, w.C, cu_t, T_out=None if args.no_t_out else T_out, W_out=W_out, U_out=U_out,
-                      kernel=args.kernel, materialize_T=not args.no_t_out, T_dtype=T_dtype)
+                      kernel=args.kernel, materialize_T=not args.no_t_out, T_dtype=T_dtype, g=g)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -226,7 +229,7 @@ def bench_ours(args, rank, world, local):
     # workspace clear and launch gaps.  Inputs that fit in L2: every step gets its own events and
     # L2 is flushed before it (a write of twice its size, outside the events).
     K = args.steps
-    in_bytes = sum(x.numel() * x.element_size() for x in (k, v, beta))
+    in_bytes = sum(x.numel() * x.element_size() for x in (k, v, beta, g) if x is not None)
     flush = in_bytes <= L2_BYTES
     scrub = torch.empty(2 * L2_BYTES // 4, dtype=torch.int32, device=dev) if flush else None
     barrier(world)
@@ -256,24 +259,26 @@ def bench_ours(args, rank, world, local):
     units = w.tokens * w.H
     io_bytes = 4 if w.io == "f32" else 2
     alg_bytes = units * costmodel.bytes_per_unit(w.C, w.dk, w.dv, io_bytes, t_out=not args.no_t_out,
-                                                  t_bytes=2 if args.t_f16 else 4)
+                                                  t_bytes=2 if args.t_f16 else 4, gated=args.gated)
     tokens_per_s = aggregate_value(w.tokens * K, world, max_ms / 1e3)
     peak, peak_src = hbm_peak()
     achieved = alg_bytes / (launch_ms / 1e3) / 1e9
     # the recorded counters are those of the default call (fp32 T)
-    traffic = None if (args.no_t_out or args.t_f16) else recorded_traffic(kernel, args.workload)
+    traffic = None if (args.no_t_out or args.t_f16 or args.gated) else recorded_traffic(kernel, args.workload)
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     runner = HostRunner(k.shape[0], k.shape[1], w.H, w.dk, w.dv, w.C, dtype=k.dtype, cu_seqlens=cu,
-                        kernel=args.kernel, device=dev, materialize_T=not args.no_t_out, T_dtype=T_dtype)
+                        kernel=args.kernel, device=dev, materialize_T=not args.no_t_out, T_dtype=T_dtype,
+                        gated=args.gated)
     kh, vh, bh = (x.cpu().pin_memory() for x in (k, v, beta))
+    gh = g.cpu().pin_memory() if g is not None else None
     for _ in range(2):
-        runner(kh, vh, bh)
+        runner(kh, vh, bh, g_host=gh)
     n_e2e = max(3, args.e2e_steps)
     barrier(world)
     t0 = time.perf_counter()
     for _ in range(n_e2e):
-        runner(kh, vh, bh)
+        runner(kh, vh, bh, g_host=gh)
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
     e2e = {"value": aggregate_value(w.tokens * n_e2e, world, e2e_s), "unit": "tokens/s",
            "h2d_bytes_per_step": runner.h2d_bytes, "d2h_bytes_per_step": runner.d2h_bytes,
@@ -287,6 +292,7 @@ def bench_ours(args, rank, world, local):
         "config": {"workload": args.workload, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
                    "C": w.C, "tokens_per_step": w.tokens, "kernel": kernel,
                    "T_out": False if args.no_t_out else "fp16" if args.t_f16 else "fp32",
+                   "gated": args.gated,
                    "l2": (f"inputs ({in_bytes / 1e6:.0f} MB) fit in the 129 MB L2: flushed before every step"
                           if flush else f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB > 129 MB), no flush")},
         "hbm_gbs": achieved, "hbm_frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
@@ -298,25 +304,29 @@ def bench_ours(args, rank, world, local):
         "clocks": clocks, "e2e": e2e, "gpu_launches": K,
     }
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(k, v, beta, cu, w)
+        line["cpu_baseline"] = cpu_baseline(k, v, beta, cu, w, g=g)
     return line
 
 
-def cpu_baseline(k, v, beta, cu, w, max_tokens=None):
+def cpu_baseline(k, v, beta, cu, w, max_tokens=None, g=None):
     """The oracle, as it stands, on the host cores over a bounded sample of the workload."""
     import oracle
     oracle.build()
+    gs = None
     if cu is None:
         nseq = w.B if max_tokens is None else max(1, min(w.B, max_tokens // w.T))
         ks, vs, bs = (x[:nseq].cpu().double().numpy() for x in (k, v, beta))
+        if g is not None:
+            gs = g[:nseq].cpu().double().numpy()
         sample = f"{nseq} of {w.B} sequences x {w.T} tokens x {w.H} heads (fp64 oracle on bf16-rounded inputs)"
         tokens, cus = nseq * w.T, None
     else:
         ks, vs, bs = (x.cpu().double().numpy() for x in (k, v, beta))
+        gs = None if g is None else g.cpu().double().numpy()
         tokens, cus, sample = w.tokens, cu, f"all {w.tokens} packed tokens x {w.H} heads"
     cores = oracle.oracle_threads(0)
     t0 = time.perf_counter()
-    oracle.oracle_fwd(ks, vs, bs, w.C, cu_seqlens=cus, nthreads=cores)
+    oracle.oracle_fwd(ks, vs, bs, w.C, cu_seqlens=cus, nthreads=cores, g=gs)
     dt = time.perf_counter() - t0
     return {"value": tokens / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": sample, "seconds": dt}
@@ -339,18 +349,20 @@ def bench_reference(args, rank, world):
     probe_tokens = w.C * 4
     k, v, b = make_inputs(1, probe_tokens, w.H, w.dk, w.dv, seed=0)
     kd, vd, bd = (x.double().numpy() for x in (k, v, b))
+    gd = make_gate(1, probe_tokens, w.H, seed=0).double().numpy() if args.gated else None
     t0 = time.perf_counter()
-    oracle.oracle_fwd(kd, vd, bd, w.C, nthreads=cores)
+    oracle.oracle_fwd(kd, vd, bd, w.C, nthreads=cores, g=gd)
     per_token = (time.perf_counter() - t0) / probe_tokens
     budget = 120.0 / max(1, args.steps + args.warmup)
     tokens = int(max(w.C, min(w.T, (budget / per_token) // w.C * w.C)))
     k, v, b = make_inputs(1, tokens, w.H, w.dk, w.dv, seed=0)
     kd, vd, bd = (x.double().numpy() for x in (k, v, b))
+    gd = make_gate(1, tokens, w.H, seed=0).double().numpy() if args.gated else None
     for _ in range(args.warmup):
-        oracle.oracle_fwd(kd, vd, bd, w.C, nthreads=cores)
+        oracle.oracle_fwd(kd, vd, bd, w.C, nthreads=cores, g=gd)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.oracle_fwd(kd, vd, bd, w.C, nthreads=cores)
+        oracle.oracle_fwd(kd, vd, bd, w.C, nthreads=cores, g=gd)
     dt = time.perf_counter() - t0
     val = tokens * args.steps / dt
     sample = f"{tokens} tokens x {w.H} heads of one {w.T}-token sequence per step (fp64 oracle)"
@@ -359,7 +371,8 @@ def bench_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": args.workload, "B": w.B, "T": w.T, "H": w.H,
-                                        "dk": w.dk, "dv": w.dv, "C": w.C, "tokens_per_step": tokens},
+                                        "dk": w.dk, "dv": w.dv, "C": w.C, "tokens_per_step": tokens,
+                                        "gated": args.gated},
         "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,

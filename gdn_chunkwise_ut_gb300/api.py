@@ -48,12 +48,14 @@ def _workspace(device: torch.device) -> torch.Tensor:
 def kkt_solve_fwd(k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor, C: int,
                   cu_seqlens: torch.Tensor | None = None, *, T_out=None, W_out=None, U_out=None,
                   kernel: str = "auto", workspace="auto", stream=None, materialize_T: bool = True,
-                  T_dtype=torch.float32):
+                  T_dtype=torch.float32, g: torch.Tensor | None = None):
     """UT transform of every chunk: returns (T_out, W, U).
 
     ``materialize_T=False`` computes T but does not write it: the call returns (None, W, U) and
     moves 4C bytes less per token and head.  ``T_dtype=torch.float16`` writes T rounded to fp16
-    (2C bytes per token and head); W and U are the same as with fp32 T.
+    (2C bytes per token and head); W and U are the same as with fp32 T.  ``g`` [B, T, H] fp32 (the
+    per-token log decays) selects the gated variant: A = I + strictLower(diag(beta)(Gamma o K K^T))
+    with Gamma[i][j] = exp(g_{j+1} + ... + g_i) inside each chunk.
 
     k [B, T, H, dk] and v [B, T, H, dv] (bf16, or fp32 for the fp32-I/O path),
     beta [B, T, H] fp32.  With ``cu_seqlens`` (int32 [N+1] on the device) the
@@ -77,6 +79,8 @@ def kkt_solve_fwd(k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor, C: int,
     _check(k, "k", k.dtype, (Bt, T, H, dk))
     _check(v, "v", k.dtype, (Bt, T, H, dv))
     _check(beta, "beta", torch.float32, (Bt, T, H))
+    if g is not None:
+        _check(g, "g", torch.float32, (Bt, T, H))
     if cu_seqlens is not None:
         if Bt != 1:
             raise ValueError("with cu_seqlens the batch dimension must be 1")
@@ -111,10 +115,15 @@ def kkt_solve_fwd(k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor, C: int,
         if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda:
             raise ValueError("workspace must be a CUDA tensor, 'auto' or None")
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
-    rc = _lib.lib().kkt_solve_fwd_ex(k.data_ptr(), v.data_ptr(), beta.data_ptr(), cu_ptr,
-                                     B, T, H, dk, dv, C, T_out.data_ptr() if materialize_T else None,
-                                     W_out.data_ptr(),
-                                     U_out.data_ptr(), io | t_flag, kern, ws_ptr, ws_bytes, _stream_handle(stream))
+    t_ptr = T_out.data_ptr() if materialize_T else None
+    if g is None:
+        rc = _lib.lib().kkt_solve_fwd_ex(k.data_ptr(), v.data_ptr(), beta.data_ptr(), cu_ptr, B, T, H, dk, dv, C,
+                                         t_ptr, W_out.data_ptr(), U_out.data_ptr(), io | t_flag, kern, ws_ptr,
+                                         ws_bytes, _stream_handle(stream))
+    else:
+        rc = _lib.lib().kkt_solve_fwd_gated(k.data_ptr(), v.data_ptr(), beta.data_ptr(), g.data_ptr(), cu_ptr, B, T,
+                                            H, dk, dv, C, t_ptr, W_out.data_ptr(), U_out.data_ptr(), io | t_flag,
+                                            kern, ws_ptr, ws_bytes, _stream_handle(stream))
     if rc != _lib.KKT_OK:
         raise _lib.KktError(rc, "kkt_solve_fwd")
     return T_out, W_out, U_out
@@ -142,12 +151,14 @@ class HostRunner:
     """
 
     def __init__(self, B, T, H, dk, dv, C, *, dtype=torch.bfloat16, cu_seqlens=None,
-                 kernel="auto", device="cuda", materialize_T: bool = True, T_dtype=torch.float32):
+                 kernel="auto", device="cuda", materialize_T: bool = True, T_dtype=torch.float32,
+                 gated: bool = False):
         self.C, self.kernel, self.materialize_T, self.T_dtype = C, kernel, materialize_T, T_dtype
         dev = torch.device(device)
         self.k = torch.empty((B, T, H, dk), device=dev, dtype=dtype)
         self.v = torch.empty((B, T, H, dv), device=dev, dtype=dtype)
         self.beta = torch.empty((B, T, H), device=dev, dtype=torch.float32)
+        self.g = torch.empty((B, T, H), device=dev, dtype=torch.float32) if gated else None
         self.cu = None if cu_seqlens is None else torch.as_tensor(cu_seqlens, dtype=torch.int32).to(dev)
         self.T_out = torch.empty((B, T, H, C), device=dev, dtype=T_dtype) if materialize_T else None
         self.W = torch.empty((B, T, H, dk), device=dev, dtype=dtype)
@@ -159,19 +170,21 @@ class HostRunner:
 
     @property
     def h2d_bytes(self) -> int:
-        return sum(t.numel() * t.element_size() for t in (self.k, self.v, self.beta))
+        return sum(t.numel() * t.element_size() for t in (self.k, self.v, self.beta, self.g) if t is not None)
 
     @property
     def d2h_bytes(self) -> int:
         return sum(t.numel() * t.element_size() for t in (self.T_out, self.W, self.U) if t is not None)
 
-    def __call__(self, k_host, v_host, beta_host, sync: bool = True):
+    def __call__(self, k_host, v_host, beta_host, sync: bool = True, g_host=None):
         self.k.copy_(k_host, non_blocking=True)
         self.v.copy_(v_host, non_blocking=True)
         self.beta.copy_(beta_host, non_blocking=True)
+        if self.g is not None:
+            self.g.copy_(g_host, non_blocking=True)
         kkt_solve_fwd(self.k, self.v, self.beta, self.C, self.cu, T_out=self.T_out, W_out=self.W,
                       U_out=self.U, kernel=self.kernel, materialize_T=self.materialize_T,
-                      T_dtype=self.T_dtype)
+                      T_dtype=self.T_dtype, g=self.g)
         if self.T_out is not None:
             self.T_host.copy_(self.T_out, non_blocking=True)
         self.W_host.copy_(self.W, non_blocking=True)

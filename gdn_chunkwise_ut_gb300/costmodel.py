@@ -89,10 +89,12 @@ def main_gemm_per_token(C: int, dk: int, dv: int) -> int:
     return 2 * dk * dv + C * (dk + dv)
 
 
-def bytes_per_unit(C: int, dk: int, dv: int, io_bytes: int = 2, t_out: bool = True, t_bytes: int = 4) -> int:
-    """Algorithmic HBM bytes per (token, head): read K, V, beta; write T (t_bytes per element:
-    4 for fp32, 2 for fp16; nothing when the call produces W and U only), W, U."""
-    return io_bytes * (dk + dv) + 4 + (t_bytes * C if t_out else 0) + io_bytes * (dk + dv)
+def bytes_per_unit(C: int, dk: int, dv: int, io_bytes: int = 2, t_out: bool = True, t_bytes: int = 4,
+                   gated: bool = False) -> int:
+    """Algorithmic HBM bytes per (token, head): read K, V, beta (and the fp32 log decay g when
+    gated); write T (t_bytes per element: 4 for fp32, 2 for fp16; nothing when the call produces
+    W and U only), W, U."""
+    return io_bytes * (dk + dv) + 4 + (4 if gated else 0) + (t_bytes * C if t_out else 0) + io_bytes * (dk + dv)
 
 
 def bytes_written_per_unit(C: int, dk: int, dv: int, io_bytes: int = 2) -> int:

@@ -58,11 +58,12 @@ extern "C" int kkt_select_kernel(int dk, int dv, int C, int io_dtype, int kernel
     }
 }
 
-extern "C" int kkt_solve_fwd_ex(const void *k, const void *v, const float *beta, const int32_t *cu_seqlens,
-                                int B, int T, int H, int dk, int dv, int C,
-                                void *T_out, void *W_out, void *U_out,
-                                int io_dtype, int kernel, void *workspace, size_t workspace_bytes,
-                                struct CUstream_st *stream) {
+namespace {
+
+// kkt_solve_fwd_ex and kkt_solve_fwd_gated: g == nullptr is the ungated call.
+int solve(const void *k, const void *v, const float *beta, const float *g, const int32_t *cu_seqlens,
+          int B, int T, int H, int dk, int dv, int C, void *T_out, void *W_out, void *U_out,
+          int io_dtype, int kernel, void *workspace, size_t workspace_bytes, struct CUstream_st *stream) {
     if (!k || !v || !beta || !W_out || !U_out) return KKT_ERR_ARG;  // T_out may be NULL
     if (workspace && workspace_bytes < KKT_WORKSPACE_BYTES) return KKT_ERR_ARG;
     if (workspace && !aligned16(workspace)) return KKT_ERR_ALIGN;
@@ -70,7 +71,7 @@ extern "C" int kkt_solve_fwd_ex(const void *k, const void *v, const float *beta,
     const int which = kkt_select_kernel(dk, dv, C, io_dtype, kernel);
     if (which < 0) return -which;
     if (!aligned16(k) || !aligned16(v) || !aligned16(T_out) || !aligned16(W_out) || !aligned16(U_out) ||
-        !aligned4(beta) || (cu_seqlens && !aligned4(cu_seqlens)))
+        !aligned4(beta) || (g && !aligned4(g)) || (cu_seqlens && !aligned4(cu_seqlens)))
         return KKT_ERR_ALIGN;
     const int64_t ntok = cu_seqlens ? (int64_t)T : (int64_t)B * T;
     if (ntok == 0) return KKT_OK;
@@ -78,7 +79,7 @@ extern "C" int kkt_solve_fwd_ex(const void *k, const void *v, const float *beta,
     if (ntok / C + B > 0x7fffffffLL) return KKT_ERR_ARG;
 
     kkt::Problem p;
-    p.k = k; p.v = v; p.beta = beta; p.cu_seqlens = cu_seqlens;
+    p.k = k; p.v = v; p.beta = beta; p.g = g; p.cu_seqlens = cu_seqlens;
     p.nseq = B; p.T = T; p.ntok = ntok;
     p.H = H; p.dk = dk; p.dv = dv; p.C = C;
     p.T_out = T_out; p.W_out = W_out; p.U_out = U_out;
@@ -96,6 +97,26 @@ extern "C" int kkt_solve_fwd_ex(const void *k, const void *v, const float *beta,
     // the workspace is zero on entry (zero-filled before first use, and left zero by every call)
     if (which == KKT_KERNEL_TC && workspace) p.tile_counter = static_cast<unsigned long long *>(workspace);
     return which == KKT_KERNEL_TC ? kkt::launch_tc(p) : kkt::launch_simt(p);
+}
+
+}  // namespace
+
+extern "C" int kkt_solve_fwd_ex(const void *k, const void *v, const float *beta, const int32_t *cu_seqlens,
+                                int B, int T, int H, int dk, int dv, int C,
+                                void *T_out, void *W_out, void *U_out,
+                                int io_dtype, int kernel, void *workspace, size_t workspace_bytes,
+                                struct CUstream_st *stream) {
+    return solve(k, v, beta, nullptr, cu_seqlens, B, T, H, dk, dv, C, T_out, W_out, U_out, io_dtype, kernel,
+                 workspace, workspace_bytes, stream);
+}
+
+extern "C" int kkt_solve_fwd_gated(const void *k, const void *v, const float *beta, const float *g,
+                                   const int32_t *cu_seqlens, int B, int T, int H, int dk, int dv, int C,
+                                   void *T_out, void *W_out, void *U_out,
+                                   int io_dtype, int kernel, void *workspace, size_t workspace_bytes,
+                                   struct CUstream_st *stream) {
+    return solve(k, v, beta, g, cu_seqlens, B, T, H, dk, dv, C, T_out, W_out, U_out, io_dtype, kernel,
+                 workspace, workspace_bytes, stream);
 }
 
 extern "C" int kkt_solve_fwd(const void *k, const void *v, const float *beta, const int32_t *cu_seqlens,
@@ -119,7 +140,7 @@ extern "C" const char *kkt_status_string(int status) {
         case KKT_OK: return "ok";
         case KKT_ERR_ARG: return "invalid argument";
         case KKT_ERR_UNSUPPORTED: return "unsupported chunk size, head dimension, dtype or kernel";
-        case KKT_ERR_ALIGN: return "pointer misaligned (16 B for k, v, T_out, W_out, U_out; 4 B for beta, cu_seqlens)";
+        case KKT_ERR_ALIGN: return "pointer misaligned (16 B for k, v, T_out, W_out, U_out; 4 B for beta, g, cu_seqlens)";
         case KKT_ERR_CUDA: return "CUDA error";
         case KKT_ERR_SEQLENS: return "malformed cu_seqlens";
         case KKT_ERR_TIMEOUT: return "device-side wait timed out";

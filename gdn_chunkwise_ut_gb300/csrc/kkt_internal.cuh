@@ -13,6 +13,7 @@ struct Problem {
     const void *k;
     const void *v;
     const float *beta;
+    const float *g = nullptr;   // per-token log decays of the gated variant, or nullptr
     const int32_t *cu_seqlens;  // nullptr: nseq sequences of T tokens each
     int nseq;                   // number of sequences (B)
     int T;                      // tokens per sequence, or the packed total with cu_seqlens

@@ -8,7 +8,7 @@
 // levels -L11^-1 L10 L00^-1 at s = 16, 32, ..., C/2 as shared-memory GEMMs.
 //
 // Shared memory (fp32): K [C][dk+1], V [C][dv+1], A/T [C][C+1], beta [C],
-// coupling scratch [C/2][C/2+1].  The +1 row padding keeps the column walks of
+// gate prefix sums [C], coupling scratch [C/2][C/2+1].  The +1 row padding keeps the column walks of
 // the Gram and epilogue loops on distinct banks.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -29,6 +29,7 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
 struct SimtParams {
     const void *k, *v;
     const float *beta;
+    const float *g;  // per-token log decays (gated variant), or nullptr
     const int32_t *cu;
     int nseq, T;
     int64_t ntok;
@@ -49,7 +50,8 @@ __global__ void __launch_bounds__(kSimtThreads) kkt_simt_kernel(const SimtParams
     float *Vs = Ks + C * KS;     // [C][VS]
     float *Ts = Vs + C * VS;     // [C][TS]: A, overwritten in place by T, then by T diag(beta)
     float *bs = Ts + C * TS;     // [C]
-    float *Ys = bs + C;          // coupling scratch, up to (C/2) x (C/2 + 1)
+    float *gs = bs + C;          // [C]: prefix sums G of the chunk's log decays (gated variant)
+    float *Ys = gs + C;          // coupling scratch, up to (C/2) x (C/2 + 1)
 
     const int64_t id = blockIdx.x;
     const int h = blockIdx.y;
@@ -76,9 +78,18 @@ __global__ void __launch_bounds__(kSimtThreads) kkt_simt_kernel(const SimtParams
         Vs[i * VS + d] = (i < Lc) ? to_f(vg[((t0 + i) * H + h) * DV + d]) : 0.f;
     }
     for (int i = tid; i < C; i += kSimtThreads) bs[i] = (i < Lc) ? p.beta[(t0 + i) * H + h] : 0.f;
+    if (p.g && tid == 0) {
+        // G_i = g_0 + ... + g_i over the chunk's tokens, so that Gamma[i][j] = exp(G_i - G_j)
+        float acc = 0.f;
+        for (int i = 0; i < C; ++i) {
+            acc += (i < Lc) ? p.g[(t0 + i) * H + h] : 0.f;
+            gs[i] = acc;
+        }
+    }
     __syncthreads();
 
-    // 2. A = I + strictLower(diag(beta) K K^T)   (§1; beta on rows, unit diagonal, §3.2)
+    // 2. A = I + strictLower(diag(beta) K K^T)   (§1; beta on rows, unit diagonal, §3.2), times
+    //    Gamma elementwise in the gated variant (§5 item 12)
     for (int e = tid; e < C * C; e += kSimtThreads) {
         const int i = e / C, j = e % C;
         float a = 0.f;
@@ -88,6 +99,7 @@ __global__ void __launch_bounds__(kSimtThreads) kkt_simt_kernel(const SimtParams
             float s = 0.f;
             for (int d = 0; d < DK; ++d) s = fmaf(Ks[i * KS + d], Ks[j * KS + d], s);
             a = bs[i] * s;
+            if (p.g) a *= expf(gs[i] - gs[j]);
         }
         Ts[i * TS + j] = a;
     }
@@ -182,12 +194,12 @@ __global__ void __launch_bounds__(kSimtThreads) kkt_simt_kernel(const SimtParams
 template <typename TIn, int C>
 int launch_simt_t(const Problem &pb) {
     const size_t smem = sizeof(float) * ((size_t)C * (pb.dk + 1) + (size_t)C * (pb.dv + 1) +
-                                         (size_t)C * (C + 1) + C + (size_t)(C / 2) * (C / 2 + 1));
+                                         (size_t)C * (C + 1) + 2 * C + (size_t)(C / 2) * (C / 2 + 1));
     auto kern = kkt_simt_kernel<TIn, C>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return KKT_ERR_CUDA;
     SimtParams p;
-    p.k = pb.k; p.v = pb.v; p.beta = pb.beta; p.cu = pb.cu_seqlens;
+    p.k = pb.k; p.v = pb.v; p.beta = pb.beta; p.g = pb.g; p.cu = pb.cu_seqlens;
     p.nseq = pb.nseq; p.T = pb.T; p.ntok = pb.ntok;
     p.H = pb.H; p.dk = pb.dk; p.dv = pb.dv;
     p.T_out = pb.T_out; p.t_f16 = pb.t_f16; p.W_out = pb.W_out; p.U_out = pb.U_out; p.status = pb.status;

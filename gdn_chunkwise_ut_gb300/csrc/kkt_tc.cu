@@ -79,7 +79,9 @@ template <int C>
 struct Cfg {
     static constexpr int G = 128 / C;                         // heads per tile
     static constexpr int KV_BYTES = 65536;                    // K 32 KB + V 32 KB, [box][row][128 B]
-    static constexpr int META_BYTES = 544;                    // beta[128] + TileInfo (at byte 512)
+    // per stage: beta[128]; gated kernels: the gate's prefix sums G[128] (log2 units), the column
+    // factors w[128] and one "factorable" flag per 32-row block (int[4]); then the TileInfo
+    static constexpr int META_BYTES = 1584;
     static constexpr int T_HALVES = C / 32;                   // 128-byte column blocks of a T row
     static constexpr int OFF_T = kNS * KV_BYTES;              // T of the tile: [half][128 rows][128 B]
     // W / U~ staging per epilogue warp: two 4 KB buffers, one at C = 128 (whose T takes 64 KB)
@@ -110,6 +112,7 @@ struct Barriers {
 
 struct TcParams {
     const float *beta;
+    const float *g;  // per-token log decays (GATED kernels)
     const int32_t *cu;
     int nseq, T;
     int64_t ntok;
@@ -424,7 +427,29 @@ __device__ __forceinline__ bool level64(const int w, uint8_t *tm, int lane, uint
 }
 
 // ---------------------------------------------------------------------------------------------
-template <int C, bool TF16>
+// Inclusive prefix sums of x over the C rows of each head of a tile, value e of a lane being row
+// (lane + 32 e) % C of head (lane + 32 e) / C: a warp scan of each 32-row segment, then the totals
+// of the earlier segments of the same head.
+template <int C>
+__device__ __forceinline__ void head_prefix_sums(float (&x)[4], int lane) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, x[e], o);
+            if (lane >= o) x[e] += y;
+        }
+    float carry = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        if ((32 * e) % C == 0) carry = 0.f;  // first segment of a head
+        const float total = __shfl_sync(0xffffffffu, x[e], 31);
+        x[e] += carry;
+        carry += total;
+    }
+}
+
+template <int C, bool TF16, bool GATED>
 __global__ void __launch_bounds__(kThreads, 1)
     kkt_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                   const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_u,
@@ -439,13 +464,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     auto stage_kv = [&](int s) { return smem + s * CF::KV_BYTES; };
     auto stage_beta = [&](int s) { return reinterpret_cast<float *>(smem + CF::OFF_META + s * CF::META_BYTES); };
+    auto stage_gate = [&](int s) { return reinterpret_cast<float *>(smem + CF::OFF_META + s * CF::META_BYTES + 512); };
+    auto stage_gw = [&](int s) { return reinterpret_cast<float *>(smem + CF::OFF_META + s * CF::META_BYTES + 1024); };
+    auto stage_gflag = [&](int s) { return reinterpret_cast<int *>(smem + CF::OFF_META + s * CF::META_BYTES + 1536); };
     auto stage_info = [&](int s) {
-        return reinterpret_cast<TileInfo *>(smem + CF::OFF_META + s * CF::META_BYTES + 512);
+        return reinterpret_cast<TileInfo *>(smem + CF::OFF_META + s * CF::META_BYTES + 1552);
     };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kNS; ++s) {
-            mbar_init(&bars->full[s], 1);
+            // gated kernels: a second arrival once the stage's gate data is written (after the loads)
+            mbar_init(&bars->full[s], GATED ? 2 : 1);
             mbar_init(&bars->empty[s], 1);
         }
         mbar_init(&bars->gram_full, 1);
@@ -517,6 +546,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int g = idx / C, r = idx % C;
                 bv[e] = (r < ch.Lc && h0 + g < p.H) ? __ldg(p.beta + (ch.t0 + r) * p.H + h0 + g) : 0.f;
             }
+            // gated: prefix sums G of the log decays over each head's chunk, in log2 units, so that
+            // Gamma[i][j] = exp2(G_i - G_j).  For a column j of 32-row block b, with R_b = G at the
+            // block's first row: Gamma[i][j] = exp2(G_i - R_b) * w_j, w_j = exp2(R_b - G_j), one power
+            // per row and block instead of one per element.  That is exact up to rounding while the
+            // factors stay in range: |R_b - G_j| <= 96 over the block (a decay of at most 2^-96
+            // inside 32 tokens), recorded as the block's flag; other blocks take one power per element.
+            // (the loads are issued here and consumed after the stage wait, which hides their latency)
+            float gv[4] = {0.f, 0.f, 0.f, 0.f}, wv[4] = {0.f, 0.f, 0.f, 0.f};
+            int fv[4] = {0, 0, 0, 0};
+            if constexpr (GATED) {
+                constexpr float kLog2e = 1.4426950408889634f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int idx = lane + 32 * e;
+                    const int g = idx / C, r = idx % C;
+                    gv[e] = (r < ch.Lc && h0 + g < p.H) ? kLog2e * __ldg(p.g + (ch.t0 + r) * p.H + h0 + g) : 0.f;
+                }
+            }
             const int s = i % kNS;
             const uint32_t u = (uint32_t)(i / kNS);
             if (!wait_bar(&bars->empty[s], (u & 1u) ^ 1u, bars, p.status)) { ok = false; break; }
@@ -544,6 +591,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 KKT_TRACE_EVENT(EV_P_ISSUE, i);
             }
+            if constexpr (GATED) {
+                // the gate data, while the loads are in flight; the stage completes with this arrival
+                head_prefix_sums<C>(gv, lane);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float ref = __shfl_sync(0xffffffffu, gv[e], 0);
+                    float dev = fabsf(ref - gv[e]);
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) dev = fmaxf(dev, __shfl_xor_sync(0xffffffffu, dev, o));
+                    fv[e] = dev <= 96.f;
+                    wv[e] = exp2f(ref - gv[e]);
+                }
+                float *sg = stage_gate(s), *sw = stage_gw(s);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    sg[lane + 32 * e] = gv[e];
+                    sw[lane + 32 * e] = wv[e];
+                }
+                if (lane == 0)
+                    for (int e = 0; e < 4; ++e) stage_gflag(s)[e] = fv[e];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->full[s]);
+            }
             __syncwarp();
             ++i;
         }
@@ -554,6 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     stage_info(s)->done = 1;
                     mbar_arrive(&bars->full[s]);
+                    if (GATED) mbar_arrive(&bars->full[s]);
                 }
             } else {
                 ok = false;
@@ -706,6 +777,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (info.done) break;
             const float *sb = stage_beta(s) + g * C;
             const float beta_r = sb[r];
+            // gated: Gamma[r][j], the decay from token j to token r (j < r), for columns 32 h + c ..
+            // + 3 is exp2(G_r - R_h) w_j when every block of the head is factorable (fac); otherwise
+            // the row is formed without it and multiplied by exp2(G_r - G_j) element by element after
+            // (a compact loop: such gates are rare, and the unrolled code stays small)
+            const float *sg = stage_gate(s) + g * C;
+            const float *sw = stage_gw(s) + g * C;
+            bool fac = true;
+            float g_r = 0.f;
+            if constexpr (GATED) {
+                g_r = sg[r];
+                const int *sf = stage_gflag(s) + g * C / 32;
+#pragma unroll
+                for (int h = 0; h < CF::T_HALVES; ++h) fac = fac && sf[h] != 0;
+            }
+            auto gamma4 = [&](float u, int h, int c) -> float4 {
+                if (!fac) return make_float4(1.f, 1.f, 1.f, 1.f);
+                const float4 w4 = *reinterpret_cast<const float4 *>(sw + 32 * h + c);
+                return make_float4(u * w4.x, u * w4.y, u * w4.z, u * w4.w);
+            };
+            auto row_factor = [&](int h) { return fac ? exp2f(g_r - sg[32 * h]) : 1.f; };
 
             if (!wait_bar(&bars->gram_full, (uint32_t)i & 1u, bars, p.status)) break;
             tc_fence_after();
@@ -715,21 +806,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_BW, i);
             // Gram row -> row of A = I + strictLower(diag(beta) S) (beta on rows, unit diagonal,
-            // §3.2) into the T buffer; columns above 32 (wp + 1) stay zero
+            // §3.2), times Gamma elementwise when gated (§5 item 12), into the T buffer; columns
+            // above 32 (wp + 1) stay zero
             if constexpr (C == 128) {
                 // up to four 32-column blocks: one tensor-memory load at a time
 #pragma unroll 1
                 for (int h = 0; h <= wp; ++h) {
                     uint32_t v[32];
                     tmem_ld32(tmem + lane_base + kColGram + 32 * h, v);
+                    const float uh = GATED ? row_factor(h) : 1.f;
                     tmem_wait_ld();
 #pragma unroll
                     for (int c = 0; c < 32; c += 4) {
                         float e[4];
+                        float gm[4] = {1.f, 1.f, 1.f, 1.f};
+                        if constexpr (GATED) {
+                            const float4 g4 = gamma4(uh, h, c);
+                            gm[0] = g4.x; gm[1] = g4.y; gm[2] = g4.z; gm[3] = g4.w;
+                        }
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
                             const int j = 32 * h + c + u;
-                            e[u] = (j < r) ? beta_r * __uint_as_float(v[c + u]) : (j == r ? 1.f : 0.f);
+                            e[u] = (j < r) ? beta_r * __uint_as_float(v[c + u]) * gm[u] : (j == r ? 1.f : 0.f);
                         }
                         *tm_vec(tm, m, 32 * h + c) = make_float4(e[0], e[1], e[2], e[3]);
                     }
@@ -742,13 +840,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_wait_ld();
 #pragma unroll
                 for (int h = 0; h < CF::T_HALVES; ++h) {
+                    const float uh = GATED ? row_factor(h) : 1.f;
                     if (h < wp) {
                         // the whole block lies below the diagonal (columns < 32 wp <= r): beta scale only
                         const float2 bb = make_float2(beta_r, beta_r);
 #pragma unroll
                         for (int c = 0; c < 32; c += 4) {
-                            const float2 e0 = fmul2(make_float2(__uint_as_float(v[h][c]), __uint_as_float(v[h][c + 1])), bb);
-                            const float2 e1 = fmul2(make_float2(__uint_as_float(v[h][c + 2]), __uint_as_float(v[h][c + 3])), bb);
+                            float2 e0 = fmul2(make_float2(__uint_as_float(v[h][c]), __uint_as_float(v[h][c + 1])), bb);
+                            float2 e1 = fmul2(make_float2(__uint_as_float(v[h][c + 2]), __uint_as_float(v[h][c + 3])), bb);
+                            if constexpr (GATED) {
+                                const float4 g4 = gamma4(uh, h, c);
+                                e0 = fmul2(e0, make_float2(g4.x, g4.y));
+                                e1 = fmul2(e1, make_float2(g4.z, g4.w));
+                            }
                             *tm_vec(tm, m, 32 * h + c) = make_float4(e0.x, e0.y, e1.x, e1.y);
                         }
                     } else if (h == wp) {
@@ -756,12 +860,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int c = 0; c < 32; c += 4) {
                             float e[4];
+                            float gm[4] = {1.f, 1.f, 1.f, 1.f};
+                            if constexpr (GATED) {
+                                const float4 g4 = gamma4(uh, h, c);
+                                gm[0] = g4.x; gm[1] = g4.y; gm[2] = g4.z; gm[3] = g4.w;
+                            }
 #pragma unroll
                             for (int u = 0; u < 4; ++u)
-                                e[u] = (c + u < lane) ? beta_r * __uint_as_float(v[h][c + u]) : (c + u == lane ? 1.f : 0.f);
+                                e[u] = (c + u < lane) ? beta_r * __uint_as_float(v[h][c + u]) * gm[u]
+                                                      : (c + u == lane ? 1.f : 0.f);
                             *tm_vec(tm, m, 32 * h + c) = make_float4(e[0], e[1], e[2], e[3]);
                         }
                     }
+                }
+            }
+            if constexpr (GATED) {
+                if (!fac) {
+#pragma unroll 1
+                    for (int j = 0; j < r; ++j) *tm_elem(tm, m, j) *= exp2f(g_r - sg[j]);
                 }
             }
             tc_fence_before();
@@ -1120,6 +1236,7 @@ int launch_tc_t(const Problem &pb) {
     if (!pb.T_out || (pb.t_f16 && C < 64)) mt = CUtensorMap{};  // never used: no T, or fp16 T by plain stores
     TcParams p;
     p.beta = pb.beta;
+    p.g = pb.g;
     p.cu = pb.cu_seqlens;
     p.nseq = pb.nseq;
     p.T = pb.T;
@@ -1134,7 +1251,8 @@ int launch_tc_t(const Problem &pb) {
     p.trace = static_cast<unsigned long long *>(pb.trace);
     p.tile_counter = pb.tile_counter;
     p.stall_first_tile = pb.stall_first_tile;
-    auto kern = pb.t_f16 ? kkt_tc_kernel<C, true> : kkt_tc_kernel<C, false>;
+    auto kern = pb.g ? (pb.t_f16 ? kkt_tc_kernel<C, true, true> : kkt_tc_kernel<C, false, true>)
+                     : (pb.t_f16 ? kkt_tc_kernel<C, true, false> : kkt_tc_kernel<C, false, false>);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_BYTES) != cudaSuccess)
         return KKT_ERR_CUDA;
     const int sms = sm_count();

@@ -11,7 +11,10 @@ stand in for that data):
     is L2-normalised upstream of the kernel, "TileLang 实战：单位下三角矩阵求逆"
     §1), then rounded to the I/O dtype (bf16, or fp32 for the small case);
   * V: N(0, 1) rounded to the I/O dtype;
-  * beta: sigmoid(N(0, 1)) in fp32, so beta in (0, 1) (§1: the write strength).
+  * beta: sigmoid(N(0, 1)) in fp32, so beta in (0, 1) (§1: the write strength);
+  * g (gated variant only): log sigmoid(N(2.5, 1)) in fp32, a per-token log decay with
+    alpha = exp(g) in (0, 1) (the FlashQLA page's gate, "Gate 衰减性质" section), mean decay
+    about 0.9 per token, so that Gamma falls to about e^-6 across a 64-token chunk.
 Variable-length batches draw 32 lengths uniform in [100, 8192] with
 ``numpy.random.default_rng(1234)``.
 """
@@ -33,6 +36,14 @@ def make_inputs(B: int, T: int, H: int, dk: int, dv: int, *, seed: int = 0,
     v = torch.randn((B, T, H, dv), generator=g, device=device, dtype=torch.float32)
     beta = torch.sigmoid(torch.randn((B, T, H), generator=g, device=device, dtype=torch.float32))
     return k.to(dtype).contiguous(), v.to(dtype).contiguous(), beta.contiguous()
+
+
+def make_gate(B: int, T: int, H: int, *, seed: int = 0, device="cpu"):
+    """g [B,T,H] fp32: per-token log decays log sigmoid(N(2.5, 1)), all < 0."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed + 7919)
+    x = torch.randn((B, T, H), generator=gen, device=device, dtype=torch.float32) + 2.5
+    return torch.nn.functional.logsigmoid(x).contiguous()
 
 
 def varlen_lengths(n: int = 32, lo: int = 100, hi: int = 8192, seed: int = 1234) -> np.ndarray:

@@ -133,6 +133,32 @@ int kkt_solve_fwd_ex(const void *k, const void *v, const float *beta, const int3
                      int io_dtype, int kernel, void *workspace, size_t workspace_bytes,
                      struct CUstream_st *stream);
 
+/*
+ * kkt_solve_fwd_gated -- the gated variant of kkt_solve_fwd_ex.  With a gate
+ * the coefficient becomes diag(beta)(Gamma o K K^T) ("TileLang 实战：单位下三角
+ * 矩阵求逆" section 5 item 12):
+ *
+ *   A = I + strictLower(diag(beta) (Gamma o K K^T)),
+ *   Gamma[i][j] = exp(g_{j+1} + ... + g_i)   (i > j, tokens of the same chunk),
+ *
+ * the product of the per-token decays alpha_t = exp(g_t) between token j and
+ * token i.  T = A^-1, W = T diag(beta) K and U~ = T diag(beta) V as in the
+ * ungated call (the page states no other change).  The gate restarts at every
+ * chunk.
+ *
+ *   g [B, T, H]   input fp32, the per-token log decay (the `g` argument of the
+ *                 FlashQLA API, "FlashQLA" page, usage section); expected <= 0
+ *                 (decays in (0, 1]).  Layout as beta; 4-byte aligned.
+ *
+ * g == NULL is the ungated call.  Every other argument, the layouts,
+ * ownership and errors are those of kkt_solve_fwd_ex.
+ */
+int kkt_solve_fwd_gated(const void *k, const void *v, const float *beta, const float *g,
+                        const int32_t *cu_seqlens, int B, int T, int H, int dk, int dv, int C,
+                        void *T_out, void *W_out, void *U_out,
+                        int io_dtype, int kernel, void *workspace, size_t workspace_bytes,
+                        struct CUstream_st *stream);
+
 /* Size of the scratch array compiled into the library for kkt_solve_fwd_noalloc. */
 #define KKT_NOALLOC_SCRATCH_BYTES 256
 

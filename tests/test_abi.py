@@ -117,6 +117,20 @@ def test_argument_errors_return_before_launch(lib):
                              0x4000, 0x5000, 0x6000, None) == _lib.KKT_ERR_ARG
 
 
+def test_gated_argument_errors(lib):
+    """The gated entry point checks g like beta (4-byte aligned) and otherwise as kkt_solve_fwd_ex."""
+    def call(g=0x9000, **kw):
+        a = dict(k=0x1000, v=0x2000, beta=0x3000, T=64, C=64, T_out=0x4000)
+        a.update(kw)
+        return lib.kkt_solve_fwd_gated(a["k"], 0x2000, a["beta"], g, None, 1, a["T"], 1, 128, 128, a["C"],
+                                       a["T_out"], 0x5000, 0x6000, 0, 0, None, 0, None)
+    assert call(g=0x9002) == _lib.KKT_ERR_ALIGN
+    assert call(k=None) == _lib.KKT_ERR_ARG
+    assert call(C=48) == _lib.KKT_ERR_UNSUPPORTED
+    assert call(T=0) == _lib.KKT_OK
+    assert call(g=None, T=0) == _lib.KKT_OK  # g == NULL is the ungated call
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     """The product path has no fallback: without libkkt.so every call raises."""
     monkeypatch.setattr(_lib, "LIB_PATH", tmp_path / "libkkt.so")

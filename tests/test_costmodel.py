@@ -53,6 +53,7 @@ def test_bytes_per_unit():
     assert cm.bytes_per_unit(128, 128, 128) == 1540
     assert cm.bytes_per_unit(64, 128, 128, t_out=False) == 1028  # W and U~ only
     assert cm.bytes_per_unit(64, 128, 128, t_bytes=2) == 1028 + 128  # T in fp16
+    assert cm.bytes_per_unit(64, 128, 128, gated=True) == 1284 + 4  # the log decay g
     assert cm.bytes_written_per_unit(64, 128, 128) == 768
     assert cm.bytes_per_unit(32, 64, 64, io_bytes=4) == 1156
 

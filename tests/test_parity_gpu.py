@@ -11,7 +11,7 @@ import torch
 
 import oracle
 from gdn_chunkwise_ut_gb300 import _lib, device_status, kkt_solve_fwd, select_kernel
-from gdn_chunkwise_ut_gb300.inputs import make_inputs, workloads
+from gdn_chunkwise_ut_gb300.inputs import make_gate, make_inputs, workloads
 from tests.compare import check_T, check_WU, chunks, to64
 from tests.pins import subdiagonal_only_case
 
@@ -38,7 +38,7 @@ def _skip_unless(kernel, dk, dv, C, io="bf16"):
         pytest.skip(f"{kernel} kernel does not cover dk={dk} dv={dv} C={C} io={io}")
 
 
-def run(k, v, beta, C, cu=None, kernel="auto", poison=True, workspace="auto"):
+def run(k, v, beta, C, cu=None, kernel="auto", poison=True, workspace="auto", g=None):
     """Calls the library with NaN-poisoned outputs; returns (T, W, U) on the device."""
     Bt, T, H, dk = k.shape
     dv = v.shape[-1]
@@ -46,14 +46,15 @@ def run(k, v, beta, C, cu=None, kernel="auto", poison=True, workspace="auto"):
     W = torch.full((Bt, T, H, dk), float("nan"), device=DEV, dtype=k.dtype)
     U = torch.full((Bt, T, H, dv), float("nan"), device=DEV, dtype=k.dtype)
     cu_t = None if cu is None else torch.as_tensor(np.asarray(cu), dtype=torch.int32, device=DEV)
-    kkt_solve_fwd(k, v, beta, C, cu_t, T_out=T_out, W_out=W, U_out=U, kernel=kernel, workspace=workspace)
+    kkt_solve_fwd(k, v, beta, C, cu_t, T_out=T_out, W_out=W, U_out=U, kernel=kernel, workspace=workspace, g=g)
     torch.cuda.synchronize()
     assert device_status() == 0
     return T_out, W, U
 
 
-def full_compare(k, v, beta, C, cu, outs, io="bf16"):
-    T_ref, W_ref, U_ref = oracle.oracle_fwd(to64(k), to64(v), to64(beta), C, cu_seqlens=cu)
+def full_compare(k, v, beta, C, cu, outs, io="bf16", g=None):
+    T_ref, W_ref, U_ref = oracle.oracle_fwd(to64(k), to64(v), to64(beta), C, cu_seqlens=cu,
+                                            g=None if g is None else to64(g))
     T_g, W_g, U_g = (to64(x) for x in outs)
     check_T(T_g, T_ref)
     check_WU(W_g, W_ref, io, "W")
@@ -178,6 +179,68 @@ def test_t_out_fp16(kernel, C, varlen):
     T_ref, _, _ = oracle.oracle_fwd(to64(k), to64(v), to64(beta), C, cu_seqlens=cu)
     err = np.abs(to64(T16) - T_ref)
     assert (err <= 1e-4 + 2.0 ** -11 * np.abs(T_ref)).all(), float(err.max())
+
+
+# --- the gated variant (diag(beta)(Gamma o K K^T)) --------------------------------------------
+
+@pytest.mark.parametrize("kernel", ALL_KERNELS)
+@pytest.mark.parametrize("C", [32, 64, 128])
+@pytest.mark.parametrize("varlen", [False, True])
+def test_gated(kernel, C, varlen):
+    """Gated coefficient against the oracle, element by element: fixed length with a ragged tail and
+    a partial head group, or varlen with empty and one-token sequences."""
+    _skip_unless(kernel, 128, 128, C)
+    if varlen:
+        lengths = [1, 63, 64, 65, 0, 130, 7, 200, 128]
+        cu = np.concatenate([[0], np.cumsum(lengths)])
+        k, v, beta = make_inputs(1, int(cu[-1]), 3, 128, 128, seed=41, device=DEV)
+        g = make_gate(1, int(cu[-1]), 3, seed=41, device=DEV)
+    else:
+        cu = None
+        k, v, beta = make_inputs(2, 3 * C + 17, 5, 128, 128, seed=42, device=DEV)
+        g = make_gate(2, 3 * C + 17, 5, seed=42, device=DEV)
+    outs = run(k, v, beta, C, cu, kernel=kernel, g=g)
+    full_compare(k, v, beta, C, cu, outs, g=g)
+
+
+@pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128)])
+def test_gated_simt_shapes_and_fp32(dk, dv):
+    """The SIMT kernel's gated path at d = 64 and with fp32 I/O (the fp32 workload's shapes)."""
+    k, v, beta = make_inputs(1, 200, 2, dk, dv, seed=43, device=DEV)
+    g = make_gate(1, 200, 2, seed=43, device=DEV)
+    full_compare(k, v, beta, 64, None, run(k, v, beta, 64, kernel="simt", g=g), g=g)
+    kf, vf, bf = make_inputs(1, 128, 1, dk, dv, seed=44, dtype=torch.float32, device=DEV)
+    gf = make_gate(1, 128, 1, seed=44, device=DEV)
+    full_compare(kf, vf, bf, 32, None, run(kf, vf, bf, 32, kernel="simt", g=gf), io="f32", g=gf)
+
+
+@pytest.mark.parametrize("kernel", ALL_KERNELS)
+def test_gate_zero_is_ungated(kernel):
+    """g = 0 (no decay): the gated call returns exactly the ungated call's T, W and U~."""
+    _skip_unless(kernel, 128, 128, 64)
+    k, v, beta = make_inputs(2, 300, 4, 128, 128, seed=45, device=DEV)
+    plain = run(k, v, beta, 64, kernel=kernel)
+    gated = run(k, v, beta, 64, kernel=kernel, g=torch.zeros_like(beta))
+    for a, b in zip(plain, gated):
+        assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("kernel", ALL_KERNELS)
+def test_gate_cut_is_block_diagonal(kernel):
+    """A token with zero decay (g = -1000) cuts its chunk: T is exactly zero across the cut, and the
+    rest matches the oracle."""
+    _skip_unless(kernel, 128, 128, 64)
+    k, v, beta = make_inputs(1, 256, 2, 128, 128, seed=46, device=DEV)
+    g = make_gate(1, 256, 2, seed=46, device=DEV)
+    cuts = [(40, 0), (64 + 33, 1), (128 + 64 + 5, 0)]
+    for t, h in cuts:
+        g[0, t, h] = -1000.0
+    T, W, U = run(k, v, beta, 64, kernel=kernel, g=g)
+    for t, h in cuts:
+        c0, cut = (t // 64) * 64, t % 64
+        blk = T[0, c0 + cut:c0 + 64, h, :cut]
+        assert torch.count_nonzero(blk) == 0
+    full_compare(k, v, beta, 64, None, (T, W, U), g=g)
 
 
 # --- degenerate cases and traps -----------------------------------------------------------
