@@ -791,10 +791,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int h = 0; h < CF::T_HALVES; ++h) fac = fac && sf[h] != 0;
             }
-            auto gamma4 = [&](float u, int h, int c) -> float4 {
-                if (!fac) return make_float4(1.f, 1.f, 1.f, 1.f);
-                const float4 w4 = *reinterpret_cast<const float4 *>(sw + 32 * h + c);
-                return make_float4(u * w4.x, u * w4.y, u * w4.z, u * w4.w);
+            // the column factors w of block h (ones when not factorable), loaded together ahead of use
+            auto load_w = [&](int h, float4 (&wq)[8]) {
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8)
+                    wq[c8] = fac ? *reinterpret_cast<const float4 *>(sw + 32 * h + 4 * c8) : make_float4(1.f, 1.f, 1.f, 1.f);
             };
             auto row_factor = [&](int h) { return fac ? exp2f(g_r - sg[32 * h]) : 1.f; };
 
@@ -814,15 +815,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int h = 0; h <= wp; ++h) {
                     uint32_t v[32];
                     tmem_ld32(tmem + lane_base + kColGram + 32 * h, v);
-                    const float uh = GATED ? row_factor(h) : 1.f;
+                    float uh = 1.f;
+                    float4 wq[8];
+                    if constexpr (GATED) {
+                        uh = row_factor(h);
+                        load_w(h, wq);
+                    }
                     tmem_wait_ld();
 #pragma unroll
                     for (int c = 0; c < 32; c += 4) {
                         float e[4];
                         float gm[4] = {1.f, 1.f, 1.f, 1.f};
                         if constexpr (GATED) {
-                            const float4 g4 = gamma4(uh, h, c);
-                            gm[0] = g4.x; gm[1] = g4.y; gm[2] = g4.z; gm[3] = g4.w;
+                            const float4 w4 = wq[c / 4];
+                            gm[0] = uh * w4.x; gm[1] = uh * w4.y; gm[2] = uh * w4.z; gm[3] = uh * w4.w;
                         }
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
@@ -837,21 +843,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int h = 0; h < CF::T_HALVES; ++h)
                     if (h <= wp) tmem_ld32(tmem + lane_base + kColGram + g * C + 32 * h, v[h]);
+                float uh[CF::T_HALVES];
+#pragma unroll
+                for (int h = 0; h < CF::T_HALVES; ++h) uh[h] = GATED ? row_factor(h) : 1.f;
                 tmem_wait_ld();
 #pragma unroll
                 for (int h = 0; h < CF::T_HALVES; ++h) {
-                    const float uh = GATED ? row_factor(h) : 1.f;
+                    float4 wq[8];
+                    if constexpr (GATED) {
+                        if (h <= wp) load_w(h, wq);
+                    }
                     if (h < wp) {
                         // the whole block lies below the diagonal (columns < 32 wp <= r): beta scale only
-                        const float2 bb = make_float2(beta_r, beta_r);
+                        const float2 bb = make_float2(beta_r * uh[h], beta_r * uh[h]);
 #pragma unroll
                         for (int c = 0; c < 32; c += 4) {
                             float2 e0 = fmul2(make_float2(__uint_as_float(v[h][c]), __uint_as_float(v[h][c + 1])), bb);
                             float2 e1 = fmul2(make_float2(__uint_as_float(v[h][c + 2]), __uint_as_float(v[h][c + 3])), bb);
                             if constexpr (GATED) {
-                                const float4 g4 = gamma4(uh, h, c);
-                                e0 = fmul2(e0, make_float2(g4.x, g4.y));
-                                e1 = fmul2(e1, make_float2(g4.z, g4.w));
+                                const float4 w4 = wq[c / 4];
+                                e0 = fmul2(e0, make_float2(w4.x, w4.y));
+                                e1 = fmul2(e1, make_float2(w4.z, w4.w));
                             }
                             *tm_vec(tm, m, 32 * h + c) = make_float4(e0.x, e0.y, e1.x, e1.y);
                         }
@@ -862,8 +874,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             float e[4];
                             float gm[4] = {1.f, 1.f, 1.f, 1.f};
                             if constexpr (GATED) {
-                                const float4 g4 = gamma4(uh, h, c);
-                                gm[0] = g4.x; gm[1] = g4.y; gm[2] = g4.z; gm[3] = g4.w;
+                                const float4 w4 = wq[c / 4];
+                                gm[0] = uh[h] * w4.x; gm[1] = uh[h] * w4.y; gm[2] = uh[h] * w4.z; gm[3] = uh[h] * w4.w;
                             }
 #pragma unroll
                             for (int u = 0; u < 4; ++u)

@@ -17,14 +17,14 @@ import numpy as np
 import torch
 
 from . import _lib, build
-from .inputs import workloads
+from .inputs import make_gate, workloads
 
 EVENTS = ["P_EMPTY", "P_ISSUE", "M_FULL", "M_GRAM", "M_EPI", "I_GRAM", "I_INV", "I_TSTORE", "I_TT",
           "E_DFULL", "E_DEMPTY", "E_DONE", "I_LD", "I_DIAG", "I_C16", "I_PAIR", "M_LATE", "M_READY", "I_BW", "I_TTW"]
 TRACE_CTAS, TRACE_TILES, TRACE_SLOTS = 160, 64, 24
 
 
-def run(workload: str, warmup: int = 3, dynamic: bool = True):
+def run(workload: str, warmup: int = 3, dynamic: bool = True, gated: bool = False):
     path = build.build(trace=True)
     lib = _lib.lib(path)
     lib.kkt_set_trace_buffer.argtypes = [ctypes.c_void_p]
@@ -33,6 +33,7 @@ def run(workload: str, warmup: int = 3, dynamic: bool = True):
     k, v, beta, cu = w.make(seed=0, device="cuda")
     cu_t = None if cu is None else torch.as_tensor(cu, dtype=torch.int32, device="cuda")
     B = len(cu) - 1 if cu is not None else w.B
+    g = make_gate(k.shape[0], k.shape[1], w.H, device="cuda") if gated else None
     T_out = torch.empty((k.shape[0], k.shape[1], w.H, w.C), device="cuda")
     W = torch.empty_like(k)
     U = torch.empty_like(v)
@@ -41,11 +42,12 @@ def run(workload: str, warmup: int = 3, dynamic: bool = True):
     stream = torch.cuda.current_stream().cuda_stream
 
     def call():
-        rc = lib.kkt_solve_fwd_ex(k.data_ptr(), v.data_ptr(), beta.data_ptr(),
-                                  None if cu_t is None else cu_t.data_ptr(), B, k.shape[1], w.H, w.dk, w.dv,
-                                  w.C, T_out.data_ptr(), W.data_ptr(), U.data_ptr(), _lib.KKT_IO_BF16,
-                                  _lib.KKT_KERNEL_TC, None if ws is None else ws.data_ptr(),
-                                  0 if ws is None else ws.numel() * 4, stream)
+        rc = lib.kkt_solve_fwd_gated(k.data_ptr(), v.data_ptr(), beta.data_ptr(),
+                                     None if g is None else g.data_ptr(),
+                                     None if cu_t is None else cu_t.data_ptr(), B, k.shape[1], w.H, w.dk, w.dv,
+                                     w.C, T_out.data_ptr(), W.data_ptr(), U.data_ptr(), _lib.KKT_IO_BF16,
+                                     _lib.KKT_KERNEL_TC, None if ws is None else ws.data_ptr(),
+                                     0 if ws is None else ws.numel() * 4, stream)
         if rc != 0:
             raise _lib.KktError(rc, "kkt_solve_fwd_ex")
 
@@ -173,8 +175,9 @@ def main():
     ap.add_argument("--tiles", type=int, default=12)
     ap.add_argument("--static", action="store_true", help="fixed round-robin schedule (no workspace)")
     ap.add_argument("--save", default=None, help="also save the raw cycle counts (.npy)")
+    ap.add_argument("--gated", action="store_true", help="the gated variant (seeded log decays)")
     a = ap.parse_args()
-    tr = run(a.workload, dynamic=not a.static)
+    tr = run(a.workload, dynamic=not a.static, gated=a.gated)
     print(f"untraced launch of the trace build: {run.last_ms * 1e3:.1f} us")
     print(report(tr, a.ctas, a.tiles))
     if a.save:
