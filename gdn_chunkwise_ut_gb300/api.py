@@ -7,6 +7,8 @@ library's CUDA kernels.
 """
 from __future__ import annotations
 
+import os
+
 import torch
 
 from . import _lib
@@ -48,7 +50,7 @@ def _workspace(device: torch.device) -> torch.Tensor:
 def kkt_solve_fwd(k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor, C: int,
                   cu_seqlens: torch.Tensor | None = None, *, T_out=None, W_out=None, U_out=None,
                   kernel: str = "auto", workspace="auto", stream=None, materialize_T: bool = True,
-                  T_dtype=torch.float32, g: torch.Tensor | None = None):
+                  T_dtype=torch.float32, g: torch.Tensor | None = None, check: bool | None = None):
     """UT transform of every chunk: returns (T_out, W, U).
 
     ``materialize_T=False`` computes T but does not write it: the call returns (None, W, U) and
@@ -65,6 +67,9 @@ def kkt_solve_fwd(k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor, C: int,
     scheduling; calls on concurrent streams should pass their own), a CUDA tensor
     of at least KKT_WORKSPACE_BYTES, zero-filled before its first use (every call
     leaves it zero), or None for the fixed round-robin schedule.
+    ``check=True`` (default: the environment variable KKT_CHECK=1) is the checked mode: the call
+    synchronises the stream, reads and clears the device status word, and raises KktError when the
+    kernel recorded an error (a malformed cu_seqlens, an expired bounded wait).
     """
     if k.dim() != 4 or v.dim() != 4 or beta.dim() != 3:
         raise ValueError("expected k [B,T,H,dk], v [B,T,H,dv], beta [B,T,H]")
@@ -126,6 +131,12 @@ def kkt_solve_fwd(k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor, C: int,
                                             kern, ws_ptr, ws_bytes, _stream_handle(stream))
     if rc != _lib.KKT_OK:
         raise _lib.KktError(rc, "kkt_solve_fwd")
+    if check is None:
+        check = os.environ.get("KKT_CHECK", "0") == "1"
+    if check:
+        st = device_status(stream)
+        if st != _lib.KKT_OK:
+            raise _lib.KktError(st, "kkt_solve_fwd (device)")
     return T_out, W_out, U_out
 
 

@@ -306,6 +306,21 @@ def test_malformed_cu_seqlens_is_reported_not_faulted():
     full_compare(k, v, beta, 64, cu_ok, outs)
 
 
+def test_checked_mode_raises_device_errors(monkeypatch):
+    """check=True (or KKT_CHECK=1) reads the status word after the call and raises on a device error."""
+    k, v, beta = make_inputs(1, 300, 2, 128, 128, seed=6, device=DEV)
+    bad = torch.tensor([0, 200, 100, 300], dtype=torch.int32, device=DEV)
+    with pytest.raises(_lib.KktError) as e:
+        kkt_solve_fwd(k, v, beta, 64, bad, check=True)
+    assert e.value.status == _lib.KKT_ERR_SEQLENS
+    monkeypatch.setenv("KKT_CHECK", "1")
+    with pytest.raises(_lib.KktError):
+        kkt_solve_fwd(k, v, beta, 64, bad)
+    good = torch.tensor([0, 100, 300], dtype=torch.int32, device=DEV)
+    kkt_solve_fwd(k, v, beta, 64, good)  # checked, no error
+    assert device_status() == 0
+
+
 # --- full-size workloads, sampled -----------------------------------------------------------
 
 FULL = ["c2_t8192_h16", "c3_b4_t8192_h16", "c3_b4_t8192_h64", "c4_varlen32_h32",
