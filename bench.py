@@ -17,6 +17,7 @@ times the fp64 CPU oracle on the host cores instead (rank 0 only).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -57,6 +58,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-t-out", action="store_true", help="W and U~ only: T computed, not written")
     ap.add_argument("--t-f16", action="store_true", help="T written in fp16 instead of fp32")
+    ap.add_argument("--chunk", type=int, default=None,
+                    help="override the workload's chunk size C (32, 64 or 128): the chunk-size study")
     ap.add_argument("--gated", action="store_true",
                     help="gated variant: coefficient diag(beta)(Gamma o K K^T) from per-token log decays g")
     args = ap.parse_args()
@@ -194,9 +197,16 @@ def recorded_traffic(kernel: str, workload: str):
 
 # --- our path -----------------------------------------------------------------------------------
 
+def select_workload(args):
+    w = workloads()[args.workload]
+    if args.chunk is not None and args.chunk != w.C:
+        w = dataclasses.replace(w, name=f"{w.name}@C{args.chunk}", C=args.chunk)
+    return w
+
+
 def bench_ours(args, rank, world, local):
     from gdn_chunkwise_ut_gb300 import HostRunner, kkt_solve_fwd, select_kernel
-    w = workloads()[args.workload]
+    w = select_workload(args)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     kernel = select_kernel(w.dk, w.dv, w.C, w.io, args.kernel)
@@ -264,7 +274,7 @@ def bench_ours(args, rank, world, local):
     peak, peak_src = hbm_peak()
     achieved = alg_bytes / (launch_ms / 1e3) / 1e9
     # the recorded counters are those of the default call (fp32 T)
-    traffic = None if (args.no_t_out or args.t_f16 or args.gated) else recorded_traffic(kernel, args.workload)
+    traffic = None if (args.no_t_out or args.t_f16 or args.gated) else recorded_traffic(kernel, w.name)
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     runner = HostRunner(k.shape[0], k.shape[1], w.H, w.dk, w.dv, w.C, dtype=k.dtype, cu_seqlens=cu,
@@ -289,7 +299,7 @@ def bench_ours(args, rank, world, local):
         "steps": K, "warmup": args.warmup, "ms_per_step": max_ms / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.io == "bf16" else "f32",
         "data": "synthetic (seeded K rows L2-normalised N(0,1), V ~ N(0,1), beta = sigmoid(N(0,1)))",
-        "config": {"workload": args.workload, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
                    "C": w.C, "tokens_per_step": w.tokens, "kernel": kernel,
                    "T_out": False if args.no_t_out else "fp16" if args.t_f16 else "fp32",
                    "gated": args.gated,
@@ -339,7 +349,7 @@ def bench_reference(args, rank, world):
         return None
     import oracle
     oracle.build()
-    w = workloads()[args.workload]
+    w = select_workload(args)
     if w.varlen:
         raise SystemExit("reference arm covers fixed-length workloads")
     # each step: one chunk-aligned slice of one sequence, all heads, sized so that
@@ -370,7 +380,7 @@ def bench_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": args.workload, "B": w.B, "T": w.T, "H": w.H,
+        "data": "synthetic", "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H,
                                         "dk": w.dk, "dv": w.dv, "C": w.C, "tokens_per_step": tokens,
                                         "gated": args.gated},
         "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
