@@ -13,9 +13,9 @@ and raises AssertionError when the oracle disagrees with:
     full one), the varlen/fixed-length equivalence and the tensor layout,
   * the page's measured cond(A) bounds,
   * the gated coefficient diag(beta)(Gamma o K K^T) (§5 item 12): no decay is the
-    ungated oracle; the page's two differently scaled copies of K; a constant gate
-    is a diagonal similarity of the ungated matrix; a token with zero decay cuts the
-    chunk into independent blocks; the tensor layout of the gate.
+    ungated oracle; the page's two differently scaled copies of K; any gate is a
+    diagonal similarity of the ungated matrix, so T = Gamma o T0; a token with zero
+    decay cuts the chunk into independent blocks; the tensor layout of the gate.
 Sources: "TileLang 实战：单位下三角矩阵求逆" §1, §2.1, §2.2, §2.4, §3.2, §4, §5.
 """
 from __future__ import annotations
@@ -312,20 +312,22 @@ def pin_gate_two_scaled_keys(lib):
         np.testing.assert_allclose(A, expect, atol=1e-13, rtol=0)
 
 
-def pin_gate_constant_similarity(lib):
-    """A constant gate g_t = c gives Gamma[i][j] = e^{c (i - j)}: A = D A0 D^-1 with D = diag(e^{c i})
-    and A0 the ungated matrix, so T = D T0 D^-1 with T0 the ungated inverse."""
+def pin_gate_similarity(lib):
+    """Gamma[i][j] = e^{G_i - G_j} makes the gated A a diagonal similarity of the ungated one,
+    A = D A0 D^-1 with D = diag(e^{G_i}), so T = D T0 D^-1: T[i][j] = e^{G_i - G_j} T0[i][j] with T0
+    the ungated inverse, for any gate (a constant one, e^{c (i - j)}, and a random one)."""
     rng = np.random.default_rng(32)
-    Lc, C, c = 48, 64, -0.15
+    Lc, C = 48, 64
     k, v, beta = _rand_chunk(rng, Lc, 32, 16)
     T0, _, _, _ = oracle.oracle_chunk(k, v, beta, C, lib=lib)
-    T, W, U, _ = oracle.oracle_chunk(k, v, beta, C, lib=lib, g=np.full(Lc, c))
-    idx = np.arange(Lc)
-    expect = T0[:, :Lc] * np.exp(c * (idx[:, None] - idx[None, :]))
-    np.testing.assert_allclose(T[:, :Lc], expect, atol=1e-13, rtol=0)
-    assert np.all(T[:, Lc:] == 0.0)
-    np.testing.assert_allclose(W, expect @ (beta[:, None] * k), atol=1e-12, rtol=0)
-    np.testing.assert_allclose(U, expect @ (beta[:, None] * v), atol=1e-12, rtol=0)
+    for g in (np.full(Lc, -0.15), rng.uniform(-0.4, 0.0, Lc)):
+        T, W, U, _ = oracle.oracle_chunk(k, v, beta, C, lib=lib, g=g)
+        G = np.cumsum(g)
+        expect = T0[:, :Lc] * np.exp(G[:, None] - G[None, :])
+        np.testing.assert_allclose(T[:, :Lc], expect, atol=1e-13, rtol=0)
+        assert np.all(T[:, Lc:] == 0.0)
+        np.testing.assert_allclose(W, expect @ (beta[:, None] * k), atol=1e-12, rtol=0)
+        np.testing.assert_allclose(U, expect @ (beta[:, None] * v), atol=1e-12, rtol=0)
 
 
 def pin_gate_cut_decouples(lib):
@@ -393,7 +395,7 @@ PINS = [
     pin_cond_bounds,
     pin_gate_zero_is_ungated,
     pin_gate_two_scaled_keys,
-    pin_gate_constant_similarity,
+    pin_gate_similarity,
     pin_gate_cut_decouples,
     pin_gate_tensor_layout,
 ]
