@@ -359,3 +359,47 @@ def test_full_size_sampled(name):
     col = torch.arange(C, device=DEV).reshape(1, 1, C)
     assert torch.all(Tf[(col == row).expand_as(Tf)] == 1.0)
     assert torch.all(Tf[(col > row).expand_as(Tf)] == 0.0)
+
+
+@pytest.mark.parametrize("name", ["c3_b4_t8192_h16", "c4_varlen32_h32", "c5_b2_t16384_h24_c128"])
+def test_gated_full_size(name):
+    """The gated variant at full size, in the bench's launch configuration: 24 sampled (chunk, head)
+    units against the oracle, and over the whole tensor the similarity that holds for any gate,
+    T = Gamma o T0 with T0 the ungated call's T (each within 1e-4 of the exact value, Gamma <= 1)."""
+    w = workloads()[name]
+    k, v, beta, cu = w.make(seed=0, device=DEV)
+    g = make_gate(k.shape[0], k.shape[1], w.H, seed=0, device=DEV)
+    Tg, Wg, Ug = run(k, v, beta, w.C, cu, g=g)
+    T0, _, _ = run(k, v, beta, w.C, cu)
+    H, C = w.H, w.C
+    flat = lambda x: x.reshape(w.tokens, H, -1)
+    kf, vf, bf, gf = flat(k), flat(v), beta.reshape(w.tokens, H), g.reshape(w.tokens, H)
+    Tgf, Wgf, Ugf, T0f = flat(Tg), flat(Wg), flat(Ug), flat(T0)
+    ch = chunks(C, w.B, w.T, cu)
+    rng = np.random.default_rng(2)
+    picks = [ch[0], ch[-1]] + [ch[i] for i in rng.integers(0, len(ch), 22)]
+    heads = [0, H - 1] + list(rng.integers(0, H, 22))
+    for (t0, Lc), h in zip(picks, heads):
+        h = int(h)
+        Tr, Wr, Ur, _ = oracle.oracle_chunk(to64(kf[t0:t0 + Lc, h]), to64(vf[t0:t0 + Lc, h]),
+                                            to64(bf[t0:t0 + Lc, h]), C, g=to64(gf[t0:t0 + Lc, h]))
+        check_T(to64(Tgf[t0:t0 + Lc, h]), Tr)
+        check_WU(to64(Wgf[t0:t0 + Lc, h]), Wr, "bf16", "W")
+        check_WU(to64(Ugf[t0:t0 + Lc, h]), Ur, "bf16", "U")
+    # Gamma[t][j] = exp(G_t - G_{t0 + j}) with G the prefix sums of g inside each chunk (fp64)
+    G = torch.zeros((w.tokens, H), dtype=torch.float64, device=DEV)
+    gd = gf.double()
+    for t0, Lc in ch:
+        G[t0:t0 + Lc] = torch.cumsum(gd[t0:t0 + Lc], dim=0)
+    starts = torch.zeros(w.tokens, dtype=torch.long, device=DEV)
+    for t0, Lc in ch:
+        starts[t0:t0 + Lc] = t0
+    col = torch.arange(C, device=DEV)
+    src = (starts.reshape(-1, 1) + col.reshape(1, -1)).clamp_max(w.tokens - 1)  # token of column j
+    Gcol = G[src]                                                               # [N, C, H]
+    gamma = torch.exp(G.reshape(-1, 1, H) - Gcol).permute(0, 2, 1)             # [N, H, C]
+    lower = (col.reshape(1, 1, C) <= (torch.arange(w.tokens, device=DEV) - starts).reshape(-1, 1, 1))
+    expect = torch.where(lower, T0f.double() * gamma, torch.zeros_like(gamma))
+    assert torch.all(torch.isfinite(Tgf))
+    err = (Tgf.double() - expect).abs().max().item()
+    assert err <= 2e-4, err
