@@ -60,6 +60,8 @@ def parse_args():
     ap.add_argument("--t-f16", action="store_true", help="T written in fp16 instead of fp32")
     ap.add_argument("--chunk", type=int, default=None,
                     help="override the workload's chunk size C (32, 64 or 128): the chunk-size study")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture the K timed steps into one CUDA graph and time its replay")
     ap.add_argument("--gated", action="store_true",
                     help="gated variant: coefficient diag(beta)(Gamma o K K^T) from per-token log decays g")
     args = ap.parse_args()
@@ -253,6 +255,27 @@ def bench_ours(args, rank, world, local):
             evs[i][1].record(stream)
         torch.cuda.synchronize()
         total_ms = sum(a.elapsed_time(b) for a, b in evs)
+    elif args.graph:
+        # the K steps as one CUDA graph (captured on a side stream after a warm-up there), replayed
+        # once untimed and once between the events
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            for i in range(K):
+                step()
+        graph.replay()
+        torch.cuda.synchronize()
+        t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        graph.replay()
+        t_stop.record(stream)
+        torch.cuda.synchronize()
+        total_ms = t_start.elapsed_time(t_stop)
     else:
         t_start, t_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
@@ -302,7 +325,7 @@ def bench_ours(args, rank, world, local):
         "config": {"workload": w.name, "B": w.B, "T": w.T, "H": w.H, "dk": w.dk, "dv": w.dv,
                    "C": w.C, "tokens_per_step": w.tokens, "kernel": kernel,
                    "T_out": False if args.no_t_out else "fp16" if args.t_f16 else "fp32",
-                   "gated": args.gated,
+                   "gated": args.gated, "cuda_graph": bool(args.graph and not flush),
                    "l2": (f"inputs ({in_bytes / 1e6:.0f} MB) fit in the 129 MB L2: flushed before every step"
                           if flush else f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB > 129 MB), no flush")},
         "hbm_gbs": achieved, "hbm_frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,

@@ -1,12 +1,28 @@
 // kkt_internal.cuh -- shared host/device definitions of libkkt (not installed).
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
 #include "kkt.h"
 
 namespace kkt {
+
+// Raises a kernel's dynamic shared-memory limit to `bytes` once per device (the setting persists in
+// the context), so that a call makes no such runtime call after the first, and calls made while a
+// stream is being captured into a CUDA graph launch only.
+template <auto Kern>
+inline bool ensure_max_smem(int bytes) {
+    static std::atomic<unsigned long long> done{0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    const unsigned long long bit = 1ull << dev;
+    if (done.load(std::memory_order_acquire) & bit) return true;
+    if (cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+    done.fetch_or(bit, std::memory_order_acq_rel);
+    return true;
+}
 
 // Everything a launcher needs, validated by the C entry points.
 struct Problem {

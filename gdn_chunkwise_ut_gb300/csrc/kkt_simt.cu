@@ -196,8 +196,11 @@ int launch_simt_t(const Problem &pb) {
     const size_t smem = sizeof(float) * ((size_t)C * (pb.dk + 1) + (size_t)C * (pb.dv + 1) +
                                          (size_t)C * (C + 1) + 2 * C + (size_t)(C / 2) * (C / 2 + 1));
     auto kern = kkt_simt_kernel<TIn, C>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-        return KKT_ERR_CUDA;
+    // the limit is raised once, to the size at d_k = d_v = 128, the largest head dimension
+    constexpr size_t kMaxSmem = sizeof(float) * ((size_t)C * 129 * 2 + (size_t)C * (C + 1) + 2 * C +
+                                                 (size_t)(C / 2) * (C / 2 + 1));
+    static_assert(kMaxSmem <= 232448, "SIMT shared memory over the per-block limit");
+    if (smem > kMaxSmem || !ensure_max_smem<kkt_simt_kernel<TIn, C>>((int)kMaxSmem)) return KKT_ERR_CUDA;
     SimtParams p;
     p.k = pb.k; p.v = pb.v; p.beta = pb.beta; p.g = pb.g; p.cu = pb.cu_seqlens;
     p.nseq = pb.nseq; p.T = pb.T; p.ntok = pb.ntok;

@@ -1265,8 +1265,11 @@ int launch_tc_t(const Problem &pb) {
     p.stall_first_tile = pb.stall_first_tile;
     auto kern = pb.g ? (pb.t_f16 ? kkt_tc_kernel<C, true, true> : kkt_tc_kernel<C, false, true>)
                      : (pb.t_f16 ? kkt_tc_kernel<C, true, false> : kkt_tc_kernel<C, false, false>);
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM_BYTES) != cudaSuccess)
-        return KKT_ERR_CUDA;
+    const bool attr_ok = pb.g ? (pb.t_f16 ? ensure_max_smem<kkt_tc_kernel<C, true, true>>(CF::SMEM_BYTES)
+                                          : ensure_max_smem<kkt_tc_kernel<C, false, true>>(CF::SMEM_BYTES))
+                              : (pb.t_f16 ? ensure_max_smem<kkt_tc_kernel<C, true, false>>(CF::SMEM_BYTES)
+                                          : ensure_max_smem<kkt_tc_kernel<C, false, false>>(CF::SMEM_BYTES));
+    if (!attr_ok) return KKT_ERR_CUDA;
     const int sms = sm_count();
     if (sms <= 0) return KKT_ERR_CUDA;
     const int64_t grid = p.tiles < sms ? p.tiles : sms;

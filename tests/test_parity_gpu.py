@@ -403,3 +403,38 @@ def test_gated_full_size(name):
     assert torch.all(torch.isfinite(Tgf))
     err = (Tgf.double() - expect).abs().max().item()
     assert err <= 2e-4, err
+
+
+@pytest.mark.parametrize("kernel", ALL_KERNELS)
+def test_cuda_graph_capture_and_replay(kernel):
+    """Calls captured into a CUDA graph replay to the eager results, bit for bit: the launch carries
+    no host state between calls (the work counter in the workspace clears itself), so replays
+    and back-to-back launches with programmatic dependent launch are safe."""
+    _skip_unless(kernel, 128, 128, 64)
+    k, v, beta = make_inputs(2, 700, 3, 128, 128, seed=51, device=DEV)
+    g = make_gate(2, 700, 3, seed=51, device=DEV)
+    eager = run(k, v, beta, 64, kernel=kernel)
+    eager_g = run(k, v, beta, 64, kernel=kernel, g=g)
+    T1, W1, U1 = (torch.full_like(x, float("nan")) for x in eager)
+    T2, W2, U2 = (torch.full_like(x, float("nan")) for x in eager_g)
+    ws = torch.zeros(64, dtype=torch.int32, device=DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # warm-up on the capture stream
+        kkt_solve_fwd(k, v, beta, 64, T_out=T1, W_out=W1, U_out=U1, kernel=kernel, workspace=ws)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(3):
+            kkt_solve_fwd(k, v, beta, 64, T_out=T1, W_out=W1, U_out=U1, kernel=kernel, workspace=ws)
+            kkt_solve_fwd(k, v, beta, 64, T_out=T2, W_out=W2, U_out=U2, kernel=kernel, workspace=ws, g=g)
+    for x in (T1, W1, U1, T2, W2, U2):
+        x.fill_(float("nan"))
+    for _ in range(4):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert device_status() == 0
+    assert torch.count_nonzero(ws).item() == 0
+    for a, b in zip(eager + eager_g, (T1, W1, U1, T2, W2, U2)):
+        assert torch.equal(a, b)
