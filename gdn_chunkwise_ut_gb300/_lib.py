@@ -44,6 +44,7 @@ SIGNATURES = {
     "kkt_solve_fwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
     "kkt_test_stalled_solve": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
     "kkt_device_status": (_i, [_vp]),
+    "kkt_debug_bounds": (_i, [_vp, _vp]),
     "kkt_select_kernel": (_i, [_i, _i, _i, _i, _i]),
     "kkt_status_string": (ctypes.c_char_p, [_i]),
     "kkt_version": (_i, []),

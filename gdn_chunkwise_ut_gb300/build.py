@@ -40,16 +40,24 @@ def _stale(out: Path, deps) -> bool:
     return any(Path(d).stat().st_mtime > t for d in deps)
 
 
-def build(verbose: bool = False, force: bool = False, extra_flags=(), trace: bool = False) -> Path:
+def build(verbose: bool = False, force: bool = False, extra_flags=(), trace: bool = False,
+          debug_bounds: bool = False) -> Path:
     """Compile every csrc/*.cu and link libkkt.so; returns the library path.
 
     ``trace=True`` builds a separate libkkt_trace.so (in _build/trace) with the
     pipeline time stamps of the tensor-core kernel compiled in (see trace.py).
+    ``debug_bounds=True`` builds a separate libkkt_bounds.so (in _build/bounds) with
+    every shared-memory, array and plain global access range-checked (kkt_debug.cuh;
+    read with kkt_debug_bounds()).
     """
-    out_dir = BUILD / "trace" if trace else BUILD
-    lib_path = out_dir / ("libkkt_trace.so" if trace else "libkkt.so")
+    if trace and debug_bounds:
+        raise ValueError("trace and debug_bounds are separate builds")
+    out_dir = BUILD / "trace" if trace else BUILD / "bounds" if debug_bounds else BUILD
+    lib_path = out_dir / ("libkkt_trace.so" if trace else "libkkt_bounds.so" if debug_bounds else "libkkt.so")
     if trace:
         extra_flags = (*extra_flags, "-DKKT_TRACE")
+    if debug_bounds:
+        extra_flags = (*extra_flags, "-DKKT_DEBUG_BOUNDS")
     out_dir.mkdir(parents=True, exist_ok=True)
     headers = list(CSRC.glob("*.cuh")) + list(INCLUDE.glob("*.h"))
     nvcc = _nvcc()

@@ -151,6 +151,15 @@ extern "C" const char *kkt_status_string(int status) {
 
 extern "C" int kkt_version(void) { return (0 << 16) | (1 << 8) | 0; }
 
+extern "C" int kkt_debug_bounds(unsigned long long *first, int *kind) {
+    kkt::BoundsRecord tc = {0u, 0u, 0ull}, simt = {0u, 0u, 0ull};
+    if (kkt::debug_bounds_tc(&tc) < 0 || kkt::debug_bounds_simt(&simt) < 0) return -1;
+    const kkt::BoundsRecord &f = tc.count ? tc : simt;
+    if (first) *first = f.first;
+    if (kind) *kind = (int)f.kind;
+    return (int)(tc.count + simt.count);
+}
+
 #ifdef KKT_TRACE
 // Trace builds only: device buffer of kTraceCtas x kTraceTiles x 16 uint64 time stamps
 // (see trace.py), or NULL to stop tracing.

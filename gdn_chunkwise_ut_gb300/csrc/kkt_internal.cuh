@@ -117,6 +117,17 @@ int status_ptr(int **out);
 
 int launch_simt(const Problem &p);
 int launch_tc(const Problem &p);
+
+// Bounds-checked debug builds (-DKKT_DEBUG_BOUNDS, kkt_debug.cuh): violation count, kind of the
+// first (1 shared memory, 2 array index, 3 global index) and its shared address or index.  Each
+// kernel file reads and clears its own record; -1 in the default build.
+struct BoundsRecord {
+    unsigned int count;
+    unsigned int kind;
+    unsigned long long first;
+};
+int debug_bounds_tc(BoundsRecord *out);
+int debug_bounds_simt(BoundsRecord *out);
 bool tc_supports(int dk, int dv, int C, int io);
 
 }  // namespace kkt

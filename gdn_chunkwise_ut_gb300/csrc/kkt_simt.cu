@@ -13,6 +13,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "kkt_debug.cuh"
 #include "kkt_internal.cuh"
 
 namespace kkt {
@@ -52,6 +53,13 @@ __global__ void __launch_bounds__(kSimtThreads) kkt_simt_kernel(const SimtParams
     float *bs = Ts + C * TS;     // [C]
     float *gs = bs + C;          // [C]: prefix sums G of the chunk's log decays (gated variant)
     float *Ys = gs + C;          // coupling scratch, up to (C/2) x (C/2 + 1)
+    // element access of each array (range-checked in the bounds-checked debug build)
+    auto K_ = [&](int64_t i) -> float & { return arr_at(Ks, i, (int64_t)C * KS); };
+    auto V_ = [&](int64_t i) -> float & { return arr_at(Vs, i, (int64_t)C * VS); };
+    auto T_ = [&](int64_t i) -> float & { return arr_at(Ts, i, (int64_t)C * TS); };
+    auto B_ = [&](int64_t i) -> float & { return arr_at(bs, i, (int64_t)C); };
+    auto G_ = [&](int64_t i) -> float & { return arr_at(gs, i, (int64_t)C); };
+    auto Y_ = [&](int64_t i) -> float & { return arr_at(Ys, i, (int64_t)(C / 2) * (C / 2 + 1)); };
 
     const int64_t id = blockIdx.x;
     const int h = blockIdx.y;
@@ -71,19 +79,19 @@ __global__ void __launch_bounds__(kSimtThreads) kkt_simt_kernel(const SimtParams
     // 1. stage K, V, beta; rows >= Lc are zero
     for (int e = tid; e < C * DK; e += kSimtThreads) {
         const int i = e / DK, d = e - (e / DK) * DK;
-        Ks[i * KS + d] = (i < Lc) ? to_f(kg[((t0 + i) * H + h) * DK + d]) : 0.f;
+        K_(i * KS + d) = (i < Lc) ? to_f(*gmem_chk(kg, ((t0 + i) * H + h) * DK + d, p.ntok * H * DK)) : 0.f;
     }
     for (int e = tid; e < C * DV; e += kSimtThreads) {
         const int i = e / DV, d = e - (e / DV) * DV;
-        Vs[i * VS + d] = (i < Lc) ? to_f(vg[((t0 + i) * H + h) * DV + d]) : 0.f;
+        V_(i * VS + d) = (i < Lc) ? to_f(*gmem_chk(vg, ((t0 + i) * H + h) * DV + d, p.ntok * H * DV)) : 0.f;
     }
-    for (int i = tid; i < C; i += kSimtThreads) bs[i] = (i < Lc) ? p.beta[(t0 + i) * H + h] : 0.f;
+    for (int i = tid; i < C; i += kSimtThreads) B_(i) = (i < Lc) ? *gmem_chk(p.beta, (t0 + i) * H + h, p.ntok * H) : 0.f;
     if (p.g && tid == 0) {
         // G_i = g_0 + ... + g_i over the chunk's tokens, so that Gamma[i][j] = exp(G_i - G_j)
         float acc = 0.f;
         for (int i = 0; i < C; ++i) {
-            acc += (i < Lc) ? p.g[(t0 + i) * H + h] : 0.f;
-            gs[i] = acc;
+            acc += (i < Lc) ? *gmem_chk(p.g, (t0 + i) * H + h, p.ntok * H) : 0.f;
+            G_(i) = acc;
         }
     }
     __syncthreads();
@@ -97,11 +105,11 @@ __global__ void __launch_bounds__(kSimtThreads) kkt_simt_kernel(const SimtParams
             a = 1.f;
         } else if (i > j) {
             float s = 0.f;
-            for (int d = 0; d < DK; ++d) s = fmaf(Ks[i * KS + d], Ks[j * KS + d], s);
-            a = bs[i] * s;
-            if (p.g) a *= expf(gs[i] - gs[j]);
+            for (int d = 0; d < DK; ++d) s = fmaf(K_(i * KS + d), K_(j * KS + d), s);
+            a = B_(i) * s;
+            if (p.g) a *= expf(G_(i) - G_(j));
         }
-        Ts[i * TS + j] = a;
+        T_(i * TS + j) = a;
     }
     __syncthreads();
 
@@ -111,22 +119,21 @@ __global__ void __launch_bounds__(kSimtThreads) kkt_simt_kernel(const SimtParams
     const bool sub = tid < NB * 16;
     const int b = tid >> 4, c = tid & 15;
     float x[16];
+    const int64_t d0 = (int64_t)(16 * b) * TS + 16 * b;  // the diagonal block's first element
     if (sub) {
-        const float *L = Ts + (16 * b) * TS + 16 * b;
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
             float s = (r == c) ? 1.f : 0.f;
 #pragma unroll
-            for (int m = 0; m < r; ++m) s = fmaf(-L[r * TS + m], x[m], s);
+            for (int m = 0; m < r; ++m) s = fmaf(-T_(d0 + r * TS + m), x[m], s);
             x[r] = s;
         }
     }
     __syncthreads();  // every read of the block's L is done before it is overwritten
     if (sub) {
-        float *X = Ts + (16 * b) * TS + 16 * b;
 #pragma unroll
         for (int r = 1; r < 16; ++r)
-            if (r > c) X[r * TS + c] = x[r];
+            if (r > c) T_(d0 + r * TS + c) = x[r];
     }
     __syncthreads();
 
@@ -138,21 +145,19 @@ __global__ void __launch_bounds__(kSimtThreads) kkt_simt_kernel(const SimtParams
         for (int e = tid; e < n; e += kSimtThreads) {
             const int pr = e / (s * s), r = (e / s) % s, cc = e % s;
             const int o = 2 * s * pr;
-            const float *L10 = Ts + (o + s) * TS + o;
-            const float *X00 = Ts + o * TS + o;
-            float acc = 0.f;
-            for (int m = cc; m < s; ++m) acc = fmaf(L10[r * TS + m], X00[m * TS + cc], acc);
-            Ys[pr * s * YS + r * YS + cc] = acc;
+            float acc = 0.f;  // (L10 X00)[r][cc], L10 at rows o + s.., columns o..; X00 at (o, o)
+            for (int m = cc; m < s; ++m)
+                acc = fmaf(T_((int64_t)(o + s + r) * TS + o + m), T_((int64_t)(o + m) * TS + o + cc), acc);
+            Y_(pr * s * YS + r * YS + cc) = acc;
         }
         __syncthreads();
         for (int e = tid; e < n; e += kSimtThreads) {
             const int pr = e / (s * s), r = (e / s) % s, cc = e % s;
             const int o = 2 * s * pr;
-            const float *X11 = Ts + (o + s) * TS + (o + s);
-            const float *Y = Ys + pr * s * YS;
-            float acc = 0.f;
-            for (int m = 0; m <= r; ++m) acc = fmaf(X11[r * TS + m], Y[m * YS + cc], acc);
-            Ts[(o + s + r) * TS + o + cc] = -acc;
+            float acc = 0.f;  // (X11 Y)[r][cc], X11 at (o + s, o + s)
+            for (int m = 0; m <= r; ++m)
+                acc = fmaf(T_((int64_t)(o + s + r) * TS + o + s + m), Y_(pr * s * YS + m * YS + cc), acc);
+            T_((int64_t)(o + s + r) * TS + o + cc) = -acc;
         }
         __syncthreads();
     }
@@ -160,19 +165,19 @@ __global__ void __launch_bounds__(kSimtThreads) kkt_simt_kernel(const SimtParams
     // 5. T_out rows of the chunk (zeros in columns >= Lc); none without T_out (W and U~ only)
     for (int e = tid; p.T_out && e < Lc * C; e += kSimtThreads) {
         const int i = e / C, j = e % C;
-        const float x = (j < Lc) ? Ts[i * TS + j] : 0.f;
+        const float x = (j < Lc) ? T_(i * TS + j) : 0.f;
         const int64_t at = ((t0 + i) * H + h) * C + j;
         if (p.t_f16)
-            static_cast<__half *>(p.T_out)[at] = __float2half_rn(x);
+            *gmem_chk(static_cast<__half *>(p.T_out), at, p.ntok * H * C) = __float2half_rn(x);
         else
-            static_cast<float *>(p.T_out)[at] = x;
+            *gmem_chk(static_cast<float *>(p.T_out), at, p.ntok * H * C) = x;
     }
     __syncthreads();
 
     // 6. T~ = T diag(beta), in place
     for (int e = tid; e < C * C; e += kSimtThreads) {
         const int i = e / C, j = e % C;
-        Ts[i * TS + j] *= bs[j];
+        T_(i * TS + j) *= B_(j);
     }
     __syncthreads();
 
@@ -180,14 +185,14 @@ __global__ void __launch_bounds__(kSimtThreads) kkt_simt_kernel(const SimtParams
     for (int e = tid; e < Lc * DK; e += kSimtThreads) {
         const int i = e / DK, d = e - (e / DK) * DK;
         float acc = 0.f;
-        for (int j = 0; j <= i; ++j) acc = fmaf(Ts[i * TS + j], Ks[j * KS + d], acc);
-        wg[((t0 + i) * H + h) * DK + d] = from_f<TIn>(acc);
+        for (int j = 0; j <= i; ++j) acc = fmaf(T_(i * TS + j), K_(j * KS + d), acc);
+        *gmem_chk(wg, ((t0 + i) * H + h) * DK + d, p.ntok * H * DK) = from_f<TIn>(acc);
     }
     for (int e = tid; e < Lc * DV; e += kSimtThreads) {
         const int i = e / DV, d = e - (e / DV) * DV;
         float acc = 0.f;
-        for (int j = 0; j <= i; ++j) acc = fmaf(Ts[i * TS + j], Vs[j * VS + d], acc);
-        ug[((t0 + i) * H + h) * DV + d] = from_f<TIn>(acc);
+        for (int j = 0; j <= i; ++j) acc = fmaf(T_(i * TS + j), V_(j * VS + d), acc);
+        *gmem_chk(ug, ((t0 + i) * H + h) * DV + d, p.ntok * H * DV) = from_f<TIn>(acc);
     }
 }
 
@@ -223,6 +228,8 @@ int dispatch_c(const Problem &p) {
 }
 
 }  // namespace
+
+int debug_bounds_simt(BoundsRecord *out) { return read_bounds_record(out); }
 
 int launch_simt(const Problem &p) {
     return p.io == KKT_IO_F32 ? dispatch_c<float>(p) : dispatch_c<__nv_bfloat16>(p);

@@ -46,6 +46,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include "kkt_debug.cuh"
 #include "kkt_internal.cuh"
 #include "sm100_ptx.cuh"
 
@@ -194,11 +195,11 @@ __device__ __forceinline__ bool group_sync(uint64_t *bar, uint32_t &uses, Barrie
 // [half][128 rows][128 B], with the 128-byte swizzle that TMA uses (16-byte chunk index XOR
 // row mod 8): rows are conflict-free for a thread per row, and a row is a TMA box row.
 __device__ __forceinline__ float *tm_elem(uint8_t *tm, int m, int j) {
-    return reinterpret_cast<float *>(tm + (j >> 5) * 16384 + m * 128 + ((((j & 31) >> 2) ^ (m & 7)) << 4) +
-                                     (j & 3) * 4);
+    return smem_chk(reinterpret_cast<float *>(tm + (j >> 5) * 16384 + m * 128 + ((((j & 31) >> 2) ^ (m & 7)) << 4) +
+                                              (j & 3) * 4));
 }
 __device__ __forceinline__ float4 *tm_vec(uint8_t *tm, int m, int j) {  // j a multiple of 4
-    return reinterpret_cast<float4 *>(tm + (j >> 5) * 16384 + m * 128 + ((((j & 31) >> 2) ^ (m & 7)) << 4));
+    return smem_chk(reinterpret_cast<float4 *>(tm + (j >> 5) * 16384 + m * 128 + ((((j & 31) >> 2) ^ (m & 7)) << 4)));
 }
 
 // Two fp16 (round to nearest even) in the bits of one float: lo in bits 0..15, hi in 16..31.
@@ -268,14 +269,14 @@ __device__ __forceinline__ void tile4x4_fma(float2 (&y)[4][2], const uint8_t *co
         const uint32_t ca = (uint32_t)((acol0 >> 2) + 2 * kb) << 4;
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr) {
-            const float4 a0 = *reinterpret_cast<const float4 *>(arow[rr] + (ca ^ axor[rr]));
-            const float4 a1 = *reinterpret_cast<const float4 *>(arow[rr] + ((ca + 16u) ^ axor[rr]));
+            const float4 a0 = *smem_chk(reinterpret_cast<const float4 *>(arow[rr] + (ca ^ axor[rr])));
+            const float4 a1 = *smem_chk(reinterpret_cast<const float4 *>(arow[rr] + ((ca + 16u) ^ axor[rr])));
             av[rr][0] = a0.x; av[rr][1] = a0.y; av[rr][2] = a0.z; av[rr][3] = a0.w;
             av[rr][4] = a1.x; av[rr][5] = a1.y; av[rr][6] = a1.z; av[rr][7] = a1.w;
         }
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-            const float4 b = *reinterpret_cast<const float4 *>(brow0 + (8 * kb + kk) * 128 + bsw[kk]);
+            const float4 b = *smem_chk(reinterpret_cast<const float4 *>(brow0 + (8 * kb + kk) * 128 + bsw[kk]));
             const float2 b01 = make_float2(b.x, b.y), b23 = make_float2(b.z, b.w);
 #pragma unroll
             for (int rr = 0; rr < 4; ++rr) {
@@ -468,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto stage_gw = [&](int s) { return reinterpret_cast<float *>(smem + CF::OFF_META + s * CF::META_BYTES + 1024); };
     auto stage_gflag = [&](int s) { return reinterpret_cast<int *>(smem + CF::OFF_META + s * CF::META_BYTES + 1536); };
     auto stage_info = [&](int s) {
-        return reinterpret_cast<TileInfo *>(smem + CF::OFF_META + s * CF::META_BYTES + 1552);
+        return smem_chk(reinterpret_cast<TileInfo *>(smem + CF::OFF_META + s * CF::META_BYTES + 1552));
     };
 
     if (threadIdx.x == 0) {
@@ -544,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 4; ++e) {
                 const int idx = lane + 32 * e;
                 const int g = idx / C, r = idx % C;
-                bv[e] = (r < ch.Lc && h0 + g < p.H) ? __ldg(p.beta + (ch.t0 + r) * p.H + h0 + g) : 0.f;
+                bv[e] = (r < ch.Lc && h0 + g < p.H) ? __ldg(gmem_chk(p.beta, (ch.t0 + r) * p.H + h0 + g, p.ntok * p.H)) : 0.f;
             }
             // gated: prefix sums G of the log decays over each head's chunk, in log2 units, so that
             // Gamma[i][j] = exp2(G_i - G_j).  For a column j of 32-row block b, with R_b = G at the
@@ -561,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < 4; ++e) {
                     const int idx = lane + 32 * e;
                     const int g = idx / C, r = idx % C;
-                    gv[e] = (r < ch.Lc && h0 + g < p.H) ? kLog2e * __ldg(p.g + (ch.t0 + r) * p.H + h0 + g) : 0.f;
+                    gv[e] = (r < ch.Lc && h0 + g < p.H) ? kLog2e * __ldg(gmem_chk(p.g, (ch.t0 + r) * p.H + h0 + g, p.ntok * p.H)) : 0.f;
                 }
             }
             const int s = i % kNS;
@@ -570,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) KKT_TRACE_EVENT(EV_P_EMPTY, i);
             float *sb = stage_beta(s);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sb[lane + 32 * e] = bv[e];
+            for (int e = 0; e < 4; ++e) *smem_chk(sb + lane + 32 * e) = bv[e];
             if (lane == 0) {
                 TileInfo *info = stage_info(s);
                 info->t0 = ch.t0;
@@ -606,11 +607,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float *sg = stage_gate(s), *sw = stage_gw(s);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    sg[lane + 32 * e] = gv[e];
-                    sw[lane + 32 * e] = wv[e];
+                    *smem_chk(sg + lane + 32 * e) = gv[e];
+                    *smem_chk(sw + lane + 32 * e) = wv[e];
                 }
                 if (lane == 0)
-                    for (int e = 0; e < 4; ++e) stage_gflag(s)[e] = fv[e];
+                    for (int e = 0; e < 4; ++e) *smem_chk(stage_gflag(s) + e) = fv[e];
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->full[s]);
             }
@@ -670,8 +671,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = lane; e < G * 4 * per_box; e += 32) {
                     const int box = e / per_box, w = e % per_box;
                     const int g = box % G, kvh = box / G;  // kvh: K half 0, 1, V half 0, 1
-                    *reinterpret_cast<uint4 *>(st + kvh * 16384 + g * C * 128 + (info.Lc + w / 8) * 128 +
-                                               (w % 8) * 16) = make_uint4(0, 0, 0, 0);
+                    *smem_chk(reinterpret_cast<uint4 *>(st + kvh * 16384 + g * C * 128 + (info.Lc + w / 8) * 128 +
+                                                        (w % 8) * 16)) = make_uint4(0, 0, 0, 0);
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -776,7 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const TileInfo info = *stage_info(s);
             if (info.done) break;
             const float *sb = stage_beta(s) + g * C;
-            const float beta_r = sb[r];
+            const float beta_r = *smem_chk(sb + r);
             // gated: Gamma[r][j], the decay from token j to token r (j < r), for columns 32 h + c ..
             // + 3 is exp2(G_r - R_h) w_j when every block of the head is factorable (fac); otherwise
             // the row is formed without it and multiplied by exp2(G_r - G_j) element by element after
@@ -786,18 +787,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool fac = true;
             float g_r = 0.f;
             if constexpr (GATED) {
-                g_r = sg[r];
+                g_r = *smem_chk(sg + r);
                 const int *sf = stage_gflag(s) + g * C / 32;
 #pragma unroll
-                for (int h = 0; h < CF::T_HALVES; ++h) fac = fac && sf[h] != 0;
+                for (int h = 0; h < CF::T_HALVES; ++h) fac = fac && *smem_chk(sf + h) != 0;
             }
             // the column factors w of block h (ones when not factorable), loaded together ahead of use
             auto load_w = [&](int h, float4 (&wq)[8]) {
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8)
-                    wq[c8] = fac ? *reinterpret_cast<const float4 *>(sw + 32 * h + 4 * c8) : make_float4(1.f, 1.f, 1.f, 1.f);
+                    wq[c8] = fac ? *smem_chk(reinterpret_cast<const float4 *>(sw + 32 * h + 4 * c8)) : make_float4(1.f, 1.f, 1.f, 1.f);
             };
-            auto row_factor = [&](int h) { return fac ? exp2f(g_r - sg[32 * h]) : 1.f; };
+            auto row_factor = [&](int h) { return fac ? exp2f(g_r - *smem_chk(sg + 32 * h)) : 1.f; };
 
             if (!wait_bar(&bars->gram_full, (uint32_t)i & 1u, bars, p.status)) break;
             tc_fence_after();
@@ -889,7 +890,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (GATED) {
                 if (!fac) {
 #pragma unroll 1
-                    for (int j = 0; j < r; ++j) *tm_elem(tm, m, j) *= exp2f(g_r - sg[j]);
+                    for (int j = 0; j < r; ++j) *tm_elem(tm, m, j) *= exp2f(g_r - *smem_chk(sg + j));
                 }
             }
             tc_fence_before();
@@ -1032,8 +1033,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     bulk_commit();
                 }
             } else if (r < info.Lc && info.h0 + g < p.H) {
-                float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.T_out) +
-                                                         ((info.t0 + r) * p.H + info.h0 + g) * C);
+                float4 *dst = reinterpret_cast<float4 *>(gmem_chk(static_cast<float *>(p.T_out),
+                                                                  ((info.t0 + r) * p.H + info.h0 + g) * C,
+                                                                  p.ntok * p.H * C, C));
 #pragma unroll
                 for (int j = 0; j < C; j += 4) dst[j / 4] = *tm_vec(tm, m, j);
             }
@@ -1061,8 +1063,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int c = 0; c < 32; c += 8) {
                             const float4 ta = *tm_vec(tm, m, 32 * blk + c);
                             const float4 tb = *tm_vec(tm, m, 32 * blk + c + 4);
-                            const float4 ba = *reinterpret_cast<const float4 *>(sb + 32 * blk + c);
-                            const float4 bb = *reinterpret_cast<const float4 *>(sb + 32 * blk + c + 4);
+                            const float4 ba = *smem_chk(reinterpret_cast<const float4 *>(sb + 32 * blk + c));
+                            const float4 bb = *smem_chk(reinterpret_cast<const float4 *>(sb + 32 * blk + c + 4));
                             split_bf16(fmul2(make_float2(ta.x, ta.y), make_float2(ba.x, ba.y)), hi[c / 2], lo[c / 2]);
                             split_bf16(fmul2(make_float2(ta.z, ta.w), make_float2(ba.z, ba.w)), hi[c / 2 + 1], lo[c / 2 + 1]);
                             split_bf16(fmul2(make_float2(tb.x, tb.y), make_float2(bb.x, bb.y)), hi[c / 2 + 2], lo[c / 2 + 2]);
@@ -1071,10 +1073,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 const float4 h8 = make_float4(pack_f16(ta.x, ta.y), pack_f16(ta.z, ta.w),
                                                               pack_f16(tb.x, tb.y), pack_f16(tb.z, tb.w));
                                 if (t16_tma)
-                                    t16s[(4 * (blk & 1) + c / 8) ^ (m & 7)] = h8;
+                                    *smem_chk(t16s + ((4 * (blk & 1) + c / 8) ^ (m & 7))) = h8;
                                 else if (t16_row)
-                                    *reinterpret_cast<float4 *>(static_cast<__half *>(p.T_out) +
-                                                                ((info.t0 + r) * p.H + info.h0 + g) * C + 32 * blk + c) = h8;
+                                    *reinterpret_cast<float4 *>(gmem_chk(static_cast<__half *>(p.T_out),
+                                                                         ((info.t0 + r) * p.H + info.h0 + g) * C + 32 * blk + c,
+                                                                         p.ntok * p.H * C, 8)) = h8;
                             }
                         }
                         const uint32_t col = (uint32_t)(g * C + 32 * blk) / 2;
@@ -1086,10 +1089,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             if (t16_tma)
-                                t16s[(4 * (blk & 1) + e) ^ (m & 7)] = z;
+                                *smem_chk(t16s + ((4 * (blk & 1) + e) ^ (m & 7))) = z;
                             else if (t16_row)
-                                *reinterpret_cast<float4 *>(static_cast<__half *>(p.T_out) +
-                                                            ((info.t0 + r) * p.H + info.h0 + g) * C + 32 * blk + 8 * e) = z;
+                                *reinterpret_cast<float4 *>(gmem_chk(static_cast<__half *>(p.T_out),
+                                                                     ((info.t0 + r) * p.H + info.h0 + g) * C + 32 * blk + 8 * e,
+                                                                     p.ntok * p.H * C, 8)) = z;
                         }
                     }
                 }
@@ -1162,7 +1166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
-                        *reinterpret_cast<uint4 *>(buf + sw128((uint32_t)(lane * 128 + 16 * e))) =
+                        *smem_chk(reinterpret_cast<uint4 *>(buf + sw128((uint32_t)(lane * 128 + 16 * e)))) =
                             make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -1173,7 +1177,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ++nstore;
                 } else if (row_ok) {
-                    __nv_bfloat16 *base = (cc < 2 ? p.W_out : p.U_out) + grow * 128 + 64 * (cc & 1);
+                    __nv_bfloat16 *base = gmem_chk(cc < 2 ? p.W_out : p.U_out, grow * 128 + 64 * (cc & 1),
+                                                   p.ntok * p.H * 128, 64);
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         reinterpret_cast<uint4 *>(base)[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
@@ -1294,6 +1299,8 @@ int launch_tc_t(const Problem &pb) {
 bool tc_supports(int dk, int dv, int C, int io) {
     return io == KKT_IO_BF16 && dk == 128 && dv == 128 && (C == 32 || C == 64 || C == 128);
 }
+
+int debug_bounds_tc(BoundsRecord *out) { return read_bounds_record(out); }
 
 int launch_tc(const Problem &p) {
     switch (p.C) {

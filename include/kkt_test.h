@@ -34,6 +34,20 @@ int kkt_test_stalled_solve(const void *k, const void *v, const float *beta, cons
                            int B, int T, int H, int dk, int dv, int C,
                            float *T_out, void *W_out, void *U_out, struct CUstream_st *stream);
 
+/*
+ * kkt_debug_bounds -- the range checks of a bounds-checked build (library built with
+ * -DKKT_DEBUG_BOUNDS, e.g. gdn_chunkwise_ut_gb300.build.build(debug_bounds=True)).
+ *
+ * In such a build every shared-memory access of the tensor-core kernel, every array access of
+ * the SIMT kernel and every plain global load or store of both is checked against its range; a
+ * failed check counts a violation and redirects the access to a scratch slot (no fault, no trap).
+ * Synchronises nothing: call it after the device work has completed.  Returns the number of
+ * violations since the last call and clears the records, writing the kind of the first violation
+ * (1 shared memory, 2 array index, 3 global index) and its shared address or index to *kind and
+ * *first (either may be NULL).  Returns -1 in the default build (no checks compiled in).
+ */
+int kkt_debug_bounds(unsigned long long *first, int *kind);
+
 #ifdef __cplusplus
 }
 #endif

@@ -131,6 +131,11 @@ def test_gated_argument_errors(lib):
     assert call(g=None, T=0) == _lib.KKT_OK  # g == NULL is the ungated call
 
 
+def test_default_build_has_no_bounds_checks(lib):
+    """kkt_debug_bounds reports -1 in the default build: no checks are compiled into the product."""
+    assert lib.kkt_debug_bounds(None, None) == -1
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     """The product path has no fallback: without libkkt.so every call raises."""
     monkeypatch.setattr(_lib, "LIB_PATH", tmp_path / "libkkt.so")
