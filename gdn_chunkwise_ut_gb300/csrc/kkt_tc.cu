@@ -6,11 +6,13 @@
 //
 //   producer warp   TMA: K and V boxes {64 cols, 1 head, C rows} (128-byte
 //                   swizzle) into a stage of a two-deep shared-memory ring;
-//                   beta with plain loads.
-//   MMA warp        an event loop, one elected lane issuing tcgen05.mma:
-//                   S = K K^T (M = N = 128, K = 128, bf16 -> fp32 in tensor
-//                   memory), and D = T~ [K | V] with T~ = T diag(beta) read from
-//                   tensor memory as a bf16 hi + lo pair (two accumulating
+//                   beta (and the gate's prefix sums, gated kernels) with plain
+//                   loads.
+//   Gram warp       one lane issuing tcgen05.mma S = K K^T (M = N = 128,
+//                   K = 128, bf16 -> fp32 in tensor memory); zeroes the rows past
+//                   a short chunk's end first.
+//   W|U warp        one lane issuing D = T~ [K | V] with T~ = T diag(beta) read
+//                   from tensor memory as a bf16 hi + lo pair (two accumulating
 //                   passes, M = 128, N = 256, K = 128; T~ is block diagonal over
 //                   the G heads).  The commit after D frees the stage.
 //   inverse warps   a thread per row loads its Gram row (tcgen05.ld), applies
