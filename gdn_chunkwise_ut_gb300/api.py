@@ -154,23 +154,59 @@ def select_kernel(dk: int, dv: int, C: int, io: str = "bf16", kernel: str = "aut
     return {_lib.KKT_KERNEL_SIMT: "simt", _lib.KKT_KERNEL_TC: "tc"}[r]
 
 
+def _pieces(seq_bounds, C: int, parts: int):
+    """Cuts a packed batch (sequence token ranges [a, b) on the flat axis, in order) into at most
+    ``parts`` consecutive pieces of about equal token counts.  A sequence is cut only at a multiple of
+    C from its start, so every piece starts its sub-sequences at chunk boundaries and the chunks, and
+    therefore the results, are those of the whole batch.  Returns [(n0, n1, cu)] with cu the piece's
+    sequence offsets relative to n0."""
+    total = sum(b - a for a, b in seq_bounds)
+    if total == 0:
+        return []
+    target = max(C, -(-total // max(1, parts)))
+    out, cur, n0 = [], [0], None
+    for a, b in seq_bounds:
+        if n0 is None:
+            n0 = a
+        pos = a
+        while True:
+            room = target - cur[-1]
+            if b - pos <= room or room < C:
+                if b - pos > room and cur[-1] > 0:
+                    out.append((n0, n0 + cur[-1], cur))  # close the piece before this sequence part
+                    cur, n0 = [0], pos
+                    continue
+                cur.append(cur[-1] + (b - pos))
+                break
+            cut = pos + (room // C) * C  # a chunk boundary of this sequence (pos is one)
+            cur.append(cur[-1] + (cut - pos))
+            out.append((n0, n0 + cur[-1], cur))
+            cur, n0, pos = [0], cut, cut
+    if cur[-1] > 0 or len(cur) > 1:
+        out.append((n0, n0 + cur[-1], cur))
+    return [(x0, x1, c) for x0, x1, c in out if x1 > x0]
+
+
 class HostRunner:
     """End-to-end calls on host tensors: pinned host -> device -> kkt_solve_fwd -> pinned host.
 
-    Device buffers are allocated once; each call copies the inputs in, runs the
-    library on the current stream and copies T, W and U back, then synchronises.
+    Device buffers are allocated once.  Each call cuts the batch into ``pieces`` parts along the
+    token axis (whole sequences, or chunk-aligned parts of one) and pipelines them: the inputs of a
+    piece are copied in on one stream, the library runs it on the current stream, and its T, W and U
+    are copied back on a third stream, so the two copy directions and the kernels overlap.  The
+    results are those of one call on the whole batch.  ``sync=True`` waits for the copies.
     """
 
     def __init__(self, B, T, H, dk, dv, C, *, dtype=torch.bfloat16, cu_seqlens=None,
                  kernel="auto", device="cuda", materialize_T: bool = True, T_dtype=torch.float32,
-                 gated: bool = False):
+                 gated: bool = False, pieces: int = 4):
         self.C, self.kernel, self.materialize_T, self.T_dtype = C, kernel, materialize_T, T_dtype
         dev = torch.device(device)
+        self.shape = (B, T, H)
         self.k = torch.empty((B, T, H, dk), device=dev, dtype=dtype)
         self.v = torch.empty((B, T, H, dv), device=dev, dtype=dtype)
         self.beta = torch.empty((B, T, H), device=dev, dtype=torch.float32)
         self.g = torch.empty((B, T, H), device=dev, dtype=torch.float32) if gated else None
-        self.cu = None if cu_seqlens is None else torch.as_tensor(cu_seqlens, dtype=torch.int32).to(dev)
         self.T_out = torch.empty((B, T, H, C), device=dev, dtype=T_dtype) if materialize_T else None
         self.W = torch.empty((B, T, H, dk), device=dev, dtype=dtype)
         self.U = torch.empty((B, T, H, dv), device=dev, dtype=dtype)
@@ -178,6 +214,15 @@ class HostRunner:
                        if materialize_T else None)
         self.W_host = torch.empty(self.W.shape, dtype=dtype, pin_memory=True)
         self.U_host = torch.empty(self.U.shape, dtype=dtype, pin_memory=True)
+        if cu_seqlens is None:
+            bounds = [(b * T, (b + 1) * T) for b in range(B)]
+        else:
+            cu = [int(x) for x in cu_seqlens]
+            bounds = list(zip(cu[:-1], cu[1:]))
+        self.plan = [(n0, n1, torch.tensor(c, dtype=torch.int32, device=dev))
+                     for n0, n1, c in _pieces(bounds, C, max(1, int(pieces)))]
+        self.s_in = torch.cuda.Stream(device=dev)
+        self.s_out = torch.cuda.Stream(device=dev)
 
     @property
     def h2d_bytes(self) -> int:
@@ -188,18 +233,35 @@ class HostRunner:
         return sum(t.numel() * t.element_size() for t in (self.T_out, self.W, self.U) if t is not None)
 
     def __call__(self, k_host, v_host, beta_host, sync: bool = True, g_host=None):
-        self.k.copy_(k_host, non_blocking=True)
-        self.v.copy_(v_host, non_blocking=True)
-        self.beta.copy_(beta_host, non_blocking=True)
-        if self.g is not None:
-            self.g.copy_(g_host, non_blocking=True)
-        kkt_solve_fwd(self.k, self.v, self.beta, self.C, self.cu, T_out=self.T_out, W_out=self.W,
-                      U_out=self.U, kernel=self.kernel, materialize_T=self.materialize_T,
-                      T_dtype=self.T_dtype, g=self.g)
-        if self.T_out is not None:
-            self.T_host.copy_(self.T_out, non_blocking=True)
-        self.W_host.copy_(self.W, non_blocking=True)
-        self.U_host.copy_(self.U, non_blocking=True)
+        B, T, H = self.shape
+        N = B * T
+        rows = lambda x: x.reshape(N, H, -1) if x.dim() == 4 else x.reshape(N, H)  # flat token axis
+        dev_in = [rows(x) for x in (self.k, self.v, self.beta, self.g) if x is not None]
+        host_in = [rows(x) for x in (k_host, v_host, beta_host, g_host) if x is not None]
+        if len(host_in) != len(dev_in):
+            raise ValueError("g_host must be given exactly when the runner is gated")
+        dev_out = [rows(x) for x in (self.T_out, self.W, self.U) if x is not None]
+        host_out = [rows(x) for x in (self.T_host, self.W_host, self.U_host) if x is not None]
+        compute = torch.cuda.current_stream()
+        # the previous call's kernels have read the inputs, and its copies have read the outputs
+        self.s_in.wait_stream(compute)
+        compute.wait_stream(self.s_out)
+        for n0, n1, cu in self.plan:
+            with torch.cuda.stream(self.s_in):
+                for d, h in zip(dev_in, host_in):
+                    d[n0:n1].copy_(h[n0:n1], non_blocking=True)
+            compute.wait_stream(self.s_in)
+            piece = [x[n0:n1].unsqueeze(0) for x in dev_in]       # [1, n, H, .] views
+            outp = [x[n0:n1].unsqueeze(0) for x in dev_out]
+            kkt_solve_fwd(piece[0], piece[1], piece[2], self.C, cu,
+                          T_out=outp[0] if self.T_out is not None else None, W_out=outp[-2], U_out=outp[-1],
+                          kernel=self.kernel, materialize_T=self.materialize_T, T_dtype=self.T_dtype,
+                          g=piece[3] if self.g is not None else None)
+            self.s_out.wait_stream(compute)
+            with torch.cuda.stream(self.s_out):
+                for d, h in zip(dev_out, host_out):
+                    h[n0:n1].copy_(d[n0:n1], non_blocking=True)
+        compute.wait_stream(self.s_out)
         if sync:
-            torch.cuda.current_stream().synchronize()
+            compute.synchronize()
         return self.T_host, self.W_host, self.U_host

@@ -438,3 +438,36 @@ def test_cuda_graph_capture_and_replay(kernel):
     assert torch.count_nonzero(ws).item() == 0
     for a, b in zip(eager + eager_g, (T1, W1, U1, T2, W2, U2)):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("case", ["batch", "one_long_sequence", "varlen", "gated_fp16"])
+def test_host_runner_pipeline(case):
+    """The end-to-end runner (pinned host buffers, the batch cut into pieces that are copied in,
+    solved and copied out on overlapping streams) returns exactly what one device call returns."""
+    from gdn_chunkwise_ut_gb300 import HostRunner
+    C, H = 64, 3
+    cu, g, t_dtype = None, None, torch.float32
+    if case == "batch":
+        k, v, beta = make_inputs(4, 700, H, 128, 128, seed=81, device=DEV)
+    elif case == "one_long_sequence":
+        k, v, beta = make_inputs(1, 3000, H, 128, 128, seed=82, device=DEV)
+    else:
+        lengths = [1, 63, 64, 0, 700, 130, 7, 1200, 5]
+        cu = np.concatenate([[0], np.cumsum(lengths)])
+        k, v, beta = make_inputs(1, int(cu[-1]), H, 128, 128, seed=83, device=DEV)
+        if case == "gated_fp16":
+            g = make_gate(1, int(cu[-1]), H, seed=83, device=DEV)
+            t_dtype = torch.float16
+    cu_t = None if cu is None else torch.as_tensor(cu, dtype=torch.int32, device=DEV)
+    ref = kkt_solve_fwd(k, v, beta, C, cu_t, g=g, T_dtype=t_dtype)
+    torch.cuda.synchronize()
+    runner = HostRunner(k.shape[0], k.shape[1], H, 128, 128, C, cu_seqlens=cu, T_dtype=t_dtype,
+                        gated=g is not None, pieces=4)
+    assert len(runner.plan) >= 2
+    hosts = [x.cpu().pin_memory() for x in (k, v, beta)]
+    gh = g.cpu().pin_memory() if g is not None else None
+    for _ in range(2):  # a second call reuses the buffers
+        outs = runner(*hosts, g_host=gh)
+        for a, b in zip(ref, outs):
+            assert torch.equal(a.cpu(), b)
+    assert device_status() == 0
