@@ -199,7 +199,7 @@ class HostRunner:
 
     def __init__(self, B, T, H, dk, dv, C, *, dtype=torch.bfloat16, cu_seqlens=None,
                  kernel="auto", device="cuda", materialize_T: bool = True, T_dtype=torch.float32,
-                 gated: bool = False, pieces: int = 4):
+                 gated: bool = False, pieces: int = 8):
         self.C, self.kernel, self.materialize_T, self.T_dtype = C, kernel, materialize_T, T_dtype
         dev = torch.device(device)
         self.shape = (B, T, H)
