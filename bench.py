@@ -42,8 +42,8 @@ DEFAULT_WORKLOAD = "c3_b4_t8192_h16"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
-KERNEL_SOURCES = {"simt": ["kkt_simt.cu", "kkt_internal.cuh"],
-                  "tc": ["kkt_tc.cu", "sm100_ptx.cuh", "kkt_internal.cuh"]}
+KERNEL_SOURCES = {"simt": ["kkt_simt.cu", "kkt_internal.cuh", "kkt_debug.cuh"],
+                  "tc": ["kkt_tc.cuh", "kkt_tc.cu", "sm100_ptx.cuh", "kkt_internal.cuh", "kkt_debug.cuh"]}
 
 
 def parse_args():
@@ -58,6 +58,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-t-out", action="store_true", help="W and U~ only: T computed, not written")
     ap.add_argument("--t-f16", action="store_true", help="T written in fp16 instead of fp32")
+    ap.add_argument("--head-dim", type=int, default=None,
+                    help="override the workload's head dimension d_k = d_v (64 or 128)")
     ap.add_argument("--chunk", type=int, default=None,
                     help="override the workload's chunk size C (32, 64 or 128): the chunk-size study")
     ap.add_argument("--graph", action="store_true",
@@ -203,6 +205,8 @@ def select_workload(args):
     w = workloads()[args.workload]
     if args.chunk is not None and args.chunk != w.C:
         w = dataclasses.replace(w, name=f"{w.name}@C{args.chunk}", C=args.chunk)
+    if args.head_dim is not None and (args.head_dim != w.dk or args.head_dim != w.dv):
+        w = dataclasses.replace(w, name=f"{w.name}@d{args.head_dim}", dk=args.head_dim, dv=args.head_dim)
     return w
 
 

@@ -152,12 +152,14 @@ extern "C" const char *kkt_status_string(int status) {
 extern "C" int kkt_version(void) { return (0 << 16) | (1 << 8) | 0; }
 
 extern "C" int kkt_debug_bounds(unsigned long long *first, int *kind) {
-    kkt::BoundsRecord tc = {0u, 0u, 0ull}, simt = {0u, 0u, 0ull};
-    if (kkt::debug_bounds_tc(&tc) < 0 || kkt::debug_bounds_simt(&simt) < 0) return -1;
-    const kkt::BoundsRecord &f = tc.count ? tc : simt;
+    kkt::BoundsRecord rec[3] = {};
+    if (kkt::debug_bounds_tc(&rec[0]) < 0 || kkt::debug_bounds_tc_d64(&rec[1]) < 0 ||
+        kkt::debug_bounds_simt(&rec[2]) < 0)
+        return -1;
+    const kkt::BoundsRecord &f = rec[0].count ? rec[0] : rec[1].count ? rec[1] : rec[2];
     if (first) *first = f.first;
     if (kind) *kind = (int)f.kind;
-    return (int)(tc.count + simt.count);
+    return (int)(rec[0].count + rec[1].count + rec[2].count);
 }
 
 #ifdef KKT_TRACE

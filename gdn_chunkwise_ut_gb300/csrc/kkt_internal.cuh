@@ -127,6 +127,7 @@ struct BoundsRecord {
     unsigned long long first;
 };
 int debug_bounds_tc(BoundsRecord *out);
+int debug_bounds_tc_d64(BoundsRecord *out);
 int debug_bounds_simt(BoundsRecord *out);
 bool tc_supports(int dk, int dv, int C, int io);
 

@@ -1,0 +1,1307 @@
+// kkt_tc.cuh -- persistent, warp-specialised tcgen05 + TMA kernel for kkt_solve (bf16 I/O),
+// templated on the chunk size C and the head dimension D = d_k = d_v (64 or 128).  Included by one
+// translation unit per head dimension (kkt_tc.cu: D = 128, kkt_tc_d64.cu: D = 64), which compile in
+// parallel; everything here has internal linkage.
+//
+// One CTA per SM walks "tiles" of 128 rows: G = 128 / C heads of one chunk,
+// row m = g * C + r (head g, token r of the chunk).  For each tile
+// ("TileLang 实战：单位下三角矩阵求逆" §1, §2.2, §3):
+//
+//   producer warp   TMA: K and V boxes {64 cols, 1 head, C rows} (128-byte
+//                   swizzle) into a stage of a two-deep shared-memory ring;
+//                   beta (and the gate's prefix sums, gated kernels) with plain
+//                   loads.
+//   Gram warp       one lane issuing tcgen05.mma S = K K^T (M = N = 128,
+//                   K = DH, bf16 -> fp32 in tensor memory); zeroes the rows past
+//                   a short chunk's end first.
+//   W|U warp        one lane issuing D = T~ [K | V] with T~ = T diag(beta) read
+//                   from tensor memory as a bf16 hi + lo pair (two accumulating
+//                   passes, M = 128, N = 2 DH, K = 128; T~ is block diagonal over
+//                   the G heads).  The commit after D frees the stage.
+//   (DH = d_k = d_v, the head dimension: 64 or 128.)
+//   inverse warps   a thread per row loads its Gram row (tcgen05.ld), applies
+//                   the beta row scale, strict-lower mask and unit diagonal
+//                   (§3.2) and writes the row of A into the tile's fp32 T
+//                   buffer in shared memory (128-byte swizzle, TMA layout),
+//                   which is then turned into T = A^-1 in place:
+//                   16 x 16 diagonal blocks by right-looking forward
+//                   substitution, one column per lane, so the dependency chain
+//                   is 15 FMAs (§2.1; in-place, with the L values read before
+//                   any column is written back, §3.4); coupling
+//                   -L11^-1 L10 L00^-1 at s = 16 (inside a warp), s = 32 (the
+//                   two warps of a 64-row block) and, at C = 128, s = 64 (all
+//                   four warps, split by columns) as register-tiled shared-
+//                   memory GEMMs with L10 consumed before it is overwritten
+//                   (§2.2, §3.5).  Each warp TMA-stores its 32 rows of T from that
+//                   buffer, and writes its rows of T~ = T diag(beta) as a bf16
+//                   hi / lo pair into tensor memory (tcgen05.st).
+//   epilogue warps  per warp: tcgen05.ld of its 32 rows of D, bf16 conversion,
+//                   a double-buffered swizzled staging and TMA stores of W, U~.
+//
+// Rows of a short last chunk (Lc < C) past Lc are zeroed in shared memory
+// before the Gram MMA; warps whose 32 rows are not all valid write their valid
+// rows with plain stores.  Every wait is bounded: on expiry the kernel records
+// KKT_ERR_TIMEOUT, stops all roles, drains its own copies and MMAs, frees
+// tensor memory and returns.
+//
+// Building with -DKKT_TRACE adds time stamps of the pipeline events of the
+// first CTAs to a caller-provided buffer (see trace.py); the default build has
+// none of it.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "kkt_debug.cuh"
+#include "kkt_internal.cuh"
+#include "sm100_ptx.cuh"
+
+namespace kkt {
+namespace {
+
+using namespace ptx;
+
+constexpr int kThreads = 384;            // 12 warps
+constexpr int kWarpProducer = 0;
+constexpr int kWarpMma = 1;              // W|U MMAs
+constexpr int kWarpGram = 2;             // Gram MMAs
+constexpr int kWarpInv0 = 4;             // warps 4..7
+constexpr int kWarpEpi0 = 8;             // warps 8..11
+constexpr int kNS = 2;                   // stages
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColGram = 0;         // 128 fp32 columns
+constexpr uint32_t kColD = 128;          // 256 fp32 columns: W | U~
+constexpr uint32_t kColTT = 384;         // 64 packed bf16x2 hi + 64 lo
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
+
+struct TileInfo {
+    int64_t t0;
+    int Lc;
+    int h0;
+    int done;
+    int pad;
+};
+
+template <int C, int DH>
+struct Cfg {
+    static constexpr int G = 128 / C;                         // heads per tile
+    static constexpr int NB = DH / 64;                         // 64-column TMA boxes per K or V row
+    static constexpr int KV_BYTES = 2 * NB * 16384;           // K then V boxes, [box][row][128 B]
+    // per stage: beta[128]; gated kernels: the gate's prefix sums G[128] (log2 units), the column
+    // factors w[128] and one "factorable" flag per 32-row block (int[4]); then the TileInfo
+    static constexpr int META_BYTES = 1584;
+    static constexpr int T_HALVES = C / 32;                   // 128-byte column blocks of a T row
+    static constexpr int OFF_T = kNS * KV_BYTES;              // T of the tile: [half][128 rows][128 B]
+    // W / U~ staging per epilogue warp: two 4 KB buffers, one at C = 128 (whose T takes 64 KB)
+    static constexpr int WU_BUFS = C == 128 ? 1 : 2;
+    static constexpr int OFF_WU = OFF_T + T_HALVES * 16384;
+    static constexpr int OFF_META = OFF_WU + 4 * WU_BUFS * 4096;  // per stage: beta[128] + TileInfo
+    static constexpr int OFF_BAR = OFF_META + kNS * META_BYTES;
+    static constexpr int BAR_BYTES = 512;
+    static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
+    static constexpr uint32_t TX_BYTES = G * 2 * NB * C * 128;      // K + V boxes of one stage
+    static_assert(SMEM_BYTES <= 232448, "shared memory over the per-block limit");
+};
+
+struct Barriers {
+    uint64_t full[kNS];
+    uint64_t empty[kNS];
+    uint64_t gram_full, gram_empty;
+    uint64_t tt_full, tt_empty;
+    uint64_t d_full, d_empty;
+    uint64_t einfo_full[2];
+    uint64_t mma_final, gram_final;
+    uint64_t pair_sync[2];   // warps 2p and 2p + 1: one 64-row block (C = 64, 128)
+    uint64_t quad_sync;      // all four inverse warps (C = 128)
+    TileInfo einfo[2];       // tile info for the epilogue warps, written by the W|U warp
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+struct TcParams {
+    const float *beta;
+    const float *g;  // per-token log decays (GATED kernels)
+    const int32_t *cu;
+    int nseq, T;
+    int64_t ntok;
+    int H;
+    int64_t tiles;   // work ids x head groups
+    int HG;          // head groups
+    void *T_out;     // fp32, or fp16 in the TF16 kernels; nullptr: T is not written
+    __nv_bfloat16 *W_out, *U_out;
+    int *status;
+    unsigned long long *trace;
+    unsigned long long *tile_counter;  // dynamic scheduling when not null: [0] tiles claimed, [1] CTAs done
+                                       // claiming; zero at launch, left zero by the last CTA
+    int stall_first_tile;              // test hook: every CTA skips the loads of its first tile
+};
+
+// ---- optional pipeline trace ------------------------------------------------------------------
+enum TraceEvent {
+    EV_P_EMPTY = 0, EV_P_ISSUE, EV_M_FULL, EV_M_GRAM, EV_M_EPI, EV_I_GRAM, EV_I_INV, EV_I_TSTORE,
+    EV_I_TT, EV_E_DFULL, EV_E_DEMPTY, EV_E_DONE, EV_I_LD, EV_I_DIAG, EV_I_C16, EV_I_PAIR, EV_M_LATE,
+    EV_M_READY, EV_I_BW, EV_I_TTW, EV_COUNT
+};
+constexpr int kTraceCtas = 160;
+constexpr int kTraceTiles = 64;  // the last tile row holds the CTA's clock calibration
+constexpr int kTraceSlots = 24;
+static_assert(EV_COUNT <= kTraceSlots, "trace slots");
+#ifdef KKT_TRACE
+// SM cycle counter at each event; trace.py maps it to ns with the (globaltimer, clock) pairs that
+// thread 0 records at the start and end of the CTA
+#define KKT_TRACE_EVENT(ev, tile)                                                                        \
+    do {                                                                                               \
+        if (p.trace && blockIdx.x < kTraceCtas && (tile) < kTraceTiles - 1)                            \
+            p.trace[((size_t)blockIdx.x * kTraceTiles + (tile)) * kTraceSlots + (ev)] = clock64();      \
+    } while (0)
+#define KKT_TRACE_CALIB(slot)                                                                            \
+    do {                                                                                               \
+        if (p.trace && blockIdx.x < kTraceCtas && threadIdx.x == 0) {                                  \
+            unsigned long long *c = p.trace + ((size_t)blockIdx.x * kTraceTiles + kTraceTiles - 1) * kTraceSlots; \
+            c[2 * (slot)] = globaltimer_ns();                                                          \
+            c[2 * (slot) + 1] = clock64();                                                             \
+        }                                                                                              \
+    } while (0)
+#else
+#define KKT_TRACE_EVENT(ev, tile) \
+    do {                          \
+    } while (0)
+#define KKT_TRACE_CALIB(slot) \
+    do {                      \
+    } while (0)
+#endif
+
+// First 1024-byte-aligned byte of the dynamic shared memory.  The offset is
+// computed in the shared window and added to the shared pointer itself, so the
+// compiler keeps the shared address space (LDS/STS rather than generic loads).
+__device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
+    const uint32_t a = smem_u32(p);
+    return p + (((a + 1023u) & ~1023u) - a);
+}
+
+__device__ __forceinline__ void fail(Barriers *bars, int *status) {
+    if (atomicExch(&bars->abort_flag, 1) == 0) record_error(status, KKT_ERR_TIMEOUT);
+}
+
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, Barriers *bars, int *status) {
+    if (mbar_wait(bar, parity, &bars->abort_flag, kWaitLimitNs)) return true;
+    fail(bars, status);
+    return false;
+}
+
+// Group barrier on an mbarrier (every member arrives, then waits for the phase):
+// unlike bar.sync it is bounded, so a member that gave up cannot hang the others.
+__device__ __forceinline__ bool group_sync(uint64_t *bar, uint32_t &uses, Barriers *bars, int *status) {
+    mbar_arrive(bar);
+    const bool ok = wait_bar(bar, uses & 1u, bars, status);
+    ++uses;
+    return ok;
+}
+
+// Element (row m, column j) of a fp32 matrix stored as 32-column halves of 128-byte rows,
+// [half][128 rows][128 B], with the 128-byte swizzle that TMA uses (16-byte chunk index XOR
+// row mod 8): rows are conflict-free for a thread per row, and a row is a TMA box row.
+__device__ __forceinline__ float *tm_elem(uint8_t *tm, int m, int j) {
+    return smem_chk(reinterpret_cast<float *>(tm + (j >> 5) * 16384 + m * 128 + ((((j & 31) >> 2) ^ (m & 7)) << 4) +
+                                              (j & 3) * 4));
+}
+__device__ __forceinline__ float4 *tm_vec(uint8_t *tm, int m, int j) {  // j a multiple of 4
+    return smem_chk(reinterpret_cast<float4 *>(tm + (j >> 5) * 16384 + m * 128 + ((((j & 31) >> 2) ^ (m & 7)) << 4)));
+}
+
+// Two fp16 (round to nearest even) in the bits of one float: lo in bits 0..15, hi in 16..31.
+__device__ __forceinline__ float pack_f16(float lo, float hi) {
+    const __half2 v = __floats2half2_rn(lo, hi);
+    return __uint_as_float(*reinterpret_cast<const uint32_t *>(&v));
+}
+
+// Two bf16 (round to nearest even) in one register: lo in bits 0..15, hi in 16..31.
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// Packed fp32 product of a pair (one f32x2 instruction): a * b, elementwise.
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+// Packed fp32 FMA on a pair (one f32x2 instruction): a * b + c, elementwise.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+// bf16 hi + lo split of a pair, packed as two bf16x2 words: hi = bf16(x), lo = bf16(x - hi)
+// (the difference is exact in fp32).
+__device__ __forceinline__ void split_bf16(float2 x, uint32_t &hi, uint32_t &lo) {
+    const uint32_t h = pack_bf16(x.x, x.y);
+    const float2 hf = make_float2(__uint_as_float(h << 16), __uint_as_float(h & 0xffff0000u));
+    hi = h;
+    const float2 r = ffma2(hf, make_float2(-1.f, -1.f), x);
+    lo = pack_bf16(r.x, r.y);
+}
+
+// D (4 x 4 tile, as 4 rows x 2 packed pairs) += A B over NKB blocks of 8 k.  A rows: byte pointers to
+// the start of the rows' 128-byte lines in the k range's half, with their swizzle phases as XOR
+// masks; acol0 is the first k column (a multiple of 8) inside that half.  B rows: base pointer of
+// row 0 of the k range (its row index a multiple of 8), bsw[kk] the byte offset of this lane's
+// 16-byte column chunk in a row with phase kk.
+// A loop over 8-k blocks rather than an unrolled sequence: the kernel is sensitive to its
+// instruction-cache footprint, so the code size of this inner product is kept small (UNROLL
+// blocks per iteration: 1 at C <= 64, 2 at C = 128, where the longer level-64 products gain).
+template <int UNROLL>
+__device__ __forceinline__ void tile4x4_fma(float2 (&y)[4][2], const uint8_t *const (&arow)[4],
+                                         const uint32_t (&axor)[4], int acol0, const uint8_t *brow0,
+                                         const uint32_t (&bsw)[8], int nkb) {
+#pragma unroll UNROLL
+    for (int kb = 0; kb < nkb; ++kb) {
+        float av[4][8];
+        const uint32_t ca = (uint32_t)((acol0 >> 2) + 2 * kb) << 4;
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+            const float4 a0 = *smem_chk(reinterpret_cast<const float4 *>(arow[rr] + (ca ^ axor[rr])));
+            const float4 a1 = *smem_chk(reinterpret_cast<const float4 *>(arow[rr] + ((ca + 16u) ^ axor[rr])));
+            av[rr][0] = a0.x; av[rr][1] = a0.y; av[rr][2] = a0.z; av[rr][3] = a0.w;
+            av[rr][4] = a1.x; av[rr][5] = a1.y; av[rr][6] = a1.z; av[rr][7] = a1.w;
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const float4 b = *smem_chk(reinterpret_cast<const float4 *>(brow0 + (8 * kb + kk) * 128 + bsw[kk]));
+            const float2 b01 = make_float2(b.x, b.y), b23 = make_float2(b.z, b.w);
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) {
+                const float2 ak = make_float2(av[rr][kk], av[rr][kk]);
+                y[rr][0] = ffma2(ak, b01, y[rr][0]);
+                y[rr][1] = ffma2(ak, b23, y[rr][1]);
+            }
+        }
+    }
+}
+
+// Level-32 coupling of one 64 x 64 diagonal block (rows m0 .. m0 + 63, columns c0 .. c0 + 63 of
+// the chunk, in the tile's T buffer) for warp WP (0 or 1) of its two warps.  With 16 x 16 blocks
+// M00^-1 = [[A, 0], [Cb, D]], M10 = [P, Q], M11^-1 = [[A', 0], [Cb', D']]:
+// Y = M10 M00^-1 = [P A + Q Cb, Q D] and Z = M11^-1 Y = [A' Y_top ; Cb' Y_top + D' Y_bot].
+// Warp 0 computes Y_left (K = 32) and Z_top (K = 16), warp 1 Y_right (K = 16) and Z_bot (K = 32):
+// the zero blocks are skipped and both warps do 384 packed FMAs per lane.  Rows 32..63, columns
+// 0..31 of the block receive -Z.  ybuf32 points at row 0 of the block's upper-right 32 x 32 (rows
+// 0..31, columns 32..63 of the block, zero in T), which holds Y and is cleared again at the end.
+template <int UNROLL>
+__device__ __forceinline__ bool level32(const int WP, uint8_t *tm, uint8_t *ybuf32, int m0, int c0, int lane,
+                                        uint64_t *pair_bar, uint32_t &pair_uses, Barriers *bars, int *status) {
+    uint8_t *th = tm + (c0 >> 5) * 16384;  // the 32-column half holding the block's first columns
+    {
+        // Y part: rows yr + 8 rr of 32, columns 16 WP + 4 yc .. + 3; k in [16 WP, 32)
+        const int yr = lane >> 2, yc = lane & 3;
+        const uint8_t *arow[4];
+        uint32_t axor[4];
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+            arow[rr] = th + (m0 + 32 + yr + 8 * rr) * 128;
+            axor[rr] = (uint32_t)(yr & 7) << 4;
+        }
+        uint32_t bsw[8];
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) bsw[kk] = (uint32_t)((4 * WP + yc) ^ kk) << 4;
+        float2 y[4][2];
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) y[rr][0] = y[rr][1] = make_float2(0.f, 0.f);
+        tile4x4_fma<UNROLL>(y, arow, axor, 16 * WP, th + (m0 + 16 * WP) * 128, bsw, 4 - 2 * WP);
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr)
+            *tm_vec(ybuf32, yr + 8 * rr, 16 * WP + 4 * yc) = make_float4(y[rr][0].x, y[rr][0].y, y[rr][1].x, y[rr][1].y);
+    }
+    if (!group_sync(pair_bar, pair_uses, bars, status)) return false;
+    {
+        // Z part: rows 16 WP + zr + 4 rr (zr = 0..3), columns 4 zc .. + 3 (zc = 0..7); k in [0, 16 + 16 WP)
+        const int zr = lane >> 3, zc = lane & 7;
+        const uint8_t *arow[4];
+        uint32_t axor[4];
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+            const int row = m0 + 32 + 16 * WP + zr + 4 * rr;
+            arow[rr] = th + 16384 + row * 128;  // columns 32..63 of the block: the next half
+            axor[rr] = (uint32_t)(row & 7) << 4;
+        }
+        uint32_t bsw[8];
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) bsw[kk] = (uint32_t)(zc ^ kk) << 4;
+        float2 z[4][2];
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) z[rr][0] = z[rr][1] = make_float2(0.f, 0.f);
+        tile4x4_fma<UNROLL>(z, arow, axor, 0, ybuf32, bsw, 2 + 2 * WP);
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr)
+            *tm_vec(tm, m0 + 32 + 16 * WP + zr + 4 * rr, c0 + 4 * zc) =
+                make_float4(-z[rr][0].x, -z[rr][0].y, -z[rr][1].x, -z[rr][1].y);
+    }
+    if (!group_sync(pair_bar, pair_uses, bars, status)) return false;
+    if (WP == 0) {
+        // ybuf32 is the block's upper-right 32 x 32, zero in T: clear it again
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) *tm_vec(ybuf32, lane, j) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    return true;
+}
+
+// Level-64 coupling of a 128-token chunk (C = 128; the tile's rows are the chunk's rows), split
+// over the four inverse warps by columns (§2.2): rows 64..127, columns 0..63 receive
+// -Z = -M11^-1 M10 M00^-1 with 64 x 64 blocks M00^-1 = T[0..63][0..63], M11^-1 = T[64..][64..],
+// M10 = L[64..][0..63].  Warp w computes columns 16w .. 16w + 15 of Y = M10 M00^-1 and of
+// Z = M11^-1 Y; a column of Z needs only the same column of Y, so Y is produced and consumed by
+// one warp.  Zero blocks are skipped: columns >= 32 of M00^-1 vanish above row 32, and rows < 32 of
+// M11^-1 vanish beyond column 32.  Y is kept in rows 0..63, columns 64..127 (zero in T) and
+// cleared again by the warp that wrote it.  Lane: rows yr + 8 rr (+ 32 for the lower row group),
+// columns 16w + 4 yc .. + 3.
+__device__ __forceinline__ bool level64(const int w, uint8_t *tm, int lane, uint64_t *quad_bar, uint32_t &uses,
+                                        Barriers *bars, int *status) {
+    const int yr = lane >> 2, yc = lane & 3;
+    const int cj = 16 * w + 4 * yc;                              // this lane's first column (0..63)
+    const uint32_t axor = (uint32_t)(yr & 7) << 4;               // swizzle phase of every A row used
+    uint32_t bsw[8];
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) bsw[kk] = (uint32_t)(((cj & 31) >> 2) ^ kk) << 4;
+    const uint32_t axr[4] = {axor, axor, axor, axor};
+    // Y = M10 M00^-1, rows 32 rg .. 32 rg + 31 of Y (chunk rows 64 + 32 rg + ...)
+#pragma unroll 1
+    for (int rg = 0; rg < 2; ++rg) {
+        float2 y[4][2];
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) y[rr][0] = y[rr][1] = make_float2(0.f, 0.f);
+        const uint8_t *brow = tm + (cj >> 5) * 16384;  // M00^-1, the half of columns cj
+#pragma unroll 1
+        for (int kh = (w < 2 ? 0 : 1); kh < 2; ++kh) {  // k in [32 kh, 32 kh + 32)
+            const uint8_t *arow[4];
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) arow[rr] = tm + kh * 16384 + (64 + 32 * rg + yr + 8 * rr) * 128;
+            tile4x4_fma<2>(y, arow, axr, 0, brow + 32 * kh * 128, bsw, 4);
+        }
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr)
+            *tm_vec(tm, 32 * rg + yr + 8 * rr, 64 + cj) = make_float4(y[rr][0].x, y[rr][0].y, y[rr][1].x, y[rr][1].y);
+    }
+    __syncwarp();
+    // Z = M11^-1 Y, both row groups kept in registers until every warp has read M10
+    float2 z[2][4][2];
+#pragma unroll
+    for (int rg = 0; rg < 2; ++rg)
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) z[rg][rr][0] = z[rg][rr][1] = make_float2(0.f, 0.f);
+    const uint8_t *ybrow = tm + (2 + (cj >> 5)) * 16384;  // Y, the half of columns 64 + cj
+#pragma unroll
+    for (int rg = 0; rg < 2; ++rg) {
+#pragma unroll 1
+        for (int kh = 0; kh <= rg; ++kh) {  // rows < 32 of M11^-1: k < 32 only
+            const uint8_t *arow[4];
+#pragma unroll
+            for (int rr = 0; rr < 4; ++rr) arow[rr] = tm + (2 + kh) * 16384 + (64 + 32 * rg + yr + 8 * rr) * 128;
+            tile4x4_fma<2>(z[rg], arow, axr, 0, ybrow + 32 * kh * 128, bsw, 4);
+        }
+    }
+    // every warp has read M10: overwrite it with -Z, and clear this warp's Y columns
+    if (!group_sync(quad_bar, uses, bars, status)) return false;
+#pragma unroll
+    for (int rg = 0; rg < 2; ++rg)
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr)
+            *tm_vec(tm, 64 + 32 * rg + yr + 8 * rr, cj) =
+                make_float4(-z[rg][rr][0].x, -z[rg][rr][0].y, -z[rg][rr][1].x, -z[rg][rr][1].y);
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int c4 = 0; c4 < 16; c4 += 4)
+            *tm_vec(tm, lane + 32 * h, 64 + 16 * w + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
+    fence_proxy_async_smem();
+    return group_sync(quad_bar, uses, bars, status);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Inclusive prefix sums of x over the C rows of each head of a tile, value e of a lane being row
+// (lane + 32 e) % C of head (lane + 32 e) / C: a warp scan of each 32-row segment, then the totals
+// of the earlier segments of the same head.
+template <int C>
+__device__ __forceinline__ void head_prefix_sums(float (&x)[4], int lane) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, x[e], o);
+            if (lane >= o) x[e] += y;
+        }
+    float carry = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        if ((32 * e) % C == 0) carry = 0.f;  // first segment of a head
+        const float total = __shfl_sync(0xffffffffu, x[e], 31);
+        x[e] += carry;
+        carry += total;
+    }
+}
+
+template <int C, int DH, bool TF16, bool GATED>
+__global__ void __launch_bounds__(kThreads, 1)
+    kkt_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                  const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_u,
+                  const __grid_constant__ CUtensorMap map_t, const TcParams p) {
+    using CF = Cfg<C, DH>;
+    constexpr int G = CF::G;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    Barriers *bars = reinterpret_cast<Barriers *>(smem + CF::OFF_BAR);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    auto stage_kv = [&](int s) { return smem + s * CF::KV_BYTES; };
+    auto stage_beta = [&](int s) { return reinterpret_cast<float *>(smem + CF::OFF_META + s * CF::META_BYTES); };
+    auto stage_gate = [&](int s) { return reinterpret_cast<float *>(smem + CF::OFF_META + s * CF::META_BYTES + 512); };
+    auto stage_gw = [&](int s) { return reinterpret_cast<float *>(smem + CF::OFF_META + s * CF::META_BYTES + 1024); };
+    auto stage_gflag = [&](int s) { return reinterpret_cast<int *>(smem + CF::OFF_META + s * CF::META_BYTES + 1536); };
+    auto stage_info = [&](int s) {
+        return smem_chk(reinterpret_cast<TileInfo *>(smem + CF::OFF_META + s * CF::META_BYTES + 1552));
+    };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kNS; ++s) {
+            // gated kernels: a second arrival once the stage's gate data is written (after the loads)
+            mbar_init(&bars->full[s], GATED ? 2 : 1);
+            mbar_init(&bars->empty[s], 1);
+        }
+        mbar_init(&bars->gram_full, 1);
+        mbar_init(&bars->gram_empty, 4);
+        mbar_init(&bars->tt_full, 4);
+        mbar_init(&bars->tt_empty, 1);
+        mbar_init(&bars->d_full, 1);
+        mbar_init(&bars->d_empty, 4);
+        mbar_init(&bars->einfo_full[0], 1);
+        mbar_init(&bars->einfo_full[1], 1);
+        mbar_init(&bars->mma_final, 1);
+        mbar_init(&bars->gram_final, 1);
+        mbar_init(&bars->pair_sync[0], 64);
+        mbar_init(&bars->pair_sync[1], 64);
+        mbar_init(&bars->quad_sync, 128);
+        bars->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kWarpMma) {
+        tmem_alloc(&bars->tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    // The next call on the stream may be scheduled now: its CTAs take SMs as this grid's CTAs leave
+    // them and run their set-up meanwhile.  This grid's own global-memory work (tile claims, loads
+    // of k / v / beta, stores of T / W / U) waits for the previous grid on the stream to complete.
+    griddep_launch_dependents();
+    griddep_wait();
+    KKT_TRACE_CALIB(0);
+
+    if (warp == kWarpProducer) {
+        // ------------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tmap(&map_k);
+            prefetch_tmap(&map_v);
+        }
+        int i = 0;
+        bool ok = true;
+        // next tile: a fixed round robin, or claimed from the shared counter one tile ahead so
+        // that the atomic's round trip overlaps the current tile
+        auto claim = [&]() -> int64_t {
+            unsigned long long v = 0;
+            if (lane == 0) v = atomicAdd(p.tile_counter, 1ull);
+            return (int64_t)__shfl_sync(0xffffffffu, v, 0);
+        };
+        const bool dyn = p.tile_counter != nullptr;
+        int64_t t = dyn ? claim() : (int64_t)blockIdx.x;
+        for (; t < p.tiles;) {
+            const int64_t t_now = t;
+            t = dyn ? claim() : t + gridDim.x;
+            const int64_t id = t_now / p.HG;
+            const int h0 = (int)(t_now % p.HG) * G;
+            if (h0 == 0 && id < p.nseq && lane == 0) check_sequence(p.cu, (int)id, p.nseq, p.ntok, p.status);
+            Chunk ch;
+            if (!map_chunk(id, p.cu, p.nseq, p.T, p.ntok, C, p.status, ch)) continue;
+            if (p.stall_first_tile && i == 0) {
+                // test hook: stage 0 is never filled, so every wait on it runs out (failure detection)
+                ++i;
+                continue;
+            }
+            // beta of the tile (G x C values, 4 per lane), loaded before waiting for the stage
+            float bv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int idx = lane + 32 * e;
+                const int g = idx / C, r = idx % C;
+                bv[e] = (r < ch.Lc && h0 + g < p.H) ? __ldg(gmem_chk(p.beta, (ch.t0 + r) * p.H + h0 + g, p.ntok * p.H)) : 0.f;
+            }
+            // gated: prefix sums G of the log decays over each head's chunk, in log2 units, so that
+            // Gamma[i][j] = exp2(G_i - G_j).  For a column j of 32-row block b, with R_b = G at the
+            // block's first row: Gamma[i][j] = exp2(G_i - R_b) * w_j, w_j = exp2(R_b - G_j), one power
+            // per row and block instead of one per element.  That is exact up to rounding while the
+            // factors stay in range: |R_b - G_j| <= 96 over the block (a decay of at most 2^-96
+            // inside 32 tokens), recorded as the block's flag; other blocks take one power per element.
+            // (the loads are issued here and consumed after the stage wait, which hides their latency)
+            float gv[4] = {0.f, 0.f, 0.f, 0.f}, wv[4] = {0.f, 0.f, 0.f, 0.f};
+            int fv[4] = {0, 0, 0, 0};
+            if constexpr (GATED) {
+                constexpr float kLog2e = 1.4426950408889634f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int idx = lane + 32 * e;
+                    const int g = idx / C, r = idx % C;
+                    gv[e] = (r < ch.Lc && h0 + g < p.H) ? kLog2e * __ldg(gmem_chk(p.g, (ch.t0 + r) * p.H + h0 + g, p.ntok * p.H)) : 0.f;
+                }
+            }
+            const int s = i % kNS;
+            const uint32_t u = (uint32_t)(i / kNS);
+            if (!wait_bar(&bars->empty[s], (u & 1u) ^ 1u, bars, p.status)) { ok = false; break; }
+            if (lane == 0) KKT_TRACE_EVENT(EV_P_EMPTY, i);
+            float *sb = stage_beta(s);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) *smem_chk(sb + lane + 32 * e) = bv[e];
+            if (lane == 0) {
+                TileInfo *info = stage_info(s);
+                info->t0 = ch.t0;
+                info->Lc = ch.Lc;
+                info->h0 = h0;
+                info->done = 0;
+            }
+            __syncwarp();
+            if (lane == 0) {
+                uint8_t *st = stage_kv(s);
+                mbar_arrive_expect_tx(&bars->full[s], CF::TX_BYTES);
+                for (int g = 0; g < G; ++g)
+                    for (int c2 = 0; c2 < CF::NB; ++c2) {
+                        tma_load_3d(st + c2 * 16384 + g * C * 128, &map_k, &bars->full[s], c2 * 64, h0 + g,
+                                    (int)ch.t0);
+                        tma_load_3d(st + CF::NB * 16384 + c2 * 16384 + g * C * 128, &map_v, &bars->full[s],
+                                    c2 * 64, h0 + g, (int)ch.t0);
+                    }
+                KKT_TRACE_EVENT(EV_P_ISSUE, i);
+            }
+            if constexpr (GATED) {
+                // the gate data, while the loads are in flight; the stage completes with this arrival
+                head_prefix_sums<C>(gv, lane);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float ref = __shfl_sync(0xffffffffu, gv[e], 0);
+                    float dev = fabsf(ref - gv[e]);
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) dev = fmaxf(dev, __shfl_xor_sync(0xffffffffu, dev, o));
+                    fv[e] = dev <= 96.f;
+                    wv[e] = exp2f(ref - gv[e]);
+                }
+                float *sg = stage_gate(s), *sw = stage_gw(s);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    *smem_chk(sg + lane + 32 * e) = gv[e];
+                    *smem_chk(sw + lane + 32 * e) = wv[e];
+                }
+                if (lane == 0)
+                    for (int e = 0; e < 4; ++e) *smem_chk(stage_gflag(s) + e) = fv[e];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->full[s]);
+            }
+            __syncwarp();
+            ++i;
+        }
+        if (ok) {
+            const int s = i % kNS;
+            const uint32_t u = (uint32_t)(i / kNS);
+            if (wait_bar(&bars->empty[s], (u & 1u) ^ 1u, bars, p.status)) {
+                if (lane == 0) {
+                    stage_info(s)->done = 1;
+                    mbar_arrive(&bars->full[s]);
+                    if (GATED) mbar_arrive(&bars->full[s]);
+                }
+            } else {
+                ok = false;
+            }
+        }
+        // This CTA claims no more tiles.  The workspace holds the tile counter and a count of CTAs
+        // done claiming; the last CTA to finish claiming zeroes both, so the next call on the same
+        // workspace starts from zero without a clear of its own (the fence orders this CTA's
+        // claims before its count; every other CTA has counted itself, so none claims again).
+        if (dyn && lane == 0) {
+            __threadfence();
+            if (atomicAdd(p.tile_counter + 1, 1ull) == gridDim.x - 1ull) {
+                atomicExch(p.tile_counter, 0ull);
+                atomicExch(p.tile_counter + 1, 0ull);
+            }
+        }
+        // after a timeout: our last TMA loads must land before shared memory is released
+        // (on the normal path every load was consumed through its full barrier)
+        if (!ok && lane == 0) {
+            for (int back = 1; back <= kNS && back <= i; ++back) {
+                const int j = i - back;
+                volatile int never = 0;
+                mbar_wait(&bars->full[j % kNS], (uint32_t)(j / kNS) & 1u, &never, kWaitLimitNs);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kWarpGram) {
+        // ------------------------------------------------------------------ Gram issuer
+        // Tile by tile: wait for the stage, zero the rows of a short chunk, wait for the Gram
+        // columns of tensor memory, issue S = K K^T.  A thread of its own, so that a Gram is never
+        // held up behind the issue of a W|U MMA (whose instructions wait for the tensor pipe).
+        const uint32_t idesc_gram = idesc_bf16_f32(128, 128, 0, 0);
+        for (int i = 0;; ++i) {
+            const int s = i % kNS;
+            if (!wait_bar(&bars->full[s], (uint32_t)(i / kNS) & 1u, bars, p.status)) break;
+            const TileInfo info = *stage_info(s);
+            if (info.done) break;
+            if (lane == 0) KKT_TRACE_EVENT(EV_M_FULL, i);
+            if (info.Lc < C) {
+                // zero rows Lc..C-1 of every head's K and V boxes
+                uint8_t *st = stage_kv(s);
+                const int per_box = (C - info.Lc) * 8;  // 16-byte chunks
+                for (int e = lane; e < G * 2 * CF::NB * per_box; e += 32) {
+                    const int box = e / per_box, w = e % per_box;
+                    const int g = box % G, kvh = box / G;  // kvh: the K boxes, then the V boxes
+                    *smem_chk(reinterpret_cast<uint4 *>(st + kvh * 16384 + g * C * 128 + (info.Lc + w / 8) * 128 +
+                                                        (w % 8) * 16)) = make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            if (!wait_bar(&bars->gram_empty, ((uint32_t)i & 1u) ^ 1u, bars, p.status)) break;
+            if (lane == 0) {
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(stage_kv(s));
+#pragma unroll
+                for (int kk = 0; kk < 4 * CF::NB; ++kk) {  // K = DH in steps of 16
+                    const uint64_t d = sw128_desc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                    mma_ss(tmem + kColGram, d, d, idesc_gram, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&bars->gram_full);
+                KKT_TRACE_EVENT(EV_M_GRAM, i);
+            }
+            __syncwarp();
+        }
+        // every MMA issued by this thread has completed before tensor memory is freed
+        if (lane == 0) {
+            mma_commit(&bars->gram_final);
+            volatile int never = 0;
+            mbar_wait(&bars->gram_final, 0u, &never, kWaitLimitNs);
+        }
+        __syncwarp();
+    } else if (warp == kWarpMma) {
+        // ------------------------------------------------------------------ W|U issuer
+        // Tile by tile: once T~ is in tensor memory and the epilogue has drained D, hand the tile
+        // info to the epilogue and issue D = T~ [K|V] (hi and lo passes); the commit frees T~, the
+        // stage, and tells the epilogue that D is ready.  The stage's info marks the end of work.
+        const uint32_t idesc_epi = idesc_bf16_f32(128, 2 * DH, 0, 1);  // N = DH columns of K, then of V
+        for (int i = 0;; ++i) {
+            const int s = i % kNS;
+            if (!wait_bar(&bars->full[s], (uint32_t)(i / kNS) & 1u, bars, p.status)) break;
+            const TileInfo info = *stage_info(s);
+            if (info.done) {
+                if (lane == 0) {
+                    bars->einfo[i & 1] = info;
+                    mbar_arrive(&bars->einfo_full[i & 1]);
+                }
+                __syncwarp();
+                break;
+            }
+            if (!wait_bar(&bars->tt_full, (uint32_t)i & 1u, bars, p.status)) break;
+            if (!wait_bar(&bars->d_empty, ((uint32_t)i & 1u) ^ 1u, bars, p.status)) break;
+            if (lane == 0) {
+                KKT_TRACE_EVENT(EV_M_READY, i);
+                bars->einfo[i & 1] = info;
+                mbar_arrive(&bars->einfo_full[i & 1]);
+                tc_fence_after();
+                const uint32_t b0 = smem_u32(stage_kv(s));
+#pragma unroll
+                for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t d = sw128_desc(b0 + kk * 2048, 16384, 1024);
+                        mma_ts(tmem + kColD, tmem + kColTT + pass * 64 + kk * 8, d, idesc_epi,
+                               (pass | kk) ? 1u : 0u);
+                    }
+                mma_commit(&bars->tt_empty);
+                mma_commit(&bars->d_full);
+                mma_commit(&bars->empty[s]);
+                KKT_TRACE_EVENT(EV_M_EPI, i);
+            }
+            __syncwarp();
+        }
+        // every MMA issued by this thread has completed before tensor memory is freed
+        if (lane == 0) {
+            mma_commit(&bars->mma_final);
+            volatile int never = 0;
+            mbar_wait(&bars->mma_final, 0u, &never, kWaitLimitNs);
+        }
+        __syncwarp();
+    } else if (warp >= kWarpInv0 && warp < kWarpInv0 + 4) {
+        // ------------------------------------------------------------------ inverse warps
+        const int q = warp & 3;             // tensor-memory lane quarter
+        const int m = 32 * q + lane;        // tile row
+        const int g = m / C;                // head within the tile
+        const int r = m % C;                // row within the chunk
+        const int wp = r / 32;              // warp position within the head (0 for C = 32)
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        uint8_t *tm = smem + CF::OFF_T;     // the tile's T, [half][128 rows][128 B], 128-byte swizzle
+        // level-32 product Y: the upper-right 32 x 32 of this warp's 64-row block (zero in T)
+        uint8_t *ybuf32 = tm + (((C == 128 ? 64 * (q >> 1) : 0) + 32) >> 5) * 16384 + 64 * (q >> 1) * 128;
+        // zero this lane's T~ columns (other heads' blocks and the upper triangle stay zero)
+        // and its row of T (the upper triangle stays zero there too)
+        {
+            uint32_t zz[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) zz[c] = 0u;
+#pragma unroll
+            for (int c = 0; c < 128; c += 16) tmem_st16(tmem + lane_base + kColTT + c, zz);
+            tmem_wait_st();
+#pragma unroll
+            for (int j = 0; j < C; j += 4) *tm_vec(tm, m, j) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        int i = 0;
+        uint32_t pair_uses = 0, quad_uses = 0;
+        while (true) {
+            const int s = i % kNS;
+            if (!wait_bar(&bars->full[s], (uint32_t)(i / kNS) & 1u, bars, p.status)) break;
+            const TileInfo info = *stage_info(s);
+            if (info.done) break;
+            const float *sb = stage_beta(s) + g * C;
+            const float beta_r = *smem_chk(sb + r);
+            // gated: Gamma[r][j], the decay from token j to token r (j < r), for columns 32 h + c ..
+            // + 3 is exp2(G_r - R_h) w_j when every block of the head is factorable (fac); otherwise
+            // the row is formed without it and multiplied by exp2(G_r - G_j) element by element after
+            // (a compact loop: such gates are rare, and the unrolled code stays small)
+            const float *sg = stage_gate(s) + g * C;
+            const float *sw = stage_gw(s) + g * C;
+            bool fac = true;
+            float g_r = 0.f;
+            if constexpr (GATED) {
+                g_r = *smem_chk(sg + r);
+                const int *sf = stage_gflag(s) + g * C / 32;
+#pragma unroll
+                for (int h = 0; h < CF::T_HALVES; ++h) fac = fac && *smem_chk(sf + h) != 0;
+            }
+            // the column factors w of block h (ones when not factorable), loaded together ahead of use
+            auto load_w = [&](int h, float4 (&wq)[8]) {
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8)
+                    wq[c8] = fac ? *smem_chk(reinterpret_cast<const float4 *>(sw + 32 * h + 4 * c8)) : make_float4(1.f, 1.f, 1.f, 1.f);
+            };
+            auto row_factor = [&](int h) { return fac ? exp2f(g_r - *smem_chk(sg + 32 * h)) : 1.f; };
+
+            if (!wait_bar(&bars->gram_full, (uint32_t)i & 1u, bars, p.status)) break;
+            tc_fence_after();
+            if (q == 0 && lane == 0) KKT_TRACE_EVENT(EV_I_GRAM, i);
+            // this warp's previous T store has read its rows of the T buffer
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
+            if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_BW, i);
+            // Gram row -> row of A = I + strictLower(diag(beta) S) (beta on rows, unit diagonal,
+            // §3.2), times Gamma elementwise when gated (§5 item 12), into the T buffer; columns
+            // above 32 (wp + 1) stay zero
+            if constexpr (C == 128) {
+                // up to four 32-column blocks: one tensor-memory load at a time
+#pragma unroll 1
+                for (int h = 0; h <= wp; ++h) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_base + kColGram + 32 * h, v);
+                    float uh = 1.f;
+                    float4 wq[8];
+                    if constexpr (GATED) {
+                        uh = row_factor(h);
+                        load_w(h, wq);
+                    }
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4) {
+                        float e[4];
+                        float gm[4] = {1.f, 1.f, 1.f, 1.f};
+                        if constexpr (GATED) {
+                            const float4 w4 = wq[c / 4];
+                            gm[0] = uh * w4.x; gm[1] = uh * w4.y; gm[2] = uh * w4.z; gm[3] = uh * w4.w;
+                        }
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int j = 32 * h + c + u;
+                            e[u] = (j < r) ? beta_r * __uint_as_float(v[c + u]) * gm[u] : (j == r ? 1.f : 0.f);
+                        }
+                        *tm_vec(tm, m, 32 * h + c) = make_float4(e[0], e[1], e[2], e[3]);
+                    }
+                }
+            } else {
+                uint32_t v[CF::T_HALVES][32];
+#pragma unroll
+                for (int h = 0; h < CF::T_HALVES; ++h)
+                    if (h <= wp) tmem_ld32(tmem + lane_base + kColGram + g * C + 32 * h, v[h]);
+                float uh[CF::T_HALVES];
+#pragma unroll
+                for (int h = 0; h < CF::T_HALVES; ++h) uh[h] = GATED ? row_factor(h) : 1.f;
+                tmem_wait_ld();
+#pragma unroll
+                for (int h = 0; h < CF::T_HALVES; ++h) {
+                    float4 wq[8];
+                    if constexpr (GATED) {
+                        if (h <= wp) load_w(h, wq);
+                    }
+                    if (h < wp) {
+                        // the whole block lies below the diagonal (columns < 32 wp <= r): beta scale only
+                        const float2 bb = make_float2(beta_r * uh[h], beta_r * uh[h]);
+#pragma unroll
+                        for (int c = 0; c < 32; c += 4) {
+                            float2 e0 = fmul2(make_float2(__uint_as_float(v[h][c]), __uint_as_float(v[h][c + 1])), bb);
+                            float2 e1 = fmul2(make_float2(__uint_as_float(v[h][c + 2]), __uint_as_float(v[h][c + 3])), bb);
+                            if constexpr (GATED) {
+                                const float4 w4 = wq[c / 4];
+                                e0 = fmul2(e0, make_float2(w4.x, w4.y));
+                                e1 = fmul2(e1, make_float2(w4.z, w4.w));
+                            }
+                            *tm_vec(tm, m, 32 * h + c) = make_float4(e0.x, e0.y, e1.x, e1.y);
+                        }
+                    } else if (h == wp) {
+                        // the diagonal block: column 32 h + cc is below the diagonal when cc < lane
+#pragma unroll
+                        for (int c = 0; c < 32; c += 4) {
+                            float e[4];
+                            float gm[4] = {1.f, 1.f, 1.f, 1.f};
+                            if constexpr (GATED) {
+                                const float4 w4 = wq[c / 4];
+                                gm[0] = uh[h] * w4.x; gm[1] = uh[h] * w4.y; gm[2] = uh[h] * w4.z; gm[3] = uh[h] * w4.w;
+                            }
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                e[u] = (c + u < lane) ? beta_r * __uint_as_float(v[h][c + u]) * gm[u]
+                                                      : (c + u == lane ? 1.f : 0.f);
+                            *tm_vec(tm, m, 32 * h + c) = make_float4(e[0], e[1], e[2], e[3]);
+                        }
+                    }
+                }
+            }
+            if constexpr (GATED) {
+                if (!fac) {
+#pragma unroll 1
+                    for (int j = 0; j < r; ++j) *tm_elem(tm, m, j) *= exp2f(g_r - *smem_chk(sg + j));
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->gram_empty);
+            if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_LD, i);
+
+            // diagonal 16 x 16 blocks (§2.1), one column per lane: right-looking substitution,
+            // s[k] <- s[k] - L[k][m] x_m once x_m = s[m] is final.  L is read four columns at a
+            // time (one 16-byte chunk per row) before the four steps that use them.
+
+            {
+                const int c = lane & 15;
+                const int rb = 32 * wp + 16 * (lane >> 4);
+                const int mb = g * C + rb;
+                float sc[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) sc[k] = (k == c) ? 1.f : 0.f;
+#pragma unroll
+                for (int m0s = 0; m0s < 16; m0s += 4) {
+                    float4 lk[16];
+#pragma unroll
+                    for (int k = m0s + 1; k < 16; ++k) lk[k] = *tm_vec(tm, mb + k, rb + m0s);
+#pragma unroll
+                    for (int d = 0; d < 4; ++d) {
+                        const int ms = m0s + d;
+                        if (ms < 15) {
+                            const float xm = sc[ms];
+#pragma unroll
+                            for (int k = ms + 1; k < 16; ++k) {
+                                const float l = d == 0 ? lk[k].x : d == 1 ? lk[k].y : d == 2 ? lk[k].z : lk[k].w;
+                                sc[k] = fmaf(-l, xm, sc[k]);
+                            }
+                        }
+                    }
+                }
+                __syncwarp();
+#pragma unroll
+                for (int k = 1; k < 16; ++k) *tm_elem(tm, mb + k, rb + c) = sc[k];
+                __syncwarp();
+            }
+            if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_DIAG, i);
+
+            // level 16 (§2.2): the warp's two diagonal blocks, T10 = -X11 (L10 X00).  Y = L10 X00 is
+            // kept in the block's upper-right 16 x 16 (rows m0 .. m0 + 15, columns c0 + 16 .. c0 + 31),
+            // zero in T and cleared again once read.
+            {
+                // lane -> rows ii and ii + 8 of the 16 x 16 result, columns jb .. jb + 3
+                const int ii = lane >> 2;
+                const int jb = (lane & 3) * 4;
+                const int m0 = g * C + 32 * wp;
+                const int c0 = 32 * wp;
+                float a[2][16];
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int k = 0; k < 16; k += 4) {
+                        const float4 t4 = *tm_vec(tm, m0 + 16 + ii + 8 * h, c0 + k);
+                        a[h][k] = t4.x; a[h][k + 1] = t4.y; a[h][k + 2] = t4.z; a[h][k + 3] = t4.w;
+                    }
+                float2 y[2][2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) y[h][0] = y[h][1] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const float4 b = *tm_vec(tm, m0 + k, c0 + jb);
+                    const float2 b01 = make_float2(b.x, b.y), b23 = make_float2(b.z, b.w);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const float2 ak = make_float2(a[h][k], a[h][k]);
+                        y[h][0] = ffma2(ak, b01, y[h][0]);
+                        y[h][1] = ffma2(ak, b23, y[h][1]);
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    *tm_vec(tm, m0 + ii + 8 * h, c0 + 16 + jb) = make_float4(y[h][0].x, y[h][0].y, y[h][1].x, y[h][1].y);
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int k = 0; k < 16; k += 4) {
+                        const float4 t4 = *tm_vec(tm, m0 + 16 + ii + 8 * h, c0 + 16 + k);
+                        a[h][k] = t4.x; a[h][k + 1] = t4.y; a[h][k + 2] = t4.z; a[h][k + 3] = t4.w;
+                    }
+                __syncwarp();
+#pragma unroll
+                for (int h = 0; h < 2; ++h) y[h][0] = y[h][1] = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const float4 b = *tm_vec(tm, m0 + k, c0 + 16 + jb);
+                    const float2 b01 = make_float2(b.x, b.y), b23 = make_float2(b.z, b.w);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const float2 ak = make_float2(a[h][k], a[h][k]);
+                        y[h][0] = ffma2(ak, b01, y[h][0]);
+                        y[h][1] = ffma2(ak, b23, y[h][1]);
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    *tm_vec(tm, m0 + 16 + ii + 8 * h, c0 + jb) = make_float4(-y[h][0].x, -y[h][0].y, -y[h][1].x, -y[h][1].y);
+                __syncwarp();
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    *tm_vec(tm, m0 + ii + 8 * h, c0 + 16 + jb) = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_C16, i);
+
+            bool ok = true;
+            if constexpr (C >= 64) {
+                // level 32 in each 64-row block (a head at C = 64, half the chunk at C = 128): its
+                // rows 32..63 get -M11^-1 M10 M00^-1 (see level32)
+                const int pr = q >> 1;
+                ok = group_sync(&bars->pair_sync[pr], pair_uses, bars, p.status);
+                if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_PAIR, i);
+                if (ok) {
+                    ok = level32<C == 128 ? 2 : 1>(wp & 1, tm, ybuf32, 64 * pr, C == 128 ? 64 * pr : 0, lane,
+                                                   &bars->pair_sync[pr], pair_uses, bars, p.status);
+                }
+                if constexpr (C == 128) {
+                    // level 64: rows 64..127 of the chunk (see level64)
+                    if (ok) ok = group_sync(&bars->quad_sync, quad_uses, bars, p.status);
+                    if (ok) ok = level64(q, tm, lane, &bars->quad_sync, quad_uses, bars, p.status);
+                }
+            } else {
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_INV, i);
+
+            // T rows in fp32: TMA store of the warp's 32 rows when all are valid, else plain stores
+            // (none without T_out: W and U~ only; fp16 T is written after T~, below)
+            if (p.T_out == nullptr || TF16) {
+            } else if (32 * wp + 32 <= info.Lc) {
+                if (lane == 0) {
+                    for (int h = 0; h < CF::T_HALVES; ++h)
+                        tma_store_3d(&map_t, tm + h * 16384 + 32 * q * 128, 32 * h, info.h0 + g,
+                                     (int)(info.t0 + 32 * wp));
+                    bulk_commit();
+                }
+            } else if (r < info.Lc && info.h0 + g < p.H) {
+                float4 *dst = reinterpret_cast<float4 *>(gmem_chk(static_cast<float *>(p.T_out),
+                                                                  ((info.t0 + r) * p.H + info.h0 + g) * C,
+                                                                  p.ntok * p.H * C, C));
+#pragma unroll
+                for (int j = 0; j < C; j += 4) dst[j / 4] = *tm_vec(tm, m, j);
+            }
+            if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_TSTORE, i);
+
+            // T~ = T diag(beta), split into bf16 hi + lo, into tensor memory (A operand)
+            if (!wait_bar(&bars->tt_empty, ((uint32_t)i & 1u) ^ 1u, bars, p.status)) break;
+            tc_fence_after();
+            if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_TTW, i);
+            // fp16 T (TF16): each row rounded to fp16 as T~ reads it.  The warp's 32 rows go out by
+            // one TMA store per 64 columns when all are valid: columns 64 h .. 64 h + 63 of a row are
+            // packed into the first 128 bytes of its block h (the 128-byte-swizzled layout of a TMA box
+            // of 64 fp16), which hold fp32 values T~ has already read.  Other rows (and C = 32) are
+            // written by plain stores.
+            const bool t16_tma = TF16 && C >= 64 && p.T_out != nullptr && 32 * wp + 32 <= info.Lc;
+            const bool t16_row = TF16 && !t16_tma && p.T_out != nullptr && r < info.Lc && info.h0 + g < p.H;
+            {
+                uint32_t hi[16], lo[16];
+#pragma unroll(C == 128 ? 1 : CF::T_HALVES)
+                for (int blk = 0; blk < CF::T_HALVES; ++blk) {
+                    float4 *t16s = tm_vec(tm, m, 0);  // row m of block blk / 2, chunk base below
+                    if constexpr (TF16) t16s = reinterpret_cast<float4 *>(tm + (blk >> 1) * 16384 + m * 128);
+                    if (blk <= wp) {
+#pragma unroll
+                        for (int c = 0; c < 32; c += 8) {
+                            const float4 ta = *tm_vec(tm, m, 32 * blk + c);
+                            const float4 tb = *tm_vec(tm, m, 32 * blk + c + 4);
+                            const float4 ba = *smem_chk(reinterpret_cast<const float4 *>(sb + 32 * blk + c));
+                            const float4 bb = *smem_chk(reinterpret_cast<const float4 *>(sb + 32 * blk + c + 4));
+                            split_bf16(fmul2(make_float2(ta.x, ta.y), make_float2(ba.x, ba.y)), hi[c / 2], lo[c / 2]);
+                            split_bf16(fmul2(make_float2(ta.z, ta.w), make_float2(ba.z, ba.w)), hi[c / 2 + 1], lo[c / 2 + 1]);
+                            split_bf16(fmul2(make_float2(tb.x, tb.y), make_float2(bb.x, bb.y)), hi[c / 2 + 2], lo[c / 2 + 2]);
+                            split_bf16(fmul2(make_float2(tb.z, tb.w), make_float2(bb.z, bb.w)), hi[c / 2 + 3], lo[c / 2 + 3]);
+                            if constexpr (TF16) {
+                                const float4 h8 = make_float4(pack_f16(ta.x, ta.y), pack_f16(ta.z, ta.w),
+                                                              pack_f16(tb.x, tb.y), pack_f16(tb.z, tb.w));
+                                if (t16_tma)
+                                    *smem_chk(t16s + ((4 * (blk & 1) + c / 8) ^ (m & 7))) = h8;
+                                else if (t16_row)
+                                    *reinterpret_cast<float4 *>(gmem_chk(static_cast<__half *>(p.T_out),
+                                                                         ((info.t0 + r) * p.H + info.h0 + g) * C + 32 * blk + c,
+                                                                         p.ntok * p.H * C, 8)) = h8;
+                            }
+                        }
+                        const uint32_t col = (uint32_t)(g * C + 32 * blk) / 2;
+                        tmem_st16(tmem + lane_base + kColTT + col, hi);
+                        tmem_st16(tmem + lane_base + kColTT + 64 + col, lo);
+                    } else if constexpr (TF16) {
+                        // columns above the diagonal block: zeros
+                        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            if (t16_tma)
+                                *smem_chk(t16s + ((4 * (blk & 1) + e) ^ (m & 7))) = z;
+                            else if (t16_row)
+                                *reinterpret_cast<float4 *>(gmem_chk(static_cast<__half *>(p.T_out),
+                                                                     ((info.t0 + r) * p.H + info.h0 + g) * C + 32 * blk + 8 * e,
+                                                                     p.ntok * p.H * C, 8)) = z;
+                        }
+                    }
+                }
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&bars->tt_full);
+                if (q == 1) KKT_TRACE_EVENT(EV_I_TT, i);
+            }
+            if (t16_tma) {
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    for (int h = 0; h < C / 64; ++h)
+                        tma_store_3d(&map_t, tm + h * 16384 + 32 * q * 128, 64 * h, info.h0 + g,
+                                     (int)(info.t0 + 32 * wp));
+                    bulk_commit();
+                }
+            }
+            ++i;
+        }
+        if (lane == 0) bulk_wait<0>();
+        __syncwarp();
+    } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
+        // ------------------------------------------------------------------ epilogue warps
+        const int q = warp & 3;
+        const int m = 32 * q + lane;
+        const int g = m / C;
+        const int r = m % C;
+        const int wp = r / 32;
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        uint8_t *wstage = smem + CF::OFF_WU + q * CF::WU_BUFS * 4096;  // WU_BUFS x [32 rows][128 B]
+        int i = 0;
+        uint32_t nstore = 0;  // TMA store groups issued by this warp
+        while (true) {
+            if (!wait_bar(&bars->einfo_full[i & 1], (uint32_t)(i >> 1) & 1u, bars, p.status)) break;
+            const TileInfo info = bars->einfo[i & 1];
+            if (info.done) break;
+            if (!wait_bar(&bars->d_full, (uint32_t)i & 1u, bars, p.status)) break;
+            tc_fence_after();
+            if (q == 0 && lane == 0) KKT_TRACE_EVENT(EV_E_DFULL, i);
+            const bool warp_full = 32 * wp + 32 <= info.Lc;
+            const bool row_ok = r < info.Lc && info.h0 + g < p.H;
+            const int64_t grow = (info.t0 + r) * p.H + info.h0 + g;
+#pragma unroll 1
+            for (int cc = 0; cc < 2 * CF::NB; ++cc) {  // 64 columns of D at a time: those of W, then of U~
+                uint32_t v0[32], v1[32];
+                tmem_ld32(tmem + lane_base + kColD + 64 * cc, v0);
+                tmem_ld32(tmem + lane_base + kColD + 64 * cc + 32, v1);
+                tmem_wait_ld();
+                if (cc == 2 * CF::NB - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&bars->d_empty);
+                        if (q == 0) KKT_TRACE_EVENT(EV_E_DEMPTY, i);
+                    }
+                }
+                uint32_t pk[32];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    pk[e] = pack_bf16(__uint_as_float(v0[2 * e]), __uint_as_float(v0[2 * e + 1]));
+                    pk[16 + e] = pack_bf16(__uint_as_float(v1[2 * e]), __uint_as_float(v1[2 * e + 1]));
+                }
+                if (warp_full) {
+                    uint8_t *buf = wstage + (nstore % CF::WU_BUFS) * 4096;
+                    if (lane == 0) bulk_wait_read<CF::WU_BUFS - 1>();
+                    __syncwarp();
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        *smem_chk(reinterpret_cast<uint4 *>(buf + sw128((uint32_t)(lane * 128 + 16 * e)))) =
+                            make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(cc < CF::NB ? &map_w : &map_u, buf, 64 * (cc % CF::NB), info.h0 + g,
+                                     (int)(info.t0 + 32 * wp));
+                        bulk_commit();
+                    }
+                    ++nstore;
+                } else if (row_ok) {
+                    __nv_bfloat16 *base = gmem_chk(cc < CF::NB ? p.W_out : p.U_out, grow * DH + 64 * (cc % CF::NB),
+                                                   p.ntok * p.H * DH, 64);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        reinterpret_cast<uint4 *>(base)[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                }
+            }
+            if (q == 0 && lane == 0) KKT_TRACE_EVENT(EV_E_DONE, i);
+            ++i;
+        }
+        if (lane == 0) bulk_wait<0>();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    KKT_TRACE_CALIB(1);
+    if (warp == kWarpMma) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------------------------
+// host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// [ntok][H][inner] row-major, box {box_inner, 1, rows}, 128-byte swizzle.
+bool make_map(CUtensorMap *map, CUtensorMapDataType dt, int esize, const void *ptr, int64_t ntok, int H, int inner,
+              int box_inner, int rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)H, (cuuint64_t)ntok};
+    cuuint64_t strides[2] = {(cuuint64_t)inner * esize, (cuuint64_t)H * inner * esize};
+    cuuint32_t box[3] = {(cuuint32_t)box_inner, 1u, (cuuint32_t)rows};
+    cuuint32_t es[3] = {1u, 1u, 1u};
+    return enc(map, dt, 3, const_cast<void *>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+template <int C, int DH>
+int launch_tc_t(const Problem &pb) {
+    using CF = Cfg<C, DH>;
+    CUtensorMap mk, mv, mw, mu, mt;
+    if (!make_map(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.k, pb.ntok, pb.H, pb.dk, 64, C) ||
+        !make_map(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.v, pb.ntok, pb.H, pb.dv, 64, C) ||
+        !make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.W_out, pb.ntok, pb.H, pb.dk, 64, 32) ||
+        !make_map(&mu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.U_out, pb.ntok, pb.H, pb.dv, 64, 32) ||
+        (pb.T_out && !pb.t_f16 && !make_map(&mt, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, pb.T_out, pb.ntok, pb.H, C, 32, 32)) ||
+        (pb.T_out && pb.t_f16 && C >= 64 && !make_map(&mt, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, pb.T_out, pb.ntok, pb.H, C, 64, 32)))
+        return KKT_ERR_CUDA;
+    if (!pb.T_out || (pb.t_f16 && C < 64)) mt = CUtensorMap{};  // never used: no T, or fp16 T by plain stores
+    TcParams p;
+    p.beta = pb.beta;
+    p.g = pb.g;
+    p.cu = pb.cu_seqlens;
+    p.nseq = pb.nseq;
+    p.T = pb.T;
+    p.ntok = pb.ntok;
+    p.H = pb.H;
+    p.HG = (pb.H + CF::G - 1) / CF::G;
+    p.tiles = total_work_ids(pb.ntok, C, pb.nseq) * p.HG;
+    p.T_out = pb.T_out;
+    p.W_out = static_cast<__nv_bfloat16 *>(pb.W_out);
+    p.U_out = static_cast<__nv_bfloat16 *>(pb.U_out);
+    p.status = pb.status;
+    p.trace = static_cast<unsigned long long *>(pb.trace);
+    p.tile_counter = pb.tile_counter;
+    p.stall_first_tile = pb.stall_first_tile;
+    auto kern = pb.g ? (pb.t_f16 ? kkt_tc_kernel<C, DH, true, true> : kkt_tc_kernel<C, DH, false, true>)
+                     : (pb.t_f16 ? kkt_tc_kernel<C, DH, true, false> : kkt_tc_kernel<C, DH, false, false>);
+    const bool attr_ok = pb.g ? (pb.t_f16 ? ensure_max_smem<kkt_tc_kernel<C, DH, true, true>>(CF::SMEM_BYTES)
+                                          : ensure_max_smem<kkt_tc_kernel<C, DH, false, true>>(CF::SMEM_BYTES))
+                              : (pb.t_f16 ? ensure_max_smem<kkt_tc_kernel<C, DH, true, false>>(CF::SMEM_BYTES)
+                                          : ensure_max_smem<kkt_tc_kernel<C, DH, false, false>>(CF::SMEM_BYTES));
+    if (!attr_ok) return KKT_ERR_CUDA;
+    const int sms = sm_count();
+    if (sms <= 0) return KKT_ERR_CUDA;
+    const int64_t grid = p.tiles < sms ? p.tiles : sms;
+    // programmatic stream serialisation: this launch may start while the previous kernel on the
+    // stream finishes (the kernel waits for it before touching global memory)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = CF::SMEM_BYTES;
+    cfg.stream = pb.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, mk, mv, mw, mu, mt, p) != cudaSuccess) return KKT_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? KKT_OK : KKT_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace kkt

@@ -80,6 +80,20 @@ def test_in_range_and_correct(blib, kernel, C, variant):
     check_WU(to64(U), U_ref, "bf16", "U")
 
 
+@pytest.mark.parametrize("C", [32, 64, 128])
+def test_tc_head_dim_64(blib, C):
+    lengths = [1, 63, 64, 65, 0, 130, 7, 200, 128]
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+    k, v, beta = make_inputs(1, int(cu[-1]), 3, 64, 64, seed=C + 95, device=DEV)
+    g = make_gate(1, int(cu[-1]), 3, seed=C + 95, device=DEV)
+    T_out, W, U = _call(blib, k, v, beta, C, cu, "tc", g=g)
+    _no_violations(blib)
+    T_ref, W_ref, U_ref = oracle.oracle_fwd(to64(k), to64(v), to64(beta), C, cu_seqlens=cu, g=to64(g))
+    check_T(to64(T_out), T_ref)
+    check_WU(to64(W), W_ref, "bf16", "W")
+    check_WU(to64(U), U_ref, "bf16", "U")
+
+
 @pytest.mark.parametrize("kernel", ["tc", "simt"])
 def test_fixed_length_partial_head_group(blib, kernel):
     """Fixed-length batch with a ragged tail and an odd head count (the last head group of the

@@ -67,9 +67,12 @@ def test_noalloc_varlen_two_calls():
 
 
 def test_noalloc_rejects_shapes_without_scratch_kernel():
+    """d_k != d_v runs only on the SIMT kernel, which the allocation-free call does not offer."""
     k = torch.zeros((1, 64, 1, 64), dtype=torch.bfloat16, device=DEV)
+    v = torch.zeros((1, 64, 1, 128), dtype=torch.bfloat16, device=DEV)
+    W, U = torch.zeros_like(k), torch.zeros_like(v)
     beta = torch.zeros((1, 64, 1), device=DEV)
     T_out = torch.zeros((1, 64, 1, 64), device=DEV)
-    rc = _lib.lib().kkt_solve_fwd_noalloc(k.data_ptr(), k.data_ptr(), beta.data_ptr(), None, 1, 64, 1, 64, 64, 64,
-                                          T_out.data_ptr(), k.data_ptr(), k.data_ptr(), None)
+    rc = _lib.lib().kkt_solve_fwd_noalloc(k.data_ptr(), v.data_ptr(), beta.data_ptr(), None, 1, 64, 1, 64, 128, 64,
+                                          T_out.data_ptr(), W.data_ptr(), U.data_ptr(), None)
     assert rc == _lib.KKT_ERR_UNSUPPORTED
