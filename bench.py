@@ -301,7 +301,9 @@ def bench_ours(args, rank, world, local):
     peak, peak_src = hbm_peak()
     achieved = alg_bytes / (launch_ms / 1e3) / 1e9
     # the recorded counters are those of the default call (fp32 T)
-    traffic = None if (args.no_t_out or args.t_f16 or args.gated) else recorded_traffic(kernel, w.name)
+    # counters recorded for the default call and the gated one (fp32 T); none for the other variants
+    traffic = None if (args.no_t_out or args.t_f16) else \
+        recorded_traffic(kernel, w.name + ("+gated" if args.gated else ""))
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     runner = HostRunner(k.shape[0], k.shape[1], w.H, w.dk, w.dv, w.C, dtype=k.dtype, cu_seqlens=cu,

@@ -1,6 +1,7 @@
 """Runs one workload a few times through the C ABI, for profilers (ncu) to capture.
 
     python -m gdn_chunkwise_ut_gb300.profile_case [--workload c3_b4_t8192_h16] [--calls 4] [--kernel auto]
+        [--gated]
 
 No timing and no checking: inputs are generated once, then ``--calls`` launches
 of the path run back to back and the process synchronises and exits.
@@ -12,7 +13,7 @@ import argparse
 import torch
 
 from .api import kkt_solve_fwd
-from .inputs import workloads
+from .inputs import make_gate, workloads
 
 
 def main():
@@ -20,18 +21,20 @@ def main():
     ap.add_argument("--workload", default="c3_b4_t8192_h16")
     ap.add_argument("--calls", type=int, default=4)
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc"])
+    ap.add_argument("--gated", action="store_true", help="the gated variant (seeded log decays)")
     a = ap.parse_args()
     w = workloads()[a.workload]
     k, v, beta, cu = w.make(seed=0, device="cuda")
+    g = make_gate(k.shape[0], k.shape[1], w.H, device="cuda") if a.gated else None
     cu_t = None if cu is None else torch.as_tensor(cu, dtype=torch.int32, device="cuda")
     outs = None
     for _ in range(a.calls):
         outs = kkt_solve_fwd(k, v, beta, w.C, cu_t, kernel=a.kernel,
                              T_out=None if outs is None else outs[0],
                              W_out=None if outs is None else outs[1],
-                             U_out=None if outs is None else outs[2])
+                             U_out=None if outs is None else outs[2], g=g)
     torch.cuda.synchronize()
-    print(f"{a.calls} calls of {a.workload} ({a.kernel})")
+    print(f"{a.calls} calls of {a.workload} ({a.kernel}{', gated' if a.gated else ''})")
 
 
 if __name__ == "__main__":
