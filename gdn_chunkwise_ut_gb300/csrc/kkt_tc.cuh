@@ -365,68 +365,93 @@ __device__ __forceinline__ bool level32(const int WP, uint8_t *tm, uint8_t *ybuf
     return true;
 }
 
-// Level-64 coupling of a 128-token chunk (C = 128; the tile's rows are the chunk's rows), split
-// over the four inverse warps by columns (§2.2): rows 64..127, columns 0..63 receive
-// -Z = -M11^-1 M10 M00^-1 with 64 x 64 blocks M00^-1 = T[0..63][0..63], M11^-1 = T[64..][64..],
-// M10 = L[64..][0..63].  Warp w computes columns 16w .. 16w + 15 of Y = M10 M00^-1 and of
-// Z = M11^-1 Y; a column of Z needs only the same column of Y, so Y is produced and consumed by
-// one warp.  Zero blocks are skipped: columns >= 32 of M00^-1 vanish above row 32, and rows < 32 of
-// M11^-1 vanish beyond column 32.  Y is kept in rows 0..63, columns 64..127 (zero in T) and
-// cleared again by the warp that wrote it.  Lane: rows yr + 8 rr (+ 32 for the lower row group),
-// columns 16w + 4 yc .. + 3.
-__device__ __forceinline__ bool level64(const int w, uint8_t *tm, int lane, uint64_t *quad_bar, uint32_t &uses,
-                                        Barriers *bars, int *status) {
+// Level-64 coupling of a 128-token chunk (C = 128; the tile's rows are the chunk's rows) (§2.2):
+// rows 64..127, columns 0..63 receive -Z = -M11^-1 M10 M00^-1 with 64 x 64 blocks
+// M00^-1 = T[0..63][0..63], M11^-1 = T[64..][64..], M10 = L[64..][0..63].  Both inverses are lower
+// triangular in 16 x 16 blocks, so column block j of Y = M10 M00^-1 needs k >= 16 j and row block i
+// of Z = M11^-1 Y needs k < 16 i + 16.  The work is balanced over the four inverse warps by pairing
+// a heavy block with a light one: warp w computes Y column blocks {0, 3} (w even) or {1, 2} (w odd)
+// on rows 32 (w / 2) .. + 31, then Z row blocks {0, 3} or {1, 2} on columns 32 (w / 2) .. + 31:
+// 80 k-steps of 16 outputs per lane in each product.  Y is kept in rows 0..63, columns 64..127
+// (zero in T) and cleared again once every warp has read it.
+
+// Y, column block j, rows 32 rh .. 32 rh + 31.  Lane: rows yr + 8 rr, columns 16 j + 4 yc .. + 3.
+__device__ __forceinline__ void level64_y_block(float2 (&y)[4][2], uint8_t *tm, int rh, int j, int lane) {
     const int yr = lane >> 2, yc = lane & 3;
-    const int cj = 16 * w + 4 * yc;                              // this lane's first column (0..63)
-    const uint32_t axor = (uint32_t)(yr & 7) << 4;               // swizzle phase of every A row used
+    const int cj = 16 * j + 4 * yc;
+    const uint32_t axor = (uint32_t)(yr & 7) << 4;  // swizzle phase of every A row used
+    const uint32_t axr[4] = {axor, axor, axor, axor};
     uint32_t bsw[8];
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) bsw[kk] = (uint32_t)(((cj & 31) >> 2) ^ kk) << 4;
-    const uint32_t axr[4] = {axor, axor, axor, axor};
-    // Y = M10 M00^-1, rows 32 rg .. 32 rg + 31 of Y (chunk rows 64 + 32 rg + ...)
+    const uint8_t *bhalf = tm + (cj >> 5) * 16384;  // M00^-1, the half of columns cj, rows k
 #pragma unroll 1
-    for (int rg = 0; rg < 2; ++rg) {
+    for (int kh = (16 * j) >> 5; kh < 2; ++kh) {    // the 32-column halves of M10 that k in [16 j, 64) spans
+        const int k0 = 16 * j > 32 * kh ? 16 * j : 32 * kh;
+        const uint8_t *arow[4];
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) arow[rr] = tm + kh * 16384 + (64 + 32 * rh + yr + 8 * rr) * 128;
+        tile4x4_fma<2>(y, arow, axr, k0 - 32 * kh, bhalf + k0 * 128, bsw, (32 * kh + 32 - k0) / 8);
+    }
+}
+
+// Z, row block i, columns 32 ch .. 32 ch + 31.  Lane: rows 16 i + zr + 4 rr, columns 32 ch + 4 zc .. + 3.
+__device__ __forceinline__ void level64_z_block(float2 (&z)[4][2], uint8_t *tm, int i, int ch, int lane) {
+    const int zr = lane >> 3, zc = lane & 7;
+    uint32_t axor[4];
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) axor[rr] = (uint32_t)((64 + 16 * i + zr + 4 * rr) & 7) << 4;
+    uint32_t bsw[8];
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) bsw[kk] = (uint32_t)(zc ^ kk) << 4;
+    const uint8_t *ybase = tm + (2 + ch) * 16384;  // Y: rows k, the half of columns 64 + 32 ch ..
+    const int kend = 16 * i + 16;
+#pragma unroll 1
+    for (int kh = 0; 32 * kh < kend; ++kh) {        // the halves 2 + kh of M11^-1 that k in [0, kend) spans
+        const uint8_t *arow[4];
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) arow[rr] = tm + (2 + kh) * 16384 + (64 + 16 * i + zr + 4 * rr) * 128;
+        const int kn = (kend < 32 * kh + 32 ? kend : 32 * kh + 32) - 32 * kh;
+        tile4x4_fma<2>(z, arow, axor, 0, ybase + 32 * kh * 128, bsw, kn / 8);
+    }
+}
+
+__device__ __forceinline__ bool level64(const int w, uint8_t *tm, int lane, uint64_t *quad_bar, uint32_t &uses,
+                                        Barriers *bars, int *status) {
+    const int half = w >> 1;                 // Y rows 32 half .., then Z columns 32 half ..
+    const int blk0 = (w & 1) ? 1 : 0, blk1 = (w & 1) ? 2 : 3;
+    // Y = M10 M00^-1
+#pragma unroll 1
+    for (int t = 0; t < 2; ++t) {
+        const int j = t ? blk1 : blk0;
         float2 y[4][2];
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr) y[rr][0] = y[rr][1] = make_float2(0.f, 0.f);
-        const uint8_t *brow = tm + (cj >> 5) * 16384;  // M00^-1, the half of columns cj
-#pragma unroll 1
-        for (int kh = (w < 2 ? 0 : 1); kh < 2; ++kh) {  // k in [32 kh, 32 kh + 32)
-            const uint8_t *arow[4];
-#pragma unroll
-            for (int rr = 0; rr < 4; ++rr) arow[rr] = tm + kh * 16384 + (64 + 32 * rg + yr + 8 * rr) * 128;
-            tile4x4_fma<2>(y, arow, axr, 0, brow + 32 * kh * 128, bsw, 4);
-        }
+        level64_y_block(y, tm, half, j, lane);
+        const int yr = lane >> 2, yc = lane & 3;
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr)
-            *tm_vec(tm, 32 * rg + yr + 8 * rr, 64 + cj) = make_float4(y[rr][0].x, y[rr][0].y, y[rr][1].x, y[rr][1].y);
+            *tm_vec(tm, 32 * half + yr + 8 * rr, 64 + 16 * j + 4 * yc) =
+                make_float4(y[rr][0].x, y[rr][0].y, y[rr][1].x, y[rr][1].y);
     }
-    __syncwarp();
-    // Z = M11^-1 Y, both row groups kept in registers until every warp has read M10
-    float2 z[2][4][2];
-#pragma unroll
-    for (int rg = 0; rg < 2; ++rg)
-#pragma unroll
-        for (int rr = 0; rr < 4; ++rr) z[rg][rr][0] = z[rg][rr][1] = make_float2(0.f, 0.f);
-    const uint8_t *ybrow = tm + (2 + (cj >> 5)) * 16384;  // Y, the half of columns 64 + cj
-#pragma unroll
-    for (int rg = 0; rg < 2; ++rg) {
-#pragma unroll 1
-        for (int kh = 0; kh <= rg; ++kh) {  // rows < 32 of M11^-1: k < 32 only
-            const uint8_t *arow[4];
-#pragma unroll
-            for (int rr = 0; rr < 4; ++rr) arow[rr] = tm + (2 + kh) * 16384 + (64 + 32 * rg + yr + 8 * rr) * 128;
-            tile4x4_fma<2>(z[rg], arow, axr, 0, ybrow + 32 * kh * 128, bsw, 4);
-        }
-    }
-    // every warp has read M10: overwrite it with -Z, and clear this warp's Y columns
+    // every warp has written its part of Y (and read M10)
     if (!group_sync(quad_bar, uses, bars, status)) return false;
+    // Z = M11^-1 Y; -Z overwrites M10, which no warp reads any more
+#pragma unroll 1
+    for (int t = 0; t < 2; ++t) {
+        const int i = t ? blk1 : blk0;
+        float2 z[4][2];
 #pragma unroll
-    for (int rg = 0; rg < 2; ++rg)
+        for (int rr = 0; rr < 4; ++rr) z[rr][0] = z[rr][1] = make_float2(0.f, 0.f);
+        level64_z_block(z, tm, i, half, lane);
+        const int zr = lane >> 3, zc = lane & 7;
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr)
-            *tm_vec(tm, 64 + 32 * rg + yr + 8 * rr, cj) =
-                make_float4(-z[rg][rr][0].x, -z[rg][rr][0].y, -z[rg][rr][1].x, -z[rg][rr][1].y);
+            *tm_vec(tm, 64 + 16 * i + zr + 4 * rr, 32 * half + 4 * zc) =
+                make_float4(-z[rr][0].x, -z[rr][0].y, -z[rr][1].x, -z[rr][1].y);
+    }
+    // every warp has read Y: clear it (this warp: 16 of its columns)
+    if (!group_sync(quad_bar, uses, bars, status)) return false;
 #pragma unroll
     for (int h = 0; h < 2; ++h)
 #pragma unroll
