@@ -552,14 +552,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         int i = 0;
         bool ok = true;
         // next tile: a fixed round robin, or claimed from the shared counter one tile ahead so
-        // that the atomic's round trip overlaps the current tile
+        // that the atomic's round trip overlaps the current tile.  The first tile is blockIdx.x in
+        // both schedules (counter value v stands for tile gridDim.x + v), which keeps the launch's
+        // burst of atomics on one address off the path to the first load.
         auto claim = [&]() -> int64_t {
             unsigned long long v = 0;
             if (lane == 0) v = atomicAdd(p.tile_counter, 1ull);
-            return (int64_t)__shfl_sync(0xffffffffu, v, 0);
+            return (int64_t)gridDim.x + (int64_t)__shfl_sync(0xffffffffu, v, 0);
         };
         const bool dyn = p.tile_counter != nullptr;
-        int64_t t = dyn ? claim() : (int64_t)blockIdx.x;
+        int64_t t = (int64_t)blockIdx.x;
         for (; t < p.tiles;) {
             const int64_t t_now = t;
             t = dyn ? claim() : t + gridDim.x;
