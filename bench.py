@@ -55,6 +55,8 @@ def parse_args():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc"])
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-pieces", type=int, default=8,
+                    help="pieces the end-to-end runner pipelines each call in (copies in, kernel, copies out)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-t-out", action="store_true", help="W and U~ only: T computed, not written")
     ap.add_argument("--t-f16", action="store_true", help="T written in fp16 instead of fp32")
@@ -308,7 +310,7 @@ def bench_ours(args, rank, world, local):
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     runner = HostRunner(k.shape[0], k.shape[1], w.H, w.dk, w.dv, w.C, dtype=k.dtype, cu_seqlens=cu,
                         kernel=args.kernel, device=dev, materialize_T=not args.no_t_out, T_dtype=T_dtype,
-                        gated=args.gated)
+                        gated=args.gated, pieces=args.e2e_pieces)
     kh, vh, bh = (x.cpu().pin_memory() for x in (k, v, beta))
     gh = g.cpu().pin_memory() if g is not None else None
     for _ in range(2):
@@ -321,7 +323,7 @@ def bench_ours(args, rank, world, local):
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
     e2e = {"value": aggregate_value(w.tokens * n_e2e, world, e2e_s), "unit": "tokens/s",
            "h2d_bytes_per_step": runner.h2d_bytes, "d2h_bytes_per_step": runner.d2h_bytes,
-           "steps": n_e2e}
+           "steps": n_e2e, "pieces": len(runner.plan)}
 
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
