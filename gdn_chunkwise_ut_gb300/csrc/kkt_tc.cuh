@@ -508,8 +508,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kNS; ++s) {
-            // gated kernels: a second arrival once the stage's gate data is written (after the loads)
-            mbar_init(&bars->full[s], GATED ? 2 : 1);
+            // the TMA transaction arrival, and a second one once beta (and the gate data) are written
+            mbar_init(&bars->full[s], 2);
             mbar_init(&bars->empty[s], 1);
         }
         mbar_init(&bars->gram_full, 1);
@@ -605,18 +605,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t u = (uint32_t)(i / kNS);
             if (!wait_bar(&bars->empty[s], (u & 1u) ^ 1u, bars, p.status)) { ok = false; break; }
             if (lane == 0) KKT_TRACE_EVENT(EV_P_EMPTY, i);
-            float *sb = stage_beta(s);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) *smem_chk(sb + lane + 32 * e) = bv[e];
             if (lane == 0) {
                 TileInfo *info = stage_info(s);
                 info->t0 = ch.t0;
                 info->Lc = ch.Lc;
                 info->h0 = h0;
                 info->done = 0;
-            }
-            __syncwarp();
-            if (lane == 0) {
                 uint8_t *st = stage_kv(s);
                 mbar_arrive_expect_tx(&bars->full[s], CF::TX_BYTES);
                 for (int g = 0; g < G; ++g)
@@ -628,8 +622,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 KKT_TRACE_EVENT(EV_P_ISSUE, i);
             }
+            // beta (and, gated, the gate data) while the loads are in flight, so that the first
+            // tile's loads do not wait for beta's; the stage completes with a second arrival
+            float *sb = stage_beta(s);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) *smem_chk(sb + lane + 32 * e) = bv[e];
             if constexpr (GATED) {
-                // the gate data, while the loads are in flight; the stage completes with this arrival
                 head_prefix_sums<C>(gv, lane);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -648,9 +646,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (lane == 0)
                     for (int e = 0; e < 4; ++e) *smem_chk(stage_gflag(s) + e) = fv[e];
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->full[s]);
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->full[s]);
             __syncwarp();
             ++i;
         }
@@ -661,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     stage_info(s)->done = 1;
                     mbar_arrive(&bars->full[s]);
-                    if (GATED) mbar_arrive(&bars->full[s]);
+                    mbar_arrive(&bars->full[s]);
                 }
             } else {
                 ok = false;
