@@ -369,8 +369,20 @@ def cpu_baseline(k, v, beta, cu, w, max_tokens=None, g=None):
     t0 = time.perf_counter()
     oracle.oracle_fwd(ks, vs, bs, w.C, cu_seqlens=cus, nthreads=cores, g=gs)
     dt = time.perf_counter() - t0
-    return {"value": tokens / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": sample, "seconds": dt}
+    out = {"value": tokens / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+           "sample": sample, "seconds": dt}
+    if cu is None:
+        # the same oracle on one core, over one sequence and up to 4 heads, as tokens/s of all H heads
+        hs = min(w.H, 4)
+        k1, v1, b1 = (np.ascontiguousarray(x[:1, :, :hs]) for x in (ks, vs, bs))
+        g1 = None if gs is None else np.ascontiguousarray(gs[:1, :, :hs])
+        t0 = time.perf_counter()
+        oracle.oracle_fwd(k1, v1, b1, w.C, nthreads=1, g=g1)
+        dt1 = time.perf_counter() - t0
+        out["one_core"] = {"value": w.T * hs / w.H / dt1, "unit": "tokens/s",
+                           "sample": f"1 sequence x {w.T} tokens x {hs} of {w.H} heads, 1 thread",
+                           "seconds": dt1}
+    return out
 
 
 # --- reference arm: the oracle on the host cores -----------------------------------------------
