@@ -185,10 +185,12 @@ __device__ __forceinline__ void fail(Barriers *bars, int *status) {
     if (atomicExch(&bars->abort_flag, 1) == 0) record_error(status, KKT_ERR_TIMEOUT);
 }
 
+// Called by every lane of a warp (all callers are whole warps).  The result is made warp-uniform,
+// so that a timeout seen by one lane is taken by all before the .sync.aligned instructions after it.
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, Barriers *bars, int *status) {
-    if (mbar_wait(bar, parity, &bars->abort_flag, kWaitLimitNs)) return true;
-    fail(bars, status);
-    return false;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, parity, &bars->abort_flag, kWaitLimitNs));
+    if (!ok) fail(bars, status);
+    return ok;
 }
 
 // Group barrier on an mbarrier (every member arrives, then waits for the phase):
