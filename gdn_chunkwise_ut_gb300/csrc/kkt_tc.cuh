@@ -496,7 +496,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     Barriers *bars = reinterpret_cast<Barriers *>(smem + CF::OFF_BAR);
-    const int warp = threadIdx.x >> 5;
+    // the warp index, broadcast from lane 0 so that the compiler knows it is warp-uniform (as are
+    // the role branches and the per-warp constants derived from it)
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
     const int lane = threadIdx.x & 31;
 
     auto stage_kv = [&](int s) { return smem + s * CF::KV_BYTES; };
@@ -786,9 +788,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------------ inverse warps
         const int q = warp & 3;             // tensor-memory lane quarter
         const int m = 32 * q + lane;        // tile row
-        const int g = m / C;                // head within the tile
-        const int r = m % C;                // row within the chunk
-        const int wp = r / 32;              // warp position within the head (0 for C = 32)
+        const int g = 32 * q / C;           // head within the tile (m / C: C is a multiple of 32)
+        const int wp = 32 * q % C / 32;     // warp position within the head (0 for C = 32)
+        const int r = 32 * wp + lane;       // row within the chunk (m % C)
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         uint8_t *tm = smem + CF::OFF_T;     // the tile's T, [half][128 rows][128 B], 128-byte swizzle
         // level-32 product Y: the upper-right 32 x 32 of this warp's 64-row block (zero in T)
@@ -1159,9 +1161,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------------ epilogue warps
         const int q = warp & 3;
         const int m = 32 * q + lane;
-        const int g = m / C;
-        const int r = m % C;
-        const int wp = r / 32;
+        const int g = 32 * q / C;
+        const int wp = 32 * q % C / 32;
+        const int r = 32 * wp + lane;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         uint8_t *wstage = smem + CF::OFF_WU + q * CF::WU_BUFS * 4096;  // WU_BUFS x [32 rows][128 B]
         int i = 0;
