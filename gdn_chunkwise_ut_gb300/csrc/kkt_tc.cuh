@@ -848,12 +848,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Gram row -> row of A = I + strictLower(diag(beta) S) (beta on rows, unit diagonal,
             // §3.2), times Gamma elementwise when gated (§5 item 12), into the T buffer; columns
             // above 32 (wp + 1) stay zero
-            if constexpr (C == 128) {
-                // up to four 32-column blocks: one tensor-memory load at a time
+            if constexpr (C == 128 || GATED) {
+                // one 32-column block at a time (up to four at C = 128; the gated kernels too, whose
+                // unrolled form costs more in code size than it saves)
 #pragma unroll 1
                 for (int h = 0; h <= wp; ++h) {
                     uint32_t v[32];
-                    tmem_ld32(tmem + lane_base + kColGram + 32 * h, v);
+                    tmem_ld32(tmem + lane_base + kColGram + g * C + 32 * h, v);
                     float uh = 1.f;
                     float4 wq[8];
                     if constexpr (GATED) {
