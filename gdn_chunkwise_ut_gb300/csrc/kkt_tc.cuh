@@ -847,83 +847,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_BW, i);
             // Gram row -> row of A = I + strictLower(diag(beta) S) (beta on rows, unit diagonal,
             // §3.2), times Gamma elementwise when gated (§5 item 12), into the T buffer; columns
-            // above 32 (wp + 1) stay zero
-            if constexpr (C == 128 || GATED) {
-                // one 32-column block at a time (up to four at C = 128; the gated kernels too, whose
-                // unrolled form costs more in code size than it saves)
+            // above 32 (wp + 1) stay zero.  One 32-column block at a time, in a loop: the kernel is
+            // sensitive to its code size, and an unrolled form measured slower (gated) or the same.
 #pragma unroll 1
-                for (int h = 0; h <= wp; ++h) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + lane_base + kColGram + g * C + 32 * h, v);
-                    float uh = 1.f;
-                    float4 wq[8];
-                    if constexpr (GATED) {
-                        uh = row_factor(h);
-                        load_w(h, wq);
-                    }
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int c = 0; c < 32; c += 4) {
-                        float e[4];
-                        float gm[4] = {1.f, 1.f, 1.f, 1.f};
-                        if constexpr (GATED) {
-                            const float4 w4 = wq[c / 4];
-                            gm[0] = uh * w4.x; gm[1] = uh * w4.y; gm[2] = uh * w4.z; gm[3] = uh * w4.w;
-                        }
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int j = 32 * h + c + u;
-                            e[u] = (j < r) ? beta_r * __uint_as_float(v[c + u]) * gm[u] : (j == r ? 1.f : 0.f);
-                        }
-                        *tm_vec(tm, m, 32 * h + c) = make_float4(e[0], e[1], e[2], e[3]);
-                    }
+            for (int h = 0; h <= wp; ++h) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_base + kColGram + g * C + 32 * h, v);
+                float uh = 1.f;
+                float4 wq[8];
+                if constexpr (GATED) {
+                    uh = row_factor(h);
+                    load_w(h, wq);
                 }
-            } else {
-                uint32_t v[CF::T_HALVES][32];
-#pragma unroll
-                for (int h = 0; h < CF::T_HALVES; ++h)
-                    if (h <= wp) tmem_ld32(tmem + lane_base + kColGram + g * C + 32 * h, v[h]);
-                float uh[CF::T_HALVES];
-#pragma unroll
-                for (int h = 0; h < CF::T_HALVES; ++h) uh[h] = GATED ? row_factor(h) : 1.f;
                 tmem_wait_ld();
 #pragma unroll
-                for (int h = 0; h < CF::T_HALVES; ++h) {
-                    float4 wq[8];
+                for (int c = 0; c < 32; c += 4) {
+                    float e[4];
+                    float gm[4] = {1.f, 1.f, 1.f, 1.f};
                     if constexpr (GATED) {
-                        if (h <= wp) load_w(h, wq);
+                        const float4 w4 = wq[c / 4];
+                        gm[0] = uh * w4.x; gm[1] = uh * w4.y; gm[2] = uh * w4.z; gm[3] = uh * w4.w;
                     }
-                    if (h < wp) {
-                        // the whole block lies below the diagonal (columns < 32 wp <= r): beta scale only
-                        const float2 bb = make_float2(beta_r * uh[h], beta_r * uh[h]);
 #pragma unroll
-                        for (int c = 0; c < 32; c += 4) {
-                            float2 e0 = fmul2(make_float2(__uint_as_float(v[h][c]), __uint_as_float(v[h][c + 1])), bb);
-                            float2 e1 = fmul2(make_float2(__uint_as_float(v[h][c + 2]), __uint_as_float(v[h][c + 3])), bb);
-                            if constexpr (GATED) {
-                                const float4 w4 = wq[c / 4];
-                                e0 = fmul2(e0, make_float2(w4.x, w4.y));
-                                e1 = fmul2(e1, make_float2(w4.z, w4.w));
-                            }
-                            *tm_vec(tm, m, 32 * h + c) = make_float4(e0.x, e0.y, e1.x, e1.y);
-                        }
-                    } else if (h == wp) {
-                        // the diagonal block: column 32 h + cc is below the diagonal when cc < lane
-#pragma unroll
-                        for (int c = 0; c < 32; c += 4) {
-                            float e[4];
-                            float gm[4] = {1.f, 1.f, 1.f, 1.f};
-                            if constexpr (GATED) {
-                                const float4 w4 = wq[c / 4];
-                                gm[0] = uh[h] * w4.x; gm[1] = uh[h] * w4.y; gm[2] = uh[h] * w4.z; gm[3] = uh[h] * w4.w;
-                            }
-#pragma unroll
-                            for (int u = 0; u < 4; ++u)
-                                e[u] = (c + u < lane) ? beta_r * __uint_as_float(v[h][c + u]) * gm[u]
-                                                      : (c + u == lane ? 1.f : 0.f);
-                            *tm_vec(tm, m, 32 * h + c) = make_float4(e[0], e[1], e[2], e[3]);
-                        }
+                    for (int u = 0; u < 4; ++u) {
+                        const int j = 32 * h + c + u;
+                        e[u] = (j < r) ? beta_r * __uint_as_float(v[c + u]) * gm[u] : (j == r ? 1.f : 0.f);
                     }
+                    *tm_vec(tm, m, 32 * h + c) = make_float4(e[0], e[1], e[2], e[3]);
                 }
             }
             if constexpr (GATED) {
@@ -1160,8 +1110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
         // ------------------------------------------------------------------ epilogue warps
-        const int q = warp & 3;
-        const int m = 32 * q + lane;
+        const int q = warp & 3;             // rows 32 q .. 32 q + 31 of D
         const int g = 32 * q / C;
         const int wp = 32 * q % C / 32;
         const int r = 32 * wp + lane;
