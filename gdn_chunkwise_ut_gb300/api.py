@@ -195,11 +195,14 @@ class HostRunner:
     piece are copied in on one stream, the library runs it on the current stream, and its T, W and U
     are copied back on a third stream, so the two copy directions and the kernels overlap.  The
     results are those of one call on the whole batch.  ``sync=True`` waits for the copies.
+    ``h2d_ahead`` (default 2) holds a piece's input copies until the outputs of the piece that many
+    places earlier are back on the host (0: no hold), which keeps the link for the larger output
+    direction.
     """
 
     def __init__(self, B, T, H, dk, dv, C, *, dtype=torch.bfloat16, cu_seqlens=None,
                  kernel="auto", device="cuda", materialize_T: bool = True, T_dtype=torch.float32,
-                 gated: bool = False, pieces: int = 8):
+                 gated: bool = False, pieces: int = 8, h2d_ahead: int = 2):
         self.C, self.kernel, self.materialize_T, self.T_dtype = C, kernel, materialize_T, T_dtype
         dev = torch.device(device)
         self.shape = (B, T, H)
@@ -223,6 +226,11 @@ class HostRunner:
                      for n0, n1, c in _pieces(bounds, C, max(1, int(pieces)))]
         self.s_in = torch.cuda.Stream(device=dev)
         self.s_out = torch.cuda.Stream(device=dev)
+        # h2d_ahead > 0: a piece's inputs are copied in only once the outputs of the piece that many
+        # places earlier are back on the host, so that the inputs do not take the link from the
+        # outputs (which are the larger direction) early on
+        self.h2d_ahead = max(0, int(h2d_ahead))
+        self._out_done = [torch.cuda.Event() for _ in self.plan] if self.h2d_ahead else []
 
     @property
     def h2d_bytes(self) -> int:
@@ -246,8 +254,10 @@ class HostRunner:
         # the previous call's kernels have read the inputs, and its copies have read the outputs
         self.s_in.wait_stream(compute)
         compute.wait_stream(self.s_out)
-        for n0, n1, cu in self.plan:
+        for idx, (n0, n1, cu) in enumerate(self.plan):
             with torch.cuda.stream(self.s_in):
+                if self.h2d_ahead and idx >= self.h2d_ahead:
+                    self.s_in.wait_event(self._out_done[idx - self.h2d_ahead])
                 for d, h in zip(dev_in, host_in):
                     d[n0:n1].copy_(h[n0:n1], non_blocking=True)
             compute.wait_stream(self.s_in)
@@ -261,6 +271,8 @@ class HostRunner:
             with torch.cuda.stream(self.s_out):
                 for d, h in zip(dev_out, host_out):
                     h[n0:n1].copy_(d[n0:n1], non_blocking=True)
+                if self.h2d_ahead:
+                    self._out_done[idx].record(self.s_out)
         compute.wait_stream(self.s_out)
         if sync:
             compute.synchronize()
