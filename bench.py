@@ -187,18 +187,24 @@ def kernel_source_hash(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if it matches the current source."""
+def recorded_counters(kernel: str, workload: str) -> dict:
+    """The committed ncu record of this kernel and workload (profiles/traffic.json), if it was taken
+    from the current source; else {}."""
     p = ROOT / "profiles" / "traffic.json"
     if not p.exists():
-        return None
+        return {}
     try:
         rec = json.loads(p.read_text()).get(f"{kernel}:{workload}")
     except Exception:
-        return None
+        return {}
     if not rec or rec.get("source_hash") != kernel_source_hash(kernel):
-        return None
-    return rec.get("dram_bytes_per_launch")
+        return {}
+    return rec
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the current source."""
+    return recorded_counters(kernel, workload).get("dram_bytes_per_launch")
 
 
 # --- our path -----------------------------------------------------------------------------------
@@ -304,8 +310,9 @@ def bench_ours(args, rank, world, local):
     achieved = alg_bytes / (launch_ms / 1e3) / 1e9
     # the recorded counters are those of the default call (fp32 T)
     # counters recorded for the default call and the gated one (fp32 T); none for the other variants
-    traffic = None if (args.no_t_out or args.t_f16) else \
-        recorded_traffic(kernel, w.name + ("+gated" if args.gated else ""))
+    counters = {} if (args.no_t_out or args.t_f16) else \
+        recorded_counters(kernel, w.name + ("+gated" if args.gated else ""))
+    traffic = counters.get("dram_bytes_per_launch")
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     runner = HostRunner(k.shape[0], k.shape[1], w.H, w.dk, w.dv, w.C, dtype=k.dtype, cu_seqlens=cu,
@@ -338,6 +345,9 @@ def bench_ours(args, rank, world, local):
                           if flush else f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB > 129 MB), no flush")},
         "hbm_gbs": achieved, "hbm_frac_of_nominal_8tbs": achieved / NOMINAL_HBM_GBS,
         "chunks_per_s": aggregate_value(units / w.C * K, world, max_ms / 1e3),
+        # secondary: the tensor pipe's busy fraction from the committed ncu record (null when absent
+        # or taken from other source)
+        "tensor_pipe_active": counters.get("tensor_pipe_active"),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
                      "kernel": f"kkt_{kernel}", "alg_bytes_per_launch": alg_bytes,
