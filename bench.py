@@ -62,6 +62,8 @@ def parse_args():
     ap.add_argument("--t-f16", action="store_true", help="T written in fp16 instead of fp32")
     ap.add_argument("--head-dim", type=int, default=None,
                     help="override the workload's head dimension d_k = d_v (64 or 128)")
+    ap.add_argument("--dv", type=int, default=None,
+                    help="override d_v alone, after --head-dim (mixed head dimensions)")
     ap.add_argument("--chunk", type=int, default=None,
                     help="override the workload's chunk size C (32, 64 or 128): the chunk-size study")
     ap.add_argument("--graph", action="store_true",
@@ -215,6 +217,8 @@ def select_workload(args):
         w = dataclasses.replace(w, name=f"{w.name}@C{args.chunk}", C=args.chunk)
     if args.head_dim is not None and (args.head_dim != w.dk or args.head_dim != w.dv):
         w = dataclasses.replace(w, name=f"{w.name}@d{args.head_dim}", dk=args.head_dim, dv=args.head_dim)
+    if args.dv is not None and args.dv != w.dv:
+        w = dataclasses.replace(w, name=f"{w.name}@v{args.dv}", dv=args.dv)
     return w
 
 

@@ -152,14 +152,21 @@ extern "C" const char *kkt_status_string(int status) {
 extern "C" int kkt_version(void) { return (0 << 16) | (1 << 8) | 0; }
 
 extern "C" int kkt_debug_bounds(unsigned long long *first, int *kind) {
-    kkt::BoundsRecord rec[3] = {};
+    constexpr int kFiles = 5;  // one record per kernel translation unit
+    kkt::BoundsRecord rec[kFiles] = {};
     if (kkt::debug_bounds_tc(&rec[0]) < 0 || kkt::debug_bounds_tc_d64(&rec[1]) < 0 ||
-        kkt::debug_bounds_simt(&rec[2]) < 0)
+        kkt::debug_bounds_tc_k128v64(&rec[2]) < 0 || kkt::debug_bounds_tc_k64v128(&rec[3]) < 0 ||
+        kkt::debug_bounds_simt(&rec[4]) < 0)
         return -1;
-    const kkt::BoundsRecord &f = rec[0].count ? rec[0] : rec[1].count ? rec[1] : rec[2];
-    if (first) *first = f.first;
-    if (kind) *kind = (int)f.kind;
-    return (int)(rec[0].count + rec[1].count + rec[2].count);
+    unsigned int total = 0;
+    const kkt::BoundsRecord *f = nullptr;
+    for (int i = 0; i < kFiles; ++i) {
+        total += rec[i].count;
+        if (!f && rec[i].count) f = &rec[i];
+    }
+    if (first) *first = f ? f->first : 0ull;
+    if (kind) *kind = f ? (int)f->kind : 0;
+    return (int)total;
 }
 
 #ifdef KKT_TRACE

@@ -128,6 +128,8 @@ struct BoundsRecord {
 };
 int debug_bounds_tc(BoundsRecord *out);
 int debug_bounds_tc_d64(BoundsRecord *out);
+int debug_bounds_tc_k128v64(BoundsRecord *out);
+int debug_bounds_tc_k64v128(BoundsRecord *out);
 int debug_bounds_simt(BoundsRecord *out);
 bool tc_supports(int dk, int dv, int C, int io);
 

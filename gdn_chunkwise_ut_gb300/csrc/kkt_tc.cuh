@@ -1,7 +1,8 @@
 // kkt_tc.cuh -- persistent, warp-specialised tcgen05 + TMA kernel for kkt_solve (bf16 I/O),
-// templated on the chunk size C and the head dimension D = d_k = d_v (64 or 128).  Included by one
-// translation unit per head dimension (kkt_tc.cu: D = 128, kkt_tc_d64.cu: D = 64), which compile in
-// parallel; everything here has internal linkage.
+// templated on the chunk size C and the head dimensions d_k and d_v (64 or 128 each).  Included by
+// one translation unit per (d_k, d_v) pair (kkt_tc.cu: 128 / 128, kkt_tc_d64.cu: 64 / 64,
+// kkt_tc_k128v64.cu and kkt_tc_k64v128.cu: the mixed pairs), which compile in parallel; everything
+// here has internal linkage.
 //
 // One CTA per SM walks "tiles" of 128 rows: G = 128 / C heads of one chunk,
 // row m = g * C + r (head g, token r of the chunk).  For each tile
@@ -12,13 +13,12 @@
 //                   beta (and the gate's prefix sums, gated kernels) with plain
 //                   loads.
 //   Gram warp       one lane issuing tcgen05.mma S = K K^T (M = N = 128,
-//                   K = DH, bf16 -> fp32 in tensor memory); zeroes the rows past
+//                   K = d_k, bf16 -> fp32 in tensor memory); zeroes the rows past
 //                   a short chunk's end first.
 //   W|U warp        one lane issuing D = T~ [K | V] with T~ = T diag(beta) read
 //                   from tensor memory as a bf16 hi + lo pair (two accumulating
-//                   passes, M = 128, N = 2 DH, K = 128; T~ is block diagonal over
+//                   passes, M = 128, N = d_k + d_v, K = 128; T~ is block diagonal over
 //                   the G heads).  The commit after D frees the stage.
-//   (DH = d_k = d_v, the head dimension: 64 or 128.)
 //   inverse warps   a thread per row loads its Gram row (tcgen05.ld), applies
 //                   the beta row scale, strict-lower mask and unit diagonal
 //                   (§3.2) and writes the row of A into the tile's fp32 T
@@ -88,11 +88,13 @@ struct TileInfo {
     int pad;
 };
 
-template <int C, int DH>
+template <int C, int DK, int DV>
 struct Cfg {
     static constexpr int G = 128 / C;                         // heads per tile
-    static constexpr int NB = DH / 64;                         // 64-column TMA boxes per K or V row
-    static constexpr int KV_BYTES = 2 * NB * 16384;           // K then V boxes, [box][row][128 B]
+    static constexpr int NBK = DK / 64;                        // 64-column TMA boxes per K row
+    static constexpr int NBV = DV / 64;                        // and per V row
+    static constexpr int NBKV = NBK + NBV;
+    static constexpr int KV_BYTES = NBKV * 16384;             // K then V boxes, [box][row][128 B]
     // per stage: beta[128]; gated kernels: the gate's prefix sums G[128] (log2 units), the column
     // factors w[128] and one "factorable" flag per 32-row block (int[4]); then the TileInfo
     static constexpr int META_BYTES = 1584;
@@ -105,7 +107,7 @@ struct Cfg {
     static constexpr int OFF_BAR = OFF_META + kNS * META_BYTES;
     static constexpr int BAR_BYTES = 512;
     static constexpr int SMEM_BYTES = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
-    static constexpr uint32_t TX_BYTES = G * 2 * NB * C * 128;      // K + V boxes of one stage
+    static constexpr uint32_t TX_BYTES = G * NBKV * C * 128;        // K + V boxes of one stage
     static_assert(SMEM_BYTES <= 232448, "shared memory over the per-block limit");
 };
 
@@ -490,12 +492,12 @@ __device__ __forceinline__ void head_prefix_sums(float (&x)[4], int lane) {
     }
 }
 
-template <int C, int DH, bool TF16, bool GATED>
+template <int C, int DK, int DV, bool TF16, bool GATED>
 __global__ void __launch_bounds__(kThreads, 1)
     kkt_tc_kernel(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                   const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_u,
                   const __grid_constant__ CUtensorMap map_t, const TcParams p) {
-    using CF = Cfg<C, DH>;
+    using CF = Cfg<C, DK, DV>;
     constexpr int G = CF::G;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
@@ -621,13 +623,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 info->done = 0;
                 uint8_t *st = stage_kv(s);
                 mbar_arrive_expect_tx(&bars->full[s], CF::TX_BYTES);
-                for (int g = 0; g < G; ++g)
-                    for (int c2 = 0; c2 < CF::NB; ++c2) {
+                for (int g = 0; g < G; ++g) {
+                    for (int c2 = 0; c2 < CF::NBK; ++c2)
                         tma_load_3d(st + c2 * 16384 + g * C * 128, &map_k, &bars->full[s], c2 * 64, h0 + g,
                                     (int)ch.t0);
-                        tma_load_3d(st + CF::NB * 16384 + c2 * 16384 + g * C * 128, &map_v, &bars->full[s],
+                    for (int c2 = 0; c2 < CF::NBV; ++c2)
+                        tma_load_3d(st + CF::NBK * 16384 + c2 * 16384 + g * C * 128, &map_v, &bars->full[s],
                                     c2 * 64, h0 + g, (int)ch.t0);
-                    }
+                }
                 KKT_TRACE_EVENT(EV_P_ISSUE, i);
             }
             // beta (and, gated, the gate data) while the loads are in flight, so that the first
@@ -710,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // zero rows Lc..C-1 of every head's K and V boxes
                 uint8_t *st = stage_kv(s);
                 const int per_box = (C - info.Lc) * 8;  // 16-byte chunks
-                for (int e = lane; e < G * 2 * CF::NB * per_box; e += 32) {
+                for (int e = lane; e < G * CF::NBKV * per_box; e += 32) {
                     const int box = e / per_box, w = e % per_box;
                     const int g = box % G, kvh = box / G;  // kvh: the K boxes, then the V boxes
                     *smem_chk(reinterpret_cast<uint4 *>(st + kvh * 16384 + g * C * 128 + (info.Lc + w / 8) * 128 +
@@ -724,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t a0 = smem_u32(stage_kv(s));
 #pragma unroll
-                for (int kk = 0; kk < 4 * CF::NB; ++kk) {  // K = DH in steps of 16
+                for (int kk = 0; kk < 4 * CF::NBK; ++kk) {  // K = d_k in steps of 16
                     const uint64_t d = sw128_desc(a0 + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
                     mma_ss(tmem + kColGram, d, d, idesc_gram, kk > 0 ? 1u : 0u);
                 }
@@ -745,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Tile by tile: once T~ is in tensor memory and the epilogue has drained D, hand the tile
         // info to the epilogue and issue D = T~ [K|V] (hi and lo passes); the commit frees T~, the
         // stage, and tells the epilogue that D is ready.  The stage's info marks the end of work.
-        const uint32_t idesc_epi = idesc_bf16_f32(128, 2 * DH, 0, 1);  // N = DH columns of K, then of V
+        const uint32_t idesc_epi = idesc_bf16_f32(128, DK + DV, 0, 1);  // N = d_k columns of K, then d_v of V
         for (int i = 0;; ++i) {
             const int s = i % kNS;
             if (!wait_bar(&bars->full[s], (uint32_t)(i / kNS) & 1u, bars, p.status)) break;
@@ -1133,12 +1136,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool row_ok = r < info.Lc && info.h0 + g < p.H;
             const int64_t grow = (info.t0 + r) * p.H + info.h0 + g;
 #pragma unroll 1
-            for (int cc = 0; cc < 2 * CF::NB; ++cc) {  // 64 columns of D at a time: those of W, then of U~
+            for (int cc = 0; cc < CF::NBKV; ++cc) {  // 64 columns of D at a time: those of W, then of U~
                 uint32_t v0[32], v1[32];
                 tmem_ld32(tmem + lane_base + kColD + 64 * cc, v0);
                 tmem_ld32(tmem + lane_base + kColD + 64 * cc + 32, v1);
                 tmem_wait_ld();
-                if (cc == 2 * CF::NB - 1) {
+                if (cc == CF::NBKV - 1) {
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) {
@@ -1163,14 +1166,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_3d(cc < CF::NB ? &map_w : &map_u, buf, 64 * (cc % CF::NB), info.h0 + g,
+                        tma_store_3d(cc < CF::NBK ? &map_w : &map_u, buf, 64 * (cc < CF::NBK ? cc : cc - CF::NBK), info.h0 + g,
                                      (int)(info.t0 + 32 * wp));
                         bulk_commit();
                     }
                     ++nstore;
                 } else if (row_ok) {
-                    __nv_bfloat16 *base = gmem_chk(cc < CF::NB ? p.W_out : p.U_out, grow * DH + 64 * (cc % CF::NB),
-                                                   p.ntok * p.H * DH, 64);
+                    const int dw = cc < CF::NBK ? DK : DV;  // this group's tensor width
+                    __nv_bfloat16 *base = gmem_chk(cc < CF::NBK ? p.W_out : p.U_out,
+                                                   grow * dw + 64 * (cc < CF::NBK ? cc : cc - CF::NBK),
+                                                   p.ntok * p.H * dw, 64);
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         reinterpret_cast<uint4 *>(base)[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
@@ -1231,9 +1236,9 @@ int sm_count() {
     return n;
 }
 
-template <int C, int DH>
+template <int C, int DK, int DV>
 int launch_tc_t(const Problem &pb) {
-    using CF = Cfg<C, DH>;
+    using CF = Cfg<C, DK, DV>;
     CUtensorMap mk, mv, mw, mu, mt;
     if (!make_map(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.k, pb.ntok, pb.H, pb.dk, 64, C) ||
         !make_map(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, pb.v, pb.ntok, pb.H, pb.dv, 64, C) ||
@@ -1260,12 +1265,13 @@ int launch_tc_t(const Problem &pb) {
     p.trace = static_cast<unsigned long long *>(pb.trace);
     p.tile_counter = pb.tile_counter;
     p.stall_first_tile = pb.stall_first_tile;
-    auto kern = pb.g ? (pb.t_f16 ? kkt_tc_kernel<C, DH, true, true> : kkt_tc_kernel<C, DH, false, true>)
-                     : (pb.t_f16 ? kkt_tc_kernel<C, DH, true, false> : kkt_tc_kernel<C, DH, false, false>);
-    const bool attr_ok = pb.g ? (pb.t_f16 ? ensure_max_smem<kkt_tc_kernel<C, DH, true, true>>(CF::SMEM_BYTES)
-                                          : ensure_max_smem<kkt_tc_kernel<C, DH, false, true>>(CF::SMEM_BYTES))
-                              : (pb.t_f16 ? ensure_max_smem<kkt_tc_kernel<C, DH, true, false>>(CF::SMEM_BYTES)
-                                          : ensure_max_smem<kkt_tc_kernel<C, DH, false, false>>(CF::SMEM_BYTES));
+    auto kern = pb.g ? (pb.t_f16 ? kkt_tc_kernel<C, DK, DV, true, true> : kkt_tc_kernel<C, DK, DV, false, true>)
+                     : (pb.t_f16 ? kkt_tc_kernel<C, DK, DV, true, false> : kkt_tc_kernel<C, DK, DV, false, false>);
+    const bool attr_ok =
+        pb.g ? (pb.t_f16 ? ensure_max_smem<kkt_tc_kernel<C, DK, DV, true, true>>(CF::SMEM_BYTES)
+                         : ensure_max_smem<kkt_tc_kernel<C, DK, DV, false, true>>(CF::SMEM_BYTES))
+             : (pb.t_f16 ? ensure_max_smem<kkt_tc_kernel<C, DK, DV, true, false>>(CF::SMEM_BYTES)
+                         : ensure_max_smem<kkt_tc_kernel<C, DK, DV, false, false>>(CF::SMEM_BYTES));
     if (!attr_ok) return KKT_ERR_CUDA;
     const int sms = sm_count();
     if (sms <= 0) return KKT_ERR_CUDA;

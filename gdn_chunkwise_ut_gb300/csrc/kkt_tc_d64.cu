@@ -8,9 +8,9 @@ int debug_bounds_tc_d64(BoundsRecord *out) { return read_bounds_record(out); }
 
 int launch_tc_d64(const Problem &p) {
     switch (p.C) {
-        case 32: return launch_tc_t<32, 64>(p);
-        case 64: return launch_tc_t<64, 64>(p);
-        case 128: return launch_tc_t<128, 64>(p);
+        case 32: return launch_tc_t<32, 64, 64>(p);
+        case 64: return launch_tc_t<64, 64, 64>(p);
+        case 128: return launch_tc_t<128, 64, 64>(p);
         default: return KKT_ERR_UNSUPPORTED;
     }
 }

@@ -91,7 +91,7 @@ enum { KKT_IO_BF16 = 0, KKT_IO_F32 = 1 };
 enum {
     KKT_KERNEL_AUTO = 0, /* tcgen05/TMA kernel when it supports the shape, else the SIMT kernel */
     KKT_KERNEL_SIMT = 1, /* one CTA per (chunk, head), fp32 CUDA-core arithmetic throughout */
-    KKT_KERNEL_TC = 2    /* persistent tcgen05 + TMA kernel (bf16 I/O, dk == dv) */
+    KKT_KERNEL_TC = 2    /* persistent tcgen05 + TMA kernel (bf16 I/O, dk, dv in {64, 128}) */
 };
 
 /*
@@ -110,8 +110,9 @@ int kkt_solve_fwd(const void *k, const void *v, const float *beta, const int32_t
  * kkt_solve_fwd_ex -- as kkt_solve_fwd, with the I/O dtype (KKT_IO_BF16 or
  * KKT_IO_F32, optionally ORed with KKT_T_OUT_F16) and the kernel (KKT_KERNEL_*)
  * chosen explicitly.  fp32 I/O runs
- * the SIMT kernel only; asking for KKT_KERNEL_TC with it, or with a shape the
- * tcgen05 kernel does not cover (dk != dv), returns KKT_ERR_UNSUPPORTED.
+ * the SIMT kernel only; asking for KKT_KERNEL_TC with it returns
+ * KKT_ERR_UNSUPPORTED (the tcgen05 kernel covers every bf16 shape, d_k and d_v
+ * each 64 or 128, d_k = d_v or not).
  * KKT_KERNEL_AUTO takes the tcgen05 kernel whenever it covers the call.
  *
  * workspace: NULL, or caller-owned device memory of at least
@@ -178,8 +179,8 @@ int kkt_solve_fwd_gated(const void *k, const void *v, const float *beta, const f
  * allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
  *
  *   Arguments, layouts, ownership and errors: as kkt_solve_fwd (bf16 I/O), run
- *   on the tensor-core kernel only.  Shapes that kernel does not cover
- *   (d_k != d_v) return KKT_ERR_UNSUPPORTED; a problem that would
+ *   on the tensor-core kernel only, which covers every shape kkt_solve_fwd
+ *   accepts (bf16; other shapes return KKT_ERR_UNSUPPORTED); a problem that would
  *   need more scratch than the array holds returns KKT_ERR_ARG (a call needs
  *   16 bytes, two 64-bit counters, whatever the problem size; the array is zero
  *   when the library loads and every call leaves it zero).

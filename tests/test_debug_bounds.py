@@ -81,10 +81,11 @@ def test_in_range_and_correct(blib, kernel, C, variant):
 
 
 @pytest.mark.parametrize("C", [32, 64, 128])
-def test_tc_head_dim_64(blib, C):
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 64), (64, 128)])
+def test_tc_head_dims(blib, C, dk, dv):
     lengths = [1, 63, 64, 65, 0, 130, 7, 200, 128]
     cu = np.concatenate([[0], np.cumsum(lengths)])
-    k, v, beta = make_inputs(1, int(cu[-1]), 3, 64, 64, seed=C + 95, device=DEV)
+    k, v, beta = make_inputs(1, int(cu[-1]), 3, dk, dv, seed=C + 95, device=DEV)
     g = make_gate(1, int(cu[-1]), 3, seed=C + 95, device=DEV)
     T_out, W, U = _call(blib, k, v, beta, C, cu, "tc", g=g)
     _no_violations(blib)

@@ -245,15 +245,17 @@ def test_gate_cut_is_block_diagonal(kernel):
 
 @pytest.mark.parametrize("C", [32, 64, 128])
 @pytest.mark.parametrize("variant", ["plain", "gated", "t_fp16", "no_t"])
-def test_tc_head_dim_64(C, variant):
-    """The tensor-core kernel at d_k = d_v = 64 (one 64-column box per row, N = 128 for W|U~):
-    varlen with empty and one-token sequences and a ragged tail, every variant, against the oracle
-    (W and U~ only: bit-identical to the materialising call)."""
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 64), (64, 128)])
+def test_tc_head_dims(C, variant, dk, dv):
+    """The tensor-core kernel at the head dimensions other than 128 / 128: d_k = d_v = 64 (one
+    64-column box per row, N = 128 for W|U~) and the mixed pairs (N = 192): varlen with empty and
+    one-token sequences and a ragged tail, every variant, against the oracle (W and U~ only:
+    bit-identical to the materialising call)."""
     lengths = [1, 63, 64, 65, 0, 130, 7, 200, 128]
     cu = np.concatenate([[0], np.cumsum(lengths)])
-    k, v, beta = make_inputs(1, int(cu[-1]), 3, 64, 64, seed=C + 91, device=DEV)
+    k, v, beta = make_inputs(1, int(cu[-1]), 3, dk, dv, seed=C + 91, device=DEV)
     g = make_gate(1, int(cu[-1]), 3, seed=C + 91, device=DEV) if variant == "gated" else None
-    assert select_kernel(64, 64, C) == "tc"
+    assert select_kernel(dk, dv, C) == "tc"
     outs = run(k, v, beta, C, cu, kernel="tc", g=g)
     full_compare(k, v, beta, C, cu, outs, g=g)
     cu_t = torch.as_tensor(cu, dtype=torch.int32, device=DEV)

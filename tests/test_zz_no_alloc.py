@@ -66,13 +66,21 @@ def test_noalloc_varlen_two_calls():
         _same_within_tolerance(_noalloc(k, v, beta, 64, cu), ref)
 
 
-def test_noalloc_rejects_shapes_without_scratch_kernel():
-    """d_k != d_v runs only on the SIMT kernel, which the allocation-free call does not offer."""
-    k = torch.zeros((1, 64, 1, 64), dtype=torch.bfloat16, device=DEV)
+def test_noalloc_mixed_head_dims_and_unsupported_shapes():
+    """d_k != d_v runs on the tensor-core kernel like any other covered shape; a head dimension
+    outside {64, 128} is rejected."""
+    lengths = [5, 64, 300, 1, 129]
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32, device=DEV)
+    for dk, dv in ((64, 128), (128, 64)):
+        k, v, beta = make_inputs(1, int(sum(lengths)), 3, dk, dv, seed=37, device=DEV)
+        ref = kkt_solve_fwd(k, v, beta, 64, cu)
+        torch.cuda.synchronize()
+        _same_within_tolerance(_noalloc(k, v, beta, 64, cu), ref)
+    k = torch.zeros((1, 64, 1, 96), dtype=torch.bfloat16, device=DEV)
     v = torch.zeros((1, 64, 1, 128), dtype=torch.bfloat16, device=DEV)
     W, U = torch.zeros_like(k), torch.zeros_like(v)
     beta = torch.zeros((1, 64, 1), device=DEV)
     T_out = torch.zeros((1, 64, 1, 64), device=DEV)
-    rc = _lib.lib().kkt_solve_fwd_noalloc(k.data_ptr(), v.data_ptr(), beta.data_ptr(), None, 1, 64, 1, 64, 128, 64,
+    rc = _lib.lib().kkt_solve_fwd_noalloc(k.data_ptr(), v.data_ptr(), beta.data_ptr(), None, 1, 64, 1, 96, 128, 64,
                                           T_out.data_ptr(), W.data_ptr(), U.data_ptr(), None)
     assert rc == _lib.KKT_ERR_UNSUPPORTED
