@@ -72,11 +72,14 @@ def test_select_kernel(lib):
     assert sel(128, 128, 64, _lib.KKT_IO_F32 | _lib.KKT_T_OUT_F16, 0) == _lib.KKT_KERNEL_SIMT
     assert sel(128, 128, 64, 0x200, 0) == -_lib.KKT_ERR_ARG
     for C in (32, 64, 128):
-        # the tensor-core kernel covers bf16 with dk = dv = 128 at every chunk size
-        assert sel(128, 128, C, _lib.KKT_IO_BF16, _lib.KKT_KERNEL_AUTO) == _lib.KKT_KERNEL_TC
         for dk in (64, 128):
             for dv in (64, 128):
-                assert sel(dk, dv, C, _lib.KKT_IO_BF16, 0) in (_lib.KKT_KERNEL_SIMT, _lib.KKT_KERNEL_TC)
+                # the tensor-core kernel covers every bf16 shape (d_k = d_v or not); fp32 I/O runs
+                # on the SIMT kernel only, which also takes every bf16 shape when asked for
+                assert sel(dk, dv, C, _lib.KKT_IO_BF16, _lib.KKT_KERNEL_AUTO) == _lib.KKT_KERNEL_TC
+                assert sel(dk, dv, C, _lib.KKT_IO_BF16, _lib.KKT_KERNEL_SIMT) == _lib.KKT_KERNEL_SIMT
+                assert sel(dk, dv, C, _lib.KKT_IO_F32, _lib.KKT_KERNEL_AUTO) == _lib.KKT_KERNEL_SIMT
+                assert sel(dk, dv, C, _lib.KKT_IO_F32, _lib.KKT_KERNEL_TC) == -_lib.KKT_ERR_UNSUPPORTED
 
 
 def _call(lib, **kw):
