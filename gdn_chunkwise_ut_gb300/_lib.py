@@ -43,6 +43,7 @@ SIGNATURES = {
                                  _vp]),
     "kkt_solve_fwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
     "kkt_test_stalled_solve": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
+    "kkt_test_noalloc_scratch": (_i, [_vp]),
     "kkt_device_status": (_i, [_vp]),
     "kkt_debug_bounds": (_i, [_vp, _vp]),
     "kkt_select_kernel": (_i, [_i, _i, _i, _i, _i]),

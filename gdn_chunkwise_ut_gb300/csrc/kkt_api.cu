@@ -1,5 +1,6 @@
 // kkt_api.cu -- the C entry points of libkkt: argument checks, kernel choice,
 // the per-device status word.  Declared in include/kkt.h.
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -11,8 +12,12 @@ namespace {
 // kkt_device_status() (0 = none).
 __device__ int g_kkt_status = 0;
 
+// Device address of the status word, per device.  Host threads may fill an entry at the same time;
+// they all store the same address, and the atomics make that well defined.  cudaDeviceReset
+// invalidates the address (the module is loaded again by the next call's context), so calls after a
+// reset of the device are not supported.
 constexpr int kMaxDevices = 64;
-int *g_status_ptr[kMaxDevices] = {};
+std::atomic<int *> g_status_ptr[kMaxDevices] = {};
 
 }  // namespace
 
@@ -21,12 +26,14 @@ namespace kkt {
 int status_ptr(int **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KKT_ERR_NO_DEVICE;
-    if (!g_status_ptr[dev]) {
+    int *cached = g_status_ptr[dev].load(std::memory_order_relaxed);
+    if (!cached) {
         void *ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_kkt_status) != cudaSuccess) return KKT_ERR_CUDA;
-        g_status_ptr[dev] = static_cast<int *>(ptr);
+        if (cudaGetSymbolAddress(&ptr, g_kkt_status) != cudaSuccess || ptr == nullptr) return KKT_ERR_CUDA;
+        cached = static_cast<int *>(ptr);
+        g_status_ptr[dev].store(cached, std::memory_order_relaxed);
     }
-    *out = g_status_ptr[dev];
+    *out = cached;
     return KKT_OK;
 }
 
@@ -58,42 +65,61 @@ extern "C" int kkt_select_kernel(int dk, int dv, int C, int io_dtype, int kernel
     }
 }
 
+namespace kkt {
+
+int make_problem(const void *k, const void *v, const float *beta, const float *g, const int32_t *cu_seqlens,
+                 int B, int T, int H, int dk, int dv, int C, void *T_out, void *W_out, void *U_out,
+                 int io_dtype, int kernel, struct CUstream_st *stream, Problem *p, int *which, bool *empty) {
+    *empty = false;
+    if (!k || !v || !beta || !W_out || !U_out) return KKT_ERR_ARG;  // T_out may be NULL
+    if (B < 1 || T < 0 || H < 1 || H > 65535) return KKT_ERR_ARG;
+    const int w = kkt_select_kernel(dk, dv, C, io_dtype, kernel);
+    if (w < 0) return -w;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(T_out) || !aligned16(W_out) || !aligned16(U_out) ||
+        !aligned4(beta) || (g && !aligned4(g)) || (cu_seqlens && !aligned4(cu_seqlens)))
+        return KKT_ERR_ALIGN;
+    const int64_t ntok = cu_seqlens ? (int64_t)T : (int64_t)B * T;
+    if (ntok == 0) {
+        *empty = true;
+        return KKT_OK;
+    }
+    // the work-id space and every flat index must fit comfortably in 63 bits / grid limits
+    if (ntok / C + B > 0x7fffffffLL) return KKT_ERR_ARG;
+
+    p->k = k; p->v = v; p->beta = beta; p->g = g; p->cu_seqlens = cu_seqlens;
+    p->nseq = B; p->T = T; p->ntok = ntok;
+    p->H = H; p->dk = dk; p->dv = dv; p->C = C;
+    p->T_out = T_out; p->W_out = W_out; p->U_out = U_out;
+    p->io = io_dtype & ~KKT_T_OUT_F16;
+    p->t_f16 = (io_dtype & KKT_T_OUT_F16) != 0;
+    p->stream = reinterpret_cast<cudaStream_t>(stream);
+#ifdef KKT_TRACE
+    p->trace = g_trace;
+#else
+    p->trace = nullptr;
+#endif
+    p->tile_counter = nullptr;
+    p->stall_first_tile = 0;
+    *which = w;
+    return status_ptr(&p->status);
+}
+
+}  // namespace kkt
+
 namespace {
 
 // kkt_solve_fwd_ex and kkt_solve_fwd_gated: g == nullptr is the ungated call.
 int solve(const void *k, const void *v, const float *beta, const float *g, const int32_t *cu_seqlens,
           int B, int T, int H, int dk, int dv, int C, void *T_out, void *W_out, void *U_out,
           int io_dtype, int kernel, void *workspace, size_t workspace_bytes, struct CUstream_st *stream) {
-    if (!k || !v || !beta || !W_out || !U_out) return KKT_ERR_ARG;  // T_out may be NULL
     if (workspace && workspace_bytes < KKT_WORKSPACE_BYTES) return KKT_ERR_ARG;
     if (workspace && !aligned16(workspace)) return KKT_ERR_ALIGN;
-    if (B < 1 || T < 0 || H < 1 || H > 65535) return KKT_ERR_ARG;
-    const int which = kkt_select_kernel(dk, dv, C, io_dtype, kernel);
-    if (which < 0) return -which;
-    if (!aligned16(k) || !aligned16(v) || !aligned16(T_out) || !aligned16(W_out) || !aligned16(U_out) ||
-        !aligned4(beta) || (g && !aligned4(g)) || (cu_seqlens && !aligned4(cu_seqlens)))
-        return KKT_ERR_ALIGN;
-    const int64_t ntok = cu_seqlens ? (int64_t)T : (int64_t)B * T;
-    if (ntok == 0) return KKT_OK;
-    // the work-id space and every flat index must fit comfortably in 63 bits / grid limits
-    if (ntok / C + B > 0x7fffffffLL) return KKT_ERR_ARG;
-
     kkt::Problem p;
-    p.k = k; p.v = v; p.beta = beta; p.g = g; p.cu_seqlens = cu_seqlens;
-    p.nseq = B; p.T = T; p.ntok = ntok;
-    p.H = H; p.dk = dk; p.dv = dv; p.C = C;
-    p.T_out = T_out; p.W_out = W_out; p.U_out = U_out;
-    p.io = io_dtype & ~KKT_T_OUT_F16;
-    p.t_f16 = (io_dtype & KKT_T_OUT_F16) != 0;
-    p.stream = reinterpret_cast<cudaStream_t>(stream);
-#ifdef KKT_TRACE
-    p.trace = g_trace;
-#else
-    p.trace = nullptr;
-#endif
-    p.tile_counter = nullptr;
-    const int st = kkt::status_ptr(&p.status);
-    if (st != KKT_OK) return st;
+    int which = 0;
+    bool empty = false;
+    const int st = kkt::make_problem(k, v, beta, g, cu_seqlens, B, T, H, dk, dv, C, T_out, W_out, U_out,
+                                     io_dtype, kernel, stream, &p, &which, &empty);
+    if (st != KKT_OK || empty) return st;
     // the workspace is zero on entry (zero-filled before first use, and left zero by every call)
     if (which == KKT_KERNEL_TC && workspace) p.tile_counter = static_cast<unsigned long long *>(workspace);
     return which == KKT_KERNEL_TC ? kkt::launch_tc(p) : kkt::launch_simt(p);

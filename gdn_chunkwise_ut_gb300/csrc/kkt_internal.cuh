@@ -115,6 +115,14 @@ __device__ __forceinline__ void check_sequence(const int32_t *cu, int s, int nse
 // Address of the current device's status word (looked up once per device).
 int status_ptr(int **out);
 
+// The argument checks every entry point shares.  Validates the call, chooses the kernel (*which,
+// KKT_KERNEL_SIMT or KKT_KERNEL_TC) and fills every field of *p except the schedule (tile_counter,
+// left null) and the test hook.  Returns KKT_OK or the status the entry point returns without
+// launching; *empty is set when the call has no tokens (valid, nothing to launch).
+int make_problem(const void *k, const void *v, const float *beta, const float *g, const int32_t *cu_seqlens,
+                 int B, int T, int H, int dk, int dv, int C, void *T_out, void *W_out, void *U_out,
+                 int io_dtype, int kernel, struct CUstream_st *stream, Problem *p, int *which, bool *empty);
+
 int launch_simt(const Problem &p);
 int launch_tc(const Problem &p);
 

@@ -4,25 +4,29 @@
 // scratch memory.  kkt_solve_fwd_ex takes that scratch from the caller; this
 // entry point instead uses a small array compiled into the library, so the
 // call needs no buffer beyond the inputs and outputs and allocates nothing.
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
 #include "kkt_internal.cuh"
+#include "kkt_test.h"
 
 namespace {
 
 // The scratch of kkt_solve_fwd_noalloc: one array per device, held by every GPU
 // that loads the library until the process exits.  A call uses its first 16
-// bytes (the tile counter and the count of CTAs done claiming): zero when the
-// module loads, and left zero by every call's kernel.
+// bytes (the tile counter and the count of CTAs done claiming).
 __device__ __align__(256) unsigned char g_noalloc_scratch[KKT_NOALLOC_SCRATCH_BYTES];
 
-// Bytes of scratch one call needs: two 64-bit counters, whatever the problem size.
+// Bytes of scratch one call uses: two 64-bit counters, the same for every problem size.
 constexpr size_t kNoallocNeed = 2 * sizeof(unsigned long long);
 static_assert(kNoallocNeed <= KKT_NOALLOC_SCRATCH_BYTES, "scratch array too small");
 
+// Device address of the array, per device.  Host threads may fill an entry at the same time;
+// they all store the same address, and the atomics make that well defined.  cudaDeviceReset
+// invalidates the address, so calls after a reset of the device are not supported.
 constexpr int kMaxDevices = 64;
-unsigned long long *g_noalloc_ptr[kMaxDevices] = {};
+std::atomic<unsigned long long *> g_noalloc_ptr[kMaxDevices] = {};
 
 // Device address of the scratch array for the current device.  In host code the
 // array's name is only a host-side stand-in, so the address is looked up once per
@@ -30,48 +34,41 @@ unsigned long long *g_noalloc_ptr[kMaxDevices] = {};
 int noalloc_scratch(unsigned long long **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KKT_ERR_NO_DEVICE;
-    if (!g_noalloc_ptr[dev]) {
+    unsigned long long *cached = g_noalloc_ptr[dev].load(std::memory_order_relaxed);
+    if (!cached) {
         void *ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return KKT_ERR_CUDA;
-        g_noalloc_ptr[dev] = static_cast<unsigned long long *>(ptr);
+        cached = static_cast<unsigned long long *>(ptr);
+        g_noalloc_ptr[dev].store(cached, std::memory_order_relaxed);
     }
-    *out = g_noalloc_ptr[dev];
+    *out = cached;
     return KKT_OK;
 }
-
-bool aligned_to(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 }  // namespace
 
 extern "C" int kkt_solve_fwd_noalloc(const void *k, const void *v, const float *beta, const int32_t *cu_seqlens,
                                      int B, int T, int H, int dk, int dv, int C,
                                      float *T_out, void *W_out, void *U_out, struct CUstream_st *stream) {
-    if (!k || !v || !beta || !W_out || !U_out) return KKT_ERR_ARG;  // T_out may be NULL
-    if (B < 1 || T < 0 || H < 1 || H > 65535) return KKT_ERR_ARG;
     // only the tensor-core kernel uses scratch; shapes it does not cover are rejected
-    const int which = kkt_select_kernel(dk, dv, C, KKT_IO_BF16, KKT_KERNEL_TC);
-    if (which < 0) return -which;
-    if (!aligned_to(k, 16) || !aligned_to(v, 16) || !aligned_to(T_out, 16) || !aligned_to(W_out, 16) ||
-        !aligned_to(U_out, 16) || !aligned_to(beta, 4) || (cu_seqlens && !aligned_to(cu_seqlens, 4)))
-        return KKT_ERR_ALIGN;
-    const int64_t ntok = cu_seqlens ? (int64_t)T : (int64_t)B * T;
-    if (ntok == 0) return KKT_OK;
-    if (ntok / C + B > 0x7fffffffLL) return KKT_ERR_ARG;
-    if (kNoallocNeed > KKT_NOALLOC_SCRATCH_BYTES) return KKT_ERR_ARG;  // the problem would need more scratch
-
     kkt::Problem p;
-    p.k = k; p.v = v; p.beta = beta; p.cu_seqlens = cu_seqlens;
-    p.nseq = B; p.T = T; p.ntok = ntok;
-    p.H = H; p.dk = dk; p.dv = dv; p.C = C;
-    p.T_out = T_out; p.W_out = W_out; p.U_out = U_out;
-    p.io = KKT_IO_BF16;
-    p.stream = reinterpret_cast<cudaStream_t>(stream);
-    p.trace = nullptr;
-    int st = kkt::status_ptr(&p.status);
-    if (st != KKT_OK) return st;
+    int which = 0;
+    bool empty = false;
+    int st = kkt::make_problem(k, v, beta, nullptr, cu_seqlens, B, T, H, dk, dv, C, T_out, W_out, U_out,
+                               KKT_IO_BF16, KKT_KERNEL_TC, stream, &p, &which, &empty);
+    if (st != KKT_OK || empty) return st;
     st = noalloc_scratch(&p.tile_counter);
     if (st != KKT_OK) return st;
-    // the counters start at zero: zero-initialised with the module, and cleared by the last CTA of
-    // every earlier call
+    // Clear the counters on the stream before the launch.  Each kernel's last CTA also leaves them
+    // zero, but a call that overlapped another one on the GPU, or whose kernel gave up on a timeout,
+    // may not have; the clear keeps such a call from spoiling the calls after it.
+    if (cudaMemsetAsync(p.tile_counter, 0, kNoallocNeed, p.stream) != cudaSuccess) return KKT_ERR_CUDA;
     return kkt::launch_tc(p);
+}
+
+// Test hook (kkt_test.h): the first two 64-bit words of the scratch array on the current device.
+extern "C" int kkt_test_noalloc_scratch(unsigned long long *out2) {
+    if (!out2) return KKT_ERR_ARG;
+    if (cudaMemcpyFromSymbol(out2, g_noalloc_scratch, kNoallocNeed) != cudaSuccess) return KKT_ERR_CUDA;
+    return KKT_OK;
 }

@@ -180,16 +180,18 @@ int kkt_solve_fwd_gated(const void *k, const void *v, const float *beta, const f
  *
  *   Arguments, layouts, ownership and errors: as kkt_solve_fwd (bf16 I/O), run
  *   on the tensor-core kernel only, which covers every shape kkt_solve_fwd
- *   accepts (bf16; other shapes return KKT_ERR_UNSUPPORTED); a problem that would
- *   need more scratch than the array holds returns KKT_ERR_ARG (a call needs
- *   16 bytes, two 64-bit counters, whatever the problem size; the array is zero
- *   when the library loads and every call leaves it zero).
+ *   accepts (bf16; other shapes return KKT_ERR_UNSUPPORTED).  The scratch a call
+ *   needs does not grow with the problem: 16 bytes (two 64-bit counters) of the
+ *   array, for every problem size, so no size is rejected for want of scratch.
  *   The first call on a device looks up the array's device address (with that
  *   device current); make that first call before any stream capture.
- *   Every call shares the array and resets the counter on `stream` before its
- *   launch; calls whose work overlaps on the GPU (other streams, other host
- *   threads) race on it and must be serialised by the caller.
- */
+ *   Every call shares the array.  Each call clears the 16 bytes on `stream`
+ *   (cudaMemsetAsync, which allocates nothing) before its launch, and its kernel
+ *   leaves them zero when it ends.  Calls whose work overlaps on the GPU (other
+ *   streams, other host threads) race on the counters, which can leave tiles of
+ *   the overlapping calls uncomputed; the caller must serialise such calls.  The
+ *   clear keeps a raced or timed-out call from affecting later calls.
+  */
 int kkt_solve_fwd_noalloc(const void *k, const void *v, const float *beta, const int32_t *cu_seqlens,
                           int B, int T, int H, int dk, int dv, int C,
                           float *T_out, void *W_out, void *U_out, struct CUstream_st *stream);

@@ -48,6 +48,13 @@ int kkt_test_stalled_solve(const void *k, const void *v, const float *beta, cons
  */
 int kkt_debug_bounds(unsigned long long *first, int *kind);
 
+/*
+ * kkt_test_noalloc_scratch -- copies the two 64-bit counters at the start of the scratch array
+ * of kkt_solve_fwd_noalloc (current device) to out2[0..1], synchronously.  Tests use it to check
+ * that every call leaves the counters zero.  Returns KKT_OK, KKT_ERR_ARG or KKT_ERR_CUDA.
+ */
+int kkt_test_noalloc_scratch(unsigned long long *out2);
+
 #ifdef __cplusplus
 }
 #endif

@@ -76,3 +76,74 @@ def to64(t: torch.Tensor) -> np.ndarray:
 def relfro(a, b) -> float:
     d = np.linalg.norm(b)
     return float(np.linalg.norm(a - b) / d) if d > 0 else math.inf
+
+
+class FullComparison:
+    """Whole-tensor comparison of T, W and U~ with the oracle, accumulated slab by slab.
+
+    A slab is a group of whole sequences; the oracle runs on each slab on its own (its chunks never
+    cross a sequence start, so that is the oracle of the whole batch), and the library's outputs
+    for the slab are compared with it element by element under the tolerances above.  The relative
+    Frobenius error is accumulated over the whole tensor.  ``n_large`` counts the W / U~ elements
+    with |x_ref| >= 8, whose bound is widened by half a bf16 ulp.
+    """
+
+    def __init__(self, io: str = "bf16"):
+        self.io = io
+        self.T_max = 0.0
+        self.stats = {n: {"max_abs": 0.0, "err2": 0.0, "ref2": 0.0, "n_large": 0, "n": 0} for n in ("W", "U")}
+
+    def add(self, T_gpu, W_gpu, U_gpu, T_ref, W_ref, U_ref):
+        if T_gpu is not None:
+            self.T_max = max(self.T_max, check_T(T_gpu, T_ref))
+        for name, X, R in (("W", W_gpu, W_ref), ("U", U_gpu, U_ref)):
+            X = X.astype(np.float64)
+            assert not np.isnan(X).any(), f"{name}: NaN"
+            err = np.abs(X - R)
+            st = self.stats[name]
+            st["n"] += err.size
+            st["err2"] += float(np.square(X - R).sum())
+            st["ref2"] += float(np.square(R).sum())
+            if self.io == "f32":
+                m = float(err.max()) if err.size else 0.0
+                assert m <= WU_ATOL_F32, f"{name}: max abs error {m:.3e} > {WU_ATOL_F32}"
+                st["max_abs"] = max(st["max_abs"], m)
+                continue
+            big = np.abs(R) >= 8.0
+            small_max = float(err[~big].max()) if (~big).any() else 0.0
+            assert small_max <= WU_ATOL_BF16, f"{name}: max abs error {small_max:.3e} > {WU_ATOL_BF16}"
+            if big.any():
+                lim = WU_ATOL_BF16 + _half_ulp_bf16(R[big])
+                assert np.all(err[big] <= lim), f"{name}: error above bf16 resolution at |x| >= 8"
+                st["max_abs"] = max(st["max_abs"], float(err[big].max()))
+            st["max_abs"] = max(st["max_abs"], small_max)
+            st["n_large"] += int(big.sum())
+
+    def finish(self) -> dict:
+        out = {"T_max_abs": self.T_max}
+        for name, st in self.stats.items():
+            rel = math.sqrt(st["err2"] / st["ref2"]) if st["ref2"] > 0 else math.sqrt(st["err2"])
+            if self.io != "f32":
+                assert rel <= WU_RELFRO_BF16, f"{name}: relative Frobenius error {rel:.3e} > {WU_RELFRO_BF16}"
+            out[f"{name}_max_abs"] = st["max_abs"]
+            out[f"{name}_rel_fro"] = rel
+            out[f"{name}_n_large"] = st["n_large"]
+            out[f"{name}_elements"] = st["n"]
+        return out
+
+
+def slabs(B: int, T: int, cu_seqlens=None, max_tokens: int = 16384):
+    """Groups of whole sequences [(n0, n1, cu_rel or None)] on the flat token axis, each of about
+    ``max_tokens`` tokens or one sequence."""
+    if cu_seqlens is None:
+        per = max(1, max_tokens // max(T, 1))
+        return [(b * T, min(B, b + per) * T, None) for b in range(0, B, per)]
+    cu = [int(x) for x in cu_seqlens]
+    out, s = [], 0
+    while s < len(cu) - 1:
+        e = s + 1
+        while e < len(cu) - 1 and cu[e + 1] - cu[s] <= max_tokens:
+            e += 1
+        out.append((cu[s], cu[e], np.asarray([c - cu[s] for c in cu[s:e + 1]], dtype=np.int64)))
+        s = e
+    return out

@@ -1,9 +1,8 @@
 """CUDA path against the fp64 oracle, element by element (GPU).
 
-Every call goes through the C ABI (libkkt.so via the ctypes binding).  Small
-cases are compared in full; the full-size workloads are compared on sampled
-(chunk, head) units that the oracle computes one by one, plus properties that
-hold at any size (no NaN, unit diagonal, zero upper triangle, zero padding).
+Every call goes through the C ABI (libkkt.so via the ctypes binding).  These are
+the small and edge cases, compared in full; the full-size workloads are compared
+element by element in tests/test_full_size_gpu.py.
 """
 import numpy as np
 import pytest
@@ -60,6 +59,52 @@ def full_compare(k, v, beta, C, cu, outs, io="bf16", g=None):
     check_WU(W_g, W_ref, io, "W")
     check_WU(U_g, U_ref, io, "U")
     return T_g, T_ref
+
+
+# --- the spec entry point itself ------------------------------------------------------
+
+def _north_star_call(k, v, beta, C, cu=None):
+    """kkt_solve_fwd through ctypes: bf16, kernel auto, no workspace (the fixed round-robin
+    schedule of the tensor-core kernel)."""
+    Bt, T, H, dk = k.shape
+    dv = v.shape[-1]
+    T_out = torch.full((Bt, T, H, C), float("nan"), device=DEV)
+    W = torch.full((Bt, T, H, dk), float("nan"), device=DEV, dtype=k.dtype)
+    U = torch.full((Bt, T, H, dv), float("nan"), device=DEV, dtype=k.dtype)
+    B = Bt if cu is None else cu.shape[0] - 1
+    rc = _lib.lib().kkt_solve_fwd(k.data_ptr(), v.data_ptr(), beta.data_ptr(),
+                                  None if cu is None else cu.data_ptr(), B, T, H, dk, dv, C,
+                                  T_out.data_ptr(), W.data_ptr(), U.data_ptr(),
+                                  torch.cuda.current_stream().cuda_stream)
+    assert rc == _lib.KKT_OK, _lib.status_string(rc)
+    torch.cuda.synchronize()
+    assert device_status() == 0
+    return T_out, W, U
+
+
+@pytest.mark.parametrize("C", [32, 64, 128])
+@pytest.mark.parametrize("case", ["fixed", "varlen", "many_tiles"])
+def test_north_star_entry_point(case, C):
+    """kkt_solve_fwd, the entry point with the signature the library is specified by, against the
+    oracle element by element, and bit-identical to the kkt_solve_fwd_ex call with a workspace
+    (the dynamic schedule that the Python front end and the bench use by default): a ragged
+    fixed-length batch, a varlen batch with empty and one-token sequences, and a batch with many
+    more tiles than SMs."""
+    cu = None
+    if case == "fixed":
+        k, v, beta = make_inputs(3, 1000, 5, 128, 128, seed=101 + C, device=DEV)
+    elif case == "varlen":
+        lengths = [1, 63, 64, 65, 0, 130, 7, 200, 1500]
+        cu = np.concatenate([[0], np.cumsum(lengths)])
+        k, v, beta = make_inputs(1, int(cu[-1]), 6, 128, 128, seed=102 + C, device=DEV)
+    else:
+        k, v, beta = make_inputs(2, 4100, 12, 128, 128, seed=103 + C, device=DEV)
+    cu_t = None if cu is None else torch.as_tensor(cu, dtype=torch.int32, device=DEV)
+    outs = _north_star_call(k, v, beta, C, cu_t)
+    full_compare(k, v, beta, C, cu, outs)
+    dyn = run(k, v, beta, C, cu, kernel="auto", workspace="auto")
+    for a, b in zip(outs, dyn):
+        assert torch.equal(a, b)
 
 
 # --- small cases, compared in full --------------------------------------------------------
@@ -348,88 +393,7 @@ def test_checked_mode_raises_device_errors(monkeypatch):
     assert device_status() == 0
 
 
-# --- full-size workloads, sampled -----------------------------------------------------------
-
-FULL = ["c2_t8192_h16", "c3_b4_t8192_h16", "c3_b4_t8192_h64", "c4_varlen32_h32",
-        "c5_b2_t16384_h24_c32", "c5_b2_t16384_h24_c64", "c5_b2_t16384_h24_c128"]
-
-
-@pytest.mark.parametrize("name", FULL)
-def test_full_size_sampled(name):
-    """Full-size workload in the bench's launch configuration (kernel "auto"); 40 sampled
-    (chunk, head) units against the oracle; whole-tensor structural properties."""
-    w = workloads()[name]
-    k, v, beta, cu = w.make(seed=0, device=DEV)
-    T_out, W, U = run(k, v, beta, w.C, cu)
-    H, C = w.H, w.C
-    flat = lambda x: x.reshape(w.tokens, H, -1)
-    kf, vf, bf = flat(k), flat(v), beta.reshape(w.tokens, H)
-    Tf, Wf, Uf = flat(T_out), flat(W), flat(U)
-    assert not torch.isnan(Tf).any() and not torch.isnan(Wf.float()).any() and not torch.isnan(Uf.float()).any()
-    ch = chunks(C, w.B, w.T, cu)
-    rng = np.random.default_rng(1)
-    picks = [ch[0], ch[-1]] + [ch[i] for i in rng.integers(0, len(ch), 38)]
-    heads = [0, H - 1] + list(rng.integers(0, H, 38))
-    for (t0, Lc), h in zip(picks, heads):
-        h = int(h)
-        Tr, Wr, Ur, _ = oracle.oracle_chunk(to64(kf[t0:t0 + Lc, h]), to64(vf[t0:t0 + Lc, h]),
-                                            to64(bf[t0:t0 + Lc, h]), C)
-        check_T(to64(Tf[t0:t0 + Lc, h]), Tr)
-        check_WU(to64(Wf[t0:t0 + Lc, h]), Wr, "bf16", "W")
-        check_WU(to64(Uf[t0:t0 + Lc, h]), Ur, "bf16", "U")
-    # unit diagonal and zero upper triangle of every chunk, at full size
-    idx = torch.arange(w.tokens, device=DEV)
-    starts = torch.zeros(w.tokens, dtype=torch.long, device=DEV)
-    for t0, Lc in ch:
-        starts[t0:t0 + Lc] = t0
-    row = (idx - starts).reshape(-1, 1, 1)
-    col = torch.arange(C, device=DEV).reshape(1, 1, C)
-    assert torch.all(Tf[(col == row).expand_as(Tf)] == 1.0)
-    assert torch.all(Tf[(col > row).expand_as(Tf)] == 0.0)
-
-
-@pytest.mark.parametrize("name", ["c3_b4_t8192_h16", "c4_varlen32_h32", "c5_b2_t16384_h24_c128"])
-def test_gated_full_size(name):
-    """The gated variant at full size, in the bench's launch configuration: 24 sampled (chunk, head)
-    units against the oracle, and over the whole tensor the similarity that holds for any gate,
-    T = Gamma o T0 with T0 the ungated call's T (each within 1e-4 of the exact value, Gamma <= 1)."""
-    w = workloads()[name]
-    k, v, beta, cu = w.make(seed=0, device=DEV)
-    g = make_gate(k.shape[0], k.shape[1], w.H, seed=0, device=DEV)
-    Tg, Wg, Ug = run(k, v, beta, w.C, cu, g=g)
-    T0, _, _ = run(k, v, beta, w.C, cu)
-    H, C = w.H, w.C
-    flat = lambda x: x.reshape(w.tokens, H, -1)
-    kf, vf, bf, gf = flat(k), flat(v), beta.reshape(w.tokens, H), g.reshape(w.tokens, H)
-    Tgf, Wgf, Ugf, T0f = flat(Tg), flat(Wg), flat(Ug), flat(T0)
-    ch = chunks(C, w.B, w.T, cu)
-    rng = np.random.default_rng(2)
-    picks = [ch[0], ch[-1]] + [ch[i] for i in rng.integers(0, len(ch), 22)]
-    heads = [0, H - 1] + list(rng.integers(0, H, 22))
-    for (t0, Lc), h in zip(picks, heads):
-        h = int(h)
-        Tr, Wr, Ur, _ = oracle.oracle_chunk(to64(kf[t0:t0 + Lc, h]), to64(vf[t0:t0 + Lc, h]),
-                                            to64(bf[t0:t0 + Lc, h]), C, g=to64(gf[t0:t0 + Lc, h]))
-        check_T(to64(Tgf[t0:t0 + Lc, h]), Tr)
-        check_WU(to64(Wgf[t0:t0 + Lc, h]), Wr, "bf16", "W")
-        check_WU(to64(Ugf[t0:t0 + Lc, h]), Ur, "bf16", "U")
-    # Gamma[t][j] = exp(G_t - G_{t0 + j}) with G the prefix sums of g inside each chunk (fp64)
-    G = torch.zeros((w.tokens, H), dtype=torch.float64, device=DEV)
-    gd = gf.double()
-    for t0, Lc in ch:
-        G[t0:t0 + Lc] = torch.cumsum(gd[t0:t0 + Lc], dim=0)
-    starts = torch.zeros(w.tokens, dtype=torch.long, device=DEV)
-    for t0, Lc in ch:
-        starts[t0:t0 + Lc] = t0
-    col = torch.arange(C, device=DEV)
-    src = (starts.reshape(-1, 1) + col.reshape(1, -1)).clamp_max(w.tokens - 1)  # token of column j
-    Gcol = G[src]                                                               # [N, C, H]
-    gamma = torch.exp(G.reshape(-1, 1, H) - Gcol).permute(0, 2, 1)             # [N, H, C]
-    lower = (col.reshape(1, 1, C) <= (torch.arange(w.tokens, device=DEV) - starts).reshape(-1, 1, 1))
-    expect = torch.where(lower, T0f.double() * gamma, torch.zeros_like(gamma))
-    assert torch.all(torch.isfinite(Tgf))
-    err = (Tgf.double() - expect).abs().max().item()
-    assert err <= 2e-4, err
+# (full-size workloads: every element, tests/test_full_size_gpu.py)
 
 
 @pytest.mark.parametrize("kernel", ALL_KERNELS)
