@@ -31,10 +31,18 @@
  *   section; its decay alpha_t = exp(g_t) lies in (0, 1), "Gate 衰减性质"
  *   section).  Gamma[i][j] is the decay from token j to token i of the same
  *   chunk, the product of alpha_t over j < t <= i, computed as
- *   exp(sum_{t=j+1..i} g_t).  Only the coefficient changes: step 1 becomes
+ *   exp(sum_{t=j+1..i} g_t).  Step 1 becomes
  *          A = I + strictLower(diag(beta)(Gamma o K K^T)),
- *   steps 2 and 3 are as above (the page states no other change).  The gate
- *   restarts at every chunk: Gamma involves only tokens of the chunk.
+ *   step 2 is as above, and in step 3 the keys carry the decay from the
+ *   chunk's start through their own token, gamma_j = exp(g_0 + ... + g_j)
+ *   (token 0 being the chunk's first):
+ *          W = T diag(beta) diag(gamma) K,    U~ = T diag(beta) V.
+ *   The decay in W is what the gated delta rule needs downstream: the state
+ *   the chunk starts from reaches token j's update decayed by gamma_j, so the
+ *   chunk's correction of that state is W S (see gdn_oracle.c, which pins the
+ *   chunkwise form against the token-by-token recurrence).  With g = 0 every
+ *   gamma_j is 1 and W is the ungated one.  The gate restarts at every chunk:
+ *   Gamma and gamma involve only tokens of the chunk.
  *
  *   Output layout (the CUDA library's layout, fixed by its C header):
  *     T_out[n][h][0..C)  row n holds row (n - chunk start) of its chunk's T,
@@ -106,15 +114,31 @@ static void invert_unit_lower(const double *A, int C, double *X)
     }
 }
 
-/* Step 3: rows of Y = T diag(beta) M for M = K (width dk) or V (width dv). */
-static void apply_scaled(const double *X, const double *bc, const double *mc,
+/* gamma_j: the gate's decay from the chunk's start through token j, exp of the
+ * sum of the log decays of tokens 0 .. j. */
+static double decay_from_start(const double *gc, int j)
+{
+    double acc = 0.0;
+    for (int t = 0; t <= j; ++t)
+        acc += gc[t];
+    return exp(acc);
+}
+
+/* Step 3: rows of Y = T diag(beta) M for M = V (width dv), or for M = K
+ * (width dk) Y = T diag(beta) diag(gamma) K when the chunk has a gate (gc:
+ * its log decays; NULL for V and for ungated chunks). */
+static void apply_scaled(const double *X, const double *bc, const double *gc, const double *mc,
                          int Lc, int C, int width, double *out)
 {
     for (int i = 0; i < Lc; ++i) {
         for (int e = 0; e < width; ++e) {
             double s = 0.0;
-            for (int j = 0; j < Lc; ++j)
-                s += X[(int64_t)i * C + j] * bc[j] * mc[(int64_t)j * width + e];
+            for (int j = 0; j < Lc; ++j) {
+                double f = bc[j];
+                if (gc)
+                    f *= decay_from_start(gc, j);
+                s += X[(int64_t)i * C + j] * f * mc[(int64_t)j * width + e];
+            }
             out[(int64_t)i * width + e] = s;
         }
     }
@@ -147,8 +171,8 @@ int kkt_oracle_chunk(const double *kc, const double *vc, const double *bc,
     for (int i = 0; i < Lc; ++i)
         for (int j = 0; j < C; ++j)
             T[(int64_t)i * C + j] = (j < Lc) ? X[(int64_t)i * C + j] : 0.0;
-    apply_scaled(X, bz, kc, Lc, C, dk, W);
-    apply_scaled(X, bz, vc, Lc, C, dv, U);
+    apply_scaled(X, bz, gc, kc, Lc, C, dk, W);
+    apply_scaled(X, bz, NULL, vc, Lc, C, dv, U);
     if (A_out)
         memcpy(A_out, A, sizeof(double) * (size_t)C * C);
     free(A); free(X); free(bz);

@@ -14,7 +14,8 @@ and raises AssertionError when the oracle disagrees with:
   * the page's measured cond(A) bounds,
   * the gated coefficient diag(beta)(Gamma o K K^T) (§5 item 12): no decay is the
     ungated oracle; the page's two differently scaled copies of K; any gate is a
-    diagonal similarity of the ungated matrix, so T = Gamma o T0; a token with zero
+    diagonal similarity of the ungated matrix, so T = Gamma o T0 and W = diag(e^G) W0
+    (the keys of W carry the decay from the chunk's start); a token with zero
     decay cuts the chunk into independent blocks; the tensor layout of the gate.
 Sources: "TileLang 实战：单位下三角矩阵求逆" §1, §2.1, §2.2, §2.4, §3.2, §4, §5.
 """
@@ -315,18 +316,22 @@ def pin_gate_two_scaled_keys(lib):
 def pin_gate_similarity(lib):
     """Gamma[i][j] = e^{G_i - G_j} makes the gated A a diagonal similarity of the ungated one,
     A = D A0 D^-1 with D = diag(e^{G_i}), so T = D T0 D^-1: T[i][j] = e^{G_i - G_j} T0[i][j] with T0
-    the ungated inverse, for any gate (a constant one, e^{c (i - j)}, and a random one)."""
+    the ungated inverse, for any gate (a constant one, e^{c (i - j)}, and a random one).  The keys
+    of W carry the decay from the chunk's start, gamma = e^G, so W = T diag(beta gamma) K, which by
+    the same similarity is D T0 diag(beta) K = diag(gamma) W0 with W0 the ungated W; U~ =
+    T diag(beta) V."""
     rng = np.random.default_rng(32)
     Lc, C = 48, 64
     k, v, beta = _rand_chunk(rng, Lc, 32, 16)
-    T0, _, _, _ = oracle.oracle_chunk(k, v, beta, C, lib=lib)
+    T0, W0, _, _ = oracle.oracle_chunk(k, v, beta, C, lib=lib)
     for g in (np.full(Lc, -0.15), rng.uniform(-0.4, 0.0, Lc)):
         T, W, U, _ = oracle.oracle_chunk(k, v, beta, C, lib=lib, g=g)
         G = np.cumsum(g)
         expect = T0[:, :Lc] * np.exp(G[:, None] - G[None, :])
         np.testing.assert_allclose(T[:, :Lc], expect, atol=1e-13, rtol=0)
         assert np.all(T[:, Lc:] == 0.0)
-        np.testing.assert_allclose(W, expect @ (beta[:, None] * k), atol=1e-12, rtol=0)
+        np.testing.assert_allclose(W, expect @ ((beta * np.exp(G))[:, None] * k), atol=1e-12, rtol=0)
+        np.testing.assert_allclose(W, np.exp(G)[:, None] * W0, atol=1e-12, rtol=0)
         np.testing.assert_allclose(U, expect @ (beta[:, None] * v), atol=1e-12, rtol=0)
 
 

@@ -20,8 +20,8 @@ MUTATIONS = {
     "diagonal_keeps_beta": ("a = 1.0;", "a = 1.0 + bc[i];"),
     "substitution_sign": ("xr[c] -= arj * xj[c];", "xr[c] += arj * xj[c];"),
     "dropped_first_term": ("for (int j = 0; j < r; ++j) {", "for (int j = 1; j < r; ++j) {"),
-    "transposed_T_in_products": ("s += X[(int64_t)i * C + j] * bc[j]", "s += X[(int64_t)j * C + i] * bc[j]"),
-    "beta_dropped_in_products": ("* bc[j] * mc[", "* mc["),
+    "transposed_T_in_products": ("s += X[(int64_t)i * C + j] * f", "s += X[(int64_t)j * C + i] * f"),
+    "beta_dropped_in_products": ("double f = bc[j];", "double f = 1.0;"),
     "gram_wrong_row": ("kc[(int64_t)i * dk + d] * kc[(int64_t)j * dk + d]",
                        "kc[(int64_t)i * dk + d] * kc[(int64_t)i * dk + d]"),
     "beta_wrong_head": ("bc[i] = beta[n * H + h];", "bc[i] = beta[n * H + (H - 1 - h)];"),
@@ -33,6 +33,11 @@ MUTATIONS = {
     "gate_sign": ("return exp(s);", "return exp(-s);"),
     "gate_wrong_head": ("gc[i] = g[n * H + h];", "gc[i] = g[n * H + (H - 1 - h)];"),
     "gate_ignored": ("a *= gate_decay(gc, j, i);", "a *= 1.0;"),
+    # the decay the keys of W carry from the chunk's start
+    "w_decay_ignored": ("f *= decay_from_start(gc, j);", "f *= 1.0;"),
+    "w_decay_excludes_own_token": ("for (int t = 0; t <= j; ++t)", "for (int t = 0; t < j; ++t)"),
+    "w_decay_on_values_too": ("apply_scaled(X, bz, NULL, vc, Lc, C, dv, U);", "apply_scaled(X, bz, gc, vc, Lc, C, dv, U);"),
+    "w_decay_sign": ("return exp(acc);", "return exp(-acc);"),
 }
 
 
