@@ -174,10 +174,18 @@ __global__ void __launch_bounds__(kSimtThreads) kkt_simt_kernel(const SimtParams
     }
     __syncthreads();
 
-    // 6. T~ = T diag(beta), in place
+    // 6. T~ = T diag(beta), in place.  Gated: the keys of W carry the decay from the chunk's start
+    //    through their own token, W = T diag(beta) diag(e^G) K, so K's rows are scaled by e^{G_j}
+    //    (the Gram no longer needs them)
     for (int e = tid; e < C * C; e += kSimtThreads) {
         const int i = e / C, j = e % C;
         T_(i * TS + j) *= B_(j);
+    }
+    if (p.g) {
+        for (int e = tid; e < C * DK; e += kSimtThreads) {
+            const int j = e / DK, d = e - (e / DK) * DK;
+            K_(j * KS + d) *= expf(G_(j));
+        }
     }
     __syncthreads();
 

@@ -121,6 +121,8 @@ struct Barriers {
     uint64_t mma_final, gram_final;
     uint64_t pair_sync[2];   // warps 2p and 2p + 1: one 64-row block (C = 64, 128)
     uint64_t quad_sync;      // all four inverse warps (C = 128)
+    uint64_t kread[kNS];     // gated: the Gram MMA of the stage's tile has read its K
+    uint64_t kscaled;        // gated: the epilogue warps have scaled the tile's K rows for W
     TileInfo einfo[2];       // tile info for the epilogue warps, written by the W|U warp
     uint32_t tmem_base;
     int abort_flag;
@@ -242,6 +244,13 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
         : "=f"(d.x), "=f"(d.y)
         : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
     return d;
+}
+
+// A bf16 pair times a pair of factors, rounded back to a bf16 pair (one rounding per element).
+__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t w, float2 f) {
+    const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w));
+    const float2 y = fmul2(x, f);
+    return pack_bf16(y.x, y.y);
 }
 
 // Packed fp32 FMA on a pair (one f32x2 instruction): a * b + c, elementwise.
@@ -535,6 +544,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->pair_sync[0], 64);
         mbar_init(&bars->pair_sync[1], 64);
         mbar_init(&bars->quad_sync, 128);
+        mbar_init(&bars->kread[0], 1);
+        mbar_init(&bars->kread[1], 1);
+        mbar_init(&bars->kscaled, 4);
         bars->abort_flag = 0;
         fence_mbar_init();
     }
@@ -732,6 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_ss(tmem + kColGram, d, d, idesc_gram, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&bars->gram_full);
+                if constexpr (GATED) mma_commit(&bars->kread[s]);
                 KKT_TRACE_EVENT(EV_M_GRAM, i);
             }
             __syncwarp();
@@ -763,6 +776,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!wait_bar(&bars->tt_full, (uint32_t)i & 1u, bars, p.status)) break;
             if (!wait_bar(&bars->d_empty, ((uint32_t)i & 1u) ^ 1u, bars, p.status)) break;
+            if constexpr (GATED) {
+                if (!wait_bar(&bars->kscaled, (uint32_t)i & 1u, bars, p.status)) break;
+            }
             if (lane == 0) {
                 KKT_TRACE_EVENT(EV_M_READY, i);
                 bars->einfo[i & 1] = info;
@@ -1125,7 +1141,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t *wstage = smem + CF::OFF_WU + q * CF::WU_BUFS * 4096;  // WU_BUFS x [32 rows][128 B]
         int i = 0;
         uint32_t nstore = 0;  // TMA store groups issued by this warp
+        bool keys_done = false;  // gated: the stage that ends the work has been seen
         while (true) {
+            if constexpr (GATED) {
+                // The keys of W carry the gate's decay from the chunk's start through their own token,
+                // W = T diag(beta) diag(gamma) K with gamma_j = exp2(G_j) (G the prefix sums the
+                // producer left in the stage, log2 units).  Once the Gram MMA has read the stage's K,
+                // each thread scales its row of K in place (bf16, rounded to nearest; the Gram used
+                // the unscaled keys), before the W|U MMA of the tile reads it.  A row's 16-byte chunks
+                // are visited in swizzled order, so the 8 rows of a quarter-warp hit 8 different bank
+                // groups.
+                if (!keys_done) {
+                    const int s = i % kNS;
+                    if (!wait_bar(&bars->full[s], (uint32_t)(i / kNS) & 1u, bars, p.status)) break;
+                    if (stage_info(s)->done) {
+                        keys_done = true;
+                    } else {
+                        if (!wait_bar(&bars->kread[s], (uint32_t)(i / kNS) & 1u, bars, p.status)) break;
+                        const int m = 32 * q + lane;
+                        const float gam = exp2f(*smem_chk(stage_gate(s) + m));
+                        const float2 gg = make_float2(gam, gam);
+                        uint8_t *row = stage_kv(s) + m * 128;
+#pragma unroll
+                        for (int c2 = 0; c2 < CF::NBK; ++c2) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                uint4 *pv = smem_chk(reinterpret_cast<uint4 *>(row + c2 * 16384 + ((e ^ (m & 7)) << 4)));
+                                uint4 x = *pv;
+                                x.x = scale_bf16x2(x.x, gg);
+                                x.y = scale_bf16x2(x.y, gg);
+                                x.z = scale_bf16x2(x.z, gg);
+                                x.w = scale_bf16x2(x.w, gg);
+                                *pv = x;
+                            }
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bars->kscaled);
+                    }
+                }
+            }
             if (!wait_bar(&bars->einfo_full[i & 1], (uint32_t)(i >> 1) & 1u, bars, p.status)) break;
             const TileInfo info = bars->einfo[i & 1];
             if (info.done) break;
