@@ -42,6 +42,8 @@ SIGNATURES = {
     "kkt_solve_fwd_gated": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _i, _i, _vp, _sz,
                                  _vp]),
     "kkt_solve_fwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
+    "gdn_chunk_state_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, ctypes.c_float, _vp,
+                                 _vp, _vp]),
     "kkt_test_stalled_solve": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
     "kkt_test_noalloc_scratch": (_i, [_vp]),
     "kkt_device_status": (_i, [_vp]),

@@ -140,6 +140,76 @@ def kkt_solve_fwd(k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor, C: int,
     return T_out, W_out, U_out
 
 
+def gdn_chunk_state_fwd(q: torch.Tensor, k: torch.Tensor, w: torch.Tensor, u: torch.Tensor, C: int = 64, *,
+                        g: torch.Tensor | None = None, initial_state: torch.Tensor | None = None, scale=None,
+                        cu_seqlens: torch.Tensor | None = None, output_final_state: bool = True, o=None,
+                        final_state=None, stream=None, check: bool | None = None):
+    """The chunk state recurrence and output that consume kkt_solve's W and U~: returns (o, final_state).
+
+    q, k, w [B, T, H, dk] and u [B, T, H, dv] bf16 (w, u: the W and U of ``kkt_solve_fwd`` on the same k,
+    beta, g, cu_seqlens and C); ``g`` [B, T, H] fp32 log decays or None; ``initial_state`` [N, H, dk, dv]
+    fp32 or None (zero), N the number of sequences; ``scale`` defaults to dk ** -0.5.  o is [B, T, H, dv]
+    bf16; final_state [N, H, dk, dv] fp32, or None when ``output_final_state`` is False.  The recurrence
+    is S_t = alpha_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T, o_t = scale S_t^T q_t, with
+    alpha_t = exp(g_t); the library computes it chunk by chunk (see include/kkt.h).
+    """
+    if q.dim() != 4 or k.dim() != 4 or w.dim() != 4 or u.dim() != 4:
+        raise ValueError("expected q, k, w [B,T,H,dk] and u [B,T,H,dv]")
+    Bt, T, H, dk = k.shape
+    dv = u.shape[-1]
+    for name, x, d in (("q", q, dk), ("k", k, dk), ("w", w, dk), ("u", u, dv)):
+        _check(x, name, torch.bfloat16, (Bt, T, H, d))
+    if g is not None:
+        _check(g, "g", torch.float32, (Bt, T, H))
+    if cu_seqlens is not None:
+        if Bt != 1:
+            raise ValueError("with cu_seqlens the batch dimension must be 1")
+        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda or cu_seqlens.dim() != 1:
+            raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor")
+        N, cu_ptr = cu_seqlens.shape[0] - 1, cu_seqlens.data_ptr()
+    else:
+        N, cu_ptr = Bt, None
+    dev = k.device
+    if initial_state is not None:
+        _check(initial_state, "initial_state", torch.float32, (N, H, dk, dv))
+    if o is None:
+        o = torch.empty((Bt, T, H, dv), device=dev, dtype=torch.bfloat16)
+    _check(o, "o", torch.bfloat16, (Bt, T, H, dv))
+    if output_final_state:
+        if final_state is None:
+            final_state = torch.empty((N, H, dk, dv), device=dev, dtype=torch.float32)
+        _check(final_state, "final_state", torch.float32, (N, H, dk, dv))
+    else:
+        final_state = None
+    if scale is None:
+        scale = dk ** -0.5
+    rc = _lib.lib().gdn_chunk_state_fwd(q.data_ptr(), k.data_ptr(), w.data_ptr(), u.data_ptr(),
+                                        None if g is None else g.data_ptr(),
+                                        None if initial_state is None else initial_state.data_ptr(), cu_ptr,
+                                        N, T, H, dk, dv, C, float(scale), o.data_ptr(),
+                                        None if final_state is None else final_state.data_ptr(),
+                                        _stream_handle(stream))
+    if rc != _lib.KKT_OK:
+        raise _lib.KktError(rc, "gdn_chunk_state_fwd")
+    if check is None:
+        check = os.environ.get("KKT_CHECK", "0") == "1"
+    if check:
+        st = device_status(stream)
+        if st != _lib.KKT_OK:
+            raise _lib.KktError(st, "gdn_chunk_state_fwd (device)")
+    return o, final_state
+
+
+def chunk_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None, output_final_state: bool = False,
+                           cu_seqlens=None, *, C: int = 64, stream=None):
+    """The forward pass of Gated DeltaNet chunked prefill, in the argument order of the FlashQLA API:
+    kkt_solve (W and U~ only, T not written) then the chunk state recurrence and output.  ``g`` may
+    be None (the ungated delta rule).  Returns (o, final_state or None)."""
+    _, W, U = kkt_solve_fwd(k, v, beta, C, cu_seqlens, materialize_T=False, g=g, stream=stream)
+    return gdn_chunk_state_fwd(q, k, W, U, C, g=g, initial_state=initial_state, scale=scale, cu_seqlens=cu_seqlens,
+                               output_final_state=output_final_state, stream=stream)
+
+
 def device_status(stream=None) -> int:
     """Synchronises the stream and returns (and clears) the device status word."""
     return int(_lib.lib().kkt_device_status(_stream_handle(stream)))

@@ -61,6 +61,7 @@
 #include "kkt_debug.cuh"
 #include "kkt_internal.cuh"
 #include "sm100_ptx.cuh"
+#include "tma_host.cuh"
 
 namespace kkt {
 namespace {
@@ -1162,18 +1163,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float gam = exp2f(*smem_chk(stage_gate(s) + m));
                         const float2 gg = make_float2(gam, gam);
                         uint8_t *row = stage_kv(s) + m * 128;
-#pragma unroll
-                        for (int c2 = 0; c2 < CF::NBK; ++c2) {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                uint4 *pv = smem_chk(reinterpret_cast<uint4 *>(row + c2 * 16384 + ((e ^ (m & 7)) << 4)));
-                                uint4 x = *pv;
-                                x.x = scale_bf16x2(x.x, gg);
-                                x.y = scale_bf16x2(x.y, gg);
-                                x.z = scale_bf16x2(x.z, gg);
-                                x.w = scale_bf16x2(x.w, gg);
-                                *pv = x;
-                            }
+                        // a loop, not unrolled: the kernel is sensitive to its code size
+#pragma unroll 1
+                        for (int ce = 0; ce < 8 * CF::NBK; ++ce) {
+                            uint4 *pv = smem_chk(reinterpret_cast<uint4 *>(row + (ce >> 3) * 16384 + (((ce & 7) ^ (m & 7)) << 4)));
+                            uint4 x = *pv;
+                            x.x = scale_bf16x2(x.x, gg);
+                            x.y = scale_bf16x2(x.y, gg);
+                            x.z = scale_bf16x2(x.z, gg);
+                            x.w = scale_bf16x2(x.w, gg);
+                            *pv = x;
                         }
                         fence_proxy_async_smem();
                         __syncwarp();
@@ -1252,44 +1251,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------------------------------------
 // host side
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
-    return fn;
-}
-
-// [ntok][H][inner] row-major, box {box_inner, 1, rows}, 128-byte swizzle.
-bool make_map(CUtensorMap *map, CUtensorMapDataType dt, int esize, const void *ptr, int64_t ntok, int H, int inner,
-              int box_inner, int rows) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return false;
-    cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)H, (cuuint64_t)ntok};
-    cuuint64_t strides[2] = {(cuuint64_t)inner * esize, (cuuint64_t)H * inner * esize};
-    cuuint32_t box[3] = {(cuuint32_t)box_inner, 1u, (cuuint32_t)rows};
-    cuuint32_t es[3] = {1u, 1u, 1u};
-    return enc(map, dt, 3, const_cast<void *>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-int sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    return n;
-}
 
 template <int C, int DK, int DV>
 int launch_tc_t(const Problem &pb) {

@@ -15,6 +15,8 @@ stand in for that data):
   * g (gated variant only): log sigmoid(N(2.5, 1)) in fp32, a per-token log decay with
     alpha = exp(g) in (0, 1) (the FlashQLA page's gate, "Gate 衰减性质" section), mean decay
     about 0.9 per token, so that Gamma falls to about e^-6 across a 64-token chunk.
+  * q (the chunk recurrence): rows ~ N(0, 1), L2-normalised like K, rounded to bf16;
+  * initial state (the chunk recurrence): N(0, 1) / sqrt(d_k) in fp32.
 Variable-length batches draw 32 lengths uniform in [100, 8192] with
 ``numpy.random.default_rng(1234)``.
 """
@@ -44,6 +46,21 @@ def make_gate(B: int, T: int, H: int, *, seed: int = 0, device="cpu"):
     gen.manual_seed(seed + 7919)
     x = torch.randn((B, T, H), generator=gen, device=device, dtype=torch.float32) + 2.5
     return torch.nn.functional.logsigmoid(x).contiguous()
+
+
+def make_query(B: int, T: int, H: int, dk: int, *, seed: int = 0, device="cpu"):
+    """q [B,T,H,dk] bf16: rows ~ N(0, 1), L2-normalised like the keys (the recurrence's queries)."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed + 104729)
+    q = torch.randn((B, T, H, dk), generator=gen, device=device, dtype=torch.float32)
+    return (q / q.norm(dim=-1, keepdim=True).clamp_min(1e-12)).to(torch.bfloat16).contiguous()
+
+
+def make_state(N: int, H: int, dk: int, dv: int, *, seed: int = 0, device="cpu"):
+    """An initial state [N,H,dk,dv] fp32: N(0, 1) / sqrt(dk), about the size the recurrence keeps."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed + 1299709)
+    return (torch.randn((N, H, dk, dv), generator=gen, device=device, dtype=torch.float32) * dk ** -0.5).contiguous()
 
 
 def varlen_lengths(n: int = 32, lo: int = 100, hi: int = 8192, seed: int = 1234) -> np.ndarray:

@@ -197,6 +197,45 @@ int kkt_solve_fwd_noalloc(const void *k, const void *v, const float *beta, const
                           float *T_out, void *W_out, void *U_out, struct CUstream_st *stream);
 
 /*
+ * gdn_chunk_state_fwd -- the chunk state recurrence and output of Gated DeltaNet chunked prefill,
+ * the computation that consumes kkt_solve's W and U~ (the FlashQLA page, section "Tilelang
+ * Warp-Specialized Kernel", forward: V', S and O per chunk; the API's q, k, g, scale,
+ * initial_state and final state, section "使用方式").  The pages' own formula of the recurrence
+ * was lost; the one taken is the gated delta rule,
+ *
+ *   S_t = alpha_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T,   o_t = scale S_t^T q_t,
+ *
+ * alpha_t = exp(g_t) (1 without a gate), S_0 the initial state (zero when NULL), which the call
+ * computes chunk by chunk from W and U~: for a chunk of Lc tokens entered with state S, with
+ * G_i = g_0 + ... + g_i from the chunk's first token and Gamma[i][j] = exp(G_i - G_j),
+ *
+ *   V' = U~ - W S
+ *   O  = scale (diag(e^G) Q S + (Gamma o tril(Q K^T)) V')      (the diagonal included)
+ *   S <- e^{G_{Lc-1}} S + (diag(e^{G_{Lc-1} - G}) K)^T V'.
+ *
+ * The chunks are those of kkt_solve: C tokens, restarting at every sequence start.  W and U~ are
+ * the W_out and U_out of kkt_solve_fwd (ungated, g == NULL here) or kkt_solve_fwd_gated (with the
+ * same g) on the same k, beta, cu_seqlens and C.
+ *
+ *   q, k, w   [B, T, H, dk] bf16       u, o  [B, T, H, dv] bf16 (o: output)
+ *   g         [B, T, H] fp32 per-token log decays (<= 0), or NULL (no gate)
+ *   initial_state, final_state   [nseq, H, dk, dv] fp32 (nseq = B), each may be NULL
+ *   cu_seqlens, B, T, H           as in kkt_solve_fwd
+ *   dk = dv = 128 and C = 64 (other values return KKT_ERR_UNSUPPORTED)
+ *   scale     multiplies o (the FlashQLA API's `scale`; commonly dk^-1/2)
+ *
+ * Precision: the products run on the tensor cores with bf16 operands (S, V' and the masked
+ * Q K^T rounded to bf16) and fp32 accumulation; the state is kept and returned in fp32.
+ * Ownership, alignment (16 B for the bf16 tensors and the states, 4 B for g and cu_seqlens),
+ * asynchrony and errors: as kkt_solve_fwd.  With no tokens the call copies the initial state (or
+ * zero) to final_state.  o rows of padding do not exist: only the tokens' rows are written.
+ */
+int gdn_chunk_state_fwd(const void *q, const void *k, const void *w, const void *u, const float *g,
+                        const float *initial_state, const int32_t *cu_seqlens, int B, int T, int H,
+                        int dk, int dv, int C, float scale, void *o, float *final_state,
+                        struct CUstream_st *stream);
+
+/*
  * kkt_device_status -- synchronises `stream`, then returns and clears the
  * status word of the current device: KKT_OK, or the first device-side error
  * (KKT_ERR_SEQLENS, KKT_ERR_TIMEOUT) recorded since the last call; KKT_ERR_CUDA

@@ -149,4 +149,4 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
 
 def test_ctypes_signature_arity():
     for name, (_, args) in _lib.SIGNATURES.items():
-        assert all(a in (ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t) for a in args), name
+        assert all(a in (ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float) for a in args), name
