@@ -70,6 +70,9 @@ def parse_args():
                     help="capture the K timed steps into one CUDA graph and time its replay")
     ap.add_argument("--gated", action="store_true",
                     help="gated variant: coefficient diag(beta)(Gamma o K K^T) from per-token log decays g")
+    ap.add_argument("--consumer", action="store_true",
+                    help="also time the chunk state recurrence and output (gdn_chunk_state_fwd) that consumes "
+                         "W and U~ on the same workload, and the two calls back to back")
     args = ap.parse_args()
     if args.no_t_out and args.t_f16:
         ap.error("--no-t-out and --t-f16 exclude each other")
@@ -344,6 +347,10 @@ def bench_ours(args, rank, world, local):
         north_star = time_north_star_call(k, v, beta, cu_t, w, T_out, W_out, U_out, K, flush, scrub, stream)
         north_star["headline_us_per_call"] = launch_ms * 1e3
 
+    consumer = None
+    if args.consumer:
+        consumer = time_consumer(k, v, beta, g, cu_t, w, K, flush, scrub, stream, rank, peak)
+
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": max_ms / K, "higher_is_better": True,
@@ -366,10 +373,72 @@ def bench_ours(args, rank, world, local):
                      "avg_launch_ms": launch_ms},
         "clocks": clocks, "e2e": e2e, "gpu_launches": K,
         "north_star_call": north_star,
+        "gdn_chunk_state": consumer,
     }
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(k, v, beta, cu, w, g=g)
     return line
+
+
+def _device_time(fn, K, flush, scrub, stream):
+    """Average device time (ms) of fn() over K calls: one event pair around K back-to-back calls, or,
+    when the inputs fit in L2, per-call events with L2 flushed before each call."""
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    if flush:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for i in range(K):
+            scrub.zero_()
+            evs[i][0].record(stream)
+            fn()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in evs) / K
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(K):
+        fn()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / K
+
+
+def time_consumer(k, v, beta, g, cu_t, w, K, flush, scrub, stream, seed, peak):
+    """gdn_chunk_state_fwd on the workload (W and U~ from kkt_solve, q and an initial state from the
+    input recipe, the final state written), then kkt_solve and it back to back (the whole GDN forward
+    of the chunked prefill)."""
+    from gdn_chunkwise_ut_gb300 import gdn_chunk_state_fwd, kkt_solve_fwd
+    from gdn_chunkwise_ut_gb300.inputs import make_query, make_state
+    if w.dk != 128 or w.dv != 128 or w.C != 64 or w.io != "bf16":
+        return {"skipped": "the recurrence kernel covers d_k = d_v = 128, C = 64, bf16"}
+    dev = k.device
+    q = make_query(k.shape[0], k.shape[1], w.H, w.dk, seed=seed, device=dev)
+    N = w.B if cu_t is None else cu_t.shape[0] - 1
+    S0 = make_state(N, w.H, w.dk, w.dv, seed=seed, device=dev)
+    _, W, U = kkt_solve_fwd(k, v, beta, w.C, cu_t, materialize_T=False, g=g)
+    o = torch.empty_like(v)
+    S = torch.empty_like(S0)
+
+    def rec():
+        gdn_chunk_state_fwd(q, k, W, U, w.C, g=g, initial_state=S0, cu_seqlens=cu_t, o=o, final_state=S)
+
+    def both():
+        kkt_solve_fwd(k, v, beta, w.C, cu_t, T_out=None, W_out=W, U_out=U, materialize_T=False, g=g)
+        rec()
+
+    ms = _device_time(rec, K, flush, scrub, stream)
+    ms_both = _device_time(both, K, flush, scrub, stream)
+    units = w.tokens * w.H
+    alg = units * costmodel.recurrence_bytes_per_unit(w.dk, w.dv, gated=g is not None) + \
+        N * w.H * costmodel.state_bytes(w.dk, w.dv)
+    gbs = alg / (ms / 1e3) / 1e9
+    alg_both = alg + units * costmodel.bytes_per_unit(w.C, w.dk, w.dv, 2, t_out=False, gated=g is not None)
+    return {"kernel": "gdn_chunk_kernel", "us_per_call": ms * 1e3, "tokens_per_s": w.tokens / (ms / 1e3),
+            "alg_bytes_per_launch": alg, "hbm_gbs": gbs, "frac_of_peak": gbs / peak,
+            "ctas": N * w.H, "chunks_per_cta": -(-max(w.T, max(w.lengths) if w.varlen else 0) // w.C),
+            "with_kkt_solve_us": ms_both * 1e3, "with_kkt_solve_tokens_per_s": w.tokens / (ms_both / 1e3),
+            "with_kkt_solve_gbs": alg_both / (ms_both / 1e3) / 1e9}
 
 
 def time_north_star_call(k, v, beta, cu_t, w, T_out, W_out, U_out, K, flush, scrub, stream):

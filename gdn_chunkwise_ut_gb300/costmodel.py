@@ -107,3 +107,15 @@ def triangular_mac_per_unit(C: int, dk: int, dv: int) -> float:
     inverse = blocked_fma(C) / C
     epilogue = (C + 1) / 2 * (dk + dv)
     return gram + inverse + epilogue
+
+
+def recurrence_bytes_per_unit(dk: int, dv: int, gated: bool = False) -> int:
+    """Algorithmic HBM bytes per (token, head) of the chunk state recurrence and output: read q, k, W
+    (bf16, d_k each) and U~ (bf16, d_v), the gate's log decay (fp32) when gated; write o (bf16, d_v)."""
+    return 2 * (3 * dk + dv) + 2 * dv + (4 if gated else 0)
+
+
+def state_bytes(dk: int, dv: int) -> int:
+    """Bytes per (sequence, head) of the recurrence's fp32 states: the initial one read, the final one
+    written."""
+    return 2 * 4 * dk * dv

@@ -565,14 +565,15 @@ extern "C" int gdn_chunk_state_fwd(const void *q, const void *k, const void *w, 
                                    int dk, int dv, int C, float scale, void *o, float *final_state,
                                    struct CUstream_st *stream) {
     using namespace kkt;
-    if (!q || !k || !w || !u || !o) return KKT_ERR_ARG;
     if (B < 1 || T < 0 || H < 1 || H > 65535) return KKT_ERR_ARG;
+    const int64_t ntok = cu_seqlens ? (int64_t)T : (int64_t)B * T;
+    // the token tensors may be empty (and their pointers null) only when there are no tokens
+    if (ntok > 0 && (!q || !k || !w || !u || !o)) return KKT_ERR_ARG;
     if (dk != kGcD || dv != kGcD || C != kGcC) return KKT_ERR_UNSUPPORTED;
     if (!aligned_to(q, 16) || !aligned_to(k, 16) || !aligned_to(w, 16) || !aligned_to(u, 16) || !aligned_to(o, 16) ||
         !aligned_to(initial_state, 16) || !aligned_to(final_state, 16) || !aligned_to(g, 4) ||
         !aligned_to(cu_seqlens, 4))
         return KKT_ERR_ALIGN;
-    const int64_t ntok = cu_seqlens ? (int64_t)T : (int64_t)B * T;
     if ((int64_t)B * H > 0x7fffffffLL || ntok > 0x7fffffffLL) return KKT_ERR_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const size_t state_bytes = (size_t)B * H * kGcD * kGcD * sizeof(float);
