@@ -328,8 +328,9 @@ __device__ __forceinline__ bool level32(const int WP, uint8_t *tm, uint8_t *ybuf
                                         uint64_t *pair_bar, uint32_t &pair_uses, Barriers *bars, int *status) {
     uint8_t *th = tm + (c0 >> 5) * 16384;  // the 32-column half holding the block's first columns
     {
-        // Y part: rows yr + 8 rr of 32, columns 16 WP + 4 yc .. + 3; k in [16 WP, 32)
-        const int yr = lane >> 2, yc = lane & 3;
+        // Y part: rows yr + 8 rr of 32, columns 16 WP + 4 yc .. + 3; k in [16 WP, 32).  A quarter-warp
+        // covers 8 rows of one column group: 8 different swizzled chunks, no bank conflict
+        const int yr = lane & 7, yc = lane >> 3;
         const uint8_t *arow[4];
         uint32_t axor[4];
 #pragma unroll
@@ -393,9 +394,10 @@ __device__ __forceinline__ bool level32(const int WP, uint8_t *tm, uint8_t *ybuf
 // 80 k-steps of 16 outputs per lane in each product.  Y is kept in rows 0..63, columns 64..127
 // (zero in T) and cleared again once every warp has read it.
 
-// Y, column block j, rows 32 rh .. 32 rh + 31.  Lane: rows yr + 8 rr, columns 16 j + 4 yc .. + 3.
+// Y, column block j, rows 32 rh .. 32 rh + 31.  Lane: rows yr + 8 rr, columns 16 j + 4 yc .. + 3
+// (a quarter-warp: 8 rows of one column group, 8 different swizzled chunks).
 __device__ __forceinline__ void level64_y_block(float2 (&y)[4][2], uint8_t *tm, int rh, int j, int lane) {
-    const int yr = lane >> 2, yc = lane & 3;
+    const int yr = lane & 7, yc = lane >> 3;
     const int cj = 16 * j + 4 * yc;
     const uint32_t axor = (uint32_t)(yr & 7) << 4;  // swizzle phase of every A row used
     const uint32_t axr[4] = {axor, axor, axor, axor};
@@ -446,7 +448,7 @@ __device__ __forceinline__ bool level64(const int w, uint8_t *tm, int lane, uint
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr) y[rr][0] = y[rr][1] = make_float2(0.f, 0.f);
         level64_y_block(y, tm, half, j, lane);
-        const int yr = lane >> 2, yc = lane & 3;
+        const int yr = lane & 7, yc = lane >> 3;
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr)
             *tm_vec(tm, 32 * half + yr + 8 * rr, 64 + 16 * j + 4 * yc) =
@@ -951,9 +953,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // kept in the block's upper-right 16 x 16 (rows m0 .. m0 + 15, columns c0 + 16 .. c0 + 31),
             // zero in T and cleared again once read.
             {
-                // lane -> rows ii and ii + 8 of the 16 x 16 result, columns jb .. jb + 3
-                const int ii = lane >> 2;
-                const int jb = (lane & 3) * 4;
+                // lane -> rows ii and ii + 8 of the 16 x 16 result, columns jb .. jb + 3.  The 8 lanes
+                // of a quarter-warp take 8 different rows of one column group, so their 16-byte
+                // accesses fall in 8 different swizzled chunks (no bank conflict)
+                const int ii = lane & 7;
+                const int jb = (lane >> 3) * 4;
                 const int m0 = g * C + 32 * wp;
                 const int c0 = 32 * wp;
                 float a[2][16];
