@@ -13,21 +13,24 @@
 //
 // One CTA per (sequence, head); C = 64, d_k = d_v = 128.  Warps 0-3 ("math") own tensor-memory
 // lanes 0-127, thread t holding row t of every tensor-memory matrix; warp 4 loads.
-//   tensor memory (512 columns): S [128 x 128] fp32 (row d of S in lane d); two D buffers
-//   [128 x 128] fp32; P [128 x 64] fp32.
-//   shared memory: a two-deep ring of stages, each with [Q; W] (per 64-column box: the 64 rows of
-//   Q, then the 64 rows of W, so that the pair is one 128-row operand), K and U~, all loaded by TMA
-//   with the 128-byte swizzle; the bf16 copies S_b of S, P_b of the masked P (rows 64..127 zero),
-//   V'_b of V' (and, gated, VF_b of diag(e^{G_last - G}) V'), and the staging of O.
-// Per chunk, every tcgen05.mma M = 128, one thread issuing:
-//   P  = [Q; W] K^T           (N = 64; rows 0..63 are Q K^T, rows 64..127 unused)
-//   D  = [Q; W] S_b           (N = 128; rows 0..63 Q S, rows 64..127 W S: one product for both)
-//   S += K^T V'(F)_b          (A = K^T read MN-major from the stage, N = 128, K = 64 tokens)
-//   D += [P_b; 0] V'_b        (rows 0..63 become O / scale, before the gate's row factor when gated)
-// and the math threads between them: S -> S_b (and, gated, S <- e^{G_last} S in place); P row ->
-// causal mask (times Gamma) -> P_b; W S row -> V' = U~ - W S -> V'_b; gated, Q S row -> e^{G_i} Q S;
-// O row -> scale -> bf16 -> staging -> TMA store (plain stores for a short last chunk).  The two D
-// buffers let the O of one chunk drain while the next chunk's products run.
+//   tensor memory (512 columns): S^T [128 x 128] fp32 (row e of S^T, i.e. column e of S, in lane e);
+//   two D buffers [128 x 192] fp32.
+//   shared memory: a two-deep ring of stages, each holding [Q; W] (per 64-column box: the 64 rows of
+//   Q, then the 64 rows of W, so that the pair is one 128-row operand) and [S^T_b; K] (per box: the
+//   128 rows of the bf16 copy of S^T, written by the math threads, then the 64 rows of K), Q, W and K
+//   loaded by TMA with the 128-byte swizzle; the bf16 copies P_b of the masked P (rows 64..127
+//   zero), V'_b of V' and, gated, VF_b of diag(e^{G_last - G}) V'.  U~ rows go straight from global
+//   memory to the registers of the threads that use them.
+// Per chunk, every tcgen05.mma M = 128:
+//   D   = [Q; W] [S^T_b; K]^T   (N = 192: columns 0..127 are [Q S; W S], 128..191 [Q K^T; W K^T])
+//   S^T += V'(F)_b^T K          (A = V'^T and B = K both read MN-major, N = 128, K = 64 tokens)
+//   D  += [P_b; 0] V'_b         (columns 0..127, rows 0..63 become O / scale)
+// The first and third are issued by thread 0, the second by thread 64, so that the state's chain
+// (S^T -> S^T_b, D, V', the S^T update) never waits for the output's side (P, P V', the drain of O).
+// The math threads between the products: S^T row -> S^T_b (and, gated, S^T <- e^{G_last} S^T in
+// place); rows 64..127: W S row -> V' = U~ - W S -> V'_b (and VF_b); rows 0..63: P row -> causal mask
+// (times Gamma when gated) -> P_b, gated Q S row -> e^{G_i} Q S, and O row -> scale -> bf16 -> global.
+// The two D buffers let the O of one chunk drain while the next chunk's products run.
 //
 // Every wait is bounded (2 s); on expiry the kernel records KKT_ERR_TIMEOUT, stops, waits for its
 // own copies and tensor-core work, frees tensor memory and returns.  Group syncs are mbarrier-based.
@@ -50,27 +53,26 @@ constexpr int kGcC = 64;
 constexpr int kGcD = 128;                 // d_k = d_v
 constexpr int kGcThreads = 160;           // warps 0-3 math, warp 4 loads
 constexpr uint32_t kGcTmemCols = 512;
-constexpr uint32_t kColS = 0;
-constexpr uint32_t kColD0 = 128;
-constexpr uint32_t kColD1 = 256;
-constexpr uint32_t kColP = 384;
+constexpr uint32_t kColS = 0;             // S^T: 128 columns
+constexpr uint32_t kColD0 = 128;          // D buffers: 192 columns each
+constexpr uint32_t kColD1 = 320;
+constexpr uint32_t kColDP = 128;          // the P columns inside a D buffer
 constexpr uint64_t kGcWaitNs = 2000000000ull;
 
 // shared memory, from a 1024-byte-aligned base
-constexpr int kStageBytes = 65536;        // [Q; W] 32 KB, K 16 KB, U~ 16 KB
-constexpr int kOffQW = 0;
-constexpr int kOffK = 32768;
-constexpr int kOffU = 49152;
-constexpr int kOffSb = 2 * kStageBytes;   // 2 boxes x [128 rows][128 B]
-constexpr int kOffPb = kOffSb + 32768;    // [128 rows][128 B]
+constexpr int kStageBytes = 81920;        // [Q; W] 32 KB, [S^T_b; K] 48 KB
+constexpr int kOffQW = 0;                 // 2 boxes x [128 rows][128 B]
+constexpr int kOffSK = 32768;             // 2 boxes x [192 rows][128 B]: S^T_b rows 0..127, K rows 128..191
+constexpr int kBoxSK = 24576;
+constexpr int kOffKInBox = 16384;
+constexpr int kOffPb = 2 * kStageBytes;   // [128 rows][128 B]
 constexpr int kOffVb = kOffPb + 16384;    // 2 boxes x [64 rows][128 B]
 constexpr int kOffVf = kOffVb + 16384;
-constexpr int kOffOb = kOffVf + 16384;
-constexpr int kOffMeta = kOffOb + 16384;  // per stage 512 B: G[64] (log2 units), then the chunk info
+constexpr int kOffMeta = kOffVf + 16384;  // per stage 512 B: G[64] (log2 units), then the chunk info
 constexpr int kOffBar = kOffMeta + 1024;
 constexpr int kGcSmem = kOffBar + 256 + 1024;  // + alignment slack
 static_assert(kGcSmem <= 232448, "shared memory over the per-block limit");
-constexpr uint32_t kStageTx = 65536;
+constexpr uint32_t kStageTx = 49152;      // Q, W and K boxes of one stage
 
 struct GcInfo {
     int64_t t0;
@@ -80,8 +82,8 @@ struct GcInfo {
 
 struct GcBars {
     uint64_t full[2], empty[2];
-    uint64_t bar_p, bar_d, bar_s, bar_o;
-    uint64_t grp128, grp64, fin;
+    uint64_t bar_d, bar_s, bar_o, vready;
+    uint64_t grp128, grp_out, grp_v, fin0, fin64;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -96,6 +98,7 @@ struct GcParams {
     int64_t ntok;
     int H;
     float scale;
+    const __nv_bfloat16 *u;
     __nv_bfloat16 *o;
     int *status;
 };
@@ -137,8 +140,7 @@ __device__ __forceinline__ bool gc_group(uint64_t *bar, uint32_t &uses, GcBars *
 template <bool GATED>
 __global__ void __launch_bounds__(kGcThreads, 1)
     gdn_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                     const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_u,
-                     const __grid_constant__ CUtensorMap map_o, const GcParams p) {
+                     const __grid_constant__ CUtensorMap map_w, const GcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024_gc(smem_raw);
     GcBars *bars = reinterpret_cast<GcBars *>(smem + kOffBar);
@@ -156,13 +158,15 @@ __global__ void __launch_bounds__(kGcThreads, 1)
             mbar_init(&bars->full[s], 2);  // the TMA transaction arrival, then one after the gate data
             mbar_init(&bars->empty[s], 1);
         }
-        mbar_init(&bars->bar_p, 1);
         mbar_init(&bars->bar_d, 1);
         mbar_init(&bars->bar_s, 1);
         mbar_init(&bars->bar_o, 1);
+        mbar_init(&bars->vready, 1);
         mbar_init(&bars->grp128, 4);
-        mbar_init(&bars->grp64, 2);
-        mbar_init(&bars->fin, 1);
+        mbar_init(&bars->grp_out, 2);
+        mbar_init(&bars->grp_v, 2);
+        mbar_init(&bars->fin0, 1);
+        mbar_init(&bars->fin64, 1);
         bars->abort_flag = 0;
         fence_mbar_init();
     }
@@ -195,7 +199,6 @@ __global__ void __launch_bounds__(kGcThreads, 1)
             prefetch_tmap(&map_q);
             prefetch_tmap(&map_k);
             prefetch_tmap(&map_w);
-            prefetch_tmap(&map_u);
         }
         int c = 0;
         bool ok = true;
@@ -220,8 +223,8 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                 for (int c2 = 0; c2 < 2; ++c2) {
                     tma_load_3d(st + kOffQW + c2 * 16384, &map_q, &bars->full[s], 64 * c2, h, (int)t0);
                     tma_load_3d(st + kOffQW + c2 * 16384 + 8192, &map_w, &bars->full[s], 64 * c2, h, (int)t0);
-                    tma_load_3d(st + kOffK + c2 * 8192, &map_k, &bars->full[s], 64 * c2, h, (int)t0);
-                    tma_load_3d(st + kOffU + c2 * 8192, &map_u, &bars->full[s], 64 * c2, h, (int)t0);
+                    tma_load_3d(st + kOffSK + c2 * kBoxSK + kOffKInBox, &map_k, &bars->full[s], 64 * c2, h,
+                                (int)t0);
                 }
             }
             if constexpr (GATED) {
@@ -256,79 +259,50 @@ __global__ void __launch_bounds__(kGcThreads, 1)
     } else {
         // ------------------------------------------------------------------ math warps
         const int t = threadIdx.x;                        // tensor-memory lane = row
+        const bool out_side = t < 64;                     // rows 0..63: P, O; rows 64..127: W S, V'
         const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-        uint8_t *sb = smem + kOffSb;
         uint8_t *pb = smem + kOffPb;
         uint8_t *vb = smem + kOffVb;
         uint8_t *vf = smem + kOffVf;
-        uint8_t *ob = smem + kOffOb;
-        uint32_t u128 = 0, u64 = 0;
+        uint32_t u128 = 0, uside = 0;
         bool ok = true;
-        const int64_t state_off = ((int64_t)seq * p.H + h) * kGcD * kGcD + (int64_t)t * kGcD;
+        const int64_t state_base = ((int64_t)seq * p.H + h) * kGcD * kGcD;
 
-        // the initial state into tensor memory, row t of S in lane t
+        // the initial state into tensor memory: lane t holds column t of S (row t of S^T); the loads
+        // of a warp read 32 consecutive floats of one row of S
 #pragma unroll 1
         for (int piece = 0; piece < 8; ++piece) {
             uint32_t v[16];
-            if (p.h0) {
-                const float4 *src = reinterpret_cast<const float4 *>(p.h0 + state_off + 16 * piece);
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float4 x = __ldg(src + e);
-                    v[4 * e] = __float_as_uint(x.x);
-                    v[4 * e + 1] = __float_as_uint(x.y);
-                    v[4 * e + 2] = __float_as_uint(x.z);
-                    v[4 * e + 3] = __float_as_uint(x.w);
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) v[e] = 0u;
-            }
+            for (int e = 0; e < 16; ++e)
+                v[e] = p.h0 ? __float_as_uint(__ldg(p.h0 + state_base + (int64_t)(16 * piece + e) * kGcD + t)) : 0u;
             tmem_st16(tmem + lane_base + kColS + 16 * piece, v);
         }
         tmem_wait_st();
         tc_fence_before();
 
-        // O of chunk cp (buffer cp & 1): rows 0..63, threads 0..63
+        // O of chunk cp (buffer cp & 1), rows 0..63 (threads 0..63): scale, bf16, plain stores
         auto drain_o = [&](int cp, int64_t t0p, int Lcp) -> bool {
             if (!gc_wait(&bars->bar_o, (uint32_t)cp & 1u, bars, p.status)) return false;
             tc_fence_after();
             const uint32_t dcol = (cp & 1) ? kColD1 : kColD0;
-            const bool full = Lcp == kGcC;
-            if (full) {
-                if (t == 0) bulk_wait_read<0>();  // the previous store has read the staging
-                if (!gc_group(&bars->grp64, u64, bars, p.status)) return false;
-            }
 #pragma unroll 1
             for (int piece = 0; piece < 4; ++piece) {
                 uint32_t v[32];
                 tmem_ld32(tmem + lane_base + dcol + 32 * piece, v);
                 tmem_wait_ld();
-                uint32_t pk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    pk[e] = pack2_bf16(p.scale * __uint_as_float(v[2 * e]), p.scale * __uint_as_float(v[2 * e + 1]));
-                if (full) {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        *sw_chunk(ob + (piece >> 1) * 8192, t, (piece & 1) * 4 + j) =
-                            make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-                } else if (t < Lcp) {
+                if (t < Lcp) {
                     uint4 *dst = reinterpret_cast<uint4 *>(p.o + ((t0p + t) * p.H + h) * kGcD + 32 * piece);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                    for (int j = 0; j < 4; ++j)
+                        dst[j] = make_uint4(
+                            pack2_bf16(p.scale * __uint_as_float(v[8 * j]), p.scale * __uint_as_float(v[8 * j + 1])),
+                            pack2_bf16(p.scale * __uint_as_float(v[8 * j + 2]), p.scale * __uint_as_float(v[8 * j + 3])),
+                            pack2_bf16(p.scale * __uint_as_float(v[8 * j + 4]), p.scale * __uint_as_float(v[8 * j + 5])),
+                            pack2_bf16(p.scale * __uint_as_float(v[8 * j + 6]), p.scale * __uint_as_float(v[8 * j + 7])));
                 }
             }
             tc_fence_before();
-            if (full) {
-                fence_proxy_async_smem();
-                if (!gc_group(&bars->grp64, u64, bars, p.status)) return false;
-                if (t == 0) {
-                    tma_store_3d(&map_o, ob, 0, h, (int)t0p);
-                    tma_store_3d(&map_o, ob + 8192, 64, h, (int)t0p);
-                    bulk_commit();
-                }
-            }
             return true;
         };
 
@@ -339,34 +313,31 @@ __global__ void __launch_bounds__(kGcThreads, 1)
         for (; ok && c < nchunks; ++c) {
             const int s = c & 1;
             uint8_t *st = stage(s);
+            uint8_t *sk = st + kOffSK;
             if (!gc_wait(&bars->full[s], ((uint32_t)c >> 1) & 1u, bars, p.status)) { ok = false; break; }
             const GcInfo info = *stage_info(s);
             const int Lc = info.Lc;
             const float *G = stage_G(s);
-            // rows of a short chunk past its end: K's rows enter K^T V' (times zero rows of V'), so
-            // they are zeroed (a row of the next sequence, or the fill past the tensor, stays out)
+            // rows 64..127: this chunk's row of U~, from global memory, in flight during the readback
+            const int i = t - 64;
+            uint4 ur[16];
+            if (!out_side) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(p.u + ((info.t0 + i) * p.H + h) * kGcD);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) ur[e] = (i < Lc) ? __ldg(src + e) : make_uint4(0, 0, 0, 0);
+            }
+            // rows of a short chunk past its end: K's rows enter V'^T K (times zero rows of V') and
+            // the masked columns of P, so they are zeroed (a row of the next sequence, or the fill
+            // past the tensor, stays out)
             if (Lc < kGcC) {
                 const int per = (kGcC - Lc) * 8;
                 for (int e = t; e < 2 * per; e += 128) {
                     const int box = e / per, w = e % per;
-                    *reinterpret_cast<uint4 *>(st + kOffK + box * 8192 + (Lc + w / 8) * 128 + (w % 8) * 16) =
+                    *reinterpret_cast<uint4 *>(sk + box * kBoxSK + kOffKInBox + (Lc + w / 8) * 128 + (w % 8) * 16) =
                         make_uint4(0, 0, 0, 0);
                 }
-                fence_proxy_async_smem();
             }
-            if (!gc_group(&bars->grp128, u128, bars, p.status)) { ok = false; break; }
-            // P = [Q; W] K^T
-            if (t == 0) {
-                tc_fence_after();
-                const uint32_t idesc_p = idesc_bf16_f32(128, kGcC, 0, 0);
-                const uint32_t qw = smem_u32(st + kOffQW), kk0 = smem_u32(st + kOffK);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(tmem + kColP, sw128_desc(qw + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                           sw128_desc(kk0 + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024), idesc_p, kk > 0 ? 1u : 0u);
-                mma_commit(&bars->bar_p);
-            }
-            // S -> S_b (the state this chunk starts from), and, gated, S <- e^{G_last} S in place
+            // S^T row t -> S^T_b (the state this chunk starts from), and, gated, S^T <- e^{G_last} S^T
             if (c > 0 && !gc_wait(&bars->bar_s, (uint32_t)(c - 1) & 1u, bars, p.status)) { ok = false; break; }
             tc_fence_after();
             const float glast = GATED ? exp2f(G[Lc - 1]) : 1.f;
@@ -377,7 +348,7 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    *sw_chunk(sb + (piece >> 1) * 16384, t, (piece & 1) * 4 + j) = make_uint4(
+                    *sw_chunk(sk + (piece >> 1) * kBoxSK, t, (piece & 1) * 4 + j) = make_uint4(
                         pack2_bf16(__uint_as_float(v[8 * j]), __uint_as_float(v[8 * j + 1])),
                         pack2_bf16(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
                         pack2_bf16(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
@@ -397,29 +368,75 @@ __global__ void __launch_bounds__(kGcThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             if (!gc_group(&bars->grp128, u128, bars, p.status)) { ok = false; break; }
-            // D = [Q; W] S_b
+            // D = [Q; W] [S^T_b; K]^T
             const uint32_t dcol = (c & 1) ? kColD1 : kColD0;
             if (t == 0) {
                 tc_fence_after();
-                const uint32_t idesc_d = idesc_bf16_f32(128, kGcD, 0, 1);
-                const uint32_t qw = smem_u32(st + kOffQW), s0 = smem_u32(sb);
+                const uint32_t idesc_d = idesc_bf16_f32(128, kGcD + kGcC, 0, 0);
+                const uint32_t qw = smem_u32(st + kOffQW), b0 = smem_u32(sk);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
                     mma_ss(tmem + dcol, sw128_desc(qw + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                           sw128_desc(s0 + kk * 2048, 16384, 1024), idesc_d, kk > 0 ? 1u : 0u);
+                           sw128_desc(b0 + (kk >> 2) * kBoxSK + (kk & 3) * 32, 16, 1024), idesc_d, kk > 0 ? 1u : 0u);
                 mma_commit(&bars->bar_d);
             }
-            if (t < 64) {
+            if (!out_side) {
+                // W S row -> V' = U~ - W S (zero past the chunk's end) -> V'_b (and VF_b) row i
+                if (!gc_wait(&bars->bar_d, (uint32_t)c & 1u, bars, p.status)) { ok = false; break; }
+                tc_fence_after();
+                const float fi = (GATED && i < Lc) ? exp2f(G[Lc - 1] - G[i]) : 1.f;
+#pragma unroll  // (unrolled: the U~ row stays in registers)
+                for (int piece = 0; piece < 4; ++piece) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_base + dcol + 32 * piece, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int ch = (piece & 1) * 4 + j;
+                        const uint4 uu = ur[4 * piece + j];
+                        const uint32_t uw[4] = {uu.x, uu.y, uu.z, uu.w};
+                        uint32_t o1[4], o2[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 uf = unpack2_bf16(uw[e]);
+                            float y0 = uf.x - __uint_as_float(v[8 * j + 2 * e]);
+                            float y1 = uf.y - __uint_as_float(v[8 * j + 2 * e + 1]);
+                            if (i >= Lc) y0 = y1 = 0.f;
+                            o1[e] = pack2_bf16(y0, y1);
+                            o2[e] = pack2_bf16(fi * y0, fi * y1);
+                        }
+                        *sw_chunk(vb + (piece >> 1) * 8192, i, ch) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+                        if constexpr (GATED)
+                            *sw_chunk(vf + (piece >> 1) * 8192, i, ch) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                if (!gc_group(&bars->grp_v, uside, bars, p.status)) { ok = false; break; }
+                // S^T += V'(F)_b^T K, then tell thread 0 that V'_b is ready for P V'
+                if (t == 64) {
+                    tc_fence_after();
+                    const uint32_t idesc_s = idesc_bf16_f32(128, kGcD, 1, 1);
+                    const uint32_t vs = smem_u32(GATED ? vf : vb), k0 = smem_u32(sk + kOffKInBox);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ss(tmem + kColS, sw128_desc(vs + kk * 2048, 8192, 1024),
+                               sw128_desc(k0 + kk * 2048, kBoxSK, 1024), idesc_s, 1u);
+                    mma_commit(&bars->bar_s);
+                    mma_commit(&bars->empty[s]);
+                    mbar_arrive(&bars->vready);
+                }
+            } else {
                 // the previous chunk's O, while this chunk's products run
                 if (c > 0 && !drain_o(c - 1, prev_t0, prev_Lc)) { ok = false; break; }
                 // P row t -> causal mask (times Gamma when gated) -> P_b row t
-                if (!gc_wait(&bars->bar_p, (uint32_t)c & 1u, bars, p.status)) { ok = false; break; }
+                if (!gc_wait(&bars->bar_d, (uint32_t)c & 1u, bars, p.status)) { ok = false; break; }
                 tc_fence_after();
                 const float gi = GATED ? G[t] : 0.f;
 #pragma unroll 1
                 for (int half = 0; half < 2; ++half) {
                     uint32_t v[32];
-                    tmem_ld32(tmem + lane_base + kColP + 32 * half, v);
+                    tmem_ld32(tmem + lane_base + dcol + kColDP + 32 * half, v);
                     tmem_wait_ld();
                     float x[32];
 #pragma unroll
@@ -437,8 +454,6 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                 }
                 if constexpr (GATED) {
                     // Q S row t -> e^{G_t} Q S (the state term's decay), in place
-                    if (!gc_wait(&bars->bar_d, (uint32_t)c & 1u, bars, p.status)) { ok = false; break; }
-                    tc_fence_after();
                     const float ri = exp2f(gi);
 #pragma unroll 1
                     for (int piece = 0; piece < 8; ++piece) {
@@ -451,88 +466,53 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                     }
                     tmem_wait_st();
                 }
-            } else {
-                // W S row t -> V' = U~ - W S (zero past the chunk's end) -> V'_b (and VF_b) row t - 64
-                const int i = t - 64;
-                if (!gc_wait(&bars->bar_d, (uint32_t)c & 1u, bars, p.status)) { ok = false; break; }
-                tc_fence_after();
-                const float fi = (GATED && i < Lc) ? exp2f(G[Lc - 1] - G[i]) : 1.f;
-#pragma unroll 1
-                for (int piece = 0; piece < 4; ++piece) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + lane_base + dcol + 32 * piece, v);
-                    tmem_wait_ld();
+                fence_proxy_async_smem();
+                tc_fence_before();
+                if (!gc_group(&bars->grp_out, uside, bars, p.status)) { ok = false; break; }
+                // D += [P_b; 0] V'_b, once thread 64 has seen V'_b written
+                if (t == 0) {
+                    volatile int *abort = &bars->abort_flag;
+                    if (!mbar_wait(&bars->vready, (uint32_t)c & 1u, abort, kGcWaitNs)) {
+                        if (atomicExch(&bars->abort_flag, 1) == 0) record_error(p.status, KKT_ERR_TIMEOUT);
+                    } else {
+                        tc_fence_after();
+                        const uint32_t idesc_o = idesc_bf16_f32(128, kGcD, 0, 1);
+                        const uint32_t p0 = smem_u32(pb), v0 = smem_u32(vb);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int ch = (piece & 1) * 4 + j;
-                        const uint4 uu = *sw_chunk(st + kOffU + (piece >> 1) * 8192, i, ch);
-                        const uint32_t uw[4] = {uu.x, uu.y, uu.z, uu.w};
-                        uint32_t o1[4], o2[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 uf = unpack2_bf16(uw[e]);
-                            float y0 = uf.x - __uint_as_float(v[8 * j + 2 * e]);
-                            float y1 = uf.y - __uint_as_float(v[8 * j + 2 * e + 1]);
-                            if (i >= Lc) y0 = y1 = 0.f;
-                            o1[e] = pack2_bf16(y0, y1);
-                            o2[e] = pack2_bf16(fi * y0, fi * y1);
-                        }
-                        *sw_chunk(vb + (piece >> 1) * 8192, i, ch) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-                        if constexpr (GATED)
-                            *sw_chunk(vf + (piece >> 1) * 8192, i, ch) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ss(tmem + dcol, sw128_desc(p0 + kk * 32, 16, 1024),
+                                   sw128_desc(v0 + kk * 2048, 8192, 1024), idesc_o, 1u);
+                        mma_commit(&bars->bar_o);
                     }
                 }
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            if (!gc_group(&bars->grp128, u128, bars, p.status)) { ok = false; break; }
-            // S += K^T V'(F)_b, then D += [P_b; 0] V'_b
-            if (t == 0) {
-                tc_fence_after();
-                const uint32_t idesc_s = idesc_bf16_f32(128, kGcD, 1, 1);
-                const uint32_t idesc_o = idesc_bf16_f32(128, kGcD, 0, 1);
-                const uint32_t kk0 = smem_u32(st + kOffK), vs = smem_u32(GATED ? vf : vb), v0 = smem_u32(vb);
-                const uint32_t p0 = smem_u32(pb);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_ss(tmem + kColS, sw128_desc(kk0 + kk * 2048, 8192, 1024), sw128_desc(vs + kk * 2048, 8192, 1024),
-                           idesc_s, 1u);
-                mma_commit(&bars->bar_s);
-                mma_commit(&bars->empty[s]);
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_ss(tmem + dcol, sw128_desc(p0 + kk * 32, 16, 1024), sw128_desc(v0 + kk * 2048, 8192, 1024),
-                           idesc_o, 1u);
-                mma_commit(&bars->bar_o);
+                __syncwarp();
             }
             prev_t0 = info.t0;
             prev_Lc = Lc;
         }
-        // the last chunk's O, and the final state
-        if (ok && nchunks > 0 && t < 64 && !drain_o(nchunks - 1, prev_t0, prev_Lc)) ok = false;
+        // the last chunk's O, and the final state (lane t holds column t of S)
+        if (ok && nchunks > 0 && out_side && !drain_o(nchunks - 1, prev_t0, prev_Lc)) ok = false;
         if (ok && p.ht) {
             if (nchunks > 0 && !gc_wait(&bars->bar_s, (uint32_t)(nchunks - 1) & 1u, bars, p.status)) ok = false;
             if (ok) {
                 tc_fence_after();
-                float4 *dst = reinterpret_cast<float4 *>(p.ht + state_off);
 #pragma unroll 1
                 for (int piece = 0; piece < 4; ++piece) {
                     uint32_t v[32];
                     tmem_ld32(tmem + lane_base + kColS + 32 * piece, v);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        dst[8 * piece + e] = make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
-                                                         __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3]));
+                    for (int e = 0; e < 32; ++e)
+                        p.ht[state_base + (int64_t)(32 * piece + e) * kGcD + t] = __uint_as_float(v[e]);
                 }
             }
         }
-        // every MMA this CTA issued has completed, and the O stores have left shared memory
-        if (t == 0) {
-            mma_commit(&bars->fin);
+        // every MMA this CTA issued has completed before tensor memory is released
+        if (t == 0 || t == 64) {
+            uint64_t *fin = t == 0 ? &bars->fin0 : &bars->fin64;
+            mma_commit(fin);
             volatile int never = 0;
-            mbar_wait(&bars->fin, 0u, &never, kGcWaitNs);
-            bulk_wait<0>();
+            mbar_wait(fin, 0u, &never, kGcWaitNs);
         }
         __syncwarp();
     }
@@ -595,15 +575,14 @@ extern "C" int gdn_chunk_state_fwd(const void *q, const void *k, const void *w, 
     p.ntok = ntok;
     p.H = H;
     p.scale = scale;
+    p.u = static_cast<const __nv_bfloat16 *>(u);
     p.o = static_cast<__nv_bfloat16 *>(o);
     int rc = status_ptr(&p.status);
     if (rc != KKT_OK) return rc;
-    CUtensorMap mq, mk, mw, mu, mo;
+    CUtensorMap mq, mk, mw;
     if (!make_map(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, ntok, H, kGcD, 64, kGcC) ||
         !make_map(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, ntok, H, kGcD, 64, kGcC) ||
-        !make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, ntok, H, kGcD, 64, kGcC) ||
-        !make_map(&mu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, u, ntok, H, kGcD, 64, kGcC) ||
-        !make_map(&mo, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, o, ntok, H, kGcD, 64, kGcC))
+        !make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, ntok, H, kGcD, 64, kGcC))
         return KKT_ERR_CUDA;
     auto kern = g ? gdn_chunk_kernel<true> : gdn_chunk_kernel<false>;
     if (!(g ? gc_ensure_smem<true>() : gc_ensure_smem<false>())) return KKT_ERR_CUDA;
@@ -617,6 +596,6 @@ extern "C" int gdn_chunk_state_fwd(const void *q, const void *k, const void *w, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mw, mu, mo, p) != cudaSuccess) return KKT_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mw, p) != cudaSuccess) return KKT_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? KKT_OK : KKT_ERR_CUDA;
 }
