@@ -156,7 +156,9 @@ __global__ void __launch_bounds__(kGcThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars->full[s], 2);  // the TMA transaction arrival, then one after the gate data
-            mbar_init(&bars->empty[s], 1);
+            // free again once the S^T update has read K (a tensor-core commit) and the output side has
+            // read the gate data (thread 0): the two sides run a chunk apart
+            mbar_init(&bars->empty[s], 2);
         }
         mbar_init(&bars->bar_d, 1);
         mbar_init(&bars->bar_s, 1);
@@ -469,8 +471,10 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                 fence_proxy_async_smem();
                 tc_fence_before();
                 if (!gc_group(&bars->grp_out, uside, bars, p.status)) { ok = false; break; }
-                // D += [P_b; 0] V'_b, once thread 64 has seen V'_b written
+                // this side is done with the stage (its gate data); D += [P_b; 0] V'_b once thread 64 has
+                // seen V'_b written
                 if (t == 0) {
+                    mbar_arrive(&bars->empty[s]);
                     volatile int *abort = &bars->abort_flag;
                     if (!mbar_wait(&bars->vready, (uint32_t)c & 1u, abort, kGcWaitNs)) {
                         if (atomicExch(&bars->abort_flag, 1) == 0) record_error(p.status, KKT_ERR_TIMEOUT);
