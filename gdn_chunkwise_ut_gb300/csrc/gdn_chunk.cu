@@ -101,7 +101,23 @@ struct GcParams {
     const __nv_bfloat16 *u;
     __nv_bfloat16 *o;
     int *status;
+    unsigned long long *trace;  // KKT_TRACE builds: per-chunk time stamps of the first CTAs, else nullptr
 };
+
+// Pipeline trace (builds with -DKKT_TRACE only): SM cycle counter at each event of the first chunks of the
+// first CTAs, [cta][chunk][event].
+constexpr int kGcTraceCtas = 4, kGcTraceChunks = 64, kGcTraceEvents = 16;
+#ifdef KKT_TRACE
+#define GC_TRACE(ev, c)                                                                                   \
+    do {                                                                                                  \
+        if (p.trace && blockIdx.x < kGcTraceCtas && (c) < kGcTraceChunks)                                 \
+            p.trace[((size_t)blockIdx.x * kGcTraceChunks + (c)) * kGcTraceEvents + (ev)] = clock64();     \
+    } while (0)
+#else
+#define GC_TRACE(ev, c) \
+    do {                \
+    } while (0)
+#endif
 
 __device__ __forceinline__ uint8_t *align1024_gc(uint8_t *p) {
     const uint32_t a = smem_u32(p);
@@ -217,6 +233,7 @@ __global__ void __launch_bounds__(kGcThreads, 1)
             }
             if (!gc_wait(&bars->empty[s], (((uint32_t)c >> 1) & 1u) ^ 1u, bars, p.status)) { ok = false; break; }
             if (lane == 0) {
+                GC_TRACE(10, c);
                 GcInfo *info = stage_info(s);
                 info->t0 = t0;
                 info->Lc = Lc;
@@ -317,6 +334,7 @@ __global__ void __launch_bounds__(kGcThreads, 1)
             uint8_t *st = stage(s);
             uint8_t *sk = st + kOffSK;
             if (!gc_wait(&bars->full[s], ((uint32_t)c >> 1) & 1u, bars, p.status)) { ok = false; break; }
+            if (t == 0) GC_TRACE(0, c);
             const GcInfo info = *stage_info(s);
             const int Lc = info.Lc;
             const float *G = stage_G(s);
@@ -342,6 +360,7 @@ __global__ void __launch_bounds__(kGcThreads, 1)
             // S^T row t -> S^T_b (the state this chunk starts from), and, gated, S^T <- e^{G_last} S^T
             if (c > 0 && !gc_wait(&bars->bar_s, (uint32_t)(c - 1) & 1u, bars, p.status)) { ok = false; break; }
             tc_fence_after();
+            if (t == 0) GC_TRACE(1, c);
             const float glast = GATED ? exp2f(G[Lc - 1]) : 1.f;
 #pragma unroll 1
             for (int piece = 0; piece < 4; ++piece) {
@@ -370,6 +389,7 @@ __global__ void __launch_bounds__(kGcThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             if (!gc_group(&bars->grp128, u128, bars, p.status)) { ok = false; break; }
+            if (t == 0) GC_TRACE(11, c);
             // D = [Q; W] [S^T_b; K]^T
             const uint32_t dcol = (c & 1) ? kColD1 : kColD0;
             if (t == 0) {
@@ -381,11 +401,13 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                     mma_ss(tmem + dcol, sw128_desc(qw + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
                            sw128_desc(b0 + (kk >> 2) * kBoxSK + (kk & 3) * 32, 16, 1024), idesc_d, kk > 0 ? 1u : 0u);
                 mma_commit(&bars->bar_d);
+                GC_TRACE(2, c);
             }
             if (!out_side) {
                 // W S row -> V' = U~ - W S (zero past the chunk's end) -> V'_b (and VF_b) row i
                 if (!gc_wait(&bars->bar_d, (uint32_t)c & 1u, bars, p.status)) { ok = false; break; }
                 tc_fence_after();
+                if (t == 64) GC_TRACE(3, c);
                 const float fi = (GATED && i < Lc) ? exp2f(G[Lc - 1] - G[i]) : 1.f;
 #pragma unroll  // (unrolled: the U~ row stays in registers)
                 for (int piece = 0; piece < 4; ++piece) {
@@ -417,6 +439,7 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                 if (!gc_group(&bars->grp_v, uside, bars, p.status)) { ok = false; break; }
                 // S^T += V'(F)_b^T K, then tell thread 0 that V'_b is ready for P V'
                 if (t == 64) {
+                    GC_TRACE(4, c);
                     tc_fence_after();
                     const uint32_t idesc_s = idesc_bf16_f32(128, kGcD, 1, 1);
                     const uint32_t vs = smem_u32(GATED ? vf : vb), k0 = smem_u32(sk + kOffKInBox);
@@ -427,13 +450,16 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                     mma_commit(&bars->bar_s);
                     mma_commit(&bars->empty[s]);
                     mbar_arrive(&bars->vready);
+                    GC_TRACE(5, c);
                 }
             } else {
                 // the previous chunk's O, while this chunk's products run
                 if (c > 0 && !drain_o(c - 1, prev_t0, prev_Lc)) { ok = false; break; }
+                if (t == 0) GC_TRACE(6, c);
                 // P row t -> causal mask (times Gamma when gated) -> P_b row t
                 if (!gc_wait(&bars->bar_d, (uint32_t)c & 1u, bars, p.status)) { ok = false; break; }
                 tc_fence_after();
+                if (t == 0) GC_TRACE(7, c);
                 const float gi = GATED ? G[t] : 0.f;
 #pragma unroll 1
                 for (int half = 0; half < 2; ++half) {
@@ -474,6 +500,7 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                 // this side is done with the stage (its gate data); D += [P_b; 0] V'_b once thread 64 has
                 // seen V'_b written
                 if (t == 0) {
+                    GC_TRACE(8, c);
                     mbar_arrive(&bars->empty[s]);
                     volatile int *abort = &bars->abort_flag;
                     if (!mbar_wait(&bars->vready, (uint32_t)c & 1u, abort, kGcWaitNs)) {
@@ -487,6 +514,7 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                             mma_ss(tmem + dcol, sw128_desc(p0 + kk * 32, 16, 1024),
                                    sw128_desc(v0 + kk * 2048, 8192, 1024), idesc_o, 1u);
                         mma_commit(&bars->bar_o);
+                        GC_TRACE(9, c);
                     }
                 }
                 __syncwarp();
@@ -541,8 +569,18 @@ bool gc_ensure_smem() {
 
 bool aligned_to(const void *ptr, uintptr_t n) { return (reinterpret_cast<uintptr_t>(ptr) & (n - 1)) == 0; }
 
+#ifdef KKT_TRACE
+void *g_gc_trace = nullptr;
+#endif
+
 }  // namespace
 }  // namespace kkt
+
+#ifdef KKT_TRACE
+// Trace builds only: device buffer of kGcTraceCtas x kGcTraceChunks x kGcTraceEvents uint64 cycle counts of
+// the recurrence kernel, or NULL to stop tracing.
+extern "C" void gdn_set_trace_buffer(void *buf) { kkt::g_gc_trace = buf; }
+#endif
 
 extern "C" int gdn_chunk_state_fwd(const void *q, const void *k, const void *w, const void *u, const float *g,
                                    const float *initial_state, const int32_t *cu_seqlens, int B, int T, int H,
@@ -581,6 +619,11 @@ extern "C" int gdn_chunk_state_fwd(const void *q, const void *k, const void *w, 
     p.scale = scale;
     p.u = static_cast<const __nv_bfloat16 *>(u);
     p.o = static_cast<__nv_bfloat16 *>(o);
+#ifdef KKT_TRACE
+    p.trace = static_cast<unsigned long long *>(g_gc_trace);
+#else
+    p.trace = nullptr;
+#endif
     int rc = status_ptr(&p.status);
     if (rc != KKT_OK) return rc;
     CUtensorMap mq, mk, mw;
