@@ -11,27 +11,26 @@
 // W carries the decay e^{G_j} in its keys (kkt_solve's gated W), so V' row i is beta_i times token
 // i's correction v_i - alpha_i S_{i-1}^T k_i of the delta rule.
 //
-// One CTA per (sequence, head); C = 64, d_k = d_v = 128.  Seven warps: warps 0-3 carry the state
-// (thread t owns tensor-memory lane t), warps 4-5 the output (lanes 0-63, thread 128 + r owns lane r),
-// warp 6 loads.
+// One CTA per (sequence, head); C = 64, d_k = d_v = 128.  Warps 0-3 ("math") own tensor-memory
+// lanes 0-127, thread t holding row t of every tensor-memory matrix; warp 4 loads.
 //   tensor memory (512 columns): S^T [128 x 128] fp32 (row e of S^T, i.e. column e of S, in lane e);
 //   two D buffers [128 x 192] fp32.
 //   shared memory: a two-deep ring of stages, each holding [Q; W] (per 64-column box: the 64 rows of
 //   Q, then the 64 rows of W, so that the pair is one 128-row operand) and [S^T_b; K] (per box: the
-//   128 rows of the bf16 copy of S^T, written by the state warps, then the 64 rows of K), Q, W and K
+//   128 rows of the bf16 copy of S^T, written by the math threads, then the 64 rows of K), Q, W and K
 //   loaded by TMA with the 128-byte swizzle; the bf16 copies P_b of the masked P (rows 64..127
-//   zero), V'_b of V' (two buffers) and, gated, VF_b of diag(e^{G_last - G}) V'.  U~ rows go from
-//   global memory (prefetched into L2 a chunk ahead) to the registers of the threads that use them.
+//   zero), V'_b of V' and, gated, VF_b of diag(e^{G_last - G}) V'.  U~ rows go straight from global
+//   memory to the registers of the threads that use them.
 // Per chunk, every tcgen05.mma M = 128:
 //   D   = [Q; W] [S^T_b; K]^T   (N = 192: columns 0..127 are [Q S; W S], 128..191 [Q K^T; W K^T])
 //   S^T += V'(F)_b^T K          (A = V'^T and B = K both read MN-major, N = 128, K = 64 tokens)
 //   D  += [P_b; 0] V'_b         (columns 0..127, rows 0..63 become O / scale)
-// issued by threads 0, 64 and 128.  The state's chain (S^T -> S^T_b, D, V', the S^T update) runs on
-// warps 0-3 and never waits for the output side, which works a chunk behind on its own warps: P row
-// -> causal mask (times Gamma when gated) -> P_b, gated Q S row -> e^{G_i} Q S, then P V', and the O
-// of the chunk before -> scale -> bf16 -> global.  The two D buffers and the two V'_b buffers carry
-// the output side's chunk while the state side starts the next; barriers that one side may meet two
-// chunks ahead of the other come in pairs, one per chunk parity.
+// The first and third are issued by thread 0, the second by thread 64, so that the state's chain
+// (S^T -> S^T_b, D, V', the S^T update) never waits for the output's side (P, P V', the drain of O).
+// The math threads between the products: S^T row -> S^T_b (and, gated, S^T <- e^{G_last} S^T in
+// place); rows 64..127: W S row -> V' = U~ - W S -> V'_b (and VF_b); rows 0..63: P row -> causal mask
+// (times Gamma when gated) -> P_b, gated Q S row -> e^{G_i} Q S, and O row -> scale -> bf16 -> global.
+// The two D buffers let the O of one chunk drain while the next chunk's products run.
 //
 // Every wait is bounded (2 s); on expiry the kernel records KKT_ERR_TIMEOUT, stops, waits for its
 // own copies and tensor-core work, frees tensor memory and returns.  Group syncs are mbarrier-based.
@@ -52,7 +51,7 @@ using namespace ptx;
 
 constexpr int kGcC = 64;
 constexpr int kGcD = 128;                 // d_k = d_v
-constexpr int kGcThreads = 224;           // warps 0-3 state, 4-5 output, 6 loads
+constexpr int kGcThreads = 160;           // warps 0-3 math, warp 4 loads
 constexpr uint32_t kGcTmemCols = 512;
 constexpr uint32_t kColS = 0;             // S^T: 128 columns
 constexpr uint32_t kColD0 = 128;          // D buffers: 192 columns each
@@ -67,8 +66,8 @@ constexpr int kOffSK = 32768;             // 2 boxes x [192 rows][128 B]: S^T_b 
 constexpr int kBoxSK = 24576;
 constexpr int kOffKInBox = 16384;
 constexpr int kOffPb = 2 * kStageBytes;   // [128 rows][128 B]
-constexpr int kOffVb = kOffPb + 16384;    // two buffers, each 2 boxes x [64 rows][128 B]
-constexpr int kOffVf = kOffVb + 32768;
+constexpr int kOffVb = kOffPb + 16384;    // 2 boxes x [64 rows][128 B]
+constexpr int kOffVf = kOffVb + 16384;
 constexpr int kOffMeta = kOffVf + 16384;  // per stage 512 B: G[64] (log2 units), then the chunk info
 constexpr int kOffBar = kOffMeta + 1024;
 constexpr int kGcSmem = kOffBar + 256 + 1024;  // + alignment slack
@@ -83,9 +82,8 @@ struct GcInfo {
 
 struct GcBars {
     uint64_t full[2], empty[2];
-    uint64_t bar_d[2], bar_o[2], dfree[2], vready[2];  // one per chunk parity
-    uint64_t bar_s;
-    uint64_t grp_state, grp_v, grp_out, fin0, fin64, fin128;
+    uint64_t bar_d, bar_s, bar_o, vready;
+    uint64_t grp128, grp_out, grp_v, fin0, fin64;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -155,20 +153,10 @@ __device__ __forceinline__ bool gc_group(uint64_t *bar, uint32_t &uses, GcBars *
     return ok;
 }
 
-// Loads 32 x N consecutive tensor-memory columns of the calling warp's lanes with N loads in flight, then
-// waits once.
-template <int N>
-__device__ __forceinline__ void tmem_ld32xN(uint32_t taddr, uint32_t (&v)[N][32]) {
-#pragma unroll
-    for (int i = 0; i < N; ++i) tmem_ld32(taddr + 32 * i, v[i]);
-    tmem_wait_ld();
-}
-
 template <bool GATED>
 __global__ void __launch_bounds__(kGcThreads, 1)
     gdn_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                     const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_u,
-                     const GcParams p) {
+                     const __grid_constant__ CUtensorMap map_w, const GcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024_gc(smem_raw);
     GcBars *bars = reinterpret_cast<GcBars *>(smem + kOffBar);
@@ -185,20 +173,18 @@ __global__ void __launch_bounds__(kGcThreads, 1)
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars->full[s], 2);  // the TMA transaction arrival, then one after the gate data
             // free again once the S^T update has read K (a tensor-core commit) and the output side has
-            // read the gate data (thread 128)
+            // read the gate data (thread 0): the two sides run a chunk apart
             mbar_init(&bars->empty[s], 2);
-            mbar_init(&bars->bar_d[s], 1);
-            mbar_init(&bars->bar_o[s], 1);
-            mbar_init(&bars->dfree[s], 1);
-            mbar_init(&bars->vready[s], 1);
         }
+        mbar_init(&bars->bar_d, 1);
         mbar_init(&bars->bar_s, 1);
-        mbar_init(&bars->grp_state, 4);
-        mbar_init(&bars->grp_v, 2);
+        mbar_init(&bars->bar_o, 1);
+        mbar_init(&bars->vready, 1);
+        mbar_init(&bars->grp128, 4);
         mbar_init(&bars->grp_out, 2);
+        mbar_init(&bars->grp_v, 2);
         mbar_init(&bars->fin0, 1);
         mbar_init(&bars->fin64, 1);
-        mbar_init(&bars->fin128, 1);
         bars->abort_flag = 0;
         fence_mbar_init();
     }
@@ -225,17 +211,12 @@ __global__ void __launch_bounds__(kGcThreads, 1)
     if (!seq_ok && threadIdx.x == 0 && h == 0) record_error(p.status, KKT_ERR_SEQLENS);
     const int nchunks = seq_ok ? (int)((b - a + kGcC - 1) / kGcC) : 0;
 
-    if (warp == 6) {
+    if (warp == 4) {
         // ------------------------------------------------------------------ loads
         if (lane == 0) {
             prefetch_tmap(&map_q);
             prefetch_tmap(&map_k);
             prefetch_tmap(&map_w);
-            prefetch_tmap(&map_u);
-            if (nchunks > 0) {  // U~ rows of the first chunk into L2
-                tma_prefetch_3d(&map_u, 0, h, (int)a);
-                tma_prefetch_3d(&map_u, 64, h, (int)a);
-            }
         }
         int c = 0;
         bool ok = true;
@@ -263,10 +244,6 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                     tma_load_3d(st + kOffQW + c2 * 16384 + 8192, &map_w, &bars->full[s], 64 * c2, h, (int)t0);
                     tma_load_3d(st + kOffSK + c2 * kBoxSK + kOffKInBox, &map_k, &bars->full[s], 64 * c2, h,
                                 (int)t0);
-                }
-                if (c + 1 < nchunks) {  // the next chunk's U~ rows into L2
-                    tma_prefetch_3d(&map_u, 0, h, (int)(t0 + kGcC));
-                    tma_prefetch_3d(&map_u, 64, h, (int)(t0 + kGcC));
                 }
             }
             if constexpr (GATED) {
@@ -298,12 +275,15 @@ __global__ void __launch_bounds__(kGcThreads, 1)
             }
         }
         __syncwarp();
-    } else if (warp < 4) {
-        // ------------------------------------------------------------------ state warps
+    } else {
+        // ------------------------------------------------------------------ math warps
         const int t = threadIdx.x;                        // tensor-memory lane = row
+        const bool out_side = t < 64;                     // rows 0..63: P, O; rows 64..127: W S, V'
         const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+        uint8_t *pb = smem + kOffPb;
+        uint8_t *vb = smem + kOffVb;
         uint8_t *vf = smem + kOffVf;
-        uint32_t ug = 0, uv = 0;
+        uint32_t u128 = 0, uside = 0;
         bool ok = true;
         const int64_t state_base = ((int64_t)seq * p.H + h) * kGcD * kGcD;
 
@@ -320,22 +300,48 @@ __global__ void __launch_bounds__(kGcThreads, 1)
         tmem_wait_st();
         tc_fence_before();
 
+        // O of chunk cp (buffer cp & 1), rows 0..63 (threads 0..63): scale, bf16, plain stores
+        auto drain_o = [&](int cp, int64_t t0p, int Lcp) -> bool {
+            if (!gc_wait(&bars->bar_o, (uint32_t)cp & 1u, bars, p.status)) return false;
+            tc_fence_after();
+            const uint32_t dcol = (cp & 1) ? kColD1 : kColD0;
+#pragma unroll 1
+            for (int piece = 0; piece < 4; ++piece) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_base + dcol + 32 * piece, v);
+                tmem_wait_ld();
+                if (t < Lcp) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + ((t0p + t) * p.H + h) * kGcD + 32 * piece);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        dst[j] = make_uint4(
+                            pack2_bf16(p.scale * __uint_as_float(v[8 * j]), p.scale * __uint_as_float(v[8 * j + 1])),
+                            pack2_bf16(p.scale * __uint_as_float(v[8 * j + 2]), p.scale * __uint_as_float(v[8 * j + 3])),
+                            pack2_bf16(p.scale * __uint_as_float(v[8 * j + 4]), p.scale * __uint_as_float(v[8 * j + 5])),
+                            pack2_bf16(p.scale * __uint_as_float(v[8 * j + 6]), p.scale * __uint_as_float(v[8 * j + 7])));
+                }
+            }
+            tc_fence_before();
+            return true;
+        };
+
+        if (!gc_group(&bars->grp128, u128, bars, p.status)) ok = false;
+        int64_t prev_t0 = 0;
+        int prev_Lc = 0;
         int c = 0;
         for (; ok && c < nchunks; ++c) {
             const int s = c & 1;
             uint8_t *st = stage(s);
             uint8_t *sk = st + kOffSK;
-            uint8_t *vb = smem + kOffVb + (c & 1) * 16384;
             if (!gc_wait(&bars->full[s], ((uint32_t)c >> 1) & 1u, bars, p.status)) { ok = false; break; }
             if (t == 0) GC_TRACE(0, c);
             const GcInfo info = *stage_info(s);
             const int Lc = info.Lc;
             const float *G = stage_G(s);
-            // rows 64..127: this chunk's row of U~ (in L2 since the previous chunk), in flight during
-            // the readback
+            // rows 64..127: this chunk's row of U~, from global memory, in flight during the readback
             const int i = t - 64;
             uint4 ur[16];
-            if (t >= 64) {
+            if (!out_side) {
                 const uint4 *src = reinterpret_cast<const uint4 *>(p.u + ((info.t0 + i) * p.H + h) * kGcD);
 #pragma unroll
                 for (int e = 0; e < 16; ++e) ur[e] = (i < Lc) ? __ldg(src + e) : make_uint4(0, 0, 0, 0);
@@ -356,100 +362,82 @@ __global__ void __launch_bounds__(kGcThreads, 1)
             tc_fence_after();
             if (t == 0) GC_TRACE(1, c);
             const float glast = GATED ? exp2f(G[Lc - 1]) : 1.f;
+#pragma unroll 1
+            for (int piece = 0; piece < 4; ++piece) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_base + kColS + 32 * piece, v);
+                tmem_wait_ld();
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t v[2][32];
-                tmem_ld32xN<2>(tmem + lane_base + kColS + 64 * half, v);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t *x = &v[j >> 2][8 * (j & 3)];
-                    *sw_chunk(sk + half * kBoxSK, t, j) =
-                        make_uint4(pack2_bf16(__uint_as_float(x[0]), __uint_as_float(x[1])),
-                                   pack2_bf16(__uint_as_float(x[2]), __uint_as_float(x[3])),
-                                   pack2_bf16(__uint_as_float(x[4]), __uint_as_float(x[5])),
-                                   pack2_bf16(__uint_as_float(x[6]), __uint_as_float(x[7])));
-                }
+                for (int j = 0; j < 4; ++j)
+                    *sw_chunk(sk + (piece >> 1) * kBoxSK, t, (piece & 1) * 4 + j) = make_uint4(
+                        pack2_bf16(__uint_as_float(v[8 * j]), __uint_as_float(v[8 * j + 1])),
+                        pack2_bf16(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
+                        pack2_bf16(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
+                        pack2_bf16(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
                 if constexpr (GATED) {
+                    uint32_t w0[16], w1[16];
 #pragma unroll
-                    for (int q2 = 0; q2 < 2; ++q2) {
-                        uint32_t w0[16], w1[16];
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            w0[e] = __float_as_uint(glast * __uint_as_float(v[q2][e]));
-                            w1[e] = __float_as_uint(glast * __uint_as_float(v[q2][16 + e]));
-                        }
-                        tmem_st16(tmem + lane_base + kColS + 64 * half + 32 * q2, w0);
-                        tmem_st16(tmem + lane_base + kColS + 64 * half + 32 * q2 + 16, w1);
+                    for (int e = 0; e < 16; ++e) {
+                        w0[e] = __float_as_uint(glast * __uint_as_float(v[e]));
+                        w1[e] = __float_as_uint(glast * __uint_as_float(v[16 + e]));
                     }
+                    tmem_st16(tmem + lane_base + kColS + 32 * piece, w0);
+                    tmem_st16(tmem + lane_base + kColS + 32 * piece + 16, w1);
                 }
             }
             if constexpr (GATED) tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
-            if (!gc_group(&bars->grp_state, ug, bars, p.status)) { ok = false; break; }
+            if (!gc_group(&bars->grp128, u128, bars, p.status)) { ok = false; break; }
             if (t == 0) GC_TRACE(11, c);
-            // D = [Q; W] [S^T_b; K]^T, into the buffer the output side drained two chunks ago
+            // D = [Q; W] [S^T_b; K]^T
             const uint32_t dcol = (c & 1) ? kColD1 : kColD0;
             if (t == 0) {
-                volatile int *abort = &bars->abort_flag;
-                bool fine = true;
-                if (c >= 2 && !mbar_wait(&bars->dfree[c & 1], ((uint32_t)(c - 2) >> 1) & 1u, abort, kGcWaitNs)) {
-                    fine = false;
-                    if (atomicExch(&bars->abort_flag, 1) == 0) record_error(p.status, KKT_ERR_TIMEOUT);
-                }
-                if (fine) {
-                    tc_fence_after();
-                    const uint32_t idesc_d = idesc_bf16_f32(128, kGcD + kGcC, 0, 0);
-                    const uint32_t qw = smem_u32(st + kOffQW), b0 = smem_u32(sk);
+                tc_fence_after();
+                const uint32_t idesc_d = idesc_bf16_f32(128, kGcD + kGcC, 0, 0);
+                const uint32_t qw = smem_u32(st + kOffQW), b0 = smem_u32(sk);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ss(tmem + dcol, sw128_desc(qw + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                               sw128_desc(b0 + (kk >> 2) * kBoxSK + (kk & 3) * 32, 16, 1024), idesc_d,
-                               kk > 0 ? 1u : 0u);
-                    mma_commit(&bars->bar_d[c & 1]);
-                    GC_TRACE(2, c);
-                }
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss(tmem + dcol, sw128_desc(qw + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                           sw128_desc(b0 + (kk >> 2) * kBoxSK + (kk & 3) * 32, 16, 1024), idesc_d, kk > 0 ? 1u : 0u);
+                mma_commit(&bars->bar_d);
+                GC_TRACE(2, c);
             }
-            __syncwarp();
-            if (t >= 64) {
-                // W S row -> V' = U~ - W S (zero past the chunk's end) -> V'_b (and VF_b) row i.  The
-                // V'_b buffer was last read by the P V' product of chunk c - 2.
-                if (!gc_wait(&bars->bar_d[c & 1], ((uint32_t)c >> 1) & 1u, bars, p.status)) { ok = false; break; }
-                if (c >= 2 && !gc_wait(&bars->bar_o[c & 1], ((uint32_t)(c - 2) >> 1) & 1u, bars, p.status)) {
-                    ok = false;
-                    break;
-                }
+            if (!out_side) {
+                // W S row -> V' = U~ - W S (zero past the chunk's end) -> V'_b (and VF_b) row i
+                if (!gc_wait(&bars->bar_d, (uint32_t)c & 1u, bars, p.status)) { ok = false; break; }
                 tc_fence_after();
                 if (t == 64) GC_TRACE(3, c);
                 const float fi = (GATED && i < Lc) ? exp2f(G[Lc - 1] - G[i]) : 1.f;
+#pragma unroll  // (unrolled: the U~ row stays in registers)
+                for (int piece = 0; piece < 4; ++piece) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_base + dcol + 32 * piece, v);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t v[2][32];
-                    tmem_ld32xN<2>(tmem + lane_base + dcol + 64 * half, v);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint32_t *x = &v[j >> 2][8 * (j & 3)];
-                        const uint4 uu = ur[8 * half + j];
+                    for (int j = 0; j < 4; ++j) {
+                        const int ch = (piece & 1) * 4 + j;
+                        const uint4 uu = ur[4 * piece + j];
                         const uint32_t uw[4] = {uu.x, uu.y, uu.z, uu.w};
                         uint32_t o1[4], o2[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const float2 uf = unpack2_bf16(uw[e]);
-                            float y0 = uf.x - __uint_as_float(x[2 * e]);
-                            float y1 = uf.y - __uint_as_float(x[2 * e + 1]);
+                            float y0 = uf.x - __uint_as_float(v[8 * j + 2 * e]);
+                            float y1 = uf.y - __uint_as_float(v[8 * j + 2 * e + 1]);
                             if (i >= Lc) y0 = y1 = 0.f;
                             o1[e] = pack2_bf16(y0, y1);
                             o2[e] = pack2_bf16(fi * y0, fi * y1);
                         }
-                        *sw_chunk(vb + half * 8192, i, j) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+                        *sw_chunk(vb + (piece >> 1) * 8192, i, ch) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
                         if constexpr (GATED)
-                            *sw_chunk(vf + half * 8192, i, j) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+                            *sw_chunk(vf + (piece >> 1) * 8192, i, ch) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
                     }
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                if (!gc_group(&bars->grp_v, uv, bars, p.status)) { ok = false; break; }
-                // S^T += V'(F)_b^T K; then V'_b is ready for the output side's P V'
+                if (!gc_group(&bars->grp_v, uside, bars, p.status)) { ok = false; break; }
+                // S^T += V'(F)_b^T K, then tell thread 0 that V'_b is ready for P V'
                 if (t == 64) {
                     GC_TRACE(4, c);
                     tc_fence_after();
@@ -461,13 +449,81 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                                sw128_desc(k0 + kk * 2048, kBoxSK, 1024), idesc_s, 1u);
                     mma_commit(&bars->bar_s);
                     mma_commit(&bars->empty[s]);
-                    mbar_arrive(&bars->vready[c & 1]);
+                    mbar_arrive(&bars->vready);
                     GC_TRACE(5, c);
+                }
+            } else {
+                // the previous chunk's O, while this chunk's products run
+                if (c > 0 && !drain_o(c - 1, prev_t0, prev_Lc)) { ok = false; break; }
+                if (t == 0) GC_TRACE(6, c);
+                // P row t -> causal mask (times Gamma when gated) -> P_b row t
+                if (!gc_wait(&bars->bar_d, (uint32_t)c & 1u, bars, p.status)) { ok = false; break; }
+                tc_fence_after();
+                if (t == 0) GC_TRACE(7, c);
+                const float gi = GATED ? G[t] : 0.f;
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_base + dcol + kColDP + 32 * half, v);
+                    tmem_wait_ld();
+                    float x[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int j = 32 * half + e;
+                        float y = (j <= t && t < Lc) ? __uint_as_float(v[e]) : 0.f;
+                        if constexpr (GATED) y = (j <= t && t < Lc) ? y * exp2f(gi - G[j]) : 0.f;
+                        x[e] = y;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        *sw_chunk(pb, t, 4 * half + j) =
+                            make_uint4(pack2_bf16(x[8 * j], x[8 * j + 1]), pack2_bf16(x[8 * j + 2], x[8 * j + 3]),
+                                       pack2_bf16(x[8 * j + 4], x[8 * j + 5]), pack2_bf16(x[8 * j + 6], x[8 * j + 7]));
+                }
+                if constexpr (GATED) {
+                    // Q S row t -> e^{G_t} Q S (the state term's decay), in place
+                    const float ri = exp2f(gi);
+#pragma unroll 1
+                    for (int piece = 0; piece < 8; ++piece) {
+                        uint32_t v[16];
+                        tmem_ld16(tmem + lane_base + dcol + 16 * piece, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(ri * __uint_as_float(v[e]));
+                        tmem_st16(tmem + lane_base + dcol + 16 * piece, v);
+                    }
+                    tmem_wait_st();
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                if (!gc_group(&bars->grp_out, uside, bars, p.status)) { ok = false; break; }
+                // this side is done with the stage (its gate data); D += [P_b; 0] V'_b once thread 64 has
+                // seen V'_b written
+                if (t == 0) {
+                    GC_TRACE(8, c);
+                    mbar_arrive(&bars->empty[s]);
+                    volatile int *abort = &bars->abort_flag;
+                    if (!mbar_wait(&bars->vready, (uint32_t)c & 1u, abort, kGcWaitNs)) {
+                        if (atomicExch(&bars->abort_flag, 1) == 0) record_error(p.status, KKT_ERR_TIMEOUT);
+                    } else {
+                        tc_fence_after();
+                        const uint32_t idesc_o = idesc_bf16_f32(128, kGcD, 0, 1);
+                        const uint32_t p0 = smem_u32(pb), v0 = smem_u32(vb);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ss(tmem + dcol, sw128_desc(p0 + kk * 32, 16, 1024),
+                                   sw128_desc(v0 + kk * 2048, 8192, 1024), idesc_o, 1u);
+                        mma_commit(&bars->bar_o);
+                        GC_TRACE(9, c);
+                    }
                 }
                 __syncwarp();
             }
+            prev_t0 = info.t0;
+            prev_Lc = Lc;
         }
-        // the final state (lane t holds column t of S)
+        // the last chunk's O, and the final state (lane t holds column t of S)
+        if (ok && nchunks > 0 && out_side && !drain_o(nchunks - 1, prev_t0, prev_Lc)) ok = false;
         if (ok && p.ht) {
             if (nchunks > 0 && !gc_wait(&bars->bar_s, (uint32_t)(nchunks - 1) & 1u, bars, p.status)) ok = false;
             if (ok) {
@@ -483,142 +539,12 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                 }
             }
         }
-        // every MMA this thread issued has completed before tensor memory is released
+        // every MMA this CTA issued has completed before tensor memory is released
         if (t == 0 || t == 64) {
             uint64_t *fin = t == 0 ? &bars->fin0 : &bars->fin64;
             mma_commit(fin);
             volatile int never = 0;
             mbar_wait(fin, 0u, &never, kGcWaitNs);
-        }
-        __syncwarp();
-    } else {
-        // ------------------------------------------------------------------ output warps (4, 5)
-        const int r = threadIdx.x - 128;                  // tensor-memory lane = row of Q / O / P
-        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-        uint8_t *pb = smem + kOffPb;
-        uint32_t uo = 0;
-        bool ok = true;
-
-        // O of chunk cp (buffer cp & 1): scale, bf16, plain stores; then the buffer is free
-        auto drain_o = [&](int cp, int64_t t0p, int Lcp) -> bool {
-            if (!gc_wait(&bars->bar_o[cp & 1], ((uint32_t)cp >> 1) & 1u, bars, p.status)) return false;
-            tc_fence_after();
-            const uint32_t dcol = (cp & 1) ? kColD1 : kColD0;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t v[2][32];
-                tmem_ld32xN<2>(tmem + lane_base + dcol + 64 * half, v);
-                if (r < Lcp) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + ((t0p + r) * p.H + h) * kGcD + 64 * half);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint32_t *x = &v[j >> 2][8 * (j & 3)];
-                        dst[j] = make_uint4(
-                            pack2_bf16(p.scale * __uint_as_float(x[0]), p.scale * __uint_as_float(x[1])),
-                            pack2_bf16(p.scale * __uint_as_float(x[2]), p.scale * __uint_as_float(x[3])),
-                            pack2_bf16(p.scale * __uint_as_float(x[4]), p.scale * __uint_as_float(x[5])),
-                            pack2_bf16(p.scale * __uint_as_float(x[6]), p.scale * __uint_as_float(x[7])));
-                    }
-                }
-            }
-            tc_fence_before();
-            if (!gc_group(&bars->grp_out, uo, bars, p.status)) return false;
-            if (r == 0) mbar_arrive(&bars->dfree[cp & 1]);
-            return true;
-        };
-
-        int64_t prev_t0 = 0;
-        int prev_Lc = 0;
-        int c = 0;
-        for (; ok && c < nchunks; ++c) {
-            const int s = c & 1;
-            const uint32_t dcol = (c & 1) ? kColD1 : kColD0;
-            if (!gc_wait(&bars->full[s], ((uint32_t)c >> 1) & 1u, bars, p.status)) { ok = false; break; }
-            const GcInfo info = *stage_info(s);
-            const int Lc = info.Lc;
-            const float *G = stage_G(s);
-            // the previous chunk's O, while this chunk's products run
-            if (c > 0 && !drain_o(c - 1, prev_t0, prev_Lc)) { ok = false; break; }
-            if (r == 0) GC_TRACE(6, c);
-            // P row r -> causal mask (times Gamma when gated) -> P_b row r
-            if (!gc_wait(&bars->bar_d[c & 1], ((uint32_t)c >> 1) & 1u, bars, p.status)) { ok = false; break; }
-            tc_fence_after();
-            if (r == 0) GC_TRACE(7, c);
-            const float gi = GATED ? G[r] : 0.f;
-            {
-                uint32_t v[2][32];
-                tmem_ld32xN<2>(tmem + lane_base + dcol + kColDP, v);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float y[2];
-#pragma unroll
-                        for (int u2 = 0; u2 < 2; ++u2) {
-                            const int col = 8 * j + 2 * e + u2;
-                            float z = (col <= r && r < Lc) ? __uint_as_float(v[j >> 2][8 * (j & 3) + 2 * e + u2]) : 0.f;
-                            if constexpr (GATED) z = (col <= r && r < Lc) ? z * exp2f(gi - G[col]) : 0.f;
-                            y[u2] = z;
-                        }
-                        w[e] = pack2_bf16(y[0], y[1]);
-                    }
-                    *sw_chunk(pb, r, j) = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-            }
-            if constexpr (GATED) {
-                // Q S row r -> e^{G_r} Q S (the state term's decay), in place
-                const float ri = exp2f(gi);
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t v[2][32];
-                    tmem_ld32xN<2>(tmem + lane_base + dcol + 64 * half, v);
-#pragma unroll
-                    for (int q2 = 0; q2 < 2; ++q2) {
-                        uint32_t w0[16], w1[16];
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            w0[e] = __float_as_uint(ri * __uint_as_float(v[q2][e]));
-                            w1[e] = __float_as_uint(ri * __uint_as_float(v[q2][16 + e]));
-                        }
-                        tmem_st16(tmem + lane_base + dcol + 64 * half + 32 * q2, w0);
-                        tmem_st16(tmem + lane_base + dcol + 64 * half + 32 * q2 + 16, w1);
-                    }
-                }
-                tmem_wait_st();
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            if (!gc_group(&bars->grp_out, uo, bars, p.status)) { ok = false; break; }
-            // done with the stage (its gate data); D += [P_b; 0] V'_b once V'_b is written
-            if (r == 0) {
-                GC_TRACE(8, c);
-                mbar_arrive(&bars->empty[s]);
-                volatile int *abort = &bars->abort_flag;
-                if (!mbar_wait(&bars->vready[c & 1], ((uint32_t)c >> 1) & 1u, abort, kGcWaitNs)) {
-                    if (atomicExch(&bars->abort_flag, 1) == 0) record_error(p.status, KKT_ERR_TIMEOUT);
-                } else {
-                    tc_fence_after();
-                    const uint32_t idesc_o = idesc_bf16_f32(128, kGcD, 0, 1);
-                    const uint32_t p0 = smem_u32(pb), v0 = smem_u32(smem + kOffVb + (c & 1) * 16384);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_ss(tmem + dcol, sw128_desc(p0 + kk * 32, 16, 1024),
-                               sw128_desc(v0 + kk * 2048, 8192, 1024), idesc_o, 1u);
-                    mma_commit(&bars->bar_o[c & 1]);
-                    GC_TRACE(9, c);
-                }
-            }
-            __syncwarp();
-            prev_t0 = info.t0;
-            prev_Lc = Lc;
-        }
-        // the last chunk's O
-        if (ok && nchunks > 0 && !drain_o(nchunks - 1, prev_t0, prev_Lc)) ok = false;
-        if (r == 0) {
-            mma_commit(&bars->fin128);
-            volatile int never = 0;
-            mbar_wait(&bars->fin128, 0u, &never, kGcWaitNs);
         }
         __syncwarp();
     }
@@ -700,11 +626,10 @@ extern "C" int gdn_chunk_state_fwd(const void *q, const void *k, const void *w, 
 #endif
     int rc = status_ptr(&p.status);
     if (rc != KKT_OK) return rc;
-    CUtensorMap mq, mk, mw, mu;
+    CUtensorMap mq, mk, mw;
     if (!make_map(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, ntok, H, kGcD, 64, kGcC) ||
         !make_map(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, ntok, H, kGcD, 64, kGcC) ||
-        !make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, ntok, H, kGcD, 64, kGcC) ||
-        !make_map(&mu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, u, ntok, H, kGcD, 64, kGcC))
+        !make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, ntok, H, kGcD, 64, kGcC))
         return KKT_ERR_CUDA;
     auto kern = g ? gdn_chunk_kernel<true> : gdn_chunk_kernel<false>;
     if (!(g ? gc_ensure_smem<true>() : gc_ensure_smem<false>())) return KKT_ERR_CUDA;
@@ -718,6 +643,6 @@ extern "C" int gdn_chunk_state_fwd(const void *q, const void *k, const void *w, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mw, mu, p) != cudaSuccess) return KKT_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mw, p) != cudaSuccess) return KKT_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? KKT_OK : KKT_ERR_CUDA;
 }
