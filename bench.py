@@ -43,7 +43,8 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
 KERNEL_SOURCES = {"simt": ["kkt_simt.cu", "kkt_internal.cuh", "kkt_debug.cuh"],
-                  "tc": ["kkt_tc.cuh", "kkt_tc.cu", "sm100_ptx.cuh", "kkt_internal.cuh", "kkt_debug.cuh"]}
+                  "tc": ["kkt_tc.cuh", "kkt_tc.cu", "sm100_ptx.cuh", "kkt_internal.cuh", "kkt_debug.cuh",
+                         "tma_host.cuh"]}
 
 
 def parse_args():
