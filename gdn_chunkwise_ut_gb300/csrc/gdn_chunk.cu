@@ -19,14 +19,17 @@
 //   Q, then the 64 rows of W, so that the pair is one 128-row operand) and [S^T_b; K] (per box: the
 //   128 rows of the bf16 copy of S^T, written by the math threads, then the 64 rows of K), Q, W and K
 //   loaded by TMA with the 128-byte swizzle; the bf16 copies P_b of the masked P (rows 64..127
-//   zero), V'_b of V' and, gated, VF_b of diag(e^{G_last - G}) V'.  U~ rows go straight from global
-//   memory to the registers of the threads that use them.
+//   zero), V'_b of V' and, gated, VF_b of diag(e^{G_last - G}) V'.  U~ rows go from global memory
+//   (prefetched into L2 a chunk ahead by the loading warp) to the registers of the threads that use
+//   them.
 // Per chunk, every tcgen05.mma M = 128:
 //   D   = [Q; W] [S^T_b; K]^T   (N = 192: columns 0..127 are [Q S; W S], 128..191 [Q K^T; W K^T])
 //   S^T += V'(F)_b^T K          (A = V'^T and B = K both read MN-major, N = 128, K = 64 tokens)
 //   D  += [P_b; 0] V'_b         (columns 0..127, rows 0..63 become O / scale)
-// The first and third are issued by thread 0, the second by thread 64, so that the state's chain
-// (S^T -> S^T_b, D, V', the S^T update) never waits for the output's side (P, P V', the drain of O).
+// The first two are issued by thread 64, whose warps wait for D anyway, the third by thread 0, so that
+// the state's chain (S^T -> S^T_b, D, V', the S^T update) does not wait for the output side's
+// instructions (P, P V', the drain of O), which run on warps 0-1 and hold their lanes for the next
+// S^T readback.
 // The math threads between the products: S^T row -> S^T_b (and, gated, S^T <- e^{G_last} S^T in
 // place); rows 64..127: W S row -> V' = U~ - W S -> V'_b (and VF_b); rows 0..63: P row -> causal mask
 // (times Gamma when gated) -> P_b, gated Q S row -> e^{G_i} Q S, and O row -> scale -> bf16 -> global.
@@ -153,10 +156,20 @@ __device__ __forceinline__ bool gc_group(uint64_t *bar, uint32_t &uses, GcBars *
     return ok;
 }
 
+// Loads 32 x N consecutive tensor-memory columns of the calling warp's lanes with N loads in flight, then
+// waits once.
+template <int N>
+__device__ __forceinline__ void tmem_ld32xN(uint32_t taddr, uint32_t (&v)[N][32]) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) tmem_ld32(taddr + 32 * i, v[i]);
+    tmem_wait_ld();
+}
+
 template <bool GATED>
 __global__ void __launch_bounds__(kGcThreads, 1)
     gdn_chunk_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                     const __grid_constant__ CUtensorMap map_w, const GcParams p) {
+                     const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_u,
+                     const GcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024_gc(smem_raw);
     GcBars *bars = reinterpret_cast<GcBars *>(smem + kOffBar);
@@ -217,6 +230,11 @@ __global__ void __launch_bounds__(kGcThreads, 1)
             prefetch_tmap(&map_q);
             prefetch_tmap(&map_k);
             prefetch_tmap(&map_w);
+            prefetch_tmap(&map_u);
+            if (nchunks > 0) {  // U~ rows of the first chunk into L2
+                tma_prefetch_3d(&map_u, 0, h, (int)a);
+                tma_prefetch_3d(&map_u, 64, h, (int)a);
+            }
         }
         int c = 0;
         bool ok = true;
@@ -244,6 +262,10 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                     tma_load_3d(st + kOffQW + c2 * 16384 + 8192, &map_w, &bars->full[s], 64 * c2, h, (int)t0);
                     tma_load_3d(st + kOffSK + c2 * kBoxSK + kOffKInBox, &map_k, &bars->full[s], 64 * c2, h,
                                 (int)t0);
+                }
+                if (c + 1 < nchunks) {  // the next chunk's U~ rows into L2 (the math threads load them)
+                    tma_prefetch_3d(&map_u, 0, h, (int)(t0 + kGcC));
+                    tma_prefetch_3d(&map_u, 64, h, (int)(t0 + kGcC));
                 }
             }
             if constexpr (GATED) {
@@ -305,20 +327,21 @@ __global__ void __launch_bounds__(kGcThreads, 1)
             if (!gc_wait(&bars->bar_o, (uint32_t)cp & 1u, bars, p.status)) return false;
             tc_fence_after();
             const uint32_t dcol = (cp & 1) ? kColD1 : kColD0;
-#pragma unroll 1
-            for (int piece = 0; piece < 4; ++piece) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_base + dcol + 32 * piece, v);
-                tmem_wait_ld();
-                if (t < Lcp) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + ((t0p + t) * p.H + h) * kGcD + 32 * piece);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
+            for (int half = 0; half < 2; ++half) {
+                uint32_t v[2][32];
+                tmem_ld32xN<2>(tmem + lane_base + dcol + 64 * half, v);
+                if (t < Lcp) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + ((t0p + t) * p.H + h) * kGcD + 64 * half);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t *x = &v[j >> 2][8 * (j & 3)];
                         dst[j] = make_uint4(
-                            pack2_bf16(p.scale * __uint_as_float(v[8 * j]), p.scale * __uint_as_float(v[8 * j + 1])),
-                            pack2_bf16(p.scale * __uint_as_float(v[8 * j + 2]), p.scale * __uint_as_float(v[8 * j + 3])),
-                            pack2_bf16(p.scale * __uint_as_float(v[8 * j + 4]), p.scale * __uint_as_float(v[8 * j + 5])),
-                            pack2_bf16(p.scale * __uint_as_float(v[8 * j + 6]), p.scale * __uint_as_float(v[8 * j + 7])));
+                            pack2_bf16(p.scale * __uint_as_float(x[0]), p.scale * __uint_as_float(x[1])),
+                            pack2_bf16(p.scale * __uint_as_float(x[2]), p.scale * __uint_as_float(x[3])),
+                            pack2_bf16(p.scale * __uint_as_float(x[4]), p.scale * __uint_as_float(x[5])),
+                            pack2_bf16(p.scale * __uint_as_float(x[6]), p.scale * __uint_as_float(x[7])));
+                    }
                 }
             }
             tc_fence_before();
@@ -362,27 +385,31 @@ __global__ void __launch_bounds__(kGcThreads, 1)
             tc_fence_after();
             if (t == 0) GC_TRACE(1, c);
             const float glast = GATED ? exp2f(G[Lc - 1]) : 1.f;
-#pragma unroll 1
-            for (int piece = 0; piece < 4; ++piece) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_base + kColS + 32 * piece, v);
-                tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    *sw_chunk(sk + (piece >> 1) * kBoxSK, t, (piece & 1) * 4 + j) = make_uint4(
-                        pack2_bf16(__uint_as_float(v[8 * j]), __uint_as_float(v[8 * j + 1])),
-                        pack2_bf16(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
-                        pack2_bf16(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
-                        pack2_bf16(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+            for (int half = 0; half < 2; ++half) {
+                uint32_t v[2][32];
+                tmem_ld32xN<2>(tmem + lane_base + kColS + 64 * half, v);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t *x = &v[j >> 2][8 * (j & 3)];
+                    *sw_chunk(sk + half * kBoxSK, t, j) =
+                        make_uint4(pack2_bf16(__uint_as_float(x[0]), __uint_as_float(x[1])),
+                                   pack2_bf16(__uint_as_float(x[2]), __uint_as_float(x[3])),
+                                   pack2_bf16(__uint_as_float(x[4]), __uint_as_float(x[5])),
+                                   pack2_bf16(__uint_as_float(x[6]), __uint_as_float(x[7])));
+                }
                 if constexpr (GATED) {
-                    uint32_t w0[16], w1[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        w0[e] = __float_as_uint(glast * __uint_as_float(v[e]));
-                        w1[e] = __float_as_uint(glast * __uint_as_float(v[16 + e]));
+                    for (int q2 = 0; q2 < 2; ++q2) {
+                        uint32_t w0[16], w1[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            w0[e] = __float_as_uint(glast * __uint_as_float(v[q2][e]));
+                            w1[e] = __float_as_uint(glast * __uint_as_float(v[q2][16 + e]));
+                        }
+                        tmem_st16(tmem + lane_base + kColS + 64 * half + 32 * q2, w0);
+                        tmem_st16(tmem + lane_base + kColS + 64 * half + 32 * q2 + 16, w1);
                     }
-                    tmem_st16(tmem + lane_base + kColS + 32 * piece, w0);
-                    tmem_st16(tmem + lane_base + kColS + 32 * piece + 16, w1);
                 }
             }
             if constexpr (GATED) tmem_wait_st();
@@ -390,9 +417,9 @@ __global__ void __launch_bounds__(kGcThreads, 1)
             tc_fence_before();
             if (!gc_group(&bars->grp128, u128, bars, p.status)) { ok = false; break; }
             if (t == 0) GC_TRACE(11, c);
-            // D = [Q; W] [S^T_b; K]^T
+            // D = [Q; W] [S^T_b; K]^T, issued from the V' side (thread 64), which waits for it anyway
             const uint32_t dcol = (c & 1) ? kColD1 : kColD0;
-            if (t == 0) {
+            if (t == 64) {
                 tc_fence_after();
                 const uint32_t idesc_d = idesc_bf16_f32(128, kGcD + kGcC, 0, 0);
                 const uint32_t qw = smem_u32(st + kOffQW), b0 = smem_u32(sk);
@@ -406,16 +433,19 @@ __global__ void __launch_bounds__(kGcThreads, 1)
             if (!out_side) {
                 // W S row -> V' = U~ - W S (zero past the chunk's end) -> V'_b (and VF_b) row i
                 if (!gc_wait(&bars->bar_d, (uint32_t)c & 1u, bars, p.status)) { ok = false; break; }
+                // V'_b was last read by the P V' product of chunk c - 1, issued by thread 0
+                if (c > 0 && !gc_wait(&bars->bar_o, (uint32_t)(c - 1) & 1u, bars, p.status)) { ok = false; break; }
                 tc_fence_after();
                 if (t == 64) GC_TRACE(3, c);
                 const float fi = (GATED && i < Lc) ? exp2f(G[Lc - 1] - G[i]) : 1.f;
 #pragma unroll  // (unrolled: the U~ row stays in registers)
-                for (int piece = 0; piece < 4; ++piece) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + lane_base + dcol + 32 * piece, v);
-                    tmem_wait_ld();
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t vv[2][32];
+                    tmem_ld32xN<2>(tmem + lane_base + dcol + 64 * half, vv);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
+                    for (int jj = 0; jj < 8; ++jj) {
+                        const int piece = 2 * half + (jj >> 2), j = jj & 3;
+                        const uint32_t *v = vv[jj >> 2];
                         const int ch = (piece & 1) * 4 + j;
                         const uint4 uu = ur[4 * piece + j];
                         const uint32_t uw[4] = {uu.x, uu.y, uu.z, uu.w};
@@ -461,11 +491,11 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                 tc_fence_after();
                 if (t == 0) GC_TRACE(7, c);
                 const float gi = GATED ? G[t] : 0.f;
-#pragma unroll 1
+                uint32_t vp[2][32];
+                tmem_ld32xN<2>(tmem + lane_base + dcol + kColDP, vp);
+#pragma unroll
                 for (int half = 0; half < 2; ++half) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + lane_base + dcol + kColDP + 32 * half, v);
-                    tmem_wait_ld();
+                    const uint32_t *v = vp[half];
                     float x[32];
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
@@ -626,10 +656,11 @@ extern "C" int gdn_chunk_state_fwd(const void *q, const void *k, const void *w, 
 #endif
     int rc = status_ptr(&p.status);
     if (rc != KKT_OK) return rc;
-    CUtensorMap mq, mk, mw;
+    CUtensorMap mq, mk, mw, mu;
     if (!make_map(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, ntok, H, kGcD, 64, kGcC) ||
         !make_map(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k, ntok, H, kGcD, 64, kGcC) ||
-        !make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, ntok, H, kGcD, 64, kGcC))
+        !make_map(&mw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, ntok, H, kGcD, 64, kGcC) ||
+        !make_map(&mu, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, u, ntok, H, kGcD, 64, kGcC))
         return KKT_ERR_CUDA;
     auto kern = g ? gdn_chunk_kernel<true> : gdn_chunk_kernel<false>;
     if (!(g ? gc_ensure_smem<true>() : gc_ensure_smem<false>())) return KKT_ERR_CUDA;
@@ -643,6 +674,6 @@ extern "C" int gdn_chunk_state_fwd(const void *q, const void *k, const void *w, 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mw, p) != cudaSuccess) return KKT_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kern, mq, mk, mw, mu, p) != cudaSuccess) return KKT_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? KKT_OK : KKT_ERR_CUDA;
 }
