@@ -54,7 +54,7 @@ using namespace ptx;
 
 constexpr int kGcC = 64;
 constexpr int kGcD = 128;                 // d_k = d_v
-constexpr int kGcThreads = 160;           // warps 0-3 math, warp 4 loads
+constexpr int kGcThreads = 192;           // warps 0-3 math, warp 4 loads, warp 5 issues the MMAs
 constexpr uint32_t kGcTmemCols = 512;
 constexpr uint32_t kColS = 0;             // S^T: 128 columns
 constexpr uint32_t kColD0 = 128;          // D buffers: 192 columns each
@@ -85,8 +85,9 @@ struct GcInfo {
 
 struct GcBars {
     uint64_t full[2], empty[2];
-    uint64_t bar_d, bar_s, bar_o, vready;
-    uint64_t grp128, grp_out, grp_v, fin0, fin64;
+    uint64_t bar_d, bar_s, bar_o;
+    uint64_t sb_ready, v_ready, p_ready;  // the math warps' operands are in shared memory
+    uint64_t grp128, fin;
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -109,8 +110,8 @@ struct GcParams {
 
 // Pipeline trace (builds with -DKKT_TRACE only): SM cycle counter at each event of the first chunks of the
 // first CTAs, [cta][chunk][event].
-constexpr int kGcTraceCtas = 4, kGcTraceChunks = 64, kGcTraceEvents = 16;
 #ifdef KKT_TRACE
+constexpr int kGcTraceCtas = 4, kGcTraceChunks = 64, kGcTraceEvents = 16;
 #define GC_TRACE(ev, c)                                                                                   \
     do {                                                                                                  \
         if (p.trace && blockIdx.x < kGcTraceCtas && (c) < kGcTraceChunks)                                 \
@@ -185,19 +186,18 @@ __global__ void __launch_bounds__(kGcThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars->full[s], 2);  // the TMA transaction arrival, then one after the gate data
-            // free again once the S^T update has read K (a tensor-core commit) and the output side has
-            // read the gate data (thread 0): the two sides run a chunk apart
-            mbar_init(&bars->empty[s], 2);
+            // free again once the S^T update has read K (a tensor-core commit) and both output warps have
+            // read the gate data: the two sides run a chunk apart
+            mbar_init(&bars->empty[s], 3);
         }
         mbar_init(&bars->bar_d, 1);
         mbar_init(&bars->bar_s, 1);
         mbar_init(&bars->bar_o, 1);
-        mbar_init(&bars->vready, 1);
+        mbar_init(&bars->sb_ready, 4);
+        mbar_init(&bars->v_ready, 2);
+        mbar_init(&bars->p_ready, 2);
         mbar_init(&bars->grp128, 4);
-        mbar_init(&bars->grp_out, 2);
-        mbar_init(&bars->grp_v, 2);
-        mbar_init(&bars->fin0, 1);
-        mbar_init(&bars->fin64, 1);
+        mbar_init(&bars->fin, 1);
         bars->abort_flag = 0;
         fence_mbar_init();
     }
@@ -297,6 +297,65 @@ __global__ void __launch_bounds__(kGcThreads, 1)
             }
         }
         __syncwarp();
+    } else if (warp == 5) {
+        // ------------------------------------------------------------------ MMA issuer
+        // One thread issues every product, in chunk order, each once the math warps have put its
+        // operands in shared memory: an issue waits while the tensor pipe is busy, and no math warp
+        // should wait there.
+        if (lane == 0) {
+            volatile int *abort = &bars->abort_flag;
+            auto wait = [&](uint64_t *bar, uint32_t parity) {
+                if (mbar_wait(bar, parity, abort, kGcWaitNs)) return true;
+                if (atomicExch(&bars->abort_flag, 1) == 0) record_error(p.status, KKT_ERR_TIMEOUT);
+                return false;
+            };
+            const uint32_t idesc_d = idesc_bf16_f32(128, kGcD + kGcC, 0, 0);
+            const uint32_t idesc_s = idesc_bf16_f32(128, kGcD, 1, 1);
+            const uint32_t idesc_o = idesc_bf16_f32(128, kGcD, 0, 1);
+            const uint32_t p0 = smem_u32(smem + kOffPb), v0 = smem_u32(smem + kOffVb);
+            const uint32_t vs = smem_u32(smem + (GATED ? kOffVf : kOffVb));
+            for (int c = 0; c < nchunks; ++c) {
+                const int s = c & 1;
+                const uint32_t ph = (uint32_t)c & 1u;
+                const uint32_t dcol = (c & 1) ? kColD1 : kColD0;
+                const uint32_t qw = smem_u32(stage(s) + kOffQW), sk0 = smem_u32(stage(s) + kOffSK);
+                // D = [Q; W] [S^T_b; K]^T.  Its buffer was drained: the output warps drain the O of chunk
+                // c - 2 before they make P_b of chunk c - 1 ready, and the P V' of chunk c - 1 was issued
+                // after that.
+                if (!wait(&bars->sb_ready, ph)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss(tmem + dcol, sw128_desc(qw + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                           sw128_desc(sk0 + (kk >> 2) * kBoxSK + (kk & 3) * 32, 16, 1024), idesc_d, kk > 0 ? 1u : 0u);
+                mma_commit(&bars->bar_d);
+                GC_TRACE(2, c);
+                // S^T += V'(F)_b^T K
+                if (!wait(&bars->v_ready, ph)) break;
+                tc_fence_after();
+                GC_TRACE(5, c);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ss(tmem + kColS, sw128_desc(vs + kk * 2048, 8192, 1024),
+                           sw128_desc(sk0 + kOffKInBox + kk * 2048, kBoxSK, 1024), idesc_s, 1u);
+                mma_commit(&bars->bar_s);
+                mma_commit(&bars->empty[s]);
+                // D += [P_b; 0] V'_b
+                if (!wait(&bars->p_ready, ph)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ss(tmem + dcol, sw128_desc(p0 + kk * 32, 16, 1024), sw128_desc(v0 + kk * 2048, 8192, 1024),
+                           idesc_o, 1u);
+                mma_commit(&bars->bar_o);
+                GC_TRACE(9, c);
+            }
+            // every MMA issued here has completed before tensor memory is released
+            mma_commit(&bars->fin);
+            volatile int never = 0;
+            mbar_wait(&bars->fin, 0u, &never, kGcWaitNs);
+        }
+        __syncwarp();
     } else {
         // ------------------------------------------------------------------ math warps
         const int t = threadIdx.x;                        // tensor-memory lane = row
@@ -305,7 +364,7 @@ __global__ void __launch_bounds__(kGcThreads, 1)
         uint8_t *pb = smem + kOffPb;
         uint8_t *vb = smem + kOffVb;
         uint8_t *vf = smem + kOffVf;
-        uint32_t u128 = 0, uside = 0;
+        uint32_t u128 = 0;
         bool ok = true;
         const int64_t state_base = ((int64_t)seq * p.H + h) * kGcD * kGcD;
 
@@ -415,26 +474,15 @@ __global__ void __launch_bounds__(kGcThreads, 1)
             if constexpr (GATED) tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
-            if (!gc_group(&bars->grp128, u128, bars, p.status)) { ok = false; break; }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->sb_ready);  // S^T_b (and the zeroed K rows) are written
             if (t == 0) GC_TRACE(11, c);
-            // D = [Q; W] [S^T_b; K]^T, issued from the V' side (thread 64), which waits for it anyway
             const uint32_t dcol = (c & 1) ? kColD1 : kColD0;
-            if (t == 64) {
-                tc_fence_after();
-                const uint32_t idesc_d = idesc_bf16_f32(128, kGcD + kGcC, 0, 0);
-                const uint32_t qw = smem_u32(st + kOffQW), b0 = smem_u32(sk);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(tmem + dcol, sw128_desc(qw + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                           sw128_desc(b0 + (kk >> 2) * kBoxSK + (kk & 3) * 32, 16, 1024), idesc_d, kk > 0 ? 1u : 0u);
-                mma_commit(&bars->bar_d);
-                GC_TRACE(2, c);
-            }
             if (!out_side) {
                 // W S row -> V' = U~ - W S (zero past the chunk's end) -> V'_b (and VF_b) row i
+                // D is in tensor memory; the P V' product of chunk c - 1, the last reader of V'_b, was
+                // issued before D by the same thread, so it has completed too
                 if (!gc_wait(&bars->bar_d, (uint32_t)c & 1u, bars, p.status)) { ok = false; break; }
-                // V'_b was last read by the P V' product of chunk c - 1, issued by thread 0
-                if (c > 0 && !gc_wait(&bars->bar_o, (uint32_t)(c - 1) & 1u, bars, p.status)) { ok = false; break; }
                 tc_fence_after();
                 if (t == 64) GC_TRACE(3, c);
                 const float fi = (GATED && i < Lc) ? exp2f(G[Lc - 1] - G[i]) : 1.f;
@@ -466,22 +514,9 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                if (!gc_group(&bars->grp_v, uside, bars, p.status)) { ok = false; break; }
-                // S^T += V'(F)_b^T K, then tell thread 0 that V'_b is ready for P V'
-                if (t == 64) {
-                    GC_TRACE(4, c);
-                    tc_fence_after();
-                    const uint32_t idesc_s = idesc_bf16_f32(128, kGcD, 1, 1);
-                    const uint32_t vs = smem_u32(GATED ? vf : vb), k0 = smem_u32(sk + kOffKInBox);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_ss(tmem + kColS, sw128_desc(vs + kk * 2048, 8192, 1024),
-                               sw128_desc(k0 + kk * 2048, kBoxSK, 1024), idesc_s, 1u);
-                    mma_commit(&bars->bar_s);
-                    mma_commit(&bars->empty[s]);
-                    mbar_arrive(&bars->vready);
-                    GC_TRACE(5, c);
-                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->v_ready);  // V'_b (and VF_b) are written
+                if (t == 64) GC_TRACE(4, c);
             } else {
                 // the previous chunk's O, while this chunk's products run
                 if (c > 0 && !drain_o(c - 1, prev_t0, prev_Lc)) { ok = false; break; }
@@ -526,28 +561,13 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                if (!gc_group(&bars->grp_out, uside, bars, p.status)) { ok = false; break; }
-                // this side is done with the stage (its gate data); D += [P_b; 0] V'_b once thread 64 has
-                // seen V'_b written
-                if (t == 0) {
-                    GC_TRACE(8, c);
-                    mbar_arrive(&bars->empty[s]);
-                    volatile int *abort = &bars->abort_flag;
-                    if (!mbar_wait(&bars->vready, (uint32_t)c & 1u, abort, kGcWaitNs)) {
-                        if (atomicExch(&bars->abort_flag, 1) == 0) record_error(p.status, KKT_ERR_TIMEOUT);
-                    } else {
-                        tc_fence_after();
-                        const uint32_t idesc_o = idesc_bf16_f32(128, kGcD, 0, 1);
-                        const uint32_t p0 = smem_u32(pb), v0 = smem_u32(vb);
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_ss(tmem + dcol, sw128_desc(p0 + kk * 32, 16, 1024),
-                                   sw128_desc(v0 + kk * 2048, 8192, 1024), idesc_o, 1u);
-                        mma_commit(&bars->bar_o);
-                        GC_TRACE(9, c);
-                    }
-                }
                 __syncwarp();
+                // P_b (and the decayed Q S) are ready, and this warp is done with the stage's gate data
+                if (lane == 0) {
+                    mbar_arrive(&bars->p_ready);
+                    mbar_arrive(&bars->empty[s]);
+                }
+                if (t == 0) GC_TRACE(8, c);
             }
             prev_t0 = info.t0;
             prev_Lc = Lc;
@@ -568,13 +588,6 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                         p.ht[state_base + (int64_t)(32 * piece + e) * kGcD + t] = __uint_as_float(v[e]);
                 }
             }
-        }
-        // every MMA this CTA issued has completed before tensor memory is released
-        if (t == 0 || t == 64) {
-            uint64_t *fin = t == 0 ? &bars->fin0 : &bars->fin64;
-            mma_commit(fin);
-            volatile int never = 0;
-            mbar_wait(fin, 0u, &never, kGcWaitNs);
         }
         __syncwarp();
     }
