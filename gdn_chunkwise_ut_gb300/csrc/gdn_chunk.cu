@@ -54,7 +54,7 @@ using namespace ptx;
 
 constexpr int kGcC = 64;
 constexpr int kGcD = 128;                 // d_k = d_v
-constexpr int kGcThreads = 192;           // warps 0-3 math, warp 4 loads, warp 5 issues the MMAs
+constexpr int kGcThreads = 320;           // warps 0-7 math, warp 8 loads, warp 9 issues the MMAs
 constexpr uint32_t kGcTmemCols = 512;
 constexpr uint32_t kColS = 0;             // S^T: 128 columns
 constexpr uint32_t kColD0 = 128;          // D buffers: 192 columns each
@@ -142,6 +142,14 @@ __device__ __forceinline__ uint4 *sw_chunk(uint8_t *box, int r, int e) {
     return reinterpret_cast<uint4 *>(box + r * 128 + ((e ^ (r & 7)) << 4));
 }
 
+// 2^x by the hardware's approximation (about 22 correct bits): enough for factors that multiply values
+// rounded to bf16 right after.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ bool gc_wait(uint64_t *bar, uint32_t parity, GcBars *bars, int *status) {
     const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, parity, &bars->abort_flag, kGcWaitNs));
     if (!ok && atomicExch(&bars->abort_flag, 1) == 0) record_error(status, KKT_ERR_TIMEOUT);
@@ -186,17 +194,17 @@ __global__ void __launch_bounds__(kGcThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars->full[s], 2);  // the TMA transaction arrival, then one after the gate data
-            // free again once the S^T update has read K (a tensor-core commit) and both output warps have
-            // read the gate data: the two sides run a chunk apart
-            mbar_init(&bars->empty[s], 3);
+            // free again once the S^T update has read K (a tensor-core commit) and the four output warps
+            // have read the gate data: the two sides run a chunk apart
+            mbar_init(&bars->empty[s], 5);
         }
         mbar_init(&bars->bar_d, 1);
         mbar_init(&bars->bar_s, 1);
         mbar_init(&bars->bar_o, 1);
-        mbar_init(&bars->sb_ready, 4);
-        mbar_init(&bars->v_ready, 2);
-        mbar_init(&bars->p_ready, 2);
-        mbar_init(&bars->grp128, 4);
+        mbar_init(&bars->sb_ready, 8);
+        mbar_init(&bars->v_ready, 4);
+        mbar_init(&bars->p_ready, 4);
+        mbar_init(&bars->grp128, 8);
         mbar_init(&bars->fin, 1);
         bars->abort_flag = 0;
         fence_mbar_init();
@@ -224,7 +232,7 @@ __global__ void __launch_bounds__(kGcThreads, 1)
     if (!seq_ok && threadIdx.x == 0 && h == 0) record_error(p.status, KKT_ERR_SEQLENS);
     const int nchunks = seq_ok ? (int)((b - a + kGcC - 1) / kGcC) : 0;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------------------ loads
         if (lane == 0) {
             prefetch_tmap(&map_q);
@@ -297,7 +305,7 @@ __global__ void __launch_bounds__(kGcThreads, 1)
             }
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ------------------------------------------------------------------ MMA issuer
         // One thread issues every product, in chunk order, each once the math warps have put its
         // operands in shared memory: an issue waits while the tensor pipe is busy, and no math warp
@@ -357,57 +365,59 @@ __global__ void __launch_bounds__(kGcThreads, 1)
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------------ math warps
-        const int t = threadIdx.x;                        // tensor-memory lane = row
-        const bool out_side = t < 64;                     // rows 0..63: P, O; rows 64..127: W S, V'
-        const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+        // ------------------------------------------------------------------ math warps (0-7)
+        // Warp w reads tensor-memory lanes 32 (w & 3) .. + 31 and the half hc = w >> 2 of the columns of
+        // each matrix there: 64 columns of S^T, of D's first 128 columns, and 32 of P's 64.
+        const int q4 = warp & 3;
+        const int hc = warp >> 2;
+        const int row = 32 * q4 + lane;                   // tensor-memory lane = matrix row
+        const bool out_side = row < 64;                   // rows 0..63: P, O; rows 64..127: W S, V'
+        const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
         uint8_t *pb = smem + kOffPb;
         uint8_t *vb = smem + kOffVb;
         uint8_t *vf = smem + kOffVf;
-        uint32_t u128 = 0;
+        uint32_t u256 = 0;
         bool ok = true;
         const int64_t state_base = ((int64_t)seq * p.H + h) * kGcD * kGcD;
 
-        // the initial state into tensor memory: lane t holds column t of S (row t of S^T); the loads
-        // of a warp read 32 consecutive floats of one row of S
+        // the initial state into tensor memory: lane r holds column r of S (row r of S^T); the loads of
+        // a warp read 32 consecutive floats of one row of S
 #pragma unroll 1
-        for (int piece = 0; piece < 8; ++piece) {
+        for (int piece = 0; piece < 4; ++piece) {
             uint32_t v[16];
+            const int d0 = 64 * hc + 16 * piece;
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-                v[e] = p.h0 ? __float_as_uint(__ldg(p.h0 + state_base + (int64_t)(16 * piece + e) * kGcD + t)) : 0u;
-            tmem_st16(tmem + lane_base + kColS + 16 * piece, v);
+                v[e] = p.h0 ? __float_as_uint(__ldg(p.h0 + state_base + (int64_t)(d0 + e) * kGcD + row)) : 0u;
+            tmem_st16(tmem + lane_base + kColS + d0, v);
         }
         tmem_wait_st();
         tc_fence_before();
 
-        // O of chunk cp (buffer cp & 1), rows 0..63 (threads 0..63): scale, bf16, plain stores
+        // O of chunk cp (buffer cp & 1), this warp's 64 columns of rows 0..63: scale, bf16, plain stores
         auto drain_o = [&](int cp, int64_t t0p, int Lcp) -> bool {
             if (!gc_wait(&bars->bar_o, (uint32_t)cp & 1u, bars, p.status)) return false;
             tc_fence_after();
             const uint32_t dcol = (cp & 1) ? kColD1 : kColD0;
+            uint32_t v[2][32];
+            tmem_ld32xN<2>(tmem + lane_base + dcol + 64 * hc, v);
+            if (row < Lcp) {
+                uint4 *dst = reinterpret_cast<uint4 *>(p.o + ((t0p + row) * p.H + h) * kGcD + 64 * hc);
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                uint32_t v[2][32];
-                tmem_ld32xN<2>(tmem + lane_base + dcol + 64 * half, v);
-                if (t < Lcp) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(p.o + ((t0p + t) * p.H + h) * kGcD + 64 * half);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const uint32_t *x = &v[j >> 2][8 * (j & 3)];
-                        dst[j] = make_uint4(
-                            pack2_bf16(p.scale * __uint_as_float(x[0]), p.scale * __uint_as_float(x[1])),
-                            pack2_bf16(p.scale * __uint_as_float(x[2]), p.scale * __uint_as_float(x[3])),
-                            pack2_bf16(p.scale * __uint_as_float(x[4]), p.scale * __uint_as_float(x[5])),
-                            pack2_bf16(p.scale * __uint_as_float(x[6]), p.scale * __uint_as_float(x[7])));
-                    }
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t *x = &v[j >> 2][8 * (j & 3)];
+                    dst[j] = make_uint4(
+                        pack2_bf16(p.scale * __uint_as_float(x[0]), p.scale * __uint_as_float(x[1])),
+                        pack2_bf16(p.scale * __uint_as_float(x[2]), p.scale * __uint_as_float(x[3])),
+                        pack2_bf16(p.scale * __uint_as_float(x[4]), p.scale * __uint_as_float(x[5])),
+                        pack2_bf16(p.scale * __uint_as_float(x[6]), p.scale * __uint_as_float(x[7])));
                 }
             }
             tc_fence_before();
             return true;
         };
 
-        if (!gc_group(&bars->grp128, u128, bars, p.status)) ok = false;
+        if (!gc_group(&bars->grp128, u256, bars, p.status)) ok = false;
         int64_t prev_t0 = 0;
         int prev_Lc = 0;
         int c = 0;
@@ -416,42 +426,42 @@ __global__ void __launch_bounds__(kGcThreads, 1)
             uint8_t *st = stage(s);
             uint8_t *sk = st + kOffSK;
             if (!gc_wait(&bars->full[s], ((uint32_t)c >> 1) & 1u, bars, p.status)) { ok = false; break; }
-            if (t == 0) GC_TRACE(0, c);
+            if (threadIdx.x == 0) GC_TRACE(0, c);
             const GcInfo info = *stage_info(s);
             const int Lc = info.Lc;
             const float *G = stage_G(s);
-            // rows 64..127: this chunk's row of U~, from global memory, in flight during the readback
-            const int i = t - 64;
-            uint4 ur[16];
+            // rows 64..127: this warp's half of the chunk's row of U~ (in L2 since the previous chunk), in
+            // flight during the readback
+            const int i = row - 64;
+            uint4 ur[8];
             if (!out_side) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(p.u + ((info.t0 + i) * p.H + h) * kGcD);
+                const uint4 *src = reinterpret_cast<const uint4 *>(p.u + ((info.t0 + i) * p.H + h) * kGcD + 64 * hc);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) ur[e] = (i < Lc) ? __ldg(src + e) : make_uint4(0, 0, 0, 0);
+                for (int e = 0; e < 8; ++e) ur[e] = (i < Lc) ? __ldg(src + e) : make_uint4(0, 0, 0, 0);
             }
             // rows of a short chunk past its end: K's rows enter V'^T K (times zero rows of V') and
             // the masked columns of P, so they are zeroed (a row of the next sequence, or the fill
             // past the tensor, stays out)
             if (Lc < kGcC) {
                 const int per = (kGcC - Lc) * 8;
-                for (int e = t; e < 2 * per; e += 128) {
+                for (int e = threadIdx.x; e < 2 * per; e += 256) {
                     const int box = e / per, w = e % per;
                     *reinterpret_cast<uint4 *>(sk + box * kBoxSK + kOffKInBox + (Lc + w / 8) * 128 + (w % 8) * 16) =
                         make_uint4(0, 0, 0, 0);
                 }
             }
-            // S^T row t -> S^T_b (the state this chunk starts from), and, gated, S^T <- e^{G_last} S^T
+            // S^T row -> S^T_b (the state this chunk starts from), and, gated, S^T <- e^{G_last} S^T
             if (c > 0 && !gc_wait(&bars->bar_s, (uint32_t)(c - 1) & 1u, bars, p.status)) { ok = false; break; }
             tc_fence_after();
-            if (t == 0) GC_TRACE(1, c);
+            if (threadIdx.x == 0) GC_TRACE(1, c);
             const float glast = GATED ? exp2f(G[Lc - 1]) : 1.f;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
+            {
                 uint32_t v[2][32];
-                tmem_ld32xN<2>(tmem + lane_base + kColS + 64 * half, v);
+                tmem_ld32xN<2>(tmem + lane_base + kColS + 64 * hc, v);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const uint32_t *x = &v[j >> 2][8 * (j & 3)];
-                    *sw_chunk(sk + half * kBoxSK, t, j) =
+                    *sw_chunk(sk + hc * kBoxSK, row, j) =
                         make_uint4(pack2_bf16(__uint_as_float(x[0]), __uint_as_float(x[1])),
                                    pack2_bf16(__uint_as_float(x[2]), __uint_as_float(x[3])),
                                    pack2_bf16(__uint_as_float(x[4]), __uint_as_float(x[5])),
@@ -466,96 +476,98 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                             w0[e] = __float_as_uint(glast * __uint_as_float(v[q2][e]));
                             w1[e] = __float_as_uint(glast * __uint_as_float(v[q2][16 + e]));
                         }
-                        tmem_st16(tmem + lane_base + kColS + 64 * half + 32 * q2, w0);
-                        tmem_st16(tmem + lane_base + kColS + 64 * half + 32 * q2 + 16, w1);
+                        tmem_st16(tmem + lane_base + kColS + 64 * hc + 32 * q2, w0);
+                        tmem_st16(tmem + lane_base + kColS + 64 * hc + 32 * q2 + 16, w1);
                     }
+                    tmem_wait_st();
                 }
             }
-            if constexpr (GATED) tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->sb_ready);  // S^T_b (and the zeroed K rows) are written
-            if (t == 0) GC_TRACE(11, c);
+            if (threadIdx.x == 0) GC_TRACE(11, c);
             const uint32_t dcol = (c & 1) ? kColD1 : kColD0;
             if (!out_side) {
-                // W S row -> V' = U~ - W S (zero past the chunk's end) -> V'_b (and VF_b) row i
-                // D is in tensor memory; the P V' product of chunk c - 1, the last reader of V'_b, was
-                // issued before D by the same thread, so it has completed too
+                // W S row -> V' = U~ - W S (zero past the chunk's end) -> V'_b (and VF_b), this warp's
+                // 64 columns.  D is in tensor memory; the P V' product of chunk c - 1, the last reader of
+                // V'_b, was issued before D by the same thread, so it has completed too.
                 if (!gc_wait(&bars->bar_d, (uint32_t)c & 1u, bars, p.status)) { ok = false; break; }
                 tc_fence_after();
-                if (t == 64) GC_TRACE(3, c);
+                if (threadIdx.x == 64) GC_TRACE(3, c);
                 const float fi = (GATED && i < Lc) ? exp2f(G[Lc - 1] - G[i]) : 1.f;
-#pragma unroll  // (unrolled: the U~ row stays in registers)
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t vv[2][32];
-                    tmem_ld32xN<2>(tmem + lane_base + dcol + 64 * half, vv);
+                uint32_t vv[2][32];
+                tmem_ld32xN<2>(tmem + lane_base + dcol + 64 * hc, vv);
 #pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) {
-                        const int piece = 2 * half + (jj >> 2), j = jj & 3;
-                        const uint32_t *v = vv[jj >> 2];
-                        const int ch = (piece & 1) * 4 + j;
-                        const uint4 uu = ur[4 * piece + j];
-                        const uint32_t uw[4] = {uu.x, uu.y, uu.z, uu.w};
-                        uint32_t o1[4], o2[4];
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t *x = &vv[j >> 2][8 * (j & 3)];
+                    const uint4 uu = ur[j];
+                    const uint32_t uw[4] = {uu.x, uu.y, uu.z, uu.w};
+                    uint32_t o1[4], o2[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float2 uf = unpack2_bf16(uw[e]);
-                            float y0 = uf.x - __uint_as_float(v[8 * j + 2 * e]);
-                            float y1 = uf.y - __uint_as_float(v[8 * j + 2 * e + 1]);
-                            if (i >= Lc) y0 = y1 = 0.f;
-                            o1[e] = pack2_bf16(y0, y1);
-                            o2[e] = pack2_bf16(fi * y0, fi * y1);
-                        }
-                        *sw_chunk(vb + (piece >> 1) * 8192, i, ch) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-                        if constexpr (GATED)
-                            *sw_chunk(vf + (piece >> 1) * 8192, i, ch) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 uf = unpack2_bf16(uw[e]);
+                        float y0 = uf.x - __uint_as_float(x[2 * e]);
+                        float y1 = uf.y - __uint_as_float(x[2 * e + 1]);
+                        if (i >= Lc) y0 = y1 = 0.f;
+                        o1[e] = pack2_bf16(y0, y1);
+                        o2[e] = pack2_bf16(fi * y0, fi * y1);
                     }
+                    *sw_chunk(vb + hc * 8192, i, j) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+                    if constexpr (GATED)
+                        *sw_chunk(vf + hc * 8192, i, j) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->v_ready);  // V'_b (and VF_b) are written
-                if (t == 64) GC_TRACE(4, c);
+                if (lane == 0) mbar_arrive(&bars->v_ready);  // this warp's part of V'_b (and VF_b)
+                if (threadIdx.x == 64) GC_TRACE(4, c);
             } else {
                 // the previous chunk's O, while this chunk's products run
                 if (c > 0 && !drain_o(c - 1, prev_t0, prev_Lc)) { ok = false; break; }
-                if (t == 0) GC_TRACE(6, c);
-                // P row t -> causal mask (times Gamma when gated) -> P_b row t
+                if (threadIdx.x == 0) GC_TRACE(6, c);
+                // P row -> causal mask (times Gamma when gated) -> P_b, this warp's 32 columns
                 if (!gc_wait(&bars->bar_d, (uint32_t)c & 1u, bars, p.status)) { ok = false; break; }
                 tc_fence_after();
-                if (t == 0) GC_TRACE(7, c);
-                const float gi = GATED ? G[t] : 0.f;
-                uint32_t vp[2][32];
-                tmem_ld32xN<2>(tmem + lane_base + dcol + kColDP, vp);
+                if (threadIdx.x == 0) GC_TRACE(7, c);
+                const float gi = GATED ? G[row] : 0.f;
+                {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + lane_base + dcol + kColDP + 32 * hc, v);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const uint32_t *v = vp[half];
-                    float x[32];
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t w[4];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int j = 32 * half + e;
-                        float y = (j <= t && t < Lc) ? __uint_as_float(v[e]) : 0.f;
-                        if constexpr (GATED) y = (j <= t && t < Lc) ? y * exp2f(gi - G[j]) : 0.f;
-                        x[e] = y;
+                        for (int e = 0; e < 4; ++e) {
+                            float y[2];
+#pragma unroll
+                            for (int u2 = 0; u2 < 2; ++u2) {
+                                const int col = 32 * hc + 8 * j + 2 * e + u2;
+                                float z = (col <= row && row < Lc) ? __uint_as_float(v[8 * j + 2 * e + u2]) : 0.f;
+                                if constexpr (GATED) z = (col <= row && row < Lc) ? z * fast_exp2(gi - G[col]) : 0.f;
+                                y[u2] = z;
+                            }
+                            w[e] = pack2_bf16(y[0], y[1]);
+                        }
+                        *sw_chunk(pb, row, 4 * hc + j) = make_uint4(w[0], w[1], w[2], w[3]);
                     }
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        *sw_chunk(pb, t, 4 * half + j) =
-                            make_uint4(pack2_bf16(x[8 * j], x[8 * j + 1]), pack2_bf16(x[8 * j + 2], x[8 * j + 3]),
-                                       pack2_bf16(x[8 * j + 4], x[8 * j + 5]), pack2_bf16(x[8 * j + 6], x[8 * j + 7]));
                 }
                 if constexpr (GATED) {
-                    // Q S row t -> e^{G_t} Q S (the state term's decay), in place
+                    // Q S row -> e^{G_row} Q S (the state term's decay), in place, this warp's 64 columns
                     const float ri = exp2f(gi);
-#pragma unroll 1
-                    for (int piece = 0; piece < 8; ++piece) {
-                        uint32_t v[16];
-                        tmem_ld16(tmem + lane_base + dcol + 16 * piece, v);
-                        tmem_wait_ld();
+                    uint32_t v[2][32];
+                    tmem_ld32xN<2>(tmem + lane_base + dcol + 64 * hc, v);
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(ri * __uint_as_float(v[e]));
-                        tmem_st16(tmem + lane_base + dcol + 16 * piece, v);
+                    for (int q2 = 0; q2 < 2; ++q2) {
+                        uint32_t w0[16], w1[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            w0[e] = __float_as_uint(ri * __uint_as_float(v[q2][e]));
+                            w1[e] = __float_as_uint(ri * __uint_as_float(v[q2][16 + e]));
+                        }
+                        tmem_st16(tmem + lane_base + dcol + 64 * hc + 32 * q2, w0);
+                        tmem_st16(tmem + lane_base + dcol + 64 * hc + 32 * q2 + 16, w1);
                     }
                     tmem_wait_st();
                 }
@@ -567,26 +579,22 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                     mbar_arrive(&bars->p_ready);
                     mbar_arrive(&bars->empty[s]);
                 }
-                if (t == 0) GC_TRACE(8, c);
+                if (threadIdx.x == 0) GC_TRACE(8, c);
             }
             prev_t0 = info.t0;
             prev_Lc = Lc;
         }
-        // the last chunk's O, and the final state (lane t holds column t of S)
+        // the last chunk's O, and the final state (lane r holds column r of S)
         if (ok && nchunks > 0 && out_side && !drain_o(nchunks - 1, prev_t0, prev_Lc)) ok = false;
         if (ok && p.ht) {
             if (nchunks > 0 && !gc_wait(&bars->bar_s, (uint32_t)(nchunks - 1) & 1u, bars, p.status)) ok = false;
             if (ok) {
                 tc_fence_after();
-#pragma unroll 1
-                for (int piece = 0; piece < 4; ++piece) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem + lane_base + kColS + 32 * piece, v);
-                    tmem_wait_ld();
+                uint32_t v[2][32];
+                tmem_ld32xN<2>(tmem + lane_base + kColS + 64 * hc, v);
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        p.ht[state_base + (int64_t)(32 * piece + e) * kGcD + t] = __uint_as_float(v[e]);
-                }
+                for (int e = 0; e < 64; ++e)
+                    p.ht[state_base + (int64_t)(64 * hc + e) * kGcD + row] = __uint_as_float(v[e >> 5][e & 31]);
             }
         }
         __syncwarp();
