@@ -458,6 +458,7 @@ __global__ void __launch_bounds__(kGcThreads, 1)
             {
                 uint32_t v[2][32];
                 tmem_ld32xN<2>(tmem + lane_base + kColS + 64 * hc, v);
+                if (threadIdx.x == 0) GC_TRACE(15, c);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const uint32_t *x = &v[j >> 2][8 * (j & 3)];
@@ -498,6 +499,7 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                 const float fi = (GATED && i < Lc) ? exp2f(G[Lc - 1] - G[i]) : 1.f;
                 uint32_t vv[2][32];
                 tmem_ld32xN<2>(tmem + lane_base + dcol + 64 * hc, vv);
+                if (threadIdx.x == 64) GC_TRACE(12, c);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const uint32_t *x = &vv[j >> 2][8 * (j & 3)];
@@ -517,7 +519,9 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                     if constexpr (GATED)
                         *sw_chunk(vf + hc * 8192, i, j) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
                 }
+                if (threadIdx.x == 64) GC_TRACE(13, c);
                 fence_proxy_async_smem();
+                if (threadIdx.x == 64) GC_TRACE(14, c);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bars->v_ready);  // this warp's part of V'_b (and VF_b)
