@@ -19,9 +19,8 @@
 //   Q, then the 64 rows of W, so that the pair is one 128-row operand) and [S^T_b; K] (per box: the
 //   128 rows of the bf16 copy of S^T, written by the math threads, then the 64 rows of K), Q, W and K
 //   loaded by TMA with the 128-byte swizzle; the bf16 copies P_b of the masked P (rows 64..127
-//   zero), V'_b of V' and, gated, VF_b of diag(e^{G_last - G}) V'.  U~ rows go from global memory
-//   (prefetched into L2 a chunk ahead by the loading warp) to the registers of the threads that use
-//   them.
+//   zero), V'_b of V' and, gated, VF_b of diag(e^{G_last - G}) V'; a one-chunk buffer of U~ (TMA,
+//   prefetched into L2 a chunk earlier), refilled as soon as the V' warps have read it.
 // Per chunk, every tcgen05.mma M = 128:
 //   D   = [Q; W] [S^T_b; K]^T   (N = 192: columns 0..127 are [Q S; W S], 128..191 [Q K^T; W K^T])
 //   S^T += V'(F)_b^T K          (A = V'^T and B = K both read MN-major, N = 128, K = 64 tokens)
@@ -71,7 +70,8 @@ constexpr int kOffKInBox = 16384;
 constexpr int kOffPb = 2 * kStageBytes;   // [128 rows][128 B]
 constexpr int kOffVb = kOffPb + 16384;    // 2 boxes x [64 rows][128 B]
 constexpr int kOffVf = kOffVb + 16384;
-constexpr int kOffMeta = kOffVf + 16384;  // per stage 512 B: G[64] (log2 units), then the chunk info
+constexpr int kOffU = kOffVf + 16384;     // U~ of one chunk: 2 boxes x [64 rows][128 B]
+constexpr int kOffMeta = kOffU + 16384;   // per stage 512 B: G[64] (log2 units), then the chunk info
 constexpr int kOffBar = kOffMeta + 1024;
 constexpr int kGcSmem = kOffBar + 256 + 1024;  // + alignment slack
 static_assert(kGcSmem <= 232448, "shared memory over the per-block limit");
@@ -87,6 +87,7 @@ struct GcBars {
     uint64_t full[2], empty[2];
     uint64_t bar_d, bar_s, bar_o;
     uint64_t sb_ready, v_ready, p_ready;  // the math warps' operands are in shared memory
+    uint64_t u_full, u_empty;             // the U~ buffer (one chunk)
     uint64_t grp128, fin;
     uint32_t tmem_base;
     int abort_flag;
@@ -205,6 +206,8 @@ __global__ void __launch_bounds__(kGcThreads, 1)
         mbar_init(&bars->v_ready, 4);
         mbar_init(&bars->p_ready, 4);
         mbar_init(&bars->grp128, 8);
+        mbar_init(&bars->u_full, 1);
+        mbar_init(&bars->u_empty, 4);
         mbar_init(&bars->fin, 1);
         bars->abort_flag = 0;
         fence_mbar_init();
@@ -271,10 +274,17 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                     tma_load_3d(st + kOffSK + c2 * kBoxSK + kOffKInBox, &map_k, &bars->full[s], 64 * c2, h,
                                 (int)t0);
                 }
-                if (c + 1 < nchunks) {  // the next chunk's U~ rows into L2 (the math threads load them)
+                if (c + 1 < nchunks) {  // the next chunk's U~ rows into L2
                     tma_prefetch_3d(&map_u, 0, h, (int)(t0 + kGcC));
                     tma_prefetch_3d(&map_u, 64, h, (int)(t0 + kGcC));
                 }
+            }
+            // this chunk's U~ into the one-chunk buffer once the V' warps are done with the previous one
+            if (c > 0 && !gc_wait(&bars->u_empty, ((uint32_t)c - 1u) & 1u, bars, p.status)) { ok = false; break; }
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bars->u_full, 16384);
+                tma_load_3d(smem + kOffU, &map_u, &bars->u_full, 0, h, (int)t0);
+                tma_load_3d(smem + kOffU + 8192, &map_u, &bars->u_full, 64, h, (int)t0);
             }
             if constexpr (GATED) {
                 // inclusive prefix sums over the chunk: G_i = g_0 + ... + g_i
@@ -298,11 +308,12 @@ __global__ void __launch_bounds__(kGcThreads, 1)
         }
         // after a timeout: the loads already issued must land before shared memory is released
         if (!ok && lane == 0) {
+            volatile int never = 0;
             for (int back = 1; back <= 2 && back <= c; ++back) {
                 const int j = c - back;
-                volatile int never = 0;
                 mbar_wait(&bars->full[j & 1], ((uint32_t)j >> 1) & 1u, &never, kGcWaitNs);
             }
+            if (c > 0) mbar_wait(&bars->u_full, ((uint32_t)c - 1u) & 1u, &never, kGcWaitNs);  // the last U~ load
         }
         __syncwarp();
     } else if (warp == 9) {
@@ -430,15 +441,7 @@ __global__ void __launch_bounds__(kGcThreads, 1)
             const GcInfo info = *stage_info(s);
             const int Lc = info.Lc;
             const float *G = stage_G(s);
-            // rows 64..127: this warp's half of the chunk's row of U~ (in L2 since the previous chunk), in
-            // flight during the readback
             const int i = row - 64;
-            uint4 ur[8];
-            if (!out_side) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(p.u + ((info.t0 + i) * p.H + h) * kGcD + 64 * hc);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) ur[e] = (i < Lc) ? __ldg(src + e) : make_uint4(0, 0, 0, 0);
-            }
             // rows of a short chunk past its end: K's rows enter V'^T K (times zero rows of V') and
             // the masked columns of P, so they are zeroed (a row of the next sequence, or the fill
             // past the tensor, stays out)
@@ -494,6 +497,7 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                 // 64 columns.  D is in tensor memory; the P V' product of chunk c - 1, the last reader of
                 // V'_b, was issued before D by the same thread, so it has completed too.
                 if (!gc_wait(&bars->bar_d, (uint32_t)c & 1u, bars, p.status)) { ok = false; break; }
+                if (!gc_wait(&bars->u_full, (uint32_t)c & 1u, bars, p.status)) { ok = false; break; }
                 tc_fence_after();
                 if (threadIdx.x == 64) GC_TRACE(3, c);
                 const float fi = (GATED && i < Lc) ? exp2f(G[Lc - 1] - G[i]) : 1.f;
@@ -503,7 +507,7 @@ __global__ void __launch_bounds__(kGcThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const uint32_t *x = &vv[j >> 2][8 * (j & 3)];
-                    const uint4 uu = ur[j];
+                    const uint4 uu = *sw_chunk(smem + kOffU + hc * 8192, i, j);
                     const uint32_t uw[4] = {uu.x, uu.y, uu.z, uu.w};
                     uint32_t o1[4], o2[4];
 #pragma unroll
@@ -524,7 +528,10 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                 if (threadIdx.x == 64) GC_TRACE(14, c);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->v_ready);  // this warp's part of V'_b (and VF_b)
+                if (lane == 0) {
+                    mbar_arrive(&bars->v_ready);  // this warp's part of V'_b (and VF_b)
+                    mbar_arrive(&bars->u_empty);  // and its reads of the U~ buffer are done
+                }
                 if (threadIdx.x == 64) GC_TRACE(4, c);
             } else {
                 // the previous chunk's O, while this chunk's products run
