@@ -501,13 +501,19 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                 tc_fence_after();
                 if (threadIdx.x == 64) GC_TRACE(3, c);
                 const float fi = (GATED && i < Lc) ? exp2f(G[Lc - 1] - G[i]) : 1.f;
+                // the row's U~ chunks into registers before any store: the compiler cannot tell the
+                // V'_b stores from the U~ buffer, and would otherwise wait for each store before the
+                // next load
+                uint4 ur[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) ur[j] = *sw_chunk(smem + kOffU + hc * 8192, i, j);
                 uint32_t vv[2][32];
                 tmem_ld32xN<2>(tmem + lane_base + dcol + 64 * hc, vv);
                 if (threadIdx.x == 64) GC_TRACE(12, c);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const uint32_t *x = &vv[j >> 2][8 * (j & 3)];
-                    const uint4 uu = *sw_chunk(smem + kOffU + hc * 8192, i, j);
+                    const uint4 uu = ur[j];
                     const uint32_t uw[4] = {uu.x, uu.y, uu.z, uu.w};
                     uint32_t o1[4], o2[4];
 #pragma unroll
@@ -543,6 +549,15 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                 if (threadIdx.x == 0) GC_TRACE(7, c);
                 const float gi = GATED ? G[row] : 0.f;
                 {
+                    // gated: the 32 columns' prefix sums into registers before the P_b stores
+                    float gc[32];
+                    if constexpr (GATED) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float4 g4 = *reinterpret_cast<const float4 *>(G + 32 * hc + 4 * e);
+                            gc[4 * e] = g4.x; gc[4 * e + 1] = g4.y; gc[4 * e + 2] = g4.z; gc[4 * e + 3] = g4.w;
+                        }
+                    }
                     uint32_t v[32];
                     tmem_ld32(tmem + lane_base + dcol + kColDP + 32 * hc, v);
                     tmem_wait_ld();
@@ -556,7 +571,8 @@ __global__ void __launch_bounds__(kGcThreads, 1)
                             for (int u2 = 0; u2 < 2; ++u2) {
                                 const int col = 32 * hc + 8 * j + 2 * e + u2;
                                 float z = (col <= row && row < Lc) ? __uint_as_float(v[8 * j + 2 * e + u2]) : 0.f;
-                                if constexpr (GATED) z = (col <= row && row < Lc) ? z * fast_exp2(gi - G[col]) : 0.f;
+                                if constexpr (GATED)
+                                    z = (col <= row && row < Lc) ? z * fast_exp2(gi - gc[8 * j + 2 * e + u2]) : 0.f;
                                 y[u2] = z;
                             }
                             w[e] = pack2_bf16(y[0], y[1]);
