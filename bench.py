@@ -71,9 +71,10 @@ def parse_args():
                     help="capture the K timed steps into one CUDA graph and time its replay")
     ap.add_argument("--gated", action="store_true",
                     help="gated variant: coefficient diag(beta)(Gamma o K K^T) from per-token log decays g")
-    ap.add_argument("--consumer", action="store_true",
-                    help="also time the chunk state recurrence and output (gdn_chunk_state_fwd) that consumes "
-                         "W and U~ on the same workload, and the two calls back to back")
+    ap.add_argument("--no-consumer", dest="consumer", action="store_false",
+                    help="skip timing the chunk state recurrence (gdn_chunk_state_fwd) that consumes W and U~, "
+                         "and the two calls back to back, after the headline region")
+    ap.add_argument("--consumer", dest="consumer", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.no_t_out and args.t_f16:
         ap.error("--no-t-out and --t-f16 exclude each other")

@@ -184,7 +184,9 @@ int kkt_solve_fwd_gated(const void *k, const void *v, const float *beta, const f
  *   needs does not grow with the problem: 16 bytes (two 64-bit counters) of the
  *   array, for every problem size, so no size is rejected for want of scratch.
  *   The first call on a device looks up the array's device address (with that
- *   device current); make that first call before any stream capture.
+ *   device current) and caches it; make that first call before any stream
+ *   capture.  cudaDeviceReset invalidates the cached address, so calls after a
+ *   reset of the device are not supported.
  *   Every call shares the array.  Each call clears the 16 bytes on `stream`
  *   (cudaMemsetAsync, which allocates nothing) before its launch, and its kernel
  *   leaves them zero when it ends.  Calls whose work overlaps on the GPU (other

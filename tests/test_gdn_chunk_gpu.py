@@ -96,6 +96,22 @@ def test_unsupported_shapes_are_rejected():
     assert rc == _lib.KKT_ERR_UNSUPPORTED
 
 
+def test_malformed_cu_seqlens_is_reported_not_faulted():
+    """A decreasing cu_seqlens: the kernel skips the bad sequences, records KKT_ERR_SEQLENS in the status
+    word and leaves the context usable; a correct call right after matches the oracle."""
+    q, k, v, beta, g, S0, _ = _case(1, 300, 2, seed=14)
+    _, W, U = kkt_solve_fwd(k, v, beta, C)
+    bad = torch.tensor([0, 200, 100, 300], dtype=torch.int32, device=DEV)
+    gdn_chunk_state_fwd(q, k, W, U, C, cu_seqlens=bad)
+    torch.cuda.synchronize()
+    assert device_status() == _lib.KKT_ERR_SEQLENS
+    assert device_status() == 0
+    cu = np.array([0, 100, 300])
+    cu_t = torch.as_tensor(cu, dtype=torch.int32, device=DEV)
+    W, U, o, S = _run(q, k, v, beta, None, None, cu_t)
+    _check_both(q, k, v, beta, None, None, cu_t, W, U, o, S, 128 ** -0.5)
+
+
 def test_flashqla_signature_is_the_two_calls():
     """chunk_gated_delta_rule (the FlashQLA argument order) returns exactly kkt_solve then the
     chunk recurrence."""
@@ -106,8 +122,9 @@ def test_flashqla_signature_is_the_two_calls():
     assert torch.equal(o1, o2) and torch.equal(S1, S2)
 
 
-@pytest.mark.parametrize("name,gated", [("c3_b4_t8192_h16", False), ("c3_b4_t8192_h16", True),
-                                        ("c4_varlen32_h32", False)])
+@pytest.mark.parametrize("name,gated", [("c2_t8192_h16", False), ("c3_b4_t8192_h16", False),
+                                        ("c3_b4_t8192_h16", True), ("c4_varlen32_h32", False),
+                                        ("c4_varlen32_h32", True), ("c5_b2_t16384_h24_c64", False)])
 def test_full_size_every_element(name, gated):
     """A full-size workload: every element of o and of the final states against both oracles."""
     w = workloads()[name]
