@@ -28,11 +28,12 @@
 //                   substitution, one column per lane, so the dependency chain
 //                   is 15 FMAs (§2.1; in-place, with the L values read before
 //                   any column is written back, §3.4); coupling
-//                   -L11^-1 L10 L00^-1 at s = 16 (inside a warp), s = 32 (the
-//                   two warps of a 64-row block) and, at C = 128, s = 64 (all
-//                   four warps, each a heavy and a light 16-wide block of each
-//                   product) as register-tiled shared-memory GEMMs with L10
-//                   consumed before it is overwritten (§2.2, §3.5).  Each warp TMA-stores its 32 rows of T from that
+//                   -L11^-1 L10 L00^-1 at s = 16 (inside a warp) and s = 32 (the
+//                   two warps of a 64-row block) as register-tiled shared-memory
+//                   GEMMs with L10 consumed before it is overwritten (§2.2,
+//                   §3.5); at C = 128, s = 64 as two 3-pass bf16 tcgen05 MMAs
+//                   that the W|U warp issues between the tile's conversions of
+//                   their operands.  Each warp TMA-stores its 32 rows of T from that
 //                   buffer, and writes its rows of T~ = T diag(beta) as a bf16
 //                   hi / lo pair into tensor memory (tcgen05.st).
 //   epilogue warps  per warp: tcgen05.ld of its 32 rows of D, bf16 conversion,
@@ -79,6 +80,12 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColGram = 0;         // 128 fp32 columns
 constexpr uint32_t kColD = 128;          // 256 fp32 columns: W | U~
 constexpr uint32_t kColTT = 384;         // 64 packed bf16x2 hi + 64 lo
+// C = 128, level 64 on the tensor core, inside the D columns while D is free (after the previous
+// tile's D is drained, before this tile's W|U MMA): the A operands M10 and M11^-1 as packed bf16 hi
+// + lo pairs (32 + 32 columns each, lanes 64..127), and the fp32 product Y, then Z (64 columns)
+constexpr uint32_t kColL64M10 = 128;
+constexpr uint32_t kColL64M11 = 192;
+constexpr uint32_t kColL64D = 256;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
 struct TileInfo {
@@ -121,7 +128,10 @@ struct Barriers {
     uint64_t einfo_full[2];
     uint64_t mma_final, gram_final;
     uint64_t pair_sync[2];   // warps 2p and 2p + 1: one 64-row block (C = 64, 128)
-    uint64_t quad_sync;      // all four inverse warps (C = 128)
+    uint64_t l64_ops;        // C = 128: the operands of Y = M10 M00^-1 are in place (4 inverse warps)
+    uint64_t l64_y;          // C = 128: Y is in tensor memory (MMA commit)
+    uint64_t l64_yb;         // C = 128: Y, the B operand of Z, is in shared memory (warps 2, 3)
+    uint64_t l64_z;          // C = 128: Z = M11^-1 Y is in tensor memory (MMA commit)
     uint64_t kread[kNS];     // gated: the Gram MMA of the stage's tile has read its K
     uint64_t kscaled;        // gated: the epilogue warps have scaled the tile's K rows for W
     TileInfo einfo[2];       // tile info for the epilogue warps, written by the W|U warp
@@ -151,7 +161,7 @@ struct TcParams {
 enum TraceEvent {
     EV_P_EMPTY = 0, EV_P_ISSUE, EV_M_FULL, EV_M_GRAM, EV_M_EPI, EV_I_GRAM, EV_I_INV, EV_I_TSTORE,
     EV_I_TT, EV_E_DFULL, EV_E_DEMPTY, EV_E_DONE, EV_I_LD, EV_I_DIAG, EV_I_C16, EV_I_PAIR, EV_M_LATE,
-    EV_M_READY, EV_I_BW, EV_I_TTW, EV_COUNT
+    EV_M_READY, EV_I_BW, EV_I_TTW, EV_I_L32, EV_COUNT
 };
 constexpr int kTraceCtas = 160;
 constexpr int kTraceTiles = 64;  // the last tile row holds the CTA's clock calibration
@@ -285,7 +295,7 @@ __device__ __forceinline__ void split_bf16(float2 x, uint32_t &hi, uint32_t &lo)
 // 16-byte column chunk in a row with phase kk.
 // A loop over 8-k blocks rather than an unrolled sequence: the kernel is sensitive to its
 // instruction-cache footprint, so the code size of this inner product is kept small (UNROLL
-// blocks per iteration: 1 at C <= 64, 2 at C = 128, where the longer level-64 products gain).
+// blocks per iteration: 1 at C <= 64, 2 at C = 128).
 template <int UNROLL>
 __device__ __forceinline__ void tile4x4_fma(float2 (&y)[4][2], const uint8_t *const (&arow)[4],
                                          const uint32_t (&axor)[4], int acol0, const uint8_t *brow0,
@@ -385,100 +395,133 @@ __device__ __forceinline__ bool level32(const int WP, uint8_t *tm, uint8_t *ybuf
 }
 
 // Level-64 coupling of a 128-token chunk (C = 128; the tile's rows are the chunk's rows) (§2.2):
-// rows 64..127, columns 0..63 receive -Z = -M11^-1 M10 M00^-1 with 64 x 64 blocks
-// M00^-1 = T[0..63][0..63], M11^-1 = T[64..][64..], M10 = L[64..][0..63].  Both inverses are lower
-// triangular in 16 x 16 blocks, so column block j of Y = M10 M00^-1 needs k >= 16 j and row block i
-// of Z = M11^-1 Y needs k < 16 i + 16.  The work is balanced over the four inverse warps by pairing
-// a heavy block with a light one: warp w computes Y column blocks {0, 3} (w even) or {1, 2} (w odd)
-// on rows 32 (w / 2) .. + 31, then Z row blocks {0, 3} or {1, 2} on columns 32 (w / 2) .. + 31:
-// 80 k-steps of 16 outputs per lane in each product.  Y is kept in rows 0..63, columns 64..127
-// (zero in T) and cleared again once every warp has read it.
+// rows 64..127, columns 0..63 receive -Z = -M11^-1 M10 M00^-1 with 64 x 64 blocks M00^-1 =
+// T[0..63][0..63], M11^-1 = T[64..][64..] (both final after level 32) and M10 = L[64..][0..63].  The
+// two products run on the tensor core as 3-pass bf16 MMAs (hi hi + hi lo + lo hi of a hi + lo split
+// of each operand, fp32 accumulation; M = 128, N = 64, K = 64, lanes 0..63 of A and D unused):
+//   Y = M10 M00^-1: A = M10 from tensor memory, B = M00^-1 (rows k, MN-major) in shared memory;
+//   Z = M11^-1 Y:   A = M11^-1 from tensor memory, B = Y (rows k, MN-major) in shared memory.
+// The B operands live in rows 0..63 of the T buffer's columns 64..127 (zero in T): hi in the third
+// 32-column half, lo in the fourth, each row one 128-byte swizzled line of 64 bf16.  Warps 0 and 1
+// write M00^-1 there and clear it again once Z is done; warps 2 and 3 put M10 and M11^-1 into tensor
+// memory, turn Y into Z's B operand and write -Z over M10.  The W|U issuer issues the MMAs.
 
-// Y, column block j, rows 32 rh .. 32 rh + 31.  Lane: rows yr + 8 rr, columns 16 j + 4 yc .. + 3
-// (a quarter-warp: 8 rows of one column group, 8 different swizzled chunks).
-__device__ __forceinline__ void level64_y_block(float2 (&y)[4][2], uint8_t *tm, int rh, int j, int lane) {
-    const int yr = lane & 7, yc = lane >> 3;
-    const int cj = 16 * j + 4 * yc;
-    const uint32_t axor = (uint32_t)(yr & 7) << 4;  // swizzle phase of every A row used
-    const uint32_t axr[4] = {axor, axor, axor, axor};
-    uint32_t bsw[8];
+// bf16 hi + lo split of 8 fp32 values (two float4) into one 16-byte chunk of each.
+__device__ __forceinline__ void split8(const float4 a, const float4 b, uint4 &hi, uint4 &lo) {
+    split_bf16(make_float2(a.x, a.y), hi.x, lo.x);
+    split_bf16(make_float2(a.z, a.w), hi.y, lo.y);
+    split_bf16(make_float2(b.x, b.y), hi.z, lo.z);
+    split_bf16(make_float2(b.z, b.w), hi.w, lo.w);
+}
+
+// Chunk c (columns 8 c .. 8 c + 7) of row k of a level-64 B operand: part 0 = hi, 1 = lo.
+__device__ __forceinline__ uint4 *l64_b(uint8_t *tm, int part, int k, int c) {
+    return smem_chk(reinterpret_cast<uint4 *>(tm + (2 + part) * 16384 + k * 128 + ((c ^ (k & 7)) << 4)));
+}
+
+// Row m of the T buffer, columns c0 .. c0 + 63, as a level-64 A operand in tensor memory: packed
+// hi pairs in columns taddr .. + 31, lo pairs in taddr + 32 .. + 63 (this warp's lanes).
+__device__ __forceinline__ void l64_row_to_tmem(uint8_t *tm, int m, int c0, uint32_t taddr) {
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) bsw[kk] = (uint32_t)(((cj & 31) >> 2) ^ kk) << 4;
-    const uint8_t *bhalf = tm + (cj >> 5) * 16384;  // M00^-1, the half of columns cj, rows k
-#pragma unroll 1
-    for (int kh = (16 * j) >> 5; kh < 2; ++kh) {    // the 32-column halves of M10 that k in [16 j, 64) spans
-        const int k0 = 16 * j > 32 * kh ? 16 * j : 32 * kh;
-        const uint8_t *arow[4];
+    for (int h = 0; h < 2; ++h) {
+        uint32_t hi[16], lo[16];
 #pragma unroll
-        for (int rr = 0; rr < 4; ++rr) arow[rr] = tm + kh * 16384 + (64 + 32 * rh + yr + 8 * rr) * 128;
-        tile4x4_fma<2>(y, arow, axr, k0 - 32 * kh, bhalf + k0 * 128, bsw, (32 * kh + 32 - k0) / 8);
+        for (int c = 0; c < 32; c += 8) {
+            const float4 a = *tm_vec(tm, m, c0 + 32 * h + c), b = *tm_vec(tm, m, c0 + 32 * h + c + 4);
+            split_bf16(make_float2(a.x, a.y), hi[c / 2], lo[c / 2]);
+            split_bf16(make_float2(a.z, a.w), hi[c / 2 + 1], lo[c / 2 + 1]);
+            split_bf16(make_float2(b.x, b.y), hi[c / 2 + 2], lo[c / 2 + 2]);
+            split_bf16(make_float2(b.z, b.w), hi[c / 2 + 3], lo[c / 2 + 3]);
+        }
+        tmem_st16(taddr + 16 * h, hi);
+        tmem_st16(taddr + 32 + 16 * h, lo);
     }
 }
 
-// Z, row block i, columns 32 ch .. 32 ch + 31.  Lane: rows 16 i + zr + 4 rr, columns 32 ch + 4 zc .. + 3.
-__device__ __forceinline__ void level64_z_block(float2 (&z)[4][2], uint8_t *tm, int i, int ch, int lane) {
-    const int zr = lane >> 3, zc = lane & 7;
-    uint32_t axor[4];
+// One level-64 product (issuing thread): D = A B over K = 64 in three accumulating passes.
+__device__ __forceinline__ void l64_mma(uint32_t d, uint32_t a, uint32_t b_smem) {
+    constexpr uint32_t idesc = idesc_bf16_f32(128, 64, 0, 1);  // B MN-major: rows k of 64 bf16
 #pragma unroll
-    for (int rr = 0; rr < 4; ++rr) axor[rr] = (uint32_t)((64 + 16 * i + zr + 4 * rr) & 7) << 4;
-    uint32_t bsw[8];
+    for (int pass = 0; pass < 3; ++pass)      // hi hi, hi lo, lo hi
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) bsw[kk] = (uint32_t)(zc ^ kk) << 4;
-    const uint8_t *ybase = tm + (2 + ch) * 16384;  // Y: rows k, the half of columns 64 + 32 ch ..
-    const int kend = 16 * i + 16;
-#pragma unroll 1
-    for (int kh = 0; 32 * kh < kend; ++kh) {        // the halves 2 + kh of M11^-1 that k in [0, kend) spans
-        const uint8_t *arow[4];
-#pragma unroll
-        for (int rr = 0; rr < 4; ++rr) arow[rr] = tm + (2 + kh) * 16384 + (64 + 16 * i + zr + 4 * rr) * 128;
-        const int kn = (kend < 32 * kh + 32 ? kend : 32 * kh + 32) - 32 * kh;
-        tile4x4_fma<2>(z, arow, axor, 0, ybase + 32 * kh * 128, bsw, kn / 8);
-    }
+        for (int kk = 0; kk < 4; ++kk) {      // K = 64 in steps of 16 (8 packed columns, 16 rows)
+            const uint32_t ac = a + (pass == 2 ? 32u : 0u) + 8u * kk;
+            const uint64_t bd = sw128_desc(b_smem + (pass == 1 ? 16384u : 0u) + 2048u * kk, 16384, 1024);
+            mma_ts(d, ac, bd, idesc, (pass | kk) ? 1u : 0u);
+        }
 }
 
-__device__ __forceinline__ bool level64(const int w, uint8_t *tm, int lane, uint64_t *quad_bar, uint32_t &uses,
-                                        Barriers *bars, int *status) {
-    const int half = w >> 1;                 // Y rows 32 half .., then Z columns 32 half ..
-    const int blk0 = (w & 1) ? 1 : 0, blk1 = (w & 1) ? 2 : 3;
-    // Y = M10 M00^-1
-#pragma unroll 1
-    for (int t = 0; t < 2; ++t) {
-        const int j = t ? blk1 : blk0;
-        float2 y[4][2];
+// The inverse warps' part of level 64 for tile i (q: the warp's row quarter, m its row).
+__device__ __forceinline__ bool level64_tc(int q, int m, int i, uint8_t *tm, uint32_t tmem, uint32_t lane_base,
+                                           int lane, Barriers *bars, int *status) {
+    const uint32_t ph = (uint32_t)i & 1u;
+    if (q < 2) {
+        // M00^-1 row m (= row k of Y's B operand), split into hi + lo
 #pragma unroll
-        for (int rr = 0; rr < 4; ++rr) y[rr][0] = y[rr][1] = make_float2(0.f, 0.f);
-        level64_y_block(y, tm, half, j, lane);
-        const int yr = lane & 7, yc = lane >> 3;
+        for (int c = 0; c < 8; ++c) {
+            uint4 hi, lo;
+            split8(*tm_vec(tm, m, 8 * c), *tm_vec(tm, m, 8 * c + 4), hi, lo);
+            *l64_b(tm, 0, m, c) = hi;
+            *l64_b(tm, 1, m, c) = lo;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->l64_ops);
+        // Z done: the B operand area is read, and is cleared again (the upper right of T is zero)
+        if (!wait_bar(&bars->l64_z, ph, bars, status)) return false;
 #pragma unroll
-        for (int rr = 0; rr < 4; ++rr)
-            *tm_vec(tm, 32 * half + yr + 8 * rr, 64 + 16 * j + 4 * yc) =
-                make_float4(y[rr][0].x, y[rr][0].y, y[rr][1].x, y[rr][1].y);
+        for (int j = 64; j < 128; j += 4) *tm_vec(tm, m, j) = make_float4(0.f, 0.f, 0.f, 0.f);
+        return true;
     }
-    // every warp has written its part of Y (and read M10)
-    if (!group_sync(quad_bar, uses, bars, status)) return false;
-    // Z = M11^-1 Y; -Z overwrites M10, which no warp reads any more
-#pragma unroll 1
-    for (int t = 0; t < 2; ++t) {
-        const int i = t ? blk1 : blk0;
-        float2 z[4][2];
+    // the previous tile's D has been drained from the columns used here
+    if (!wait_bar(&bars->d_empty, ph ^ 1u, bars, status)) return false;
+    tc_fence_after();
+    l64_row_to_tmem(tm, m, 0, tmem + lane_base + kColL64M10);   // M10 (the L block, columns 0..63)
+    l64_row_to_tmem(tm, m, 64, tmem + lane_base + kColL64M11);  // M11^-1 (columns 64..127)
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->l64_ops);
+    // Y row m - 64 -> row k = m - 64 of Z's B operand
+    if (!wait_bar(&bars->l64_y, ph, bars, status)) return false;
+    tc_fence_after();
+    const int k = m - 64;
 #pragma unroll
-        for (int rr = 0; rr < 4; ++rr) z[rr][0] = z[rr][1] = make_float2(0.f, 0.f);
-        level64_z_block(z, tm, i, half, lane);
-        const int zr = lane >> 3, zc = lane & 7;
+    for (int h = 0; h < 2; ++h) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + kColL64D + 32 * h, v);
+        tmem_wait_ld();
 #pragma unroll
-        for (int rr = 0; rr < 4; ++rr)
-            *tm_vec(tm, 64 + 16 * i + zr + 4 * rr, 32 * half + 4 * zc) =
-                make_float4(-z[rr][0].x, -z[rr][0].y, -z[rr][1].x, -z[rr][1].y);
+        for (int c = 0; c < 4; ++c) {
+            uint4 hi, lo;
+            split8(make_float4(__uint_as_float(v[8 * c]), __uint_as_float(v[8 * c + 1]), __uint_as_float(v[8 * c + 2]),
+                               __uint_as_float(v[8 * c + 3])),
+                   make_float4(__uint_as_float(v[8 * c + 4]), __uint_as_float(v[8 * c + 5]),
+                               __uint_as_float(v[8 * c + 6]), __uint_as_float(v[8 * c + 7])),
+                   hi, lo);
+            *l64_b(tm, 0, k, 4 * h + c) = hi;
+            *l64_b(tm, 1, k, 4 * h + c) = lo;
+        }
     }
-    // every warp has read Y: clear it (this warp: 16 of its columns)
-    if (!group_sync(quad_bar, uses, bars, status)) return false;
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int c4 = 0; c4 < 16; c4 += 4)
-            *tm_vec(tm, lane + 32 * h, 64 + 16 * w + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
     fence_proxy_async_smem();
-    return group_sync(quad_bar, uses, bars, status);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bars->l64_yb);
+    // -Z over M10 (read into tensor memory above)
+    if (!wait_bar(&bars->l64_z, ph, bars, status)) return false;
+    tc_fence_after();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + kColL64D + 32 * h, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 32; c += 4)
+            *tm_vec(tm, m, 32 * h + c) = make_float4(-__uint_as_float(v[c]), -__uint_as_float(v[c + 1]),
+                                                     -__uint_as_float(v[c + 2]), -__uint_as_float(v[c + 3]));
+    }
+    tc_fence_before();
+    return true;
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -546,7 +589,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->gram_final, 1);
         mbar_init(&bars->pair_sync[0], 64);
         mbar_init(&bars->pair_sync[1], 64);
-        mbar_init(&bars->quad_sync, 128);
+        mbar_init(&bars->l64_ops, 4);
+        mbar_init(&bars->l64_y, 1);
+        mbar_init(&bars->l64_yb, 2);
+        mbar_init(&bars->l64_z, 1);
         mbar_init(&bars->kread[0], 1);
         mbar_init(&bars->kread[1], 1);
         mbar_init(&bars->kscaled, 4);
@@ -777,6 +823,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 break;
             }
+            if constexpr (C == 128) {
+                // the tile's level-64 products (see level64_tc), in D's columns: the previous D is
+                // drained before the operands are written there
+                const uint32_t b_smem = smem_u32(smem + CF::OFF_T + 2 * 16384);
+                if (!wait_bar(&bars->l64_ops, (uint32_t)i & 1u, bars, p.status)) break;
+                if (lane == 0) {
+                    tc_fence_after();
+                    l64_mma(tmem + kColL64D, tmem + kColL64M10, b_smem);
+                    mma_commit(&bars->l64_y);
+                }
+                __syncwarp();
+                if (!wait_bar(&bars->l64_yb, (uint32_t)i & 1u, bars, p.status)) break;
+                if (lane == 0) {
+                    tc_fence_after();
+                    l64_mma(tmem + kColL64D, tmem + kColL64M11, b_smem);
+                    mma_commit(&bars->l64_z);
+                }
+                __syncwarp();
+            }
             if (!wait_bar(&bars->tt_full, (uint32_t)i & 1u, bars, p.status)) break;
             if (!wait_bar(&bars->d_empty, ((uint32_t)i & 1u) ^ 1u, bars, p.status)) break;
             if constexpr (GATED) {
@@ -834,7 +899,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < C; j += 4) *tm_vec(tm, m, j) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         int i = 0;
-        uint32_t pair_uses = 0, quad_uses = 0;
+        uint32_t pair_uses = 0;
         while (true) {
             const int s = i % kNS;
             if (!wait_bar(&bars->full[s], (uint32_t)(i / kNS) & 1u, bars, p.status)) break;
@@ -1028,9 +1093,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                    &bars->pair_sync[pr], pair_uses, bars, p.status);
                 }
                 if constexpr (C == 128) {
-                    // level 64: rows 64..127 of the chunk (see level64)
-                    if (ok) ok = group_sync(&bars->quad_sync, quad_uses, bars, p.status);
-                    if (ok) ok = level64(q, tm, lane, &bars->quad_sync, quad_uses, bars, p.status);
+                    // level 64: rows 64..127 of the chunk, on the tensor core (see level64_tc)
+                    if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_L32, i);
+                    if (ok) ok = level64_tc(q, m, i, tm, tmem, lane_base, lane, bars, p.status);
+                    fence_proxy_async_smem();
+                    __syncwarp();
                 }
             } else {
                 fence_proxy_async_smem();

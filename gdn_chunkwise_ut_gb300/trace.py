@@ -20,7 +20,8 @@ from . import _lib, build
 from .inputs import make_gate, workloads
 
 EVENTS = ["P_EMPTY", "P_ISSUE", "M_FULL", "M_GRAM", "M_EPI", "I_GRAM", "I_INV", "I_TSTORE", "I_TT",
-          "E_DFULL", "E_DEMPTY", "E_DONE", "I_LD", "I_DIAG", "I_C16", "I_PAIR", "M_LATE", "M_READY", "I_BW", "I_TTW"]
+          "E_DFULL", "E_DEMPTY", "E_DONE", "I_LD", "I_DIAG", "I_C16", "I_PAIR", "M_LATE", "M_READY", "I_BW", "I_TTW",
+          "I_L32"]
 TRACE_CTAS, TRACE_TILES, TRACE_SLOTS = 160, 64, 24
 
 
@@ -161,6 +162,8 @@ def report(tr: np.ndarray, ctas: int, tiles: int) -> str:
         ("epilogue: D loads", span("E_DFULL", "E_DEMPTY")),
         ("epilogue: total", span("E_DFULL", "E_DONE")),
         ("D drained -> next W|U MMA ready", span("E_DEMPTY", "M_READY", shift=1)),
+        ("C=128: level-32 coupling", span("I_PAIR", "I_L32")),
+        ("C=128: level-64 coupling", span("I_L32", "I_INV")),
     ]
     lines.append("")
     for name, val in rows:
