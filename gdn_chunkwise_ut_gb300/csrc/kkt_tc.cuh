@@ -80,12 +80,13 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColGram = 0;         // 128 fp32 columns
 constexpr uint32_t kColD = 128;          // 256 fp32 columns: W | U~
 constexpr uint32_t kColTT = 384;         // 64 packed bf16x2 hi + 64 lo
-// C = 128, level 64 on the tensor core, inside the D columns while D is free (after the previous
-// tile's D is drained, before this tile's W|U MMA): the A operands M10 and M11^-1 as packed bf16 hi
-// + lo pairs (32 + 32 columns each, lanes 64..127), and the fp32 product Y, then Z (64 columns)
-constexpr uint32_t kColL64M10 = 128;
-constexpr uint32_t kColL64M11 = 192;
-constexpr uint32_t kColL64D = 256;
+// C = 128, level 64 on the tensor core.  The A operands as packed bf16 hi + lo pairs (32 + 32
+// columns, lanes 64..127): M10 in T~'s columns (free once the previous tile's W|U MMA has read T~),
+// M11^-1 in D's (free once the previous D is drained); the fp32 products Y, then Z, in the other 64
+// columns of T~'s.
+constexpr uint32_t kColL64M10 = kColTT;
+constexpr uint32_t kColL64M11 = kColD;
+constexpr uint32_t kColL64D = kColTT + 64;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
 struct TileInfo {
@@ -128,7 +129,8 @@ struct Barriers {
     uint64_t einfo_full[2];
     uint64_t mma_final, gram_final;
     uint64_t pair_sync[2];   // warps 2p and 2p + 1: one 64-row block (C = 64, 128)
-    uint64_t l64_ops;        // C = 128: the operands of Y = M10 M00^-1 are in place (4 inverse warps)
+    uint64_t l64_ops;        // C = 128: the operands of Y = M10 M00^-1 are in place (inverse warps 0, 1
+                             // and epilogue warps 2, 3)
     uint64_t l64_y;          // C = 128: Y is in tensor memory (MMA commit)
     uint64_t l64_yb;         // C = 128: Y, the B operand of Z, is in shared memory (warps 2, 3)
     uint64_t l64_z;          // C = 128: Z = M11^-1 Y is in tensor memory (MMA commit)
@@ -394,6 +396,55 @@ __device__ __forceinline__ bool level32(const int WP, uint8_t *tm, uint8_t *ybuf
     return true;
 }
 
+// Gram row -> row m of A = I + strictLower(diag(beta) S) (beta on rows, unit diagonal, §3.2), times
+// Gamma elementwise when gated (§5 item 12), into the T buffer: columns 32 h_lo .. 32 h_hi + 31.  r is
+// the row's token within the chunk and gram the tensor-memory address of its head's Gram row.  When
+// gated and every block of the head is factorable (fac), Gamma[r][j] for columns 32 h + c is
+// exp2(G_r - R_h) w_j with R_h = G at the block's first row; otherwise the row is formed without it
+// and multiplied by exp2(G_r - G_j) element by element after (a compact loop: such gates are rare,
+// and the unrolled code stays small).  One 32-column block at a time, in a loop: the kernel is
+// sensitive to its code size, and an unrolled form measured slower (gated) or the same.
+template <bool GATED>
+__device__ __forceinline__ void form_a_row(uint8_t *tm, uint32_t gram, int m, int r, int h_lo, int h_hi,
+                                           float beta_r, bool fac, float g_r, const float *sg, const float *sw) {
+#pragma unroll 1
+    for (int h = h_lo; h <= h_hi; ++h) {
+        uint32_t v[32];
+        tmem_ld32(gram + 32 * h, v);
+        float uh = 1.f;
+        float4 wq[8];
+        if constexpr (GATED) {
+            uh = fac ? exp2f(g_r - *smem_chk(sg + 32 * h)) : 1.f;
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8)
+                wq[c8] = fac ? *smem_chk(reinterpret_cast<const float4 *>(sw + 32 * h + 4 * c8)) : make_float4(1.f, 1.f, 1.f, 1.f);
+        }
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+            float e[4];
+            float gm[4] = {1.f, 1.f, 1.f, 1.f};
+            if constexpr (GATED) {
+                const float4 w4 = wq[c / 4];
+                gm[0] = uh * w4.x; gm[1] = uh * w4.y; gm[2] = uh * w4.z; gm[3] = uh * w4.w;
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int j = 32 * h + c + u;
+                e[u] = (j < r) ? beta_r * __uint_as_float(v[c + u]) * gm[u] : (j == r ? 1.f : 0.f);
+            }
+            *tm_vec(tm, m, 32 * h + c) = make_float4(e[0], e[1], e[2], e[3]);
+        }
+    }
+    if constexpr (GATED) {
+        if (!fac) {
+            const int j_end = r < 32 * h_hi + 32 ? r : 32 * h_hi + 32;
+#pragma unroll 1
+            for (int j = 32 * h_lo; j < j_end; ++j) *tm_elem(tm, m, j) *= exp2f(g_r - *smem_chk(sg + j));
+        }
+    }
+}
+
 // Level-64 coupling of a 128-token chunk (C = 128; the tile's rows are the chunk's rows) (§2.2):
 // rows 64..127, columns 0..63 receive -Z = -M11^-1 M10 M00^-1 with 64 x 64 blocks M00^-1 =
 // T[0..63][0..63], M11^-1 = T[64..][64..] (both final after level 32) and M10 = L[64..][0..63].  The
@@ -403,8 +454,11 @@ __device__ __forceinline__ bool level32(const int WP, uint8_t *tm, uint8_t *ybuf
 //   Z = M11^-1 Y:   A = M11^-1 from tensor memory, B = Y (rows k, MN-major) in shared memory.
 // The B operands live in rows 0..63 of the T buffer's columns 64..127 (zero in T): hi in the third
 // 32-column half, lo in the fourth, each row one 128-byte swizzled line of 64 bf16.  Warps 0 and 1
-// write M00^-1 there and clear it again once Z is done; warps 2 and 3 put M10 and M11^-1 into tensor
-// memory, turn Y into Z's B operand and write -Z over M10.  The W|U issuer issues the MMAs.
+// write M00^-1 there and clear it again once Z is done.  The epilogue warps of lanes 64..127 form M10
+// from the Gram rows straight into tensor memory as soon as the previous tile's W|U MMA has read T~,
+// so that Y runs while warps 2 and 3 finish their level 32 (and those warps form only the diagonal
+// half of their rows of A).  Warps 2 and 3 then put M11^-1 into tensor memory, turn Y into Z's B
+// operand and write -Z into columns 0..63 of their rows.  The W|U issuer issues the MMAs.
 
 // bf16 hi + lo split of 8 fp32 values (two float4) into one 16-byte chunk of each.
 __device__ __forceinline__ void split8(const float4 a, const float4 b, uint4 &hi, uint4 &lo) {
@@ -432,6 +486,41 @@ __device__ __forceinline__ void l64_row_to_tmem(uint8_t *tm, int m, int c0, uint
             split_bf16(make_float2(a.z, a.w), hi[c / 2 + 1], lo[c / 2 + 1]);
             split_bf16(make_float2(b.x, b.y), hi[c / 2 + 2], lo[c / 2 + 2]);
             split_bf16(make_float2(b.z, b.w), hi[c / 2 + 3], lo[c / 2 + 3]);
+        }
+        tmem_st16(taddr + 16 * h, hi);
+        tmem_st16(taddr + 32 + 16 * h, lo);
+    }
+}
+
+// M10 row r (columns 0..63 of row r >= 64 of A: beta_r S[r][j], times Gamma[r][j] when gated, all
+// strictly below the diagonal) from the Gram row in tensor memory straight into a level-64 A operand:
+// packed hi pairs at taddr .. + 31, lo pairs at taddr + 32 .. + 63 (see form_a_row for Gamma).
+template <bool GATED>
+__device__ __forceinline__ void m10_from_gram(uint32_t gram, uint32_t taddr, int r, float beta_r, bool fac, float g_r,
+                                              const float *sg, const float *sw) {
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+        uint32_t v[32];
+        tmem_ld32(gram + 32 * h, v);
+        float uh = beta_r;
+        if constexpr (GATED) uh *= fac ? exp2f(g_r - *smem_chk(sg + 32 * h)) : 1.f;
+        tmem_wait_ld();
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+            float4 w4 = make_float4(1.f, 1.f, 1.f, 1.f);
+            if constexpr (GATED) {
+                if (fac) {
+                    w4 = *smem_chk(reinterpret_cast<const float4 *>(sw + 32 * h + c));
+                } else {
+                    const float4 g4 = *smem_chk(reinterpret_cast<const float4 *>(sg + 32 * h + c));
+                    w4 = make_float4(exp2f(g_r - g4.x), exp2f(g_r - g4.y), exp2f(g_r - g4.z), exp2f(g_r - g4.w));
+                }
+            }
+            const float e0 = uh * __uint_as_float(v[c]) * w4.x, e1 = uh * __uint_as_float(v[c + 1]) * w4.y;
+            const float e2 = uh * __uint_as_float(v[c + 2]) * w4.z, e3 = uh * __uint_as_float(v[c + 3]) * w4.w;
+            split_bf16(make_float2(e0, e1), hi[c / 2], lo[c / 2]);
+            split_bf16(make_float2(e2, e3), hi[c / 2 + 1], lo[c / 2 + 1]);
         }
         tmem_st16(taddr + 16 * h, hi);
         tmem_st16(taddr + 32 + 16 * h, lo);
@@ -473,15 +562,10 @@ __device__ __forceinline__ bool level64_tc(int q, int m, int i, uint8_t *tm, uin
         for (int j = 64; j < 128; j += 4) *tm_vec(tm, m, j) = make_float4(0.f, 0.f, 0.f, 0.f);
         return true;
     }
-    // the previous tile's D has been drained from the columns used here
+    // M11^-1 (columns 64..127) into D's columns, once the previous tile's D has been drained
     if (!wait_bar(&bars->d_empty, ph ^ 1u, bars, status)) return false;
     tc_fence_after();
-    l64_row_to_tmem(tm, m, 0, tmem + lane_base + kColL64M10);   // M10 (the L block, columns 0..63)
-    l64_row_to_tmem(tm, m, 64, tmem + lane_base + kColL64M11);  // M11^-1 (columns 64..127)
-    tmem_wait_st();
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&bars->l64_ops);
+    l64_row_to_tmem(tm, m, 64, tmem + lane_base + kColL64M11);
     // Y row m - 64 -> row k = m - 64 of Z's B operand
     if (!wait_bar(&bars->l64_y, ph, bars, status)) return false;
     tc_fence_after();
@@ -503,6 +587,7 @@ __device__ __forceinline__ bool level64_tc(int q, int m, int i, uint8_t *tm, uin
             *l64_b(tm, 1, k, 4 * h + c) = lo;
         }
     }
+    tmem_wait_st();
     fence_proxy_async_smem();
     tc_fence_before();
     __syncwarp();
@@ -578,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->empty[s], 1);
         }
         mbar_init(&bars->gram_full, 1);
-        mbar_init(&bars->gram_empty, 4);
+        mbar_init(&bars->gram_empty, C == 128 ? 6 : 4);  // C = 128: + epilogue warps 2, 3 (M10)
         mbar_init(&bars->tt_full, 4);
         mbar_init(&bars->tt_empty, 1);
         mbar_init(&bars->d_full, 1);
@@ -824,8 +909,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             if constexpr (C == 128) {
-                // the tile's level-64 products (see level64_tc), in D's columns: the previous D is
-                // drained before the operands are written there
+                // the tile's level-64 products (see level64_tc); the operands' arrivals imply that the
+                // previous W|U MMA has read T~ (Y's columns) and, for Z, that D is drained
                 const uint32_t b_smem = smem_u32(smem + CF::OFF_T + 2 * 16384);
                 if (!wait_bar(&bars->l64_ops, (uint32_t)i & 1u, bars, p.status)) break;
                 if (lane == 0) {
@@ -889,12 +974,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // zero this lane's T~ columns (other heads' blocks and the upper triangle stay zero)
         // and its row of T (the upper triangle stays zero there too)
         {
-            uint32_t zz[16];
+            // (at C = 128 every T~ row is written whole, zeros included, and the epilogue warps may
+            // already be putting M10 into these columns: no clear there)
+            if constexpr (C != 128) {
+                uint32_t zz[16];
 #pragma unroll
-            for (int c = 0; c < 16; ++c) zz[c] = 0u;
+                for (int c = 0; c < 16; ++c) zz[c] = 0u;
 #pragma unroll
-            for (int c = 0; c < 128; c += 16) tmem_st16(tmem + lane_base + kColTT + c, zz);
-            tmem_wait_st();
+                for (int c = 0; c < 128; c += 16) tmem_st16(tmem + lane_base + kColTT + c, zz);
+                tmem_wait_st();
+            }
 #pragma unroll
             for (int j = 0; j < C; j += 4) *tm_vec(tm, m, j) = make_float4(0.f, 0.f, 0.f, 0.f);
         }
@@ -907,10 +996,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (info.done) break;
             const float *sb = stage_beta(s) + g * C;
             const float beta_r = *smem_chk(sb + r);
-            // gated: Gamma[r][j], the decay from token j to token r (j < r), for columns 32 h + c ..
-            // + 3 is exp2(G_r - R_h) w_j when every block of the head is factorable (fac); otherwise
-            // the row is formed without it and multiplied by exp2(G_r - G_j) element by element after
-            // (a compact loop: such gates are rare, and the unrolled code stays small)
+            // gated: the decay factors of Gamma (see form_a_row)
             const float *sg = stage_gate(s) + g * C;
             const float *sw = stage_gw(s) + g * C;
             bool fac = true;
@@ -921,13 +1007,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int h = 0; h < CF::T_HALVES; ++h) fac = fac && *smem_chk(sf + h) != 0;
             }
-            // the column factors w of block h (ones when not factorable), loaded together ahead of use
-            auto load_w = [&](int h, float4 (&wq)[8]) {
-#pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8)
-                    wq[c8] = fac ? *smem_chk(reinterpret_cast<const float4 *>(sw + 32 * h + 4 * c8)) : make_float4(1.f, 1.f, 1.f, 1.f);
-            };
-            auto row_factor = [&](int h) { return fac ? exp2f(g_r - *smem_chk(sg + 32 * h)) : 1.f; };
 
             if (!wait_bar(&bars->gram_full, (uint32_t)i & 1u, bars, p.status)) break;
             tc_fence_after();
@@ -936,43 +1015,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) bulk_wait_read<0>();
             __syncwarp();
             if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_BW, i);
-            // Gram row -> row of A = I + strictLower(diag(beta) S) (beta on rows, unit diagonal,
-            // §3.2), times Gamma elementwise when gated (§5 item 12), into the T buffer; columns
-            // above 32 (wp + 1) stay zero.  One 32-column block at a time, in a loop: the kernel is
-            // sensitive to its code size, and an unrolled form measured slower (gated) or the same.
-#pragma unroll 1
-            for (int h = 0; h <= wp; ++h) {
-                uint32_t v[32];
-                tmem_ld32(tmem + lane_base + kColGram + g * C + 32 * h, v);
-                float uh = 1.f;
-                float4 wq[8];
-                if constexpr (GATED) {
-                    uh = row_factor(h);
-                    load_w(h, wq);
-                }
-                tmem_wait_ld();
-#pragma unroll
-                for (int c = 0; c < 32; c += 4) {
-                    float e[4];
-                    float gm[4] = {1.f, 1.f, 1.f, 1.f};
-                    if constexpr (GATED) {
-                        const float4 w4 = wq[c / 4];
-                        gm[0] = uh * w4.x; gm[1] = uh * w4.y; gm[2] = uh * w4.z; gm[3] = uh * w4.w;
-                    }
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int j = 32 * h + c + u;
-                        e[u] = (j < r) ? beta_r * __uint_as_float(v[c + u]) * gm[u] : (j == r ? 1.f : 0.f);
-                    }
-                    *tm_vec(tm, m, 32 * h + c) = make_float4(e[0], e[1], e[2], e[3]);
-                }
-            }
-            if constexpr (GATED) {
-                if (!fac) {
-#pragma unroll 1
-                    for (int j = 0; j < r; ++j) *tm_elem(tm, m, j) *= exp2f(g_r - *smem_chk(sg + j));
-                }
-            }
+            // Gram row -> row of A into the T buffer; columns above 32 (wp + 1) stay zero.  At C = 128
+            // columns 0..63 of rows 64..127 (M10 of the level-64 coupling) are not formed here: the
+            // epilogue warps of those lanes form them straight into tensor memory for the level-64
+            // MMA (see level64_tc), so that these rows cost the inverse warps no more than the others.
+            form_a_row<GATED>(tm, tmem + lane_base + kColGram + g * C, m, r, (C == 128 && q >= 2) ? 2 : 0, wp, beta_r,
+                              fac, g_r, sg, sw);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->gram_empty);
@@ -1167,17 +1215,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t col = (uint32_t)(g * C + 32 * blk) / 2;
                         tmem_st16(tmem + lane_base + kColTT + col, hi);
                         tmem_st16(tmem + lane_base + kColTT + 64 + col, lo);
-                    } else if constexpr (TF16) {
-                        // columns above the diagonal block: zeros
-                        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                    } else {
+                        if constexpr (C == 128) {
+                            // the level-64 products used these columns (see level64_tc): zeros above
+                            // the diagonal block
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            if (t16_tma)
-                                *smem_chk(t16s + ((4 * (blk & 1) + e) ^ (m & 7))) = z;
-                            else if (t16_row)
-                                *reinterpret_cast<float4 *>(gmem_chk(static_cast<__half *>(p.T_out),
-                                                                     ((info.t0 + r) * p.H + info.h0 + g) * C + 32 * blk + 8 * e,
-                                                                     p.ntok * p.H * C, 8)) = z;
+                            for (int e = 0; e < 16; ++e) hi[e] = 0u;
+                            const uint32_t col = (uint32_t)(32 * blk) / 2;
+                            tmem_st16(tmem + lane_base + kColTT + col, hi);
+                            tmem_st16(tmem + lane_base + kColTT + 64 + col, hi);
+                        }
+                        if constexpr (TF16) {
+                            // columns above the diagonal block: zeros
+                            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                if (t16_tma)
+                                    *smem_chk(t16s + ((4 * (blk & 1) + e) ^ (m & 7))) = z;
+                                else if (t16_row)
+                                    *reinterpret_cast<float4 *>(gmem_chk(static_cast<__half *>(p.T_out),
+                                                                         ((info.t0 + r) * p.H + info.h0 + g) * C + 32 * blk + 8 * e,
+                                                                         p.ntok * p.H * C, 8)) = z;
+                            }
                         }
                     }
                 }
@@ -1214,7 +1273,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         int i = 0;
         uint32_t nstore = 0;  // TMA store groups issued by this warp
         bool keys_done = false;  // gated: the stage that ends the work has been seen
-        while (true) {
+        // C = 128, epilogue warps 2 and 3: M10 of tile t, formed from the tile's Gram rows straight into
+        // tensor memory (level 64's first A operand, in T~'s columns).  Runs once the previous tile's
+        // W|U MMA has read T~ (its D is full), before that D is drained; the next Gram waits for it.
+        bool m10_end = false;  // C = 128: the stage that ends the work has been seen
+        auto m10_to_tmem = [&](int t) -> bool {
+            const int s = t % kNS;
+            if (!wait_bar(&bars->full[s], (uint32_t)(t / kNS) & 1u, bars, p.status)) return false;
+            if (stage_info(s)->done) {
+                m10_end = true;
+                return true;
+            }
+            if (!wait_bar(&bars->gram_full, (uint32_t)t & 1u, bars, p.status)) return false;
+            tc_fence_after();
+            const int m = 32 * q + lane;  // the row, and its token in the chunk (one head)
+            bool fac = true;
+            float g_r = 0.f;
+            if constexpr (GATED) {
+                g_r = *smem_chk(stage_gate(s) + m);
+#pragma unroll
+                for (int h = 0; h < CF::T_HALVES; ++h) fac = fac && *smem_chk(stage_gflag(s) + h) != 0;
+            }
+            m10_from_gram<GATED>(tmem + lane_base + kColGram, tmem + lane_base + kColL64M10, m,
+                                 *smem_chk(stage_beta(s) + m), fac, g_r, stage_gate(s), stage_gw(s));
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&bars->gram_empty);
+                mbar_arrive(&bars->l64_ops);
+            }
+            return true;
+        };
+        if constexpr (C == 128) {
+            if (q >= 2 && !m10_to_tmem(0)) i = -1;  // a timeout: skip the loop
+        }
+        while (i >= 0) {
             if constexpr (GATED) {
                 // The keys of W carry the gate's decay from the chunk's start through their own token,
                 // W = T diag(beta) diag(gamma) K with gamma_j = exp2(G_j) (G the prefix sums the
@@ -1259,6 +1353,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!wait_bar(&bars->d_full, (uint32_t)i & 1u, bars, p.status)) break;
             tc_fence_after();
             if (q == 0 && lane == 0) KKT_TRACE_EVENT(EV_E_DFULL, i);
+            if constexpr (C == 128) {
+                if (q >= 2 && !m10_end && !m10_to_tmem(i + 1)) break;
+            }
             const bool warp_full = 32 * wp + 32 <= info.Lc;
             const bool row_ok = r < info.Lc && info.h0 + g < p.H;
             const int64_t grow = (info.t0 + r) * p.H + info.h0 + g;
