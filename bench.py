@@ -339,7 +339,7 @@ def bench_ours(args, rank, world, local):
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
     e2e = {"value": aggregate_value(w.tokens * n_e2e, world, e2e_s), "unit": "tokens/s",
            "h2d_bytes_per_step": runner.h2d_bytes, "d2h_bytes_per_step": runner.d2h_bytes,
-           "steps": n_e2e, "pieces": len(runner.plan)}
+           "steps": n_e2e, "pieces": runner.pieces, "call": "kkt_solve_fwd_host"}
 
     # the spec entry point itself (kkt_solve_fwd: bf16, no workspace, so the tensor-core
     # kernel deals its tiles round robin), timed the same way on the same buffers, after the

@@ -12,10 +12,12 @@ from .api import (  # noqa: F401
     chunk_gated_delta_rule,
     device_status,
     gdn_chunk_state_fwd,
+    host_workspace_bytes,
     kkt_solve_fwd,
+    kkt_solve_fwd_host,
     select_kernel,
 )
 from ._lib import KktError  # noqa: F401
 
-__all__ = ["kkt_solve_fwd", "gdn_chunk_state_fwd", "chunk_gated_delta_rule", "device_status", "select_kernel",
-           "HostRunner", "KktError"]
+__all__ = ["kkt_solve_fwd", "kkt_solve_fwd_host", "host_workspace_bytes", "gdn_chunk_state_fwd",
+           "chunk_gated_delta_rule", "device_status", "select_kernel", "HostRunner", "KktError"]

@@ -30,6 +30,7 @@ KKT_KERNEL_TC = 2
 KERNELS = {"auto": KKT_KERNEL_AUTO, "simt": KKT_KERNEL_SIMT, "tc": KKT_KERNEL_TC}
 
 KKT_WORKSPACE_BYTES = 256
+KKT_HOST_MAX_PIECES = 64
 KKT_NOALLOC_SCRATCH_BYTES = 256
 
 _vp = ctypes.c_void_p
@@ -44,8 +45,12 @@ SIGNATURES = {
     "kkt_solve_fwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
     "gdn_chunk_state_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, ctypes.c_float, _vp,
                                  _vp, _vp]),
+    "kkt_host_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i, _i, _i, _i, _i]),
+    "kkt_solve_fwd_host": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _i, _i, _i, _vp, _sz,
+                                _vp]),
     "kkt_test_stalled_solve": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp]),
     "kkt_test_noalloc_scratch": (_i, [_vp]),
+    "kkt_test_plan_pieces": (_i, [_vp, _i, _i, _i, _vp, _vp, _i, _vp, _i]),
     "kkt_device_status": (_i, [_vp]),
     "kkt_debug_bounds": (_i, [_vp, _vp]),
     "kkt_select_kernel": (_i, [_i, _i, _i, _i, _i]),

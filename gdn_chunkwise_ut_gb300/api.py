@@ -23,9 +23,9 @@ def _stream_handle(stream) -> int:
     return int(stream.cuda_stream)
 
 
-def _check(t: torch.Tensor, name: str, dtype, shape):
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
-        raise ValueError(f"{name} must be a CUDA tensor")
+def _check(t: torch.Tensor, name: str, dtype, shape, host: bool = False):
+    if not isinstance(t, torch.Tensor) or t.is_cuda != (not host):
+        raise ValueError(f"{name} must be a {'host (CPU)' if host else 'CUDA'} tensor")
     if t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     if tuple(t.shape) != tuple(shape):
@@ -224,126 +224,140 @@ def select_kernel(dk: int, dv: int, C: int, io: str = "bf16", kernel: str = "aut
     return {_lib.KKT_KERNEL_SIMT: "simt", _lib.KKT_KERNEL_TC: "tc"}[r]
 
 
-def _pieces(seq_bounds, C: int, parts: int):
-    """Cuts a packed batch (sequence token ranges [a, b) on the flat axis, in order) into at most
-    ``parts`` consecutive pieces of about equal token counts.  A sequence is cut only at a multiple of
-    C from its start, so every piece starts its sub-sequences at chunk boundaries and the chunks, and
-    therefore the results, are those of the whole batch.  Returns [(n0, n1, cu)] with cu the piece's
-    sequence offsets relative to n0."""
-    total = sum(b - a for a, b in seq_bounds)
-    if total == 0:
-        return []
-    target = max(C, -(-total // max(1, parts)))
-    out, cur, n0 = [], [0], None
-    for a, b in seq_bounds:
-        if n0 is None:
-            n0 = a
-        pos = a
-        while True:
-            room = target - cur[-1]
-            if b - pos <= room or room < C:
-                if b - pos > room and cur[-1] > 0:
-                    out.append((n0, n0 + cur[-1], cur))  # close the piece before this sequence part
-                    cur, n0 = [0], pos
-                    continue
-                cur.append(cur[-1] + (b - pos))
-                break
-            cut = pos + (room // C) * C  # a chunk boundary of this sequence (pos is one)
-            cur.append(cur[-1] + (cut - pos))
-            out.append((n0, n0 + cur[-1], cur))
-            cur, n0, pos = [0], cut, cut
-    if cur[-1] > 0 or len(cur) > 1:
-        out.append((n0, n0 + cur[-1], cur))
-    return [(x0, x1, c) for x0, x1, c in out if x1 > x0]
+def host_workspace_bytes(B: int, T: int, H: int, dk: int, dv: int, C: int, *, dtype=torch.bfloat16,
+                         T_dtype=torch.float32, gated: bool = False, varlen: bool = False, pieces: int = 8) -> int:
+    """Device workspace bytes of ``kkt_solve_fwd_host`` for these sizes (no CUDA call)."""
+    io = _IO.get(dtype)
+    if io is None:
+        raise ValueError(f"unsupported dtype {dtype}")
+    n = _lib.lib().kkt_host_workspace_bytes(B, T, H, dk, dv, C, io | _T_FLAG[T_dtype], int(gated), int(varlen),
+                                            int(pieces))
+    if n == 0:
+        raise ValueError("invalid sizes or pieces")
+    return int(n)
+
+
+def kkt_solve_fwd_host(k: torch.Tensor, v: torch.Tensor, beta: torch.Tensor, C: int, cu_seqlens=None, *,
+                       T_out=None, W_out=None, U_out=None, g: torch.Tensor | None = None,
+                       materialize_T: bool = True, T_dtype=torch.float32, kernel: str = "auto", pieces: int = 8,
+                       workspace: torch.Tensor | None = None, device="cuda", stream=None, sync: bool = True):
+    """kkt_solve on HOST tensors through the C ABI (kkt_solve_fwd_host): the library copies k, v, beta
+    (and g) to the device, runs kkt_solve and copies T, W and U back, pipelined in ``pieces`` parts
+    of the token axis.  The results equal those of ``kkt_solve_fwd`` on the device.
+
+    k, v, beta, g and the outputs are CPU tensors (pinned memory lets the copies overlap; the
+    outputs are allocated pinned when not given).  ``cu_seqlens``: None, or the B + 1 sequence
+    offsets as a CPU int32 tensor or a list.  ``workspace``: a CUDA uint8 tensor of at least
+    ``host_workspace_bytes(...)`` bytes (allocated when None; pass one to reuse it).  ``sync``
+    waits for the copies back before returning.  Returns (T_out, W, U) on the host.
+    """
+    if k.dim() != 4 or v.dim() != 4 or beta.dim() != 3:
+        raise ValueError("expected k [B,T,H,dk], v [B,T,H,dv], beta [B,T,H]")
+    Bt, T, H, dk = k.shape
+    dv = v.shape[-1]
+    io = _IO.get(k.dtype)
+    if io is None:
+        raise ValueError(f"unsupported dtype {k.dtype}")
+    t_flag = _T_FLAG.get(T_dtype)
+    if t_flag is None:
+        raise ValueError(f"T_dtype must be torch.float32 or torch.float16, got {T_dtype}")
+    _check(k, "k", k.dtype, (Bt, T, H, dk), host=True)
+    _check(v, "v", k.dtype, (Bt, T, H, dv), host=True)
+    _check(beta, "beta", torch.float32, (Bt, T, H), host=True)
+    if g is not None:
+        _check(g, "g", torch.float32, (Bt, T, H), host=True)
+    cu_host = None
+    if cu_seqlens is not None:
+        if Bt != 1:
+            raise ValueError("with cu_seqlens the batch dimension must be 1")
+        cu_host = torch.as_tensor(cu_seqlens, dtype=torch.int32).contiguous()
+        if cu_host.is_cuda or cu_host.dim() != 1:
+            raise ValueError("cu_seqlens must be a 1-D host int32 tensor or a list")
+        B = cu_host.shape[0] - 1
+    else:
+        B = Bt
+    pin = torch.cuda.is_available()
+    if not materialize_T:
+        if T_out is not None:
+            raise ValueError("T_out given with materialize_T=False")
+    elif T_out is None:
+        T_out = torch.empty((Bt, T, H, C), dtype=T_dtype, pin_memory=pin)
+    if W_out is None:
+        W_out = torch.empty((Bt, T, H, dk), dtype=k.dtype, pin_memory=pin)
+    if U_out is None:
+        U_out = torch.empty((Bt, T, H, dv), dtype=k.dtype, pin_memory=pin)
+    if materialize_T:
+        _check(T_out, "T_out", T_dtype, (Bt, T, H, C), host=True)
+    _check(W_out, "W_out", k.dtype, (Bt, T, H, dk), host=True)
+    _check(U_out, "U_out", k.dtype, (Bt, T, H, dv), host=True)
+    kern = _lib.KERNELS.get(kernel)
+    if kern is None:
+        raise ValueError(f"kernel must be one of {sorted(_lib.KERNELS)}")
+    need = host_workspace_bytes(B, T, H, dk, dv, C, dtype=k.dtype, T_dtype=T_dtype, gated=g is not None,
+                                varlen=cu_host is not None, pieces=pieces)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+        if stream is not None:  # the buffer is freed on return, in use on `stream` until the call ends
+            workspace.record_stream(stream)
+    if not isinstance(workspace, torch.Tensor) or not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA tensor")
+    rc = _lib.lib().kkt_solve_fwd_host(k.data_ptr(), v.data_ptr(), beta.data_ptr(),
+                                       None if g is None else g.data_ptr(),
+                                       None if cu_host is None else cu_host.data_ptr(), B, T, H, dk, dv, C,
+                                       T_out.data_ptr() if materialize_T else None, W_out.data_ptr(),
+                                       U_out.data_ptr(), io | t_flag, kern, int(pieces), workspace.data_ptr(),
+                                       workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if rc != _lib.KKT_OK:
+        raise _lib.KktError(rc, "kkt_solve_fwd_host")
+    if sync:
+        (stream if stream is not None else torch.cuda.current_stream()).synchronize()
+    return T_out, W_out, U_out
 
 
 class HostRunner:
-    """End-to-end calls on host tensors: pinned host -> device -> kkt_solve_fwd -> pinned host.
+    """End-to-end calls on host tensors through ``kkt_solve_fwd_host`` (the C ABI's host-buffer entry
+    point), with the device workspace and the pinned host outputs allocated once.
 
-    Device buffers are allocated once.  Each call cuts the batch into ``pieces`` parts along the
-    token axis (whole sequences, or chunk-aligned parts of one) and pipelines them: the inputs of a
-    piece are copied in on one stream, the library runs it on the current stream, and its T, W and U
-    are copied back on a third stream, so the two copy directions and the kernels overlap.  The
-    results are those of one call on the whole batch.  ``sync=True`` waits for the copies.
-    ``h2d_ahead`` (default 2) holds a piece's input copies until the outputs of the piece that many
-    places earlier are back on the host (0: no hold), which keeps the link for the larger output
-    direction.
+    Each call copies the inputs in, runs kkt_solve and copies T, W and U back, pipelined by the
+    library in ``pieces`` parts of the token axis (whole sequences, or chunk-aligned parts of one)
+    on its own copy streams and the current stream.  The results are those of one call on the whole
+    batch.  ``sync=True`` waits for the copies.
     """
 
     def __init__(self, B, T, H, dk, dv, C, *, dtype=torch.bfloat16, cu_seqlens=None,
                  kernel="auto", device="cuda", materialize_T: bool = True, T_dtype=torch.float32,
-                 gated: bool = False, pieces: int = 8, h2d_ahead: int = 2):
+                 gated: bool = False, pieces: int = 8):
         self.C, self.kernel, self.materialize_T, self.T_dtype = C, kernel, materialize_T, T_dtype
-        dev = torch.device(device)
+        self.pieces, self.gated = int(pieces), gated
+        self.cu = None if cu_seqlens is None else torch.as_tensor(
+            [int(x) for x in cu_seqlens], dtype=torch.int32)
+        nseq = B if self.cu is None else self.cu.shape[0] - 1
         self.shape = (B, T, H)
-        self.k = torch.empty((B, T, H, dk), device=dev, dtype=dtype)
-        self.v = torch.empty((B, T, H, dv), device=dev, dtype=dtype)
-        self.beta = torch.empty((B, T, H), device=dev, dtype=torch.float32)
-        self.g = torch.empty((B, T, H), device=dev, dtype=torch.float32) if gated else None
-        self.T_out = torch.empty((B, T, H, C), device=dev, dtype=T_dtype) if materialize_T else None
-        self.W = torch.empty((B, T, H, dk), device=dev, dtype=dtype)
-        self.U = torch.empty((B, T, H, dv), device=dev, dtype=dtype)
-        self.T_host = (torch.empty(self.T_out.shape, dtype=T_dtype, pin_memory=True)
-                       if materialize_T else None)
-        self.W_host = torch.empty(self.W.shape, dtype=dtype, pin_memory=True)
-        self.U_host = torch.empty(self.U.shape, dtype=dtype, pin_memory=True)
-        if cu_seqlens is None:
-            bounds = [(b * T, (b + 1) * T) for b in range(B)]
-        else:
-            cu = [int(x) for x in cu_seqlens]
-            bounds = list(zip(cu[:-1], cu[1:]))
-        self.plan = [(n0, n1, torch.tensor(c, dtype=torch.int32, device=dev))
-                     for n0, n1, c in _pieces(bounds, C, max(1, int(pieces)))]
-        self.s_in = torch.cuda.Stream(device=dev)
-        self.s_out = torch.cuda.Stream(device=dev)
-        # h2d_ahead > 0: a piece's inputs are copied in only once the outputs of the piece that many
-        # places earlier are back on the host, so that the inputs do not take the link from the
-        # outputs (which are the larger direction) early on
-        self.h2d_ahead = max(0, int(h2d_ahead))
-        self._out_done = [torch.cuda.Event() for _ in self.plan] if self.h2d_ahead else []
+        self.sizes = (dk, dv)
+        self.dtype = dtype
+        self.workspace = torch.empty(
+            host_workspace_bytes(nseq, T, H, dk, dv, C, dtype=dtype, T_dtype=T_dtype, gated=gated,
+                                 varlen=self.cu is not None, pieces=self.pieces),
+            dtype=torch.uint8, device=device)
+        self.T_host = torch.empty((B, T, H, C), dtype=T_dtype, pin_memory=True) if materialize_T else None
+        self.W_host = torch.empty((B, T, H, dk), dtype=dtype, pin_memory=True)
+        self.U_host = torch.empty((B, T, H, dv), dtype=dtype, pin_memory=True)
 
     @property
     def h2d_bytes(self) -> int:
-        return sum(t.numel() * t.element_size() for t in (self.k, self.v, self.beta, self.g) if t is not None)
+        B, T, H = self.shape
+        dk, dv = self.sizes
+        es = torch.empty((), dtype=self.dtype).element_size()
+        return B * T * H * ((dk + dv) * es + 4 + (4 if self.gated else 0))
 
     @property
     def d2h_bytes(self) -> int:
-        return sum(t.numel() * t.element_size() for t in (self.T_out, self.W, self.U) if t is not None)
+        return sum(t.numel() * t.element_size() for t in (self.T_host, self.W_host, self.U_host) if t is not None)
 
     def __call__(self, k_host, v_host, beta_host, sync: bool = True, g_host=None):
-        B, T, H = self.shape
-        N = B * T
-        rows = lambda x: x.reshape(N, H, -1) if x.dim() == 4 else x.reshape(N, H)  # flat token axis
-        dev_in = [rows(x) for x in (self.k, self.v, self.beta, self.g) if x is not None]
-        host_in = [rows(x) for x in (k_host, v_host, beta_host, g_host) if x is not None]
-        if len(host_in) != len(dev_in):
+        if (g_host is not None) != self.gated:
             raise ValueError("g_host must be given exactly when the runner is gated")
-        dev_out = [rows(x) for x in (self.T_out, self.W, self.U) if x is not None]
-        host_out = [rows(x) for x in (self.T_host, self.W_host, self.U_host) if x is not None]
-        compute = torch.cuda.current_stream()
-        # the previous call's kernels have read the inputs, and its copies have read the outputs
-        self.s_in.wait_stream(compute)
-        compute.wait_stream(self.s_out)
-        for idx, (n0, n1, cu) in enumerate(self.plan):
-            with torch.cuda.stream(self.s_in):
-                if self.h2d_ahead and idx >= self.h2d_ahead:
-                    self.s_in.wait_event(self._out_done[idx - self.h2d_ahead])
-                for d, h in zip(dev_in, host_in):
-                    d[n0:n1].copy_(h[n0:n1], non_blocking=True)
-            compute.wait_stream(self.s_in)
-            piece = [x[n0:n1].unsqueeze(0) for x in dev_in]       # [1, n, H, .] views
-            outp = [x[n0:n1].unsqueeze(0) for x in dev_out]
-            kkt_solve_fwd(piece[0], piece[1], piece[2], self.C, cu,
-                          T_out=outp[0] if self.T_out is not None else None, W_out=outp[-2], U_out=outp[-1],
-                          kernel=self.kernel, materialize_T=self.materialize_T, T_dtype=self.T_dtype,
-                          g=piece[3] if self.g is not None else None)
-            self.s_out.wait_stream(compute)
-            with torch.cuda.stream(self.s_out):
-                for d, h in zip(dev_out, host_out):
-                    h[n0:n1].copy_(d[n0:n1], non_blocking=True)
-                if self.h2d_ahead:
-                    self._out_done[idx].record(self.s_out)
-        compute.wait_stream(self.s_out)
-        if sync:
-            compute.synchronize()
-        return self.T_host, self.W_host, self.U_host
+        return kkt_solve_fwd_host(k_host, v_host, beta_host, self.C, self.cu, T_out=self.T_host, W_out=self.W_host,
+                                  U_out=self.U_host, g=g_host, materialize_T=self.materialize_T,
+                                  T_dtype=self.T_dtype, kernel=self.kernel, pieces=self.pieces,
+                                  workspace=self.workspace, sync=sync)

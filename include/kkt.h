@@ -238,6 +238,49 @@ int gdn_chunk_state_fwd(const void *q, const void *k, const void *w, const void 
                         struct CUstream_st *stream);
 
 /*
+ * kkt_solve_fwd_host -- kkt_solve on HOST buffers: the call copies the inputs to the device, runs
+ * kkt_solve and copies T, W and U~ back, pipelined in consecutive pieces of the token axis so that
+ * the two copy directions and the kernels overlap.  The operation, shapes and dtypes are those of
+ * kkt_solve_fwd_gated (the page "TileLang 实战：单位下三角矩阵求逆", section 1); the pages have no
+ * host-memory entry point: this one serves callers whose tensors live in host memory, and is the
+ * call the end-to-end measurement makes.
+ *
+ *   k, v, beta, g, T_out, W_out, U_out   HOST pointers, the shapes and dtypes of kkt_solve_fwd_ex
+ *                   (g may be NULL: ungated; T_out may be NULL: W and U~ only).  Page-locked
+ *                   (pinned) memory lets the copies run asynchronously and overlap; with pageable
+ *                   memory the results are the same, but the copies serialise.
+ *   cu_seqlens      NULL, or a HOST int32 array of B + 1 offsets, as in kkt_solve_fwd (checked on
+ *                   the host: nondecreasing, from 0 to T, else KKT_ERR_SEQLENS)
+ *   io_dtype, kernel  as in kkt_solve_fwd_ex
+ *   pieces          1 .. KKT_HOST_MAX_PIECES consecutive parts of the token axis; a sequence is cut
+ *                   only at a multiple of C from its start, so every chunk, and every result, is
+ *                   that of one call on the whole batch
+ *   workspace       DEVICE memory of at least kkt_host_workspace_bytes(...) bytes, 256-byte
+ *                   aligned, owned by the caller: the device copies of every tensor and the
+ *                   kernel's work counter.  Calls that may run at the same time need distinct
+ *                   workspaces.
+ *   stream          the call runs after the work already on `stream`, and the work enqueued on
+ *                   `stream` after it runs after it; it returns without waiting (synchronise
+ *                   `stream` before reading the outputs or reusing the inputs).  The copies run on
+ *                   two streams of the library's own per device, created on the first call and kept
+ *                   until the process exits (cudaDeviceReset invalidates them: calls after a reset
+ *                   are not supported).  Host threads may call it at the same time: the enqueueing
+ *                   is serialised.
+ *
+ * Returns the statuses of kkt_solve_fwd_gated (argument errors without enqueueing anything);
+ * KKT_ERR_ARG also for a workspace that is too small or misaligned.
+ */
+#define KKT_HOST_MAX_PIECES 64
+/* Workspace bytes of kkt_solve_fwd_host for the same B, T, H, dk, dv, C and io_dtype; gated: g != NULL;
+ * varlen: cu_seqlens != NULL (the token axis then has T rows, else B * T).  Host-only, no CUDA call. */
+size_t kkt_host_workspace_bytes(int B, int T, int H, int dk, int dv, int C, int io_dtype, int gated, int varlen,
+                                int pieces);
+int kkt_solve_fwd_host(const void *k, const void *v, const float *beta, const float *g,
+                       const int32_t *cu_seqlens, int B, int T, int H, int dk, int dv, int C,
+                       void *T_out, void *W_out, void *U_out, int io_dtype, int kernel, int pieces,
+                       void *workspace, size_t workspace_bytes, struct CUstream_st *stream);
+
+/*
  * kkt_device_status -- synchronises `stream`, then returns and clears the
  * status word of the current device: KKT_OK, or the first device-side error
  * (KKT_ERR_SEQLENS, KKT_ERR_TIMEOUT) recorded since the last call; KKT_ERR_CUDA

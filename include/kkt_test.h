@@ -55,6 +55,18 @@ int kkt_debug_bounds(unsigned long long *first, int *kind);
  */
 int kkt_test_noalloc_scratch(unsigned long long *out2);
 
+/*
+ * kkt_test_plan_pieces -- the piece plan of kkt_solve_fwd_host (host only, no CUDA call).  The
+ * sequences are [starts[s], starts[s + 1]) on the flat token axis (nseq + 1 offsets); C is the chunk
+ * size and parts the most pieces allowed.  Writes piece p's first row and last row + 1 to
+ * bounds[2 p] and bounds[2 p + 1], the number of its sub-sequences to nsub[p], and its sub-sequence
+ * offsets (relative to its first row, nsub[p] + 1 of them, the first 0) one piece after the other
+ * to cu.  Returns the number of pieces, or -1 when max_pieces or cu_cap is too small or an argument
+ * is invalid.
+ */
+int kkt_test_plan_pieces(const int64_t *starts, int nseq, int C, int parts, int64_t *bounds, int32_t *nsub,
+                         int max_pieces, int32_t *cu, int cu_cap);
+
 #ifdef __cplusplus
 }
 #endif

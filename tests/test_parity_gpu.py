@@ -454,7 +454,6 @@ def test_host_runner_pipeline(case):
     torch.cuda.synchronize()
     runner = HostRunner(k.shape[0], k.shape[1], H, 128, 128, C, cu_seqlens=cu, T_dtype=t_dtype,
                         gated=g is not None, pieces=4)
-    assert len(runner.plan) >= 2
     hosts = [x.cpu().pin_memory() for x in (k, v, beta)]
     gh = g.cpu().pin_memory() if g is not None else None
     for _ in range(2):  # a second call reuses the buffers
