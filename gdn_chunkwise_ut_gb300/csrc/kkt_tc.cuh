@@ -37,7 +37,11 @@
 //                   buffer, and writes its rows of T~ = T diag(beta) as a bf16
 //                   hi / lo pair into tensor memory (tcgen05.st).
 //   epilogue warps  per warp: tcgen05.ld of its 32 rows of D, bf16 conversion,
-//                   a double-buffered swizzled staging and TMA stores of W, U~.
+//                   a swizzled staging (double-buffered at C <= 64) and TMA
+//                   stores of W, U~.  Gated, they also scale the stage's K rows
+//                   by the decay from the chunk's start; at C = 128 the two of
+//                   lanes 64..127 form M10 from the Gram into tensor memory for
+//                   the level-64 MMA.
 //
 // Rows of a short last chunk (Lc < C) past Lc are zeroed in shared memory
 // before the Gram MMA; warps whose 32 rows are not all valid write their valid
@@ -411,10 +415,10 @@ __device__ __forceinline__ void form_a_row(uint8_t *tm, uint32_t gram, int m, in
     for (int h = h_lo; h <= h_hi; ++h) {
         uint32_t v[32];
         tmem_ld32(gram + 32 * h, v);
-        float uh = 1.f;
+        float bu = beta_r;  // beta_r, times the block's row factor when gated
         float4 wq[8];
         if constexpr (GATED) {
-            uh = fac ? exp2f(g_r - *smem_chk(sg + 32 * h)) : 1.f;
+            bu *= fac ? exp2f(g_r - *smem_chk(sg + 32 * h)) : 1.f;
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8)
                 wq[c8] = fac ? *smem_chk(reinterpret_cast<const float4 *>(sw + 32 * h + 4 * c8)) : make_float4(1.f, 1.f, 1.f, 1.f);
@@ -423,15 +427,15 @@ __device__ __forceinline__ void form_a_row(uint8_t *tm, uint32_t gram, int m, in
 #pragma unroll
         for (int c = 0; c < 32; c += 4) {
             float e[4];
-            float gm[4] = {1.f, 1.f, 1.f, 1.f};
+            float wj[4] = {1.f, 1.f, 1.f, 1.f};
             if constexpr (GATED) {
                 const float4 w4 = wq[c / 4];
-                gm[0] = uh * w4.x; gm[1] = uh * w4.y; gm[2] = uh * w4.z; gm[3] = uh * w4.w;
+                wj[0] = w4.x; wj[1] = w4.y; wj[2] = w4.z; wj[3] = w4.w;
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int j = 32 * h + c + u;
-                e[u] = (j < r) ? beta_r * __uint_as_float(v[c + u]) * gm[u] : (j == r ? 1.f : 0.f);
+                e[u] = (j < r) ? bu * __uint_as_float(v[c + u]) * wj[u] : (j == r ? 1.f : 0.f);
             }
             *tm_vec(tm, m, 32 * h + c) = make_float4(e[0], e[1], e[2], e[3]);
         }
