@@ -271,21 +271,25 @@ def test_gate_zero_is_ungated(kernel):
 
 
 @pytest.mark.parametrize("kernel", ALL_KERNELS)
-def test_gate_cut_is_block_diagonal(kernel):
+@pytest.mark.parametrize("C", [32, 64, 128])
+def test_gate_cut_is_block_diagonal(kernel, C):
     """A token with zero decay (g = -1000) cuts its chunk: T is exactly zero across the cut, and the
-    rest matches the oracle."""
-    _skip_unless(kernel, 128, 128, 64)
+    rest matches the oracle.  The cuts make their blocks of the decay matrix non-factorable, so the
+    element-by-element path runs (at C = 128 also where M10 of the level-64 coupling is formed)."""
+    _skip_unless(kernel, 128, 128, C)
     k, v, beta = make_inputs(1, 256, 2, 128, 128, seed=46, device=DEV)
     g = make_gate(1, 256, 2, seed=46, device=DEV)
-    cuts = [(40, 0), (64 + 33, 1), (128 + 64 + 5, 0)]
+    cuts = {32: [(10, 0), (32 + 20, 1), (128 + 5, 0)],
+            64: [(40, 0), (64 + 33, 1), (128 + 64 + 5, 0)],
+            128: [(40, 0), (100, 1), (128 + 70, 0)]}[C]
     for t, h in cuts:
         g[0, t, h] = -1000.0
-    T, W, U = run(k, v, beta, 64, kernel=kernel, g=g)
+    T, W, U = run(k, v, beta, C, kernel=kernel, g=g)
     for t, h in cuts:
-        c0, cut = (t // 64) * 64, t % 64
-        blk = T[0, c0 + cut:c0 + 64, h, :cut]
+        c0, cut = (t // C) * C, t % C
+        blk = T[0, c0 + cut:c0 + C, h, :cut]
         assert torch.count_nonzero(blk) == 0
-    full_compare(k, v, beta, 64, None, (T, W, U), g=g)
+    full_compare(k, v, beta, C, None, (T, W, U), g=g)
 
 
 @pytest.mark.parametrize("C", [32, 64, 128])
