@@ -86,10 +86,11 @@ constexpr uint32_t kColD = 128;          // 256 fp32 columns: W | U~
 constexpr uint32_t kColTT = 384;         // 64 packed bf16x2 hi + 64 lo
 // C = 128, level 64 on the tensor core.  The A operands as packed bf16 hi + lo pairs (32 + 32
 // columns, lanes 64..127): M10 in T~'s columns (free once the previous tile's W|U MMA has read T~),
-// M11^-1 in D's (free once the previous D is drained); the fp32 products Y, then Z, in the other 64
-// columns of T~'s.
+// M11^-1 in the Gram's columns 64..127 (in those lanes only read by the warps of rows 64..127 when
+// they form A; the next Gram MMA waits for Z); the fp32 products Y, then Z, in the other 64 columns
+// of T~'s.
 constexpr uint32_t kColL64M10 = kColTT;
-constexpr uint32_t kColL64M11 = kColD;
+constexpr uint32_t kColL64M11 = kColGram + 64;
 constexpr uint32_t kColL64D = kColTT + 64;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
@@ -167,11 +168,16 @@ struct TcParams {
 enum TraceEvent {
     EV_P_EMPTY = 0, EV_P_ISSUE, EV_M_FULL, EV_M_GRAM, EV_M_EPI, EV_I_GRAM, EV_I_INV, EV_I_TSTORE,
     EV_I_TT, EV_E_DFULL, EV_E_DEMPTY, EV_E_DONE, EV_I_LD, EV_I_DIAG, EV_I_C16, EV_I_PAIR, EV_M_LATE,
-    EV_M_READY, EV_I_BW, EV_I_TTW, EV_I_L32, EV_COUNT
+    EV_M_READY, EV_I_BW, EV_I_TTW, EV_I_L32,
+    // C = 128, level 64: rows 64..127 (warp quarter 3) end level 32, have M11^-1 in tensor memory,
+    // see Y, have Y's split in shared memory, see Z, end level 64; rows 0..63 (quarter 1) have split
+    // M00^-1; the epilogue warp of quarter 3 has formed M10; the W|U thread issues Y, then Z
+    EV_I_L32B, EV_I_M11, EV_I_Y, EV_I_YB, EV_I_Z, EV_I_INVB, EV_I_OPS, EV_E_M10, EV_M_L64Y, EV_M_L64Z,
+    EV_COUNT
 };
 constexpr int kTraceCtas = 160;
 constexpr int kTraceTiles = 64;  // the last tile row holds the CTA's clock calibration
-constexpr int kTraceSlots = 24;
+constexpr int kTraceSlots = 32;
 static_assert(EV_COUNT <= kTraceSlots, "trace slots");
 #ifdef KKT_TRACE
 // SM cycle counter at each event; trace.py maps it to ns with the (globaltimer, clock) pairs that
@@ -180,6 +186,15 @@ static_assert(EV_COUNT <= kTraceSlots, "trace slots");
     do {                                                                                               \
         if (p.trace && blockIdx.x < kTraceCtas && (tile) < kTraceTiles - 1)                            \
             p.trace[((size_t)blockIdx.x * kTraceTiles + (tile)) * kTraceSlots + (ev)] = clock64();      \
+    } while (0)
+// the event row of a tile, for functions that record events without the kernel's parameters
+#define KKT_TRACE_ROW(tile)                                                                              \
+    ((p.trace && blockIdx.x < kTraceCtas && (tile) < kTraceTiles - 1)                                  \
+         ? p.trace + ((size_t)blockIdx.x * kTraceTiles + (tile)) * kTraceSlots                         \
+         : nullptr)
+#define KKT_TRACE_AT(row, ev)                 \
+    do {                                      \
+        if (row) (row)[(ev)] = clock64();     \
     } while (0)
 #define KKT_TRACE_CALIB(slot)                                                                            \
     do {                                                                                               \
@@ -192,6 +207,10 @@ static_assert(EV_COUNT <= kTraceSlots, "trace slots");
 #else
 #define KKT_TRACE_EVENT(ev, tile) \
     do {                          \
+    } while (0)
+#define KKT_TRACE_ROW(tile) (static_cast<unsigned long long *>(nullptr))
+#define KKT_TRACE_AT(row, ev) \
+    do {                      \
     } while (0)
 #define KKT_TRACE_CALIB(slot) \
     do {                      \
@@ -546,7 +565,9 @@ __device__ __forceinline__ void l64_mma(uint32_t d, uint32_t a, uint32_t b_smem)
 
 // The inverse warps' part of level 64 for tile i (q: the warp's row quarter, m its row).
 __device__ __forceinline__ bool level64_tc(int q, int m, int i, uint8_t *tm, uint32_t tmem, uint32_t lane_base,
-                                           int lane, Barriers *bars, int *status) {
+                                           int lane, Barriers *bars, int *status, unsigned long long *trow) {
+    (void)trow;  // the tile's trace row (trace builds only)
+    const bool tr = (q == 1 || q == 3) && lane == 0;
     const uint32_t ph = (uint32_t)i & 1u;
     if (q < 2) {
         // M00^-1 row m (= row k of Y's B operand), split into hi + lo
@@ -560,19 +581,20 @@ __device__ __forceinline__ bool level64_tc(int q, int m, int i, uint8_t *tm, uin
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->l64_ops);
+        if (tr) KKT_TRACE_AT(trow, EV_I_OPS);
         // Z done: the B operand area is read, and is cleared again (the upper right of T is zero)
         if (!wait_bar(&bars->l64_z, ph, bars, status)) return false;
 #pragma unroll
         for (int j = 64; j < 128; j += 4) *tm_vec(tm, m, j) = make_float4(0.f, 0.f, 0.f, 0.f);
         return true;
     }
-    // M11^-1 (columns 64..127) into D's columns, once the previous tile's D has been drained
-    if (!wait_bar(&bars->d_empty, ph ^ 1u, bars, status)) return false;
-    tc_fence_after();
+    // M11^-1 (columns 64..127) into the Gram's columns 64..127, which this warp read when it formed A
     l64_row_to_tmem(tm, m, 64, tmem + lane_base + kColL64M11);
+    if (tr) KKT_TRACE_AT(trow, EV_I_M11);
     // Y row m - 64 -> row k = m - 64 of Z's B operand
     if (!wait_bar(&bars->l64_y, ph, bars, status)) return false;
     tc_fence_after();
+    if (tr) KKT_TRACE_AT(trow, EV_I_Y);
     const int k = m - 64;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -596,9 +618,11 @@ __device__ __forceinline__ bool level64_tc(int q, int m, int i, uint8_t *tm, uin
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars->l64_yb);
+    if (tr) KKT_TRACE_AT(trow, EV_I_YB);
     // -Z over M10 (read into tensor memory above)
     if (!wait_bar(&bars->l64_z, ph, bars, status)) return false;
     tc_fence_after();
+    if (tr) KKT_TRACE_AT(trow, EV_I_Z);
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         uint32_t v[32];
@@ -873,6 +897,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
             }
             if (!wait_bar(&bars->gram_empty, ((uint32_t)i & 1u) ^ 1u, bars, p.status)) break;
+            if constexpr (C == 128) {
+                // the previous tile's Z has read M11^-1 from the Gram's columns
+                if (!wait_bar(&bars->l64_z, ((uint32_t)i & 1u) ^ 1u, bars, p.status)) break;
+            }
             if (lane == 0) {
                 tc_fence_after();
                 const uint32_t a0 = smem_u32(stage_kv(s));
@@ -914,10 +942,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if constexpr (C == 128) {
                 // the tile's level-64 products (see level64_tc); the operands' arrivals imply that the
-                // previous W|U MMA has read T~ (Y's columns) and, for Z, that D is drained
+                // previous W|U MMA has read T~ (Y's columns)
                 const uint32_t b_smem = smem_u32(smem + CF::OFF_T + 2 * 16384);
                 if (!wait_bar(&bars->l64_ops, (uint32_t)i & 1u, bars, p.status)) break;
                 if (lane == 0) {
+                    KKT_TRACE_EVENT(EV_M_L64Y, i);
                     tc_fence_after();
                     l64_mma(tmem + kColL64D, tmem + kColL64M10, b_smem);
                     mma_commit(&bars->l64_y);
@@ -925,6 +954,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (!wait_bar(&bars->l64_yb, (uint32_t)i & 1u, bars, p.status)) break;
                 if (lane == 0) {
+                    KKT_TRACE_EVENT(EV_M_L64Z, i);
                     tc_fence_after();
                     l64_mma(tmem + kColL64D, tmem + kColL64M11, b_smem);
                     mma_commit(&bars->l64_z);
@@ -1147,9 +1177,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if constexpr (C == 128) {
                     // level 64: rows 64..127 of the chunk, on the tensor core (see level64_tc)
                     if (q == 1 && lane == 0) KKT_TRACE_EVENT(EV_I_L32, i);
-                    if (ok) ok = level64_tc(q, m, i, tm, tmem, lane_base, lane, bars, p.status);
+                    if (q == 3 && lane == 0) KKT_TRACE_EVENT(EV_I_L32B, i);
+                    if (ok) ok = level64_tc(q, m, i, tm, tmem, lane_base, lane, bars, p.status, KKT_TRACE_ROW(i));
                     fence_proxy_async_smem();
                     __syncwarp();
+                    if (q == 3 && lane == 0) KKT_TRACE_EVENT(EV_I_INVB, i);
                 }
             } else {
                 fence_proxy_async_smem();
@@ -1306,6 +1338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) {
                 mbar_arrive(&bars->gram_empty);
                 mbar_arrive(&bars->l64_ops);
+                if (q == 3) KKT_TRACE_EVENT(EV_E_M10, t);
             }
             return true;
         };

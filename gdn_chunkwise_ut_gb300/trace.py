@@ -21,8 +21,8 @@ from .inputs import make_gate, workloads
 
 EVENTS = ["P_EMPTY", "P_ISSUE", "M_FULL", "M_GRAM", "M_EPI", "I_GRAM", "I_INV", "I_TSTORE", "I_TT",
           "E_DFULL", "E_DEMPTY", "E_DONE", "I_LD", "I_DIAG", "I_C16", "I_PAIR", "M_LATE", "M_READY", "I_BW", "I_TTW",
-          "I_L32"]
-TRACE_CTAS, TRACE_TILES, TRACE_SLOTS = 160, 64, 24
+          "I_L32", "I_L32B", "I_M11", "I_Y", "I_YB", "I_Z", "I_INVB", "I_OPS", "E_M10", "M_L64Y", "M_L64Z"]
+TRACE_CTAS, TRACE_TILES, TRACE_SLOTS = 160, 64, 32
 
 
 def run(workload: str, warmup: int = 3, dynamic: bool = True, gated: bool = False):
@@ -164,6 +164,18 @@ def report(tr: np.ndarray, ctas: int, tiles: int) -> str:
         ("D drained -> next W|U MMA ready", span("E_DEMPTY", "M_READY", shift=1)),
         ("C=128: level-32 coupling", span("I_PAIR", "I_L32")),
         ("C=128: level-64 coupling", span("I_L32", "I_INV")),
+        ("C=128: Gram ready -> level 32 ends, rows 0..63", span("I_GRAM", "I_L32")),
+        ("C=128: Gram ready -> level 32 ends, rows 64..", span("I_GRAM", "I_L32B")),
+        ("C=128: Gram ready -> M10 formed (epilogue)", span("I_GRAM", "E_M10")),
+        ("C=128: level 32 end -> M00^-1 split, rows 0..", span("I_L32", "I_OPS")),
+        ("C=128: level 32 end -> M11^-1 in TMEM, 64..", span("I_L32B", "I_M11")),
+        ("C=128: M00^-1 split -> Y issued", span("I_OPS", "M_L64Y")),
+        ("C=128: Y issued -> Y seen by rows 64..", span("M_L64Y", "I_Y")),
+        ("C=128: Y seen -> Y split to shared memory", span("I_Y", "I_YB")),
+        ("C=128: Y split -> Z issued", span("I_YB", "M_L64Z")),
+        ("C=128: Z issued -> Z seen by rows 64..", span("M_L64Z", "I_Z")),
+        ("C=128: Z seen -> level 64 ends, rows 64..", span("I_Z", "I_INVB")),
+        ("C=128: level 64 ends, rows 64.. -> rows 0..", span("I_INVB", "I_INV")),
     ]
     lines.append("")
     for name, val in rows:
