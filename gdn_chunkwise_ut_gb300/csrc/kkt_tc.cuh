@@ -173,11 +173,12 @@ enum TraceEvent {
     // see Y, have Y's split in shared memory, see Z, end level 64; rows 0..63 (quarter 1) have split
     // M00^-1; the epilogue warp of quarter 3 has formed M10; the W|U thread issues Y, then Z
     EV_I_L32B, EV_I_M11, EV_I_Y, EV_I_YB, EV_I_Z, EV_I_INVB, EV_I_OPS, EV_E_M10, EV_M_L64Y, EV_M_L64Z,
-    EV_COUNT
+    // ... and the shared-memory stores of M00^-1's split (quarter 1) and of Y's (quarter 3) are issued
+    EV_I_SPLIT, EV_I_YSPL, EV_COUNT
 };
 constexpr int kTraceCtas = 160;
 constexpr int kTraceTiles = 64;  // the last tile row holds the CTA's clock calibration
-constexpr int kTraceSlots = 32;
+constexpr int kTraceSlots = 40;
 static_assert(EV_COUNT <= kTraceSlots, "trace slots");
 #ifdef KKT_TRACE
 // SM cycle counter at each event; trace.py maps it to ns with the (globaltimer, clock) pairs that
@@ -578,6 +579,7 @@ __device__ __forceinline__ bool level64_tc(int q, int m, int i, uint8_t *tm, uin
             *l64_b(tm, 0, m, c) = hi;
             *l64_b(tm, 1, m, c) = lo;
         }
+        if (tr) KKT_TRACE_AT(trow, EV_I_SPLIT);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->l64_ops);
@@ -613,6 +615,7 @@ __device__ __forceinline__ bool level64_tc(int q, int m, int i, uint8_t *tm, uin
             *l64_b(tm, 1, k, 4 * h + c) = lo;
         }
     }
+    if (tr) KKT_TRACE_AT(trow, EV_I_YSPL);
     tmem_wait_st();
     fence_proxy_async_smem();
     tc_fence_before();

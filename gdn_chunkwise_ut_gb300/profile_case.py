@@ -1,7 +1,7 @@
 """Runs one workload a few times through the C ABI, for profilers (ncu) to capture.
 
     python -m gdn_chunkwise_ut_gb300.profile_case [--workload c3_b4_t8192_h16] [--calls 4] [--kernel auto]
-        [--gated] [--consumer]
+        [--gated] [--consumer] [--head-dim 64]
 
 ``--consumer`` runs the chunk state recurrence (gdn_chunk_state_fwd) ``--calls`` times instead, on W and
 U~ from one kkt_solve call.
@@ -12,6 +12,7 @@ of the path run back to back and the process synchronises and exits.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 
 import torch
 
@@ -26,8 +27,11 @@ def main():
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc"])
     ap.add_argument("--gated", action="store_true", help="the gated variant (seeded log decays)")
     ap.add_argument("--consumer", action="store_true", help="the chunk state recurrence instead of kkt_solve")
+    ap.add_argument("--head-dim", type=int, default=None, help="override d_k = d_v (64 or 128)")
     a = ap.parse_args()
     w = workloads()[a.workload]
+    if a.head_dim is not None:
+        w = dataclasses.replace(w, dk=a.head_dim, dv=a.head_dim)
     k, v, beta, cu = w.make(seed=0, device="cuda")
     g = make_gate(k.shape[0], k.shape[1], w.H, device="cuda") if a.gated else None
     cu_t = None if cu is None else torch.as_tensor(cu, dtype=torch.int32, device="cuda")

@@ -6,12 +6,13 @@ every tile (microseconds from the CTA's first event), plus per-role averages.
 Events are SM cycle counts, mapped to the global timer with the pairs of
 (global timer, cycle count) that each CTA records at its start and end.
 
-    python -m gdn_chunkwise_ut_gb300.trace [--workload c3_b4_t8192_h16] [--ctas 2] [--tiles 12]
+    python -m gdn_chunkwise_ut_gb300.trace [--workload c3_b4_t8192_h16] [--ctas 2] [--tiles 12] [--head-dim 64]
 """
 from __future__ import annotations
 
 import argparse
 import ctypes
+import dataclasses
 
 import numpy as np
 import torch
@@ -21,16 +22,19 @@ from .inputs import make_gate, workloads
 
 EVENTS = ["P_EMPTY", "P_ISSUE", "M_FULL", "M_GRAM", "M_EPI", "I_GRAM", "I_INV", "I_TSTORE", "I_TT",
           "E_DFULL", "E_DEMPTY", "E_DONE", "I_LD", "I_DIAG", "I_C16", "I_PAIR", "M_LATE", "M_READY", "I_BW", "I_TTW",
-          "I_L32", "I_L32B", "I_M11", "I_Y", "I_YB", "I_Z", "I_INVB", "I_OPS", "E_M10", "M_L64Y", "M_L64Z"]
-TRACE_CTAS, TRACE_TILES, TRACE_SLOTS = 160, 64, 32
+          "I_L32", "I_L32B", "I_M11", "I_Y", "I_YB", "I_Z", "I_INVB", "I_OPS", "E_M10", "M_L64Y", "M_L64Z",
+          "I_SPLIT", "I_YSPL"]
+TRACE_CTAS, TRACE_TILES, TRACE_SLOTS = 160, 64, 40
 
 
-def run(workload: str, warmup: int = 3, dynamic: bool = True, gated: bool = False):
+def run(workload: str, warmup: int = 3, dynamic: bool = True, gated: bool = False, head_dim: int | None = None):
     path = build.build(trace=True)
     lib = _lib.lib(path)
     lib.kkt_set_trace_buffer.argtypes = [ctypes.c_void_p]
     lib.kkt_set_trace_buffer.restype = None
     w = workloads()[workload]
+    if head_dim is not None:
+        w = dataclasses.replace(w, dk=head_dim, dv=head_dim)
     k, v, beta, cu = w.make(seed=0, device="cuda")
     cu_t = None if cu is None else torch.as_tensor(cu, dtype=torch.int32, device="cuda")
     B = len(cu) - 1 if cu is not None else w.B
@@ -168,10 +172,12 @@ def report(tr: np.ndarray, ctas: int, tiles: int) -> str:
         ("C=128: Gram ready -> level 32 ends, rows 64..", span("I_GRAM", "I_L32B")),
         ("C=128: Gram ready -> M10 formed (epilogue)", span("I_GRAM", "E_M10")),
         ("C=128: level 32 end -> M00^-1 split, rows 0..", span("I_L32", "I_OPS")),
+        ("C=128:   of which the stores are issued", span("I_L32", "I_SPLIT")),
         ("C=128: level 32 end -> M11^-1 in TMEM, 64..", span("I_L32B", "I_M11")),
         ("C=128: M00^-1 split -> Y issued", span("I_OPS", "M_L64Y")),
         ("C=128: Y issued -> Y seen by rows 64..", span("M_L64Y", "I_Y")),
         ("C=128: Y seen -> Y split to shared memory", span("I_Y", "I_YB")),
+        ("C=128:   of which the stores are issued", span("I_Y", "I_YSPL")),
         ("C=128: Y split -> Z issued", span("I_YB", "M_L64Z")),
         ("C=128: Z issued -> Z seen by rows 64..", span("M_L64Z", "I_Z")),
         ("C=128: Z seen -> level 64 ends, rows 64..", span("I_Z", "I_INVB")),
@@ -191,8 +197,9 @@ def main():
     ap.add_argument("--static", action="store_true", help="fixed round-robin schedule (no workspace)")
     ap.add_argument("--save", default=None, help="also save the raw cycle counts (.npy)")
     ap.add_argument("--gated", action="store_true", help="the gated variant (seeded log decays)")
+    ap.add_argument("--head-dim", type=int, default=None, help="override d_k = d_v (64 or 128)")
     a = ap.parse_args()
-    tr = run(a.workload, dynamic=not a.static, gated=a.gated)
+    tr = run(a.workload, dynamic=not a.static, gated=a.gated, head_dim=a.head_dim)
     print(f"untraced launch of the trace build: {run.last_ms * 1e3:.1f} us")
     print(report(tr, a.ctas, a.tiles))
     if a.save:
