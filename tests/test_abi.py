@@ -35,6 +35,23 @@ def test_workspace_size_constant_matches_header():
     assert m and int(m.group(1), 16) == _lib.KKT_T_OUT_F16
 
 
+def test_trace_tool_matches_the_kernels_event_table():
+    """The trace tool decodes the kernel's trace buffer by the order of its event enum and by its
+    row size; both sides are written by hand, so a drift would mislabel every event."""
+    from gdn_chunkwise_ut_gb300 import trace
+    text = open(os.path.join(ROOT, "gdn_chunkwise_ut_gb300", "csrc", "kkt_tc.cuh")).read()
+    body = re.search(r"enum TraceEvent \{(.*?)\};", text, flags=re.S).group(1)
+    body = re.sub(r"//[^\n]*", "", body)
+    names = [n.strip().split("=")[0].strip() for n in body.split(",") if n.strip()]
+    assert names[-1] == "EV_COUNT"
+    assert [n[len("EV_"):] for n in names[:-1]] == trace.EVENTS
+    slots = int(re.search(r"constexpr int kTraceSlots = (\d+);", text).group(1))
+    tiles = int(re.search(r"constexpr int kTraceTiles = (\d+);", text).group(1))
+    ctas = int(re.search(r"constexpr int kTraceCtas = (\d+);", text).group(1))
+    assert (trace.TRACE_CTAS, trace.TRACE_TILES, trace.TRACE_SLOTS) == (ctas, tiles, slots)
+    assert len(trace.EVENTS) <= slots
+
+
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
     assert "kkt_solve_fwd" in names and "kkt_solve_fwd_ex" in names
