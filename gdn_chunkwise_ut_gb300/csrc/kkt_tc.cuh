@@ -481,8 +481,9 @@ __device__ __forceinline__ void form_a_row(uint8_t *tm, uint32_t gram, int m, in
 // write M00^-1 there and clear it again once Z is done.  The epilogue warps of lanes 64..127 form M10
 // from the Gram rows straight into tensor memory as soon as the previous tile's W|U MMA has read T~,
 // so that Y runs while warps 2 and 3 finish their level 32 (and those warps form only the diagonal
-// half of their rows of A).  Warps 2 and 3 then put M11^-1 into tensor memory, turn Y into Z's B
-// operand and write -Z into columns 0..63 of their rows.  The W|U issuer issues the MMAs.
+// half of their rows of A).  Warps 2 and 3 then put M11^-1 into the Gram's columns 64..127 of their
+// lanes, turn Y into Z's B operand and write -Z into columns 0..63 of their rows.  The W|U issuer
+// issues the MMAs; the next tile's Gram MMA waits for Z.
 
 // bf16 hi + lo split of 8 fp32 values (two float4) into one 16-byte chunk of each.
 __device__ __forceinline__ void split8(const float4 a, const float4 b, uint4 &hi, uint4 &lo) {
@@ -622,7 +623,7 @@ __device__ __forceinline__ bool level64_tc(int q, int m, int i, uint8_t *tm, uin
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars->l64_yb);
     if (tr) KKT_TRACE_AT(trow, EV_I_YB);
-    // -Z over M10 (read into tensor memory above)
+    // -Z into columns 0..63 of the row (M10 was formed straight into tensor memory, not here)
     if (!wait_bar(&bars->l64_z, ph, bars, status)) return false;
     tc_fence_after();
     if (tr) KKT_TRACE_AT(trow, EV_I_Z);
