@@ -341,13 +341,13 @@ def bench_ours(args, rank, world, local):
            "h2d_bytes_per_step": runner.h2d_bytes, "d2h_bytes_per_step": runner.d2h_bytes,
            "steps": n_e2e, "pieces": runner.pieces, "call": "kkt_solve_fwd_host"}
 
-    # the spec entry point itself (kkt_solve_fwd: bf16, no workspace, so the tensor-core
+    # the specified entry point itself (kkt_solve_fwd: bf16, no workspace, so the tensor-core
     # kernel deals its tiles round robin), timed the same way on the same buffers, after the
     # timed region; reported beside the headline, which times the call with the workspace
-    north_star = None
+    plain_call = None
     if w.io == "bf16" and not (args.no_t_out or args.t_f16 or args.gated or args.graph) and args.kernel == "auto":
-        north_star = time_north_star_call(k, v, beta, cu_t, w, T_out, W_out, U_out, K, flush, scrub, stream)
-        north_star["headline_us_per_call"] = launch_ms * 1e3
+        plain_call = time_kkt_solve_fwd_call(k, v, beta, cu_t, w, T_out, W_out, U_out, K, flush, scrub, stream)
+        plain_call["headline_us_per_call"] = launch_ms * 1e3
 
     consumer = None
     if args.consumer:
@@ -374,7 +374,7 @@ def bench_ours(args, rank, world, local):
                      "kernel": f"kkt_{kernel}", "alg_bytes_per_launch": alg_bytes,
                      "avg_launch_ms": launch_ms},
         "clocks": clocks, "e2e": e2e, "gpu_launches": K,
-        "north_star_call": north_star,
+        "kkt_solve_fwd_call": plain_call,
         "gdn_chunk_state": consumer,
     }
     if world == 1 and rank == 0 and not args.no_cpu_baseline:
@@ -443,7 +443,7 @@ def time_consumer(k, v, beta, g, cu_t, w, K, flush, scrub, stream, seed, peak):
             "with_kkt_solve_gbs": alg_both / (ms_both / 1e3) / 1e9}
 
 
-def time_north_star_call(k, v, beta, cu_t, w, T_out, W_out, U_out, K, flush, scrub, stream):
+def time_kkt_solve_fwd_call(k, v, beta, cu_t, w, T_out, W_out, U_out, K, flush, scrub, stream):
     """Average device time of kkt_solve_fwd (the C entry point, through ctypes) over K calls."""
     from gdn_chunkwise_ut_gb300 import _lib
     lib = _lib.lib()

@@ -3,7 +3,7 @@
 This module holds only the input recipe -- no step of the UT transform.  Both
 the CUDA path and the CPU oracle are fed from it; neither imports the other.
 
-Recipe (the workloads the spec configurations describe; the pages' own
+Recipe (the five benchmark configurations of the library's specification; the pages' own
 benchmark runs on Qwen3.5/3.6 head configurations, h_v in {64,48,32,24,16,8},
 per the FlashQLA announcement's Benchmark section, and these synthetic tensors
 stand in for that data):

@@ -1,6 +1,6 @@
 """Comparison of library outputs with the fp64 oracle, and chunk bookkeeping for tests.
 
-Tolerances (fixed by the spec contract of this library, written here):
+Tolerances (fixed by the accuracy contract of this library's specification, written here):
   * T_out (fp32):            max |T - T_ref| <= 1e-4
   * W, U~ (bf16):            max |X - X_ref| <= 2e-2 where |X_ref| < 8, and
                              <= 2e-2 + half a bf16 ulp of X_ref where |X_ref| >= 8

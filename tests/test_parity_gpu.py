@@ -61,9 +61,9 @@ def full_compare(k, v, beta, C, cu, outs, io="bf16", g=None):
     return T_g, T_ref
 
 
-# --- the spec entry point itself ------------------------------------------------------
+# --- the specified entry point itself, kkt_solve_fwd ----------------------------------------
 
-def _north_star_call(k, v, beta, C, cu=None):
+def _kkt_solve_fwd_call(k, v, beta, C, cu=None):
     """kkt_solve_fwd through ctypes: bf16, kernel auto, no workspace (the fixed round-robin
     schedule of the tensor-core kernel)."""
     Bt, T, H, dk = k.shape
@@ -84,7 +84,7 @@ def _north_star_call(k, v, beta, C, cu=None):
 
 @pytest.mark.parametrize("C", [32, 64, 128])
 @pytest.mark.parametrize("case", ["fixed", "varlen", "many_tiles"])
-def test_north_star_entry_point(case, C):
+def test_kkt_solve_fwd_entry_point(case, C):
     """kkt_solve_fwd, the entry point with the signature the library is specified by, against the
     oracle element by element, and bit-identical to the kkt_solve_fwd_ex call with a workspace
     (the dynamic schedule that the Python front end and the bench use by default): a ragged
@@ -100,7 +100,7 @@ def test_north_star_entry_point(case, C):
     else:
         k, v, beta = make_inputs(2, 4100, 12, 128, 128, seed=103 + C, device=DEV)
     cu_t = None if cu is None else torch.as_tensor(cu, dtype=torch.int32, device=DEV)
-    outs = _north_star_call(k, v, beta, C, cu_t)
+    outs = _kkt_solve_fwd_call(k, v, beta, C, cu_t)
     full_compare(k, v, beta, C, cu, outs)
     dyn = run(k, v, beta, C, cu, kernel="auto", workspace="auto")
     for a, b in zip(outs, dyn):
